@@ -1,0 +1,270 @@
+"""Seeded synthetic inputs for the decode-time MoE layer.
+
+The one module both the CUDA path's tests/benchmark and the CPU oracle's
+callers draw inputs from.  It holds no step of the method: it draws
+activations, router logits, expert ids and float weights, and encodes the
+weights into the storage formats the layer reads (FP8 E4M3 codes with
+128x128 fp32 block scales; NVFP4 E2M1 codes with per-16 E4M3 scales and a
+per-projection fp32 global scale).  How a weight is encoded is the data
+recipe, not part of the layer: the layer only decodes.
+
+Workloads (no dataset or checkpoint exists; these shapes stand in):
+  * tiny:      M=4, H=256, I=512, E=8, top_k=2, BS=16, FP8, no shared expert
+  * decode:    the 128-expert shape (H=2048, I=768, E=128, top_k=8, BS=16),
+               FP8, M in {1, 2, 4, 8}
+  * nvfp4:     the same shape with NVFP4 experts, M in {1, 8, 32}, plus an
+               FP8 shared expert of inter 512 applied to every row
+  * verify:    M=128, H=4096, I=1536, E=256, top_k=8, BS=64, FP8, router
+               logits skewed by a Zipf(s=1.1) per-expert bias
+  * align:     ids only, n = 8*M, M in {1, 64, 1024, 4096}, E in
+               {64, 256, 1024}, BS in {16, 64, 128}; uniform, Zipf(s=1.2)
+               or all one expert
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+import torch
+
+FMT_FP8 = "fp8"
+FMT_NVFP4 = "nvfp4"
+
+E4M3_MAX = 448.0
+E2M1_MAX = 6.0
+# E2M1 magnitudes in code order 0..7, and the midpoints between neighbours
+_E2M1_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+_E2M1_MIDS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+
+
+@dataclass(frozen=True)
+class LayerShape:
+    name: str
+    M: int
+    H: int
+    I: int
+    E: int
+    top_k: int
+    BS: int
+    fmt: str
+    shared_I: Optional[int] = None        # FP8 shared expert width, or None
+    zipf_s: Optional[float] = None        # per-expert router bias, or None
+    zipf_scale: float = 0.0
+
+    @property
+    def n(self) -> int:
+        return self.M * self.top_k
+
+
+def tiny(M: int = 4) -> LayerShape:
+    return LayerShape("tiny_h256_i512_e8_k2_fp8", M, 256, 512, 8, 2, 16, FMT_FP8)
+
+
+def decode_fp8(M: int) -> LayerShape:
+    return LayerShape(f"decode_h2048_i768_e128_k8_fp8_m{M}", M, 2048, 768, 128, 8, 16, FMT_FP8)
+
+
+def decode_nvfp4(M: int) -> LayerShape:
+    return LayerShape(f"decode_h2048_i768_e128_k8_nvfp4_shared512_m{M}", M, 2048, 768, 128, 8,
+                      16, FMT_NVFP4, shared_I=512)
+
+
+# Zipf bias strength for the verify batch: log-pmf times this scale.  With
+# 1.0 the hottest experts take 30+ of the 128 rows (the builder check in the
+# tests reports the realised maximum).
+VERIFY_ZIPF_SCALE = 1.0
+
+
+def verify_fp8(M: int = 128) -> LayerShape:
+    return LayerShape(f"verify_h4096_i1536_e256_k8_fp8_zipf_m{M}", M, 4096, 1536, 256, 8, 64,
+                      FMT_FP8, zipf_s=1.1, zipf_scale=VERIFY_ZIPF_SCALE)
+
+
+# --------------------------------------------------------------------------
+# weight encodings (data recipe)
+# --------------------------------------------------------------------------
+
+def encode_fp8_b128(w: torch.Tensor):
+    """w float32 [rows, cols] (multiples of 128) -> (codes uint8 [rows, cols],
+    scale float32 [rows/128, cols/128]) with scale = amax/448 per block and
+    codes = e4m3(w / scale), torch's float8_e4m3fn conversion."""
+    rows, cols = w.shape
+    blk = w.reshape(rows // 128, 128, cols // 128, 128)
+    amax = blk.abs().amax(dim=(1, 3))
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q = (blk / scale[:, None, :, None]).reshape(rows, cols).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8), scale.to(torch.float32)
+
+
+def encode_nvfp4_g16(w: torch.Tensor):
+    """w float32 [rows, cols] (cols a multiple of 32) -> (packed uint8
+    [rows, cols/2] with the even element in the low nibble, s16 uint8 E4M3
+    [rows, cols/16], global float32 scalar tensor).
+    global = amax/(448*6); s16 = e4m3(amax_g / (6*global)); code = nearest
+    E2M1 of w / (s16*global) (ties to the smaller magnitude), clamped to 6."""
+    rows, cols = w.shape
+    amax = w.abs().amax()
+    glob = (amax / (E4M3_MAX * E2M1_MAX)) if float(amax) > 0 else torch.ones((), device=w.device)
+    glob = glob.to(torch.float32)
+    g = w.reshape(rows, cols // 16, 16)
+    amax_g = g.abs().amax(dim=2)
+    s16 = (amax_g / (E2M1_MAX * glob)).to(torch.float8_e4m3fn)
+    s16f = s16.to(torch.float32)
+    denom = (s16f * glob)[:, :, None]
+    v = torch.where(denom > 0, g / torch.where(denom > 0, denom, torch.ones_like(denom)),
+                    torch.zeros_like(g))
+    mag = v.abs().clamp(max=E2M1_MAX)
+    mids = torch.tensor(_E2M1_MIDS, dtype=torch.float32, device=w.device)
+    idx = torch.bucketize(mag.contiguous(), mids, right=False).to(torch.uint8)
+    sign = ((v < 0) & (idx > 0)).to(torch.uint8) << 3
+    code = (idx | sign).reshape(rows, cols)
+    packed = code[:, 0::2] | (code[:, 1::2] << 4)
+    return packed.contiguous(), s16.view(torch.uint8).contiguous(), glob
+
+
+@dataclass
+class ProjData:
+    """One projection for all experts: torch tensors on one device.
+    FP8: codes [E, rows, cols] u8, scale [E, rows/128, cols/128] f32, glob None.
+    NVFP4: codes [E, rows, cols/2] u8, scale [E, rows, cols/16] u8, glob [E] f32."""
+    fmt: str
+    rows: int
+    cols: int
+    codes: torch.Tensor
+    scale: torch.Tensor
+    glob: Optional[torch.Tensor] = None
+
+    def nbytes_per_expert(self) -> int:
+        per = self.codes[0].numel() + self.scale[0].numel() * self.scale.element_size()
+        return per + (4 if self.glob is not None else 0)
+
+    def to(self, device) -> "ProjData":
+        return ProjData(self.fmt, self.rows, self.cols, self.codes.to(device),
+                        self.scale.to(device), None if self.glob is None else self.glob.to(device))
+
+
+@dataclass
+class ExpertData:
+    E: int
+    H: int
+    I: int
+    fmt: str
+    gate: ProjData
+    up: ProjData
+    down: ProjData
+
+    def bytes_per_expert(self) -> int:
+        return (self.gate.nbytes_per_expert() + self.up.nbytes_per_expert()
+                + self.down.nbytes_per_expert())
+
+    def to(self, device) -> "ExpertData":
+        return ExpertData(self.E, self.H, self.I, self.fmt, self.gate.to(device),
+                          self.up.to(device), self.down.to(device))
+
+
+def _proj(E: int, rows: int, cols: int, fmt: str, gen: torch.Generator, device,
+          std: float) -> ProjData:
+    codes, scales, globs = [], [], []
+    for _ in range(E):
+        w = torch.randn(rows, cols, generator=gen, device=device, dtype=torch.float32) * std
+        if fmt == FMT_FP8:
+            q, s = encode_fp8_b128(w)
+            codes.append(q)
+            scales.append(s)
+        else:
+            q, s, g = encode_nvfp4_g16(w)
+            codes.append(q)
+            scales.append(s)
+            globs.append(g.reshape(1))
+    return ProjData(fmt, rows, cols, torch.stack(codes), torch.stack(scales),
+                    torch.cat(globs) if globs else None)
+
+
+def make_experts(E: int, H: int, I: int, fmt: str, seed: int, device="cpu",
+                 std: float = 0.02) -> ExpertData:
+    """E experts, gate/up [I, H] and down [H, I], from N(0, std) encoded as fmt."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    gate = _proj(E, I, H, fmt, gen, device, std)
+    up = _proj(E, I, H, fmt, gen, device, std)
+    down = _proj(E, H, I, fmt, gen, device, std)
+    return ExpertData(E, H, I, fmt, gate, up, down)
+
+
+# --------------------------------------------------------------------------
+# activations, router logits, ids
+# --------------------------------------------------------------------------
+
+def make_x(M: int, H: int, seed: int, device="cpu") -> torch.Tensor:
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return torch.randn(M, H, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def zipf_bias(E: int, s: float, scale: float, seed: int) -> torch.Tensor:
+    """b_e = scale * log(pmf(rank_e)), pmf(r) proportional to r^-s, rank_e a
+    seeded permutation of 1..E."""
+    g = torch.Generator()
+    g.manual_seed(seed)
+    rank = torch.randperm(E, generator=g).to(torch.float64) + 1.0
+    logpmf = -s * torch.log(rank)
+    logpmf = logpmf - torch.logsumexp(logpmf, 0)
+    return (scale * logpmf).to(torch.float32)
+
+
+def make_logits(M: int, E: int, seed: int, device="cpu", zipf_s: Optional[float] = None,
+                zipf_scale: float = 0.0, bias_seed: int = 7) -> torch.Tensor:
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    lg = torch.randn(M, E, generator=gen, device=device, dtype=torch.float32)
+    if zipf_s is not None:
+        lg = lg + zipf_bias(E, zipf_s, zipf_scale, bias_seed).to(device)
+    return lg
+
+
+def align_ids(n: int, E: int, dist: str, seed: int, expert: int = 0) -> np.ndarray:
+    """int64 [n] expert ids: 'uniform', 'zipf' (Zipf(s=1.2) ranks clipped to E,
+    mapped to experts by a seeded permutation) or 'one' (all `expert`)."""
+    rng = np.random.default_rng(seed)
+    if dist == "uniform":
+        return rng.integers(0, E, size=n, dtype=np.int64)
+    if dist == "zipf":
+        perm = rng.permutation(E)
+        r = np.minimum(rng.zipf(1.2, size=n), E) - 1
+        return perm[r].astype(np.int64)
+    if dist == "one":
+        return np.full(n, expert, dtype=np.int64)
+    raise ValueError(dist)
+
+
+@dataclass
+class LayerInputs:
+    shape: LayerShape
+    x: torch.Tensor                      # bf16 [M, H]
+    logits: torch.Tensor                 # f32 [M, E]
+    experts: ExpertData
+    shared: Optional[ExpertData] = None
+    extra: dict = field(default_factory=dict)
+
+    def to(self, device) -> "LayerInputs":
+        return LayerInputs(self.shape, self.x.to(device), self.logits.to(device),
+                           self.experts.to(device),
+                           None if self.shared is None else self.shared.to(device), self.extra)
+
+
+def make_layer(shape: LayerShape, seed: int = 1000, device="cpu") -> LayerInputs:
+    """All inputs of one layer call.  Seeds: weights `seed`, shared expert
+    `seed + 1`, x `seed + 2`, logits `seed + 3`."""
+    ex = make_experts(shape.E, shape.H, shape.I, shape.fmt, seed, device)
+    sh = None
+    if shape.shared_I is not None:
+        sh = make_experts(1, shape.H, shape.shared_I, FMT_FP8, seed + 1, device)
+    x = make_x(shape.M, shape.H, seed + 2, device)
+    lg = make_logits(shape.M, shape.E, seed + 3, device, shape.zipf_s, shape.zipf_scale)
+    return LayerInputs(shape, x, lg, ex, sh)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """The uint16 bit patterns of a bf16 tensor, as numpy."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)

@@ -1,0 +1,91 @@
+"""Shared test helpers: hand synthetic data to the oracle, and an independent
+float64 PyTorch restatement of the layer built from library routines (torch's
+float8 decoding, matmul, silu, topk, softmax) that pins the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+E2M1_TABLE = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+                       -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+
+
+def oracle_proj(p: synth.ProjData) -> oracle.Proj:
+    fmt = oracle.FMT_FP8_B128 if p.fmt == synth.FMT_FP8 else oracle.FMT_NVFP4_G16
+    return oracle.Proj(fmt, p.rows, p.cols, p.codes.cpu().numpy(), p.scale.cpu().numpy(),
+                       None if p.glob is None else p.glob.cpu().numpy())
+
+
+def oracle_experts(d: synth.ExpertData) -> oracle.Experts:
+    return oracle.Experts(d.E, d.H, d.I, oracle_proj(d.gate), oracle_proj(d.up),
+                          oracle_proj(d.down))
+
+
+def subset_experts(d: synth.ExpertData, ids) -> synth.ExpertData:
+    """The experts `ids` (in that order) as a smaller expert set on the CPU."""
+    idx = torch.as_tensor(list(ids), dtype=torch.long)
+
+    def sub(p: synth.ProjData) -> synth.ProjData:
+        i = idx.to(p.codes.device)
+        return synth.ProjData(p.fmt, p.rows, p.cols, p.codes[i].cpu(), p.scale[i].cpu(),
+                              None if p.glob is None else p.glob[i].cpu())
+
+    return synth.ExpertData(len(idx), d.H, d.I, d.fmt, sub(d.gate), sub(d.up), sub(d.down))
+
+
+# --------------------------------------------------------------------------
+# torch float64 restatement (library routines)
+# --------------------------------------------------------------------------
+
+def torch_dequant(p: synth.ProjData, e: int) -> torch.Tensor:
+    if p.fmt == synth.FMT_FP8:
+        q = p.codes[e].cpu().view(torch.float8_e4m3fn).to(torch.float64)
+        s = p.scale[e].cpu().to(torch.float64)
+        s = s.repeat_interleave(128, 0).repeat_interleave(128, 1)
+        return q * s[: q.shape[0], : q.shape[1]]
+    packed = p.codes[e].cpu().numpy()
+    codes = np.empty((packed.shape[0], packed.shape[1] * 2), np.uint8)
+    codes[:, 0::2] = packed & 0xF
+    codes[:, 1::2] = packed >> 4
+    v = torch.from_numpy(E2M1_TABLE[codes])
+    s16 = p.scale[e].cpu().view(torch.float8_e4m3fn).to(torch.float64)
+    return v * s16.repeat_interleave(16, 1) * float(p.glob[e])
+
+
+def torch_ffn(d: synth.ExpertData, e: int, x: torch.Tensor) -> torch.Tensor:
+    """down(silu(gate x) * up x) for float64 rows x [m, H]."""
+    g = x @ torch_dequant(d.gate, e).T
+    u = x @ torch_dequant(d.up, e).T
+    h = torch.nn.functional.silu(g) * u
+    return h @ torch_dequant(d.down, e).T
+
+
+def torch_route(logits: torch.Tensor, k: int):
+    p = torch.softmax(logits.to(torch.float64), dim=-1)
+    vals, ids = torch.topk(logits.to(torch.float64), k, dim=-1)
+    w = torch.gather(p, 1, ids)
+    return ids, w / w.sum(dim=-1, keepdim=True)
+
+
+def torch_layer(inp: synth.LayerInputs, ids=None, w=None) -> torch.Tensor:
+    """out[t] = sum_j w[t, j] * FFN_{ids[t, j]}(x[t]) + shared(x[t]), float64."""
+    x = inp.x.cpu().to(torch.float64)
+    if ids is None:
+        ids, w = torch_route(inp.logits.cpu(), inp.shape.top_k)
+    out = torch.zeros(x.shape[0], inp.shape.H, dtype=torch.float64)
+    for t in range(x.shape[0]):
+        for j in range(ids.shape[1]):
+            out[t] += float(w[t, j]) * torch_ffn(inp.experts, int(ids[t, j]), x[t: t + 1])[0]
+    if inp.shared is not None:
+        out += torch_ffn(inp.shared, 0, x)
+    return out
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
