@@ -1,0 +1,158 @@
+// layer.cu -- the grouped expert entry points (path dispatch) and the decode
+// layer: route -> align -> gate+up -> down -> blend on one stream
+// ("metrale_model_layers/layers/moe/forward_nvfp4_grouped_decode.rs",
+// forward_nvfp4_grouped_decode; every step enqueued, no host read).
+#include "common.cuh"
+
+namespace moe {
+
+int validate_experts(const moe_experts *X, bool shared);
+int simt_gate_up(const moe_experts *routed, const moe_experts *shared, const uint16_t *x, int M,
+                 int top_k, const int32_t *off, const int32_t *sti, const int32_t *act,
+                 const int32_t *act_count, float *h, float *h_sh, void *stream);
+int simt_down(const moe_experts *routed, const moe_experts *shared, const float *h,
+              const float *h_sh, int M, int top_k, const int32_t *off, const int32_t *sti,
+              const int32_t *act, const int32_t *act_count, float *y, float *y_sh, void *stream);
+int launch_topk(const float *logits, int M, int E, int k, int32_t *ids, float *w, void *stream);
+int launch_blend(const float *y, const float *w, const int32_t *ttp, const float *y_sh,
+                 uint16_t *out, int M, int k, int H, void *stream);
+
+// The expert-kernel path of a shape class.  It depends on the shapes only,
+// never on the routing, so a captured graph stays valid for every routing.
+static int resolve_path(const moe_experts *routed, int M, int top_k, int path) {
+  (void)routed;
+  (void)M;
+  (void)top_k;
+  if (path == MOE_PATH_TC) return -1;   // no tensor-core kernels for this shape yet
+  return MOE_PATH_SIMT;
+}
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
+  if (!L || !v) return MOE_EINVAL;
+  int st = validate_experts(&L->routed, false);
+  if (st) return st;
+  if (L->shared) {
+    st = validate_experts(L->shared, true);
+    if (st) return st;
+    if (L->shared->hidden != L->routed.hidden) return MOE_EINVAL;
+  }
+  const int E = L->routed.num_experts, k = L->top_k;
+  if (M < 1 || k < 1 || k > E || L->block_size < 1) return MOE_EINVAL;
+  if (M > MOE_MAX_ROWS || k > 32) return MOE_EUNSUPPORTED;
+  if (L->path != MOE_PATH_AUTO && L->path != MOE_PATH_SIMT && L->path != MOE_PATH_TC)
+    return MOE_EINVAL;
+  const int n = M * k;
+  int max_total, max_blocks, cap;
+  st = moe_align_sizes(n, E, L->block_size, &max_total, &max_blocks, &cap);
+  if (st) return st;
+  const int H = L->routed.hidden, I = L->routed.inter;
+  const int Is = L->shared ? L->shared->inter : 0;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  v->topk_ids = take((size_t)n * 4);
+  v->topk_w = take((size_t)n * 4);
+  v->sorted_token_ids = take((size_t)max_total * 4);
+  v->sorted_expert_ids = take((size_t)max_blocks * 4);
+  v->expert_offsets = take((size_t)(E + 1) * 4);
+  v->token_to_perm = take((size_t)n * 4);
+  v->active_experts = take((size_t)cap * 4);
+  v->active_count = take(4);
+  v->num_tokens_post_padded = take(4);
+  v->h = take((size_t)max_total * I * 4);
+  v->h_shared = take((size_t)M * Is * 4);
+  v->y = take((size_t)max_total * H * 4);
+  v->y_shared = take((size_t)M * H * 4);
+  v->total_bytes = off;
+  v->max_total = max_total;
+  v->max_blocks = max_blocks;
+  v->cap = cap;
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" int moe_grouped_gate_up(const moe_experts *routed, const moe_experts *shared,
+                                   const uint16_t *x, int M, int top_k,
+                                   const int32_t *expert_offsets, const int32_t *sorted_token_ids,
+                                   const int32_t *active_experts, const int32_t *active_count,
+                                   float *h, float *h_shared, int path, void *stream) {
+  if (!routed) return MOE_EINVAL;
+  const int p = moe::resolve_path(routed, M, top_k, path);
+  if (p < 0) return MOE_EUNSUPPORTED;
+  return moe::simt_gate_up(routed, shared, x, M, top_k, expert_offsets, sorted_token_ids,
+                           active_experts, active_count, h, h_shared, stream);
+}
+
+extern "C" int moe_grouped_down(const moe_experts *routed, const moe_experts *shared,
+                                const float *h, const float *h_shared, int M, int top_k,
+                                const int32_t *expert_offsets, const int32_t *sorted_token_ids,
+                                const int32_t *active_experts, const int32_t *active_count,
+                                float *y, float *y_shared, int path, void *stream) {
+  if (!routed) return MOE_EINVAL;
+  const int p = moe::resolve_path(routed, M, top_k, path);
+  if (p < 0) return MOE_EUNSUPPORTED;
+  return moe::simt_down(routed, shared, h, h_shared, M, top_k, expert_offsets, sorted_token_ids,
+                        active_experts, active_count, y, y_shared, stream);
+}
+
+extern "C" size_t moe_decode_layer_workspace_bytes(const moe_layer_desc *layer, int max_M) {
+  moe_workspace_view v;
+  if (moe::layout(layer, max_M, &v) != MOE_OK) return 0;
+  return v.total_bytes;
+}
+
+extern "C" int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int M,
+                                               moe_workspace_view *view) {
+  return moe::layout(layer, M, view);
+}
+
+extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,
+                                const float *router_logits, const int32_t *topk_ids,
+                                const float *topk_w, uint16_t *out, void *workspace,
+                                size_t workspace_bytes, uint32_t *err_word, void *stream) {
+  moe_workspace_view v;
+  int st = moe::layout(layer, M, &v);
+  if (st) return st;
+  if (!x || !out || !workspace) return MOE_EINVAL;
+  if (!router_logits && (!topk_ids || !topk_w)) return MOE_EINVAL;
+  if (workspace_bytes < v.total_bytes || ((uintptr_t)workspace & 255)) return MOE_EINVAL;
+  if (((uintptr_t)x & 15) || ((uintptr_t)out & 7)) return MOE_EINVAL;
+  const int path = moe::resolve_path(&layer->routed, M, layer->top_k, layer->path);
+  if (path < 0) return MOE_EUNSUPPORTED;
+
+  char *ws = reinterpret_cast<char *>(workspace);
+  auto I32 = [&](size_t o) { return reinterpret_cast<int32_t *>(ws + o); };
+  auto F32 = [&](size_t o) { return reinterpret_cast<float *>(ws + o); };
+  const int E = layer->routed.num_experts, k = layer->top_k, H = layer->routed.hidden;
+  const moe_experts *S = layer->shared;
+
+  const int32_t *ids = topk_ids;
+  const float *w = topk_w;
+  if (router_logits) {
+    st = moe::launch_topk(router_logits, M, E, k, I32(v.topk_ids), F32(v.topk_w), stream);
+    if (st) return st;
+    ids = I32(v.topk_ids);
+    w = F32(v.topk_w);
+  }
+  st = moe_align(ids, 0, M * k, E, layer->block_size, I32(v.sorted_token_ids),
+                 I32(v.sorted_expert_ids), I32(v.expert_offsets), I32(v.token_to_perm),
+                 I32(v.active_experts), I32(v.active_count), I32(v.num_tokens_post_padded),
+                 err_word, stream);
+  if (st) return st;
+  st = moe::simt_gate_up(&layer->routed, S, x, M, k, I32(v.expert_offsets),
+                         I32(v.sorted_token_ids), I32(v.active_experts), I32(v.active_count),
+                         F32(v.h), S ? F32(v.h_shared) : nullptr, stream);
+  if (st) return st;
+  st = moe::simt_down(&layer->routed, S, F32(v.h), S ? F32(v.h_shared) : nullptr, M, k,
+                      I32(v.expert_offsets), I32(v.sorted_token_ids), I32(v.active_experts),
+                      I32(v.active_count), F32(v.y), S ? F32(v.y_shared) : nullptr, stream);
+  if (st) return st;
+  return moe::launch_blend(F32(v.y), w, I32(v.token_to_perm), S ? F32(v.y_shared) : nullptr, out,
+                           M, k, H, stream);
+}

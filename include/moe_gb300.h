@@ -1,0 +1,269 @@
+/*
+ * moe_gb300.h -- C ABI of the decode-time Mixture-of-Experts layer on GB300
+ * (sm_103a): router top-k ids -> deterministic device-side token alignment ->
+ * grouped FP8 / NVFP4 expert FFN (gate+up, SiLU(gate)*up, down) -> weighted
+ * blend back to token order.
+ *
+ * Conventions shared by every entry point
+ *  - All array arguments are DEVICE pointers unless stated; the caller owns
+ *    every buffer (weights, inputs, outputs, workspace).  No entry point
+ *    allocates, frees or synchronises.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is enqueued asynchronously on it and is CUDA-graph
+ *    capturable: every launch's grid depends only on the shape arguments, never
+ *    on routing results, and nothing is read back to the host.
+ *  - Return value: MOE_OK, or an error code.  Host-detected errors (a NULL
+ *    pointer, a size or shape outside what is admitted) launch nothing.
+ *    MOE_ECUDA means a launch failed; moe_last_cuda_error() gives the
+ *    cudaError_t of the calling thread's last failure.
+ *  - Device-detected errors never trap: the kernel skips the offending item
+ *    and ORs a MOE_ERR_* bit into *err_word (if err_word is not NULL), which
+ *    the caller reads when it chooses.
+ *  - Matrices are row-major.  bf16 values are passed as their uint16 bit
+ *    patterns.
+ *
+ * Sources.  The operations are those of three pages:
+ *   "nbxtensor/ops/moe_align.py" (alignment stages 1-3 and the worst-case
+ *   sizing in its module docstring), "nbxtensor/ops/moe_decode_vec.py" (SiLU
+ *   product in fp32, fixed-order combine), "metrale_model_layers/layers/ops/
+ *   fp8_moe_grouped.rs" (moe_fp8_grouped_sort, the grouped gate+up/down
+ *   launchers, fp8_grouped_active_cap, the blend) and "metrale_model_layers/
+ *   layers/moe/forward_nvfp4_grouped_decode.rs" (the layer's sequence and
+ *   its shape admission).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MOE_OK 0
+#define MOE_EINVAL 1        /* NULL pointer, negative/zero size, bad enum */
+#define MOE_EUNSUPPORTED 2  /* shape valid but not admitted by the kernels */
+#define MOE_ECUDA 3         /* a CUDA runtime call or launch failed */
+
+/* ---- device error bits, ORed into *err_word ----------------------------- */
+#define MOE_ERR_BAD_ID 0x1u   /* an expert id outside [0, E): slot skipped */
+
+/* ---- formats and paths -------------------------------------------------- */
+#define MOE_FMT_FP8_B128 1  /* E4M3 codes, fp32 scale per 128x128 block      */
+#define MOE_FMT_NVFP4_G16 2 /* E2M1 codes, E4M3 scale per 16, fp32 global    */
+
+#define MOE_PATH_AUTO 0     /* chosen per shape class (never per routing)    */
+#define MOE_PATH_SIMT 1     /* CUDA-core kernels, in-register dequant         */
+#define MOE_PATH_TC 2       /* tcgen05 tensor-core kernels (FP8 only)         */
+
+#define MOE_MAX_EXPERTS 1024      /* experts the alignment handles            */
+#define MOE_MAX_SLOTS (1 << 20)   /* n = M * top_k the alignment handles      */
+#define MOE_MAX_ROWS 128          /* M the expert kernels and layer admit     */
+
+/* One projection of all experts of a set.  Layout for `rows` x `cols`
+ * (gate/up: rows = inter, cols = hidden; down: rows = hidden, cols = inter):
+ *   FP8_B128:  codes  uint8 [E][rows][cols] E4M3;
+ *              scale  float [E][rows/128][cols/128], w = e4m3(code) * scale;
+ *              global_scale unused (NULL).
+ *   NVFP4_G16: codes  uint8 [E][rows][cols/2], element 2i in the low nibble,
+ *              2i+1 in the high nibble, E2M1;
+ *              scale  uint8 [E][rows][cols/16] E4M3;
+ *              global_scale float [E]; w = e2m1(code) * e4m3(scale) * global.
+ * Experts are packed back to back (expert e at e * one expert's size).
+ * All three pointers must be 16-byte aligned (scale: 4-byte for FP8). */
+typedef struct moe_proj {
+    const void *codes;
+    const void *scale;
+    const float *global_scale;
+} moe_proj;
+
+/* An expert set: E experts with gate/up [inter][hidden] and down
+ * [hidden][inter].  FP8 needs hidden % 128 == 0 and inter % 128 == 0;
+ * NVFP4 needs hidden % 32 == 0 and inter % 32 == 0. */
+typedef struct moe_experts {
+    int fmt;          /* MOE_FMT_* */
+    int num_experts;  /* E (1 for a shared expert) */
+    int hidden;       /* H */
+    int inter;        /* I */
+    moe_proj gate, up, down;
+} moe_experts;
+
+/* The layer: routed experts (E <= MOE_MAX_EXPERTS), top_k, alignment block
+ * size, an optional shared expert (NULL = none; applied to every row, may
+ * have its own format and inter), and the expert-kernel path. */
+typedef struct moe_layer_desc {
+    int top_k;
+    int block_size;
+    int path;                    /* MOE_PATH_* */
+    moe_experts routed;
+    const moe_experts *shared;   /* host pointer to a descriptor, or NULL */
+} moe_layer_desc;
+
+/* ---- library information ------------------------------------------------ */
+const char *moe_version(void);
+const char *moe_status_string(int status);
+int moe_last_cuda_error(void);
+
+/* ---- alignment ---------------------------------------------------------- */
+
+/* Host only.  Worst-case table sizes of n = M*top_k slots over E experts with
+ * block size BS ("nbxtensor/ops/moe_align.py", module docstring;
+ * "fp8_moe_grouped.rs", fp8_grouped_active_cap):
+ *   *max_total  = min(n*BS, n + E*(BS-1)) rounded up to a multiple of BS,
+ *   *max_blocks = *max_total / BS,   *cap = min(n, E).
+ * Returns MOE_EINVAL for n < 0, E < 1, BS < 1 or NULL outputs;
+ * MOE_EUNSUPPORTED for n > MOE_MAX_SLOTS or a max_total beyond int32. */
+int moe_align_sizes(int n, int num_experts, int block_size,
+                    int *max_total, int *max_blocks, int *cap);
+
+/* Device-side token alignment of n flat slots (slot i = token*top_k + j),
+ * one launch, no atomics on the tables: results are bit-deterministic.
+ * ("nbxtensor/ops/moe_align.py": stage 1 counts / block padding / exclusive
+ * offsets / total, stage 2 sentinel fill and block->expert map, stage 3
+ * rank = number of earlier slots with the same expert and scatter;
+ * "fp8_moe_grouped.rs", moe_fp8_grouped_sort: token_to_perm and the active
+ * list.)
+ *   topk_ids               [n] int32, or int64 if ids_is_int64
+ *   sorted_token_ids  out  [max_total] int32: slot index at its sorted
+ *                          position; padding and the tail hold n (sentinel)
+ *   sorted_expert_ids out  [max_blocks] int32: expert owning block b, -1 for
+ *                          blocks at or past the total
+ *   expert_offsets    out  [E+1] int32: exclusive block-padded offsets,
+ *                          expert_offsets[E] = total
+ *   token_to_perm     out  [n] int32: sorted position of slot i (-1 if its id
+ *                          is out of range)
+ *   active_experts    out  [cap] int32: experts with >= 1 slot, ascending,
+ *                          then -1 up to cap
+ *   active_count      out  [1] int32
+ *   num_tokens_post_padded out [1] int32: the total (= expert_offsets[E])
+ *   err_word               [1] uint32 or NULL: MOE_ERR_BAD_ID is ORed in
+ *                          when an id lies outside [0, E); that slot is
+ *                          skipped everywhere.
+ * n == 0 is valid (writes the offsets, counts and total as zero).
+ * Errors: MOE_EINVAL (NULL table pointer, n < 0, E < 1, BS < 1),
+ * MOE_EUNSUPPORTED (E > MOE_MAX_EXPERTS, n > MOE_MAX_SLOTS). */
+int moe_align(const void *topk_ids, int ids_is_int64, int n, int num_experts,
+              int block_size, int32_t *sorted_token_ids,
+              int32_t *sorted_expert_ids, int32_t *expert_offsets,
+              int32_t *token_to_perm, int32_t *active_experts,
+              int32_t *active_count, int32_t *num_tokens_post_padded,
+              uint32_t *err_word, void *stream);
+
+/* ---- routing ------------------------------------------------------------ */
+
+/* Per-row router: for each of M rows of fp32 logits [M][E] select the top_k
+ * largest logits (equal logits: the lower expert id first) and write their
+ * ids in descending order and their softmax weights renormalised over the
+ * selection (= softmax over all E, top-k, renormalised), fp32
+ * ("forward_nvfp4_grouped_decode.rs": grouped_route, GroupedRouting::PerRow;
+ * the top-k softmax kernel moe_topk_softmax_rows).  Logits must be finite.
+ *   topk_ids out [M][top_k] int32, topk_w out [M][top_k] float.
+ * Errors: MOE_EINVAL (NULL, M < 1, top_k < 1, top_k > E),
+ * MOE_EUNSUPPORTED (E > MOE_MAX_EXPERTS, top_k > 32). */
+int moe_topk_softmax(const float *logits, int M, int num_experts, int top_k,
+                     int32_t *topk_ids, float *topk_w, void *stream);
+
+/* ---- grouped expert FFN ------------------------------------------------- */
+
+/* Grouped gate+up and SiLU ("fp8_moe_grouped.rs",
+ * moe_expert_gate_up_act_fp8_grouped; the SwiGLU epilogue of
+ * "moe_decode_vec.py").  For every active expert e = active_experts[a]
+ * (a < *active_count) and every real position p of its run
+ * (expert_offsets[e] <= p < expert_offsets[e+1], sorted_token_ids[p] < n),
+ * token t = sorted_token_ids[p] / top_k:
+ *     h[p][o] = silu(g) * u,  g = Wg[e][o] . x[t],  u = Wu[e][o] . x[t]
+ * in fp32 (no intermediate bf16 rounding).  Each weight row is read once per
+ * pass for all rows routed to its expert.  With a shared expert S (host
+ * descriptor, may be NULL): h_shared[t][o] = the same with S, for every t.
+ *   x        [M][H] bf16 bits;  the tables as written by moe_align for
+ *            n = M*top_k slots and E = routed->num_experts
+ *   h    out [max_total][I] float, rows by sorted position (padding rows
+ *            untouched)
+ *   h_shared out [M][S->inter] float (NULL iff shared is NULL)
+ *   path     MOE_PATH_*; the grid is a function of (M, top_k, E, H, I, path).
+ * Errors: MOE_EINVAL (NULL, M < 1 or > MOE_MAX_ROWS, bad fmt/path),
+ * MOE_EUNSUPPORTED (shape not admitted; TC path not available for it). */
+int moe_grouped_gate_up(const moe_experts *routed, const moe_experts *shared,
+                        const uint16_t *x, int M, int top_k,
+                        const int32_t *expert_offsets,
+                        const int32_t *sorted_token_ids,
+                        const int32_t *active_experts,
+                        const int32_t *active_count, float *h,
+                        float *h_shared, int path, void *stream);
+
+/* Grouped down projection over the SiLU product ("fp8_moe_grouped.rs",
+ * moe_expert_down_act_fp8_grouped): y[p][c] = Wd[e][c] . h[p] in fp32 for
+ * every real position p of every active expert e; y_shared[t] = WdS .
+ * h_shared[t] for every token.  Rows of h and y are sorted positions.
+ *   h [max_total][I], h_shared [M][S->inter], y out [max_total][H],
+ *   y_shared out [M][H] (NULL iff shared is NULL).
+ * Errors as moe_grouped_gate_up. */
+int moe_grouped_down(const moe_experts *routed, const moe_experts *shared,
+                     const float *h, const float *h_shared, int M, int top_k,
+                     const int32_t *expert_offsets,
+                     const int32_t *sorted_token_ids,
+                     const int32_t *active_experts,
+                     const int32_t *active_count, float *y, float *y_shared,
+                     int path, void *stream);
+
+/* Weighted blend back to token order in a fixed order ("fp8_moe_grouped.rs",
+ * moe_weighted_sum_blend_fp8_grouped; fixed-order combine of
+ * "moe_decode_vec.py"):
+ *   out[t][c] = bf16_rn( sum_{j=0..top_k-1} topk_w[t][j] *
+ *                        y[token_to_perm[t*top_k+j]][c]  + y_shared[t][c] )
+ * accumulated in fp32, j ascending, then y_shared; slots with
+ * token_to_perm = -1 contribute nothing.  y_shared may be NULL.
+ *   out [M][H] bf16 bits.
+ * Errors: MOE_EINVAL (NULL, M < 1, top_k < 1, H < 1). */
+int moe_blend(const float *y, const float *topk_w, const int32_t *token_to_perm,
+              const float *y_shared, uint16_t *out, int M, int top_k,
+              int hidden, void *stream);
+
+/* ---- the layer ---------------------------------------------------------- */
+
+/* Where moe_decode_layer keeps each intermediate inside its workspace, as
+ * byte offsets from the workspace base, for M rows (host only). */
+typedef struct moe_workspace_view {
+    size_t topk_ids, topk_w;                       /* [M*k] int32, float */
+    size_t sorted_token_ids, sorted_expert_ids;    /* [max_total], [max_blocks] */
+    size_t expert_offsets, token_to_perm;          /* [E+1], [M*k] */
+    size_t active_experts, active_count;           /* [cap], [1] */
+    size_t num_tokens_post_padded;                 /* [1] */
+    size_t h, h_shared, y, y_shared;               /* float tables */
+    size_t total_bytes;
+    int max_total, max_blocks, cap;
+} moe_workspace_view;
+
+/* Host only.  Workspace bytes moe_decode_layer needs for any M <= max_M
+ * (0 if the descriptor is invalid). */
+size_t moe_decode_layer_workspace_bytes(const moe_layer_desc *layer, int max_M);
+
+/* Host only.  The workspace layout for M rows.  Returns MOE_EINVAL /
+ * MOE_EUNSUPPORTED as moe_decode_layer would. */
+int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int M,
+                                    moe_workspace_view *view);
+
+/* The decode MoE layer of M rows ("forward_nvfp4_grouped_decode.rs",
+ * forward_nvfp4_grouped_decode): route (when router_logits is not NULL:
+ * moe_topk_softmax; otherwise topk_ids [M][k] int32 and topk_w [M][k] float
+ * are taken as given), moe_align, moe_grouped_gate_up, moe_grouped_down,
+ * moe_blend, all enqueued on `stream` with no host read.
+ *   x [M][H] bf16 bits; out [M][H] bf16 bits;
+ *   workspace: device, >= moe_decode_layer_workspace_bytes(layer, M) bytes,
+ *   256-byte aligned, used only by this call (its intermediates can be read
+ *   back through moe_decode_layer_workspace_view).
+ * Shape admission (host, nothing launched on failure):
+ *   1 <= M <= MOE_MAX_ROWS, 1 <= top_k <= min(E, 32), E <= MOE_MAX_EXPERTS,
+ *   block_size >= 1, and the format's hidden/inter rules.
+ * Errors: MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA. */
+int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,
+                     const float *router_logits, const int32_t *topk_ids,
+                     const float *topk_w, uint16_t *out, void *workspace,
+                     size_t workspace_bytes, uint32_t *err_word, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

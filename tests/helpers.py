@@ -89,3 +89,53 @@ def rel_l2(a, b) -> float:
     b = np.asarray(b, np.float64)
     den = np.linalg.norm(b)
     return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
+
+
+# --------------------------------------------------------------------------
+# running the GPU path and the oracle on the same inputs
+# --------------------------------------------------------------------------
+
+# Tolerances.  Layer output (bf16): the workload statement's relative L2
+# 1e-3 and max-abs 2e-2, comparing the bf16 outputs of both sides.
+# Intermediates (fp32 on the GPU against double): fp32 accumulation of K <=
+# 4096 exact products has a typical relative error ~ sqrt(K) * 2^-24 < 4e-6;
+# 1e-5 relative L2 leaves 2.5x margin.
+LAYER_REL_L2 = 1e-3
+LAYER_MAX_ABS = 2e-2
+STAGE_REL_L2 = 1e-5
+TOPK_W_ABS = 2e-6
+
+
+def gpu_layer(moe, inp: synth.LayerInputs, path: int = 0, use_logits: bool = True,
+              ids=None, w=None, err=None):
+    """Run moe_decode_layer on device inputs; returns (out bf16 [M, H], view)."""
+    s = inp.shape
+    routed = moe.Experts.from_synth(inp.experts)
+    shared = moe.Experts.from_synth(inp.shared) if inp.shared is not None else None
+    layer = moe.LayerDesc(top_k=s.top_k, block_size=s.BS, routed=routed, shared=shared, path=path)
+    ws = moe.alloc_workspace(layer, s.M)
+    out = torch.empty(s.M, s.H, dtype=torch.bfloat16, device="cuda")
+    if use_logits:
+        moe.moe_decode_layer(layer, inp.x, out, ws, router_logits=inp.logits, err_word=err)
+    else:
+        moe.moe_decode_layer(layer, inp.x, out, ws, topk_ids=ids, topk_w=w, err_word=err)
+    torch.cuda.synchronize()
+    return out, moe.workspace_view(layer, s.M, ws), (layer, ws)
+
+
+def oracle_layer(inp: synth.LayerInputs, ids=None, w=None):
+    """The oracle's layer output for the same inputs (host copies)."""
+    s = inp.shape
+    X = oracle_experts(inp.experts.to("cpu"))
+    S = oracle_experts(inp.shared.to("cpu")) if inp.shared is not None else None
+    xb = synth.bf16_bits(inp.x)
+    if ids is None:
+        return oracle.moe_layer(X, S, xb, s.M, s.top_k, s.BS, logits=inp.logits.cpu().numpy())
+    return oracle.moe_layer(X, S, xb, s.M, s.top_k, s.BS, ids=ids, w=w)
+
+
+def compare_bf16(got: torch.Tensor, ref_bits: np.ndarray):
+    g = synth.bf16_bits(got).astype(np.uint16)
+    gf = oracle.bf16_bits_to_f64(g)
+    rf = oracle.bf16_bits_to_f64(ref_bits)
+    return rel_l2(gf, rf), float(np.abs(gf - rf).max())

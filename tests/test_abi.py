@@ -1,0 +1,141 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, and its host-only functions size, lay out and reject inputs
+without launching anything."""
+from __future__ import annotations
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import expert_routing_alignment_gb300 as moe
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \t\*]*?\b(moe_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("moe_align", "moe_grouped_gate_up", "moe_grouped_down", "moe_blend",
+                     "moe_decode_layer", "moe_topk_softmax", "moe_align_sizes",
+                     "moe_decode_layer_workspace_bytes"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = moe.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(moe.EXPORTS)
+
+
+def test_version_and_status_strings():
+    lib = moe.load()
+    assert b"sm_103a" in lib.moe_version()
+    assert lib.moe_status_string(moe.MOE_EINVAL) == b"invalid argument"
+
+
+@pytest.mark.parametrize("n,E,BS", [(0, 8, 16), (1, 64, 16), (64, 128, 16), (1024, 256, 64),
+                                    (32768, 1024, 128), (8, 4, 1)])
+def test_align_sizes_match_oracle(n, E, BS):
+    assert moe.moe_align_sizes(n, E, BS) == oracle.align_sizes(n, E, BS)
+
+
+def test_align_sizes_rejects():
+    lib = moe.load()
+    a = ctypes.c_int()
+    for args in [(-1, 8, 16), (8, 0, 16), (8, 8, 0)]:
+        assert lib.moe_align_sizes(*args, ctypes.byref(a), ctypes.byref(a),
+                                   ctypes.byref(a)) == moe.MOE_EINVAL
+    assert lib.moe_align_sizes((1 << 20) + 1, 8, 16, ctypes.byref(a), ctypes.byref(a),
+                               ctypes.byref(a)) == moe.MOE_EUNSUPPORTED
+    assert lib.moe_align_sizes(8, 8, 16, None, None, None) == moe.MOE_EINVAL
+
+
+def test_align_rejects_before_launch():
+    lib = moe.load()
+    fake = ctypes.c_void_p(256)
+    # NULL tables, too many experts: rejected on the host (nothing launched)
+    args = [fake, 0, 8, 8, 16] + [fake] * 4 + [None] + [fake] * 3 + [None]
+    assert lib.moe_align(*args) == moe.MOE_EINVAL
+    args = [fake, 0, 8, 2048, 16] + [fake] * 8 + [None]
+    assert lib.moe_align(*args) == moe.MOE_EUNSUPPORTED
+
+
+class _FakeTensor:
+    """Stands in for a device tensor: only its address is read on the host."""
+
+    def __init__(self, addr):
+        self.addr = addr
+
+    def data_ptr(self):
+        return self.addr
+
+
+def _fake_experts(fmt=moe.FMT_FP8_B128, E=128, H=2048, I=768, align=256):
+    t = lambda: _FakeTensor(align)
+    g = None if fmt == moe.FMT_FP8_B128 else _FakeTensor(align)
+    proj = (t(), t(), g)
+    return moe.Experts(fmt, E, H, I, proj, proj, proj)
+
+
+def test_workspace_layout_host_only():
+    layer = moe.LayerDesc(top_k=8, block_size=16, routed=_fake_experts())
+    nb = moe.workspace_bytes(layer, 8)
+    v = moe._WsView()
+    lib = moe.load()
+    assert lib.moe_decode_layer_workspace_view(ctypes.pointer(layer._struct), 8,
+                                               ctypes.byref(v)) == 0
+    assert v.total_bytes == nb
+    mt, mb, cap = oracle.align_sizes(64, 128, 16)
+    assert (v.max_total, v.max_blocks, v.cap) == (mt, mb, cap)
+    offs = [v.topk_ids, v.topk_w, v.sorted_token_ids, v.sorted_expert_ids, v.expert_offsets,
+            v.token_to_perm, v.active_experts, v.active_count, v.num_tokens_post_padded, v.h,
+            v.h_shared, v.y, v.y_shared]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert v.y - v.h >= mt * 768 * 4 and nb - v.y >= mt * 2048 * 4
+    # workspace grows with M
+    assert moe.workspace_bytes(layer, 1) < nb < moe.workspace_bytes(layer, 128)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=moe.FMT_FP8_B128, H=2000), moe.MOE_EUNSUPPORTED),   # FP8 needs H % 128
+    (dict(fmt=moe.FMT_NVFP4_G16, I=784), moe.MOE_EUNSUPPORTED),   # NVFP4 needs I % 32
+    (dict(fmt=7), moe.MOE_EINVAL),
+    (dict(E=1025), moe.MOE_EUNSUPPORTED),
+    (dict(align=8), moe.MOE_EINVAL),                              # codes not 16-byte aligned
+])
+def test_layer_shape_admission(kw, status):
+    layer = moe.LayerDesc(top_k=8, block_size=16, routed=_fake_experts(**kw))
+    v = moe._WsView()
+    got = moe.load().moe_decode_layer_workspace_view(ctypes.pointer(layer._struct), 8,
+                                                     ctypes.byref(v))
+    assert got == status
+
+
+def test_layer_rejects_rows_and_topk():
+    lib = moe.load()
+    v = moe._WsView()
+    layer = moe.LayerDesc(top_k=8, block_size=16, routed=_fake_experts())
+    p = ctypes.pointer(layer._struct)
+    assert lib.moe_decode_layer_workspace_view(p, 0, ctypes.byref(v)) == moe.MOE_EINVAL
+    assert lib.moe_decode_layer_workspace_view(p, 129, ctypes.byref(v)) == moe.MOE_EUNSUPPORTED
+    bad_k = moe.LayerDesc(top_k=200, block_size=16, routed=_fake_experts())
+    assert lib.moe_decode_layer_workspace_view(ctypes.pointer(bad_k._struct), 8,
+                                               ctypes.byref(v)) == moe.MOE_EINVAL
+    # moe_decode_layer itself rejects a short workspace before any launch
+    fake = ctypes.c_void_p(256)
+    assert lib.moe_decode_layer(p, fake, 8, fake, None, None, fake, fake, 16, None,
+                                None) == moe.MOE_EINVAL

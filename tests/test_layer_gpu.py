@@ -1,0 +1,220 @@
+"""The decode MoE layer on the GPU against the oracle.
+
+Stages are checked in isolation (each fed the same inputs as the oracle's
+function), then the whole layer on every workload: the tiny layer, the
+128-expert FP8 decode layer at M = 1, 2, 4, 8, the NVFP4 layer with an FP8
+shared expert at M = 1, 8, 32, and the M = 128 verify batch (sampled rows).
+Row invariance, determinism, CUDA-graph replay and out-of-range ids too."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import expert_routing_alignment_gb300 as m
+    m.load()
+    return m
+
+
+_CACHE = {}
+
+
+def layer_inputs(shape: synth.LayerShape, seed: int = 1000) -> synth.LayerInputs:
+    key = (shape, seed)
+    if key not in _CACHE:
+        _CACHE.clear()
+        _CACHE[key] = synth.make_layer(shape, seed, device="cuda")
+    return _CACHE[key]
+
+
+# --------------------------------------------------------------------------
+# routing
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,E,k", [(4, 8, 2), (8, 128, 8), (32, 128, 8), (128, 256, 8),
+                                   (3, 1024, 32), (5, 33, 1)])
+def test_topk_softmax_matches_oracle(moe, M, E, k):
+    lg = synth.make_logits(M, E, seed=M * E, device="cuda")
+    ids, w = moe.moe_topk_softmax(lg, k)
+    torch.cuda.synchronize()
+    rid, rw = oracle.topk_softmax(lg.cpu().numpy(), k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=H.TOPK_W_ABS)
+
+
+def test_topk_ties_take_lower_id(moe):
+    lg = torch.randint(-2, 3, (64, 40), generator=torch.Generator().manual_seed(2)).float()
+    ids, w = moe.moe_topk_softmax(lg.cuda(), 6)
+    torch.cuda.synchronize()
+    rid, rw = oracle.topk_softmax(lg.numpy(), 6)
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=H.TOPK_W_ABS)
+
+
+# --------------------------------------------------------------------------
+# grouped stages in isolation
+# --------------------------------------------------------------------------
+
+STAGE_SHAPES = [synth.tiny(), synth.decode_fp8(8), synth.decode_nvfp4(8)]
+
+
+@pytest.mark.parametrize("shape", STAGE_SHAPES, ids=lambda s: s.name)
+def test_grouped_stages_match_oracle(moe, shape):
+    inp = layer_inputs(shape)
+    s = shape
+    routed = moe.Experts.from_synth(inp.experts)
+    shared = moe.Experts.from_synth(inp.shared) if inp.shared is not None else None
+    ids, w = moe.moe_topk_softmax(inp.logits, s.top_k)
+    t = moe.moe_align(ids, s.E, s.BS)
+    I, Hd = s.I, s.H
+    h = torch.zeros(t["max_total"], I, device="cuda")
+    y = torch.zeros(t["max_total"], Hd, device="cuda")
+    h_sh = torch.zeros(s.M, s.shared_I, device="cuda") if shared else None
+    y_sh = torch.zeros(s.M, Hd, device="cuda") if shared else None
+    moe.moe_grouped_gate_up(routed, shared, inp.x, s.top_k, t, h, h_sh, path=moe.PATH_SIMT)
+    moe.moe_grouped_down(routed, shared, h, h_sh, s.M, s.top_k, t, y, y_sh, path=moe.PATH_SIMT)
+    out = torch.empty(s.M, Hd, dtype=torch.bfloat16, device="cuda")
+    moe.moe_blend(y, w, t["token_to_perm"], y_sh, out, s.top_k)
+    torch.cuda.synchronize()
+
+    tables = oracle.align(ids.cpu().numpy().ravel(), s.E, s.BS)
+    assert (t["sorted_token_ids"].cpu().numpy()[: t["max_total"]]
+            == tables["sorted_token_ids"]).all()
+    X = H.oracle_experts(inp.experts.to("cpu"))
+    S = H.oracle_experts(inp.shared.to("cpu")) if shared else None
+    real = tables["sorted_token_ids"] < s.n
+
+    # gate + up on the same x and tables
+    h_ref, hs_ref = oracle.grouped_gate_up(X, S, synth.bf16_bits(inp.x), s.M, s.top_k, tables)
+    h_gpu = h.cpu().numpy().astype(np.float64)
+    assert H.rel_l2(h_gpu[real], h_ref[real]) < H.STAGE_REL_L2
+    if shared:
+        assert H.rel_l2(h_sh.cpu().numpy(), hs_ref) < H.STAGE_REL_L2
+
+    # down on the GPU's own h
+    hs_gpu = h_sh.cpu().numpy().astype(np.float64) if shared else None
+    y_ref, ys_ref = oracle.grouped_down(X, S, h_gpu, hs_gpu, s.M, s.top_k, tables)
+    y_gpu = y.cpu().numpy().astype(np.float64)
+    assert H.rel_l2(y_gpu[real], y_ref[real]) < H.STAGE_REL_L2
+    if shared:
+        assert H.rel_l2(y_sh.cpu().numpy(), ys_ref) < H.STAGE_REL_L2
+
+    # blend on the GPU's own y and weights: equal bf16 bits except where the
+    # fp32 and double sums fall on two sides of a rounding boundary (1 ulp)
+    ys_gpu = y_sh.cpu().numpy().astype(np.float64) if shared else None
+    _, ob = oracle.blend(y_gpu, w.cpu().numpy().astype(np.float64), tables["token_to_perm"],
+                         ys_gpu, s.M, s.top_k, Hd)
+    gb = synth.bf16_bits(out).astype(np.int32)
+    diff = np.abs(gb - ob.astype(np.int32))
+    assert diff.max() <= 1 and (diff > 0).mean() < 0.01
+
+
+# --------------------------------------------------------------------------
+# the whole layer
+# --------------------------------------------------------------------------
+
+LAYER_SHAPES = ([synth.tiny()] + [synth.decode_fp8(M) for M in (1, 2, 4, 8)]
+                + [synth.decode_nvfp4(M) for M in (1, 8, 32)])
+
+
+@pytest.mark.parametrize("shape", LAYER_SHAPES, ids=lambda s: s.name)
+def test_layer_matches_oracle(moe, shape):
+    inp = layer_inputs(shape)
+    out, view, _ = H.gpu_layer(moe, inp)
+    _, ref_b, bad = H.oracle_layer(inp)
+    assert bad == 0
+    rl2, mx = H.compare_bf16(out, ref_b)
+    assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
+    # the layer's own tables equal the oracle's
+    rid, _ = oracle.topk_softmax(inp.logits.cpu().numpy(), shape.top_k)
+    tables = oracle.align(rid.ravel(), shape.E, shape.BS)
+    for key in ("sorted_token_ids", "expert_offsets", "token_to_perm", "sorted_expert_ids"):
+        np.testing.assert_array_equal(view[key].cpu().numpy(), tables[key], err_msg=key)
+    assert int(view["active_count"].item()) == int(tables["active_count"][0])
+
+
+def test_verify_batch_sampled_rows(moe):
+    """M = 128, H = 4096, I = 1536, E = 256, k = 8, BS = 64 with a Zipf(1.1)
+    router bias: the full batch on the GPU, the oracle on 6 sampled rows
+    (each row's output depends on that row only)."""
+    shape = synth.verify_fp8(128)
+    inp = layer_inputs(shape)
+    out, view, _ = H.gpu_layer(moe, inp)
+    counts = np.bincount(view["topk_ids"].cpu().numpy(), minlength=shape.E)
+    assert counts.max() >= 30, counts.max()           # the skew the workload asks for
+    rows = [0, 17, 63, 64, 101, 127]
+    lg = inp.logits[rows].cpu().numpy()
+    rid, rw = oracle.topk_softmax(lg, shape.top_k)
+    uniq = sorted(set(rid.ravel().tolist()))
+    remap = {e: i for i, e in enumerate(uniq)}
+    sub = H.subset_experts(inp.experts, uniq)
+    X = H.oracle_experts(sub)
+    ids_sub = np.vectorize(remap.get)(rid).astype(np.int32)
+    _, ref_b, _ = oracle.moe_layer(X, None, synth.bf16_bits(inp.x[rows]), len(rows),
+                                   shape.top_k, shape.BS, ids=ids_sub, w=rw)
+    rl2, mx = H.compare_bf16(out[rows], ref_b)
+    assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
+
+
+@pytest.mark.parametrize("shape", [synth.decode_nvfp4(32), synth.decode_fp8(8)],
+                         ids=lambda s: s.name)
+def test_row_invariance(moe, shape):
+    """Row 0's output bits are the same whether the batch has 1 or M rows."""
+    inp = layer_inputs(shape)
+    out_m, _, _ = H.gpu_layer(moe, inp)
+    one = synth.LayerInputs(
+        synth.LayerShape(shape.name + "_row0", 1, shape.H, shape.I, shape.E, shape.top_k,
+                         shape.BS, shape.fmt, shape.shared_I),
+        inp.x[:1].contiguous(), inp.logits[:1].contiguous(), inp.experts, inp.shared)
+    out_1, _, _ = H.gpu_layer(moe, one)
+    assert torch.equal(out_m[:1].view(torch.int16), out_1.view(torch.int16))
+
+
+def test_layer_deterministic_and_graph_replayable(moe):
+    shape = synth.decode_fp8(8)
+    inp = layer_inputs(shape)
+    out_a, _, (layer, ws) = H.gpu_layer(moe, inp)
+    out_b, _, _ = H.gpu_layer(moe, inp)
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+    logits = inp.logits.clone()
+    out = torch.empty_like(out_a)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        moe.moe_decode_layer(layer, inp.x, out, ws, router_logits=logits)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.moe_decode_layer(layer, inp.x, out, ws, router_logits=logits)
+    for seed in (5, 6):
+        logits.copy_(synth.make_logits(shape.M, shape.E, seed, device="cuda"))
+        g.replay()
+        torch.cuda.synchronize()
+        eager = torch.empty_like(out)
+        moe.moe_decode_layer(layer, inp.x, eager, ws, router_logits=logits)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_layer_given_ids_with_out_of_range_id(moe):
+    shape = synth.tiny(M=4)
+    inp = layer_inputs(shape)
+    ids, w = oracle.topk_softmax(inp.logits.cpu().numpy(), shape.top_k)
+    ids[1, 1] = shape.E + 3                        # out of range: skipped, flagged
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _, _ = H.gpu_layer(moe, inp, use_logits=False, ids=torch.from_numpy(ids).cuda(),
+                            w=torch.from_numpy(w.astype(np.float32)).cuda(), err=err)
+    assert int(err.item()) & moe.MOE_ERR_BAD_ID
+    _, ref_b, bad = H.oracle_layer(inp, ids=ids, w=w)
+    assert bad == 1
+    rl2, mx = H.compare_bf16(out, ref_b)
+    assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS
