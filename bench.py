@@ -1,0 +1,445 @@
+"""Benchmark of the decode-time MoE layer on GB300.
+
+Workload (the 128-expert decode layer): H=2048, I=768, E=128, top_k=8,
+BS=16, FP8 E4M3 experts with 128x128 fp32 block scales, bf16 activations
+~N(0,1), router logits N(0,1) drawn fresh for every step; M=8 rows is the
+headline, M in {1, 2, 4, 8} is reported as a sweep.  A step is one whole
+layer call (top-k softmax -> align -> grouped gate+up -> grouped down ->
+blend).  Steps rotate over 16 copies of the expert weights (16 x 604 MB), so
+no step finds its weights in the 129 MB L2.
+
+Timed regions (CUDA events on the launching stream, after W warm-up steps,
+synchronize on both sides):
+  * value:    K steps captured in one CUDA graph, replayed once;
+  * roofline: the dominant kernel (grouped gate+up) of K steps, each launch
+              bracketed by events, algorithmic bytes / mean duration;
+  * e2e:      K steps through the public API with host buffers: x and logits
+              copied in from pinned memory, the output copied back, per step.
+The CPU baseline is the oracle on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+METRIC = ("MoE decode layer µs/tokens·s⁻¹ and weight-stream HBM GB/s "
+          "(% peak), M=1..128")
+N_COPIES = 16
+NOMINAL_HBM_GBS = 8000.0
+SEED = 1001
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(HERE, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), source="measured")
+    return dict(hbm_gbs=6800.0, source="fallback")
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["unsampled"], samples=0)
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=max(mx), reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+# --------------------------------------------------------------------------
+# workload
+# --------------------------------------------------------------------------
+
+def build_workload(M: int, steps: int, device: str):
+    import synth
+    import expert_routing_alignment_gb300 as moe
+    shape = synth.decode_fp8(M)
+    base = synth.make_experts(shape.E, shape.H, shape.I, shape.fmt, SEED, device)
+    copies = [base] + [_clone_experts(base) for _ in range(N_COPIES - 1)]
+    x = synth.make_x(M, shape.H, SEED + 2, device)
+    # fresh routing for every step: logits [steps, M, E]
+    logits = torch.stack([synth.make_logits(M, shape.E, SEED + 100 + s, device)
+                          for s in range(steps)])
+    layers = [moe.LayerDesc(top_k=shape.top_k, block_size=shape.BS,
+                            routed=moe.Experts.from_synth(c)) for c in copies]
+    return shape, base, copies, layers, x, logits
+
+
+def _clone_experts(d):
+    import synth
+    c = lambda p: synth.ProjData(p.fmt, p.rows, p.cols, p.codes.clone(), p.scale.clone(),
+                                 None if p.glob is None else p.glob.clone())
+    return synth.ExpertData(d.E, d.H, d.I, d.fmt, c(d.gate), c(d.up), c(d.down))
+
+
+def active_expert_counts(logits: torch.Tensor, k: int) -> list:
+    """Distinct experts each step routes to, read from the same logits."""
+    ids = torch.topk(logits, k, dim=-1).indices
+    return [int(torch.unique(ids[s]).numel()) for s in range(logits.shape[0])]
+
+
+def layer_bytes(shape, base, n_active: int) -> int:
+    per_expert = base.bytes_per_expert()
+    n = shape.M * shape.top_k
+    mt = shape.n + min(shape.n, shape.E) * (shape.BS - 1)
+    tables = 4 * (mt + n + shape.E)
+    return (n_active * per_expert + shape.M * shape.H * 2 * 2 + shape.M * shape.E * 4 + tables)
+
+
+def gate_up_bytes(shape, base, n_active: int) -> int:
+    g = base.gate.nbytes_per_expert() + base.up.nbytes_per_expert()
+    return n_active * g + shape.M * shape.H * 2 + shape.n * shape.I * 4
+
+
+# --------------------------------------------------------------------------
+# timed regions
+# --------------------------------------------------------------------------
+
+def time_graph(moe, layers, x, logits, out, ws, K: int, W: int, stream,
+               busy: bool = False) -> float:
+    """Milliseconds for K layer calls replayed from one CUDA graph."""
+    with torch.cuda.stream(stream):
+        for s in range(W):
+            moe.moe_decode_layer(layers[s % N_COPIES], x, out, ws, router_logits=logits[s % K])
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for s in range(K):
+            moe.moe_decode_layer(layers[s % N_COPIES], x, out, ws, router_logits=logits[s])
+    t0 = time.perf_counter()
+    g.replay()                        # one untimed replay (first-touch of the graph)
+    stream.synchronize()
+    # untimed replays before and after keep the GPU loaded for ~0.5 s around
+    # the timed one, so that sampled clocks describe the timed region
+    once = max(time.perf_counter() - t0, 1e-4)
+    pad = int(min(2000, max(1, 0.25 / once)))
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(pad if busy else 0):
+            g.replay()
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+        for _ in range(pad if busy else 0):
+            g.replay()
+    end.synchronize()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def time_dominant_kernel(moe, shape, layers, x, logits, ws_views, K: int, W: int, stream):
+    """Mean duration (ms) of the grouped gate+up launch over K steps; the
+    tables it reads are produced by the same step's top-k and align."""
+    durs = []
+    v = ws_views
+    with torch.cuda.stream(stream):
+        for s in range(W + K):
+            L = layers[s % N_COPIES]
+            ids, w = moe.moe_topk_softmax(logits[s % K], shape.top_k, v["topk_ids"].view(shape.M, -1),
+                                          v["topk_w"].view(shape.M, -1))
+            moe.moe_align(ids, shape.E, shape.BS, out=v)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            moe.moe_grouped_gate_up(L.routed, None, x, shape.top_k, v, v["h"], None,
+                                    path=moe.PATH_SIMT)
+            b.record(stream)
+            moe.moe_grouped_down(L.routed, None, v["h"], None, shape.M, shape.top_k, v, v["y"],
+                                 None, path=moe.PATH_SIMT)
+            if s >= W:
+                durs.append((a, b))
+    stream.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in durs]))
+
+
+def time_e2e(moe, shape, layer, x_host, logits_host, out_host, ws, K: int, W: int, stream):
+    """K steps through the public API from pinned host buffers."""
+    x_dev = torch.empty(shape.M, shape.H, dtype=torch.bfloat16, device="cuda")
+    lg_dev = torch.empty(shape.M, shape.E, dtype=torch.float32, device="cuda")
+    out_dev = torch.empty(shape.M, shape.H, dtype=torch.bfloat16, device="cuda")
+
+    def step(s):
+        x_dev.copy_(x_host, non_blocking=True)
+        lg_dev.copy_(logits_host[s % logits_host.shape[0]], non_blocking=True)
+        moe.moe_decode_layer(layer, x_dev, out_dev, ws, router_logits=lg_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for s in range(W):
+            step(s)
+    stream.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for s in range(K):
+            step(s)
+        end.record(stream)
+    end.synchronize()
+    h2d = x_dev.numel() * 2 + lg_dev.numel() * 4
+    d2h = out_dev.numel() * 2
+    return start.elapsed_time(end), h2d, d2h
+
+
+def oracle_experts(d):
+    """synth expert data -> the oracle's host structures."""
+    import oracle
+    fmt = oracle.FMT_FP8_B128 if d.fmt == "fp8" else oracle.FMT_NVFP4_G16
+    P = lambda p: oracle.Proj(fmt, p.rows, p.cols, p.codes.cpu().numpy(), p.scale.cpu().numpy(),
+                              None if p.glob is None else p.glob.cpu().numpy())
+    return oracle.Experts(d.E, d.H, d.I, P(d.gate), P(d.up), P(d.down))
+
+
+def cpu_baseline(shape, base, x, logits, budget_s: float = 15.0) -> dict:
+    """The oracle on the host cores: whole layer calls of the workload at M
+    rows, as many as fit in the time budget (at least one)."""
+    import oracle
+    X = oracle_experts(base)
+    xb = x.cpu().view(torch.int16).numpy().view(np.uint16)
+    lg = logits.cpu().numpy()
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        oracle.moe_layer(X, None, xb, shape.M, shape.top_k, shape.BS, logits=lg[calls % len(lg)])
+        calls += 1
+        if time.perf_counter() - t0 > budget_s or calls >= len(lg):
+            break
+    dt = time.perf_counter() - t0
+    return dict(value=shape.M * calls / dt, unit="tokens/s", cores=1, kind="oracle",
+                sample=f"{calls} whole layer calls of {shape.name} ({shape.M} rows each), "
+                       f"single-threaded C oracle in double, {dt:.1f} s")
+
+
+# --------------------------------------------------------------------------
+# arms
+# --------------------------------------------------------------------------
+
+def run_reference(args, rank: int, world: int):
+    """The oracle as the reference arm: each step is one layer call of the
+    workload on the host cores (a bounded sample: 2 of the M rows)."""
+    if rank != 0:
+        return
+    import synth
+    import oracle
+    M = args.m
+    shape = synth.decode_fp8(M)
+    base = synth.make_experts(shape.E, shape.H, shape.I, shape.fmt, SEED, "cpu")
+    X = oracle_experts(base)
+    x = synth.make_x(M, shape.H, SEED + 2, "cpu")
+    rows = 2
+    xb = x[:rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    for s in range(args.warmup):
+        lg = synth.make_logits(M, shape.E, SEED + 100 + s, "cpu")[:rows].numpy()
+        oracle.moe_layer(X, None, xb, rows, shape.top_k, shape.BS, logits=lg)
+    lgs = [synth.make_logits(M, shape.E, SEED + 100 + s, "cpu")[:rows].numpy()
+           for s in range(args.steps)]
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        oracle.moe_layer(X, None, xb, rows, shape.top_k, shape.BS, logits=lgs[s])
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    line = dict(
+        impl="reference", metric=METRIC, value=value, unit="tokens/s", n_gpus=world,
+        steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * dt / args.steps,
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+        config=dict(workload=shape.name, M=M, H=shape.H, I=shape.I, E=shape.E,
+                    top_k=shape.top_k, BS=shape.BS),
+        cpu_baseline=dict(value=value, unit="tokens/s", cores=1, kind="oracle",
+                          sample=f"each step: the oracle on {rows} of the {M} rows of one "
+                                 f"layer call of {shape.name}"),
+        e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, rank: int, world: int):
+    import expert_routing_alignment_gb300 as moe
+    moe.load()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    K, W = args.steps, args.warmup
+    peaks = measured_peaks()
+    results = {}
+    sweep = []
+    for M in args.sweep:
+        shape, base, copies, layers, x, logits = build_workload(M, K, "cuda")
+        ws = moe.alloc_workspace(layers[0], M)
+        out = torch.empty(M, shape.H, dtype=torch.bfloat16, device="cuda")
+        head = M == args.m and not args.profile
+        sampler = ClockSampler(local)
+        if head:
+            sampler.__enter__()
+        ms = time_graph(moe, layers, x, logits, out, ws, K, W, stream, busy=head)
+        if head:
+            sampler.__exit__(None, None, None)
+        n_act = active_expert_counts(logits, shape.top_k)
+        nbytes = float(np.mean([layer_bytes(shape, base, a) for a in n_act]))
+        us = 1e3 * ms / K
+        gbs = nbytes / (us * 1e-6) / 1e9
+        sweep.append(dict(M=M, us_per_layer=round(us, 3), tokens_per_s=round(M / (us * 1e-6), 1),
+                          weight_stream_gbs=round(gbs, 1),
+                          pct_of_measured_hbm=round(100 * gbs / peaks["hbm_gbs"], 1),
+                          pct_of_8tbs=round(100 * gbs / NOMINAL_HBM_GBS, 1),
+                          mean_active_experts=round(float(np.mean(n_act)), 2)))
+        if head:
+            view = moe.workspace_view(layers[0], M, ws)
+            dk_ms = time_dominant_kernel(moe, shape, layers, x, logits, view, K, W, stream)
+            gu_bytes = float(np.mean([gate_up_bytes(shape, base, a) for a in n_act]))
+            x_host = x.cpu().pin_memory()
+            lg_host = logits.cpu().pin_memory()
+            out_host = torch.empty(M, shape.H, dtype=torch.bfloat16).pin_memory()
+            e2e_ms, h2d, d2h = time_e2e(moe, shape, layers[0], x_host, lg_host, out_host, ws,
+                                        K, W, stream)
+            results = dict(shape=shape, base=base, x=x, logits=logits, ms=ms, us=us, gbs=gbs,
+                           nbytes=nbytes, dk_ms=dk_ms, gu_bytes=gu_bytes, e2e_ms=e2e_ms,
+                           h2d=h2d, d2h=d2h, clocks=sampler.summary())
+        del copies, layers, base, ws
+        torch.cuda.empty_cache()
+
+    if args.profile:
+        if rank == 0:
+            print(json.dumps(dict(profile=True, sweep=sweep)), flush=True)
+        return
+    # max over ranks
+    ms_t = torch.tensor([results["ms"]], device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    if rank != 0:
+        return
+    r = results
+    shape = r["shape"]
+    value = world * shape.M * K / (ms_max * 1e-3)
+    dk_achieved = r["gu_bytes"] / (r["dk_ms"] * 1e-3) / 1e9
+    line = dict(
+        metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=W,
+        ms_per_step=ms_max / K, higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="f32", data="synthetic",
+        config=dict(workload=shape.name, M=shape.M, H=shape.H, I=shape.I, E=shape.E,
+                    top_k=shape.top_k, BS=shape.BS, weights="fp8_e4m3 128x128 fp32 block scales",
+                    routing="fresh N(0,1) logits every step",
+                    l2="inputs larger than L2: steps rotate over 16 weight copies of 604 MB",
+                    parallelism=f"replicas x{world}"),
+        us_per_layer=round(r["us"], 3), weight_stream_gbs=round(r["gbs"], 1),
+        pct_of_measured_hbm=round(100 * r["gbs"] / peaks["hbm_gbs"], 1),
+        pct_of_8tbs=round(100 * r["gbs"] / NOMINAL_HBM_GBS, 1),
+        algorithmic_bytes_per_layer=int(r["nbytes"]),
+        sweep=sweep,
+        roofline=dict(bound="hbm", kernel="grouped gate+up (SIMT)", achieved=round(dk_achieved, 1),
+                      peak=peaks["hbm_gbs"], peak_source=f"{peaks['source']} copy bandwidth",
+                      unit="GB/s", frac=round(dk_achieved / peaks["hbm_gbs"], 4),
+                      bytes_per_launch=int(r["gu_bytes"]), us_per_launch=round(1e3 * r["dk_ms"], 3),
+                      traffic=None),
+        e2e=dict(value=shape.M * K / (r["e2e_ms"] * 1e-3), unit="tokens/s",
+                 h2d_bytes_per_step=r["h2d"], d2h_bytes_per_step=r["d2h"]),
+        gpu_launches=5 * K,
+        clocks=r["clocks"])
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, r["base"], r["x"], r["logits"])
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--m", type=int, default=8, help="rows of the headline workload")
+    ap.add_argument("--sweep", type=int, nargs="*", default=[1, 2, 4, 8])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--copies", type=int, default=16,
+                    help="weight copies the steps rotate over (16 keeps weights out of L2)")
+    ap.add_argument("--profile", action="store_true",
+                    help="only the graph region, without the clock window, the dominant-kernel "
+                         "region, e2e and the CPU baseline (for profiler runs)")
+    args = ap.parse_args()
+    if args.m not in args.sweep:
+        args.sweep.append(args.m)
+    global N_COPIES
+    N_COPIES = max(1, args.copies)
+    args.warmup = max(args.warmup, 3)
+    sys.path.insert(0, HERE)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
