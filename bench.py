@@ -11,7 +11,8 @@ no step finds its weights in the 129 MB L2.
 Timed regions (CUDA events on the launching stream, after W warm-up steps,
 synchronize on both sides):
   * value:    K steps captured in one CUDA graph, replayed once;
-  * roofline: the dominant kernel (grouped gate+up) of K steps, each launch
+  * roofline: the layer's kernels of K steps (on the fused path the gate+up
+              kernel with the down+blend kernel overlapping it), each call
               bracketed by events, algorithmic bytes / mean duration;
   * e2e:      K steps through the public API with host buffers: x and logits
               copied in from pinned memory, the output copied back, per step.
@@ -151,11 +152,6 @@ def layer_bytes(shape, base, n_active: int) -> int:
     return (n_active * per_expert + shape.M * shape.H * 2 * 2 + shape.M * shape.E * 4 + tables)
 
 
-def gate_up_bytes(shape, base, n_active: int) -> int:
-    g = base.gate.nbytes_per_expert() + base.up.nbytes_per_expert()
-    return n_active * g + shape.M * shape.H * 2 + shape.n * shape.I * 4
-
-
 # --------------------------------------------------------------------------
 # timed regions
 # --------------------------------------------------------------------------
@@ -195,29 +191,24 @@ def time_graph(moe, layers, x, logits, out, ws, K: int, W: int, stream,
     return start.elapsed_time(end)
 
 
-def time_dominant_kernel(moe, shape, layers, x, logits, ws_views, K: int, W: int, stream):
-    """Mean duration (ms) of the grouped gate+up launch over K steps; the
-    tables it reads are produced by the same step's top-k and align."""
-    durs = []
-    v = ws_views
+def time_layer_launches(moe, layers, x, logits, out, ws, K: int, W: int, stream) -> float:
+    """Mean duration (ms) of one layer call's kernels, each call bracketed by
+    events on the launching stream.  On the fused decode path the call is the
+    gate+up kernel with the down+blend kernel overlapping its tail, which no
+    event can split; the brackets also stop one step from overlapping the
+    next, so this is slower than the graph replay."""
+    pairs = []
     with torch.cuda.stream(stream):
         for s in range(W + K):
-            L = layers[s % N_COPIES]
-            ids, w = moe.moe_topk_softmax(logits[s % K], shape.top_k, v["topk_ids"].view(shape.M, -1),
-                                          v["topk_w"].view(shape.M, -1))
-            moe.moe_align(ids, shape.E, shape.BS, out=v)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            moe.moe_grouped_gate_up(L.routed, None, x, shape.top_k, v, v["h"], None,
-                                    path=moe.PATH_SIMT)
+            moe.moe_decode_layer(layers[s % N_COPIES], x, out, ws, router_logits=logits[s % K])
             b.record(stream)
-            moe.moe_grouped_down(L.routed, None, v["h"], None, shape.M, shape.top_k, v, v["y"],
-                                 None, path=moe.PATH_SIMT)
             if s >= W:
-                durs.append((a, b))
+                pairs.append((a, b))
     stream.synchronize()
-    return float(np.mean([a.elapsed_time(b) for a, b in durs]))
+    return float(np.mean([a.elapsed_time(b) for a, b in pairs]))
 
 
 def time_e2e(moe, shape, layer, x_host, logits_host, out_host, ws, K: int, W: int, stream):
@@ -349,16 +340,15 @@ def run_gpu(args, rank: int, world: int):
                           pct_of_8tbs=round(100 * gbs / NOMINAL_HBM_GBS, 1),
                           mean_active_experts=round(float(np.mean(n_act)), 2)))
         if head:
-            view = moe.workspace_view(layers[0], M, ws)
-            dk_ms = time_dominant_kernel(moe, shape, layers, x, logits, view, K, W, stream)
-            gu_bytes = float(np.mean([gate_up_bytes(shape, base, a) for a in n_act]))
+            dk_ms = time_layer_launches(moe, layers, x, logits, out, ws, K, W, stream)
+            launches = moe.moe_decode_layer_launches(layers[0], M)
             x_host = x.cpu().pin_memory()
             lg_host = logits.cpu().pin_memory()
             out_host = torch.empty(M, shape.H, dtype=torch.bfloat16).pin_memory()
             e2e_ms, h2d, d2h = time_e2e(moe, shape, layers[0], x_host, lg_host, out_host, ws,
                                         K, W, stream)
             results = dict(shape=shape, base=base, x=x, logits=logits, ms=ms, us=us, gbs=gbs,
-                           nbytes=nbytes, dk_ms=dk_ms, gu_bytes=gu_bytes, e2e_ms=e2e_ms,
+                           nbytes=nbytes, dk_ms=dk_ms, launches=launches, e2e_ms=e2e_ms,
                            h2d=h2d, d2h=d2h, clocks=sampler.summary())
         del copies, layers, base, ws
         torch.cuda.empty_cache()
@@ -377,7 +367,7 @@ def run_gpu(args, rank: int, world: int):
     r = results
     shape = r["shape"]
     value = world * shape.M * K / (ms_max * 1e-3)
-    dk_achieved = r["gu_bytes"] / (r["dk_ms"] * 1e-3) / 1e9
+    dk_achieved = r["nbytes"] / (r["dk_ms"] * 1e-3) / 1e9
     line = dict(
         metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=W,
         ms_per_step=ms_max / K, higher_is_better=True, scaling="weak", vs_baseline=None,
@@ -392,14 +382,17 @@ def run_gpu(args, rank: int, world: int):
         pct_of_8tbs=round(100 * r["gbs"] / NOMINAL_HBM_GBS, 1),
         algorithmic_bytes_per_layer=int(r["nbytes"]),
         sweep=sweep,
-        roofline=dict(bound="hbm", kernel="grouped gate+up (SIMT)", achieved=round(dk_achieved, 1),
+        roofline=dict(bound="hbm",
+                      kernel=("fused decode pair (gate+up kernel, down+blend kernel overlapping "
+                              "it)" if r["launches"] == 2 else "layer call (5 launches)"),
+                      achieved=round(dk_achieved, 1),
                       peak=peaks["hbm_gbs"], peak_source=f"{peaks['source']} copy bandwidth",
                       unit="GB/s", frac=round(dk_achieved / peaks["hbm_gbs"], 4),
-                      bytes_per_launch=int(r["gu_bytes"]), us_per_launch=round(1e3 * r["dk_ms"], 3),
+                      bytes_per_launch=int(r["nbytes"]), us_per_launch=round(1e3 * r["dk_ms"], 3),
                       traffic=None),
         e2e=dict(value=shape.M * K / (r["e2e_ms"] * 1e-3), unit="tokens/s",
                  h2d_bytes_per_step=r["h2d"], d2h_bytes_per_step=r["d2h"]),
-        gpu_launches=5 * K,
+        gpu_launches=r["launches"] * K,
         clocks=r["clocks"])
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(shape, r["base"], r["x"], r["logits"])

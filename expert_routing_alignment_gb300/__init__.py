@@ -34,6 +34,8 @@ FMT_NVFP4_G16 = 2
 PATH_AUTO = 0
 PATH_SIMT = 1
 PATH_TC = 2
+PATH_SIMT_STAGED = 3
+MOE_ERR_TIMEOUT = 0x2
 MAX_EXPERTS = 1024
 MAX_ROWS = 128
 
@@ -74,7 +76,7 @@ class _WsView(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "topk_ids", "topk_w", "sorted_token_ids", "sorted_expert_ids", "expert_offsets",
         "token_to_perm", "active_experts", "active_count", "num_tokens_post_padded", "h",
-        "h_shared", "y", "y_shared", "total_bytes")] + [
+        "h_shared", "y", "y_shared", "blend_counters", "total_bytes")] + [
         ("max_total", ctypes.c_int), ("max_blocks", ctypes.c_int), ("cap", ctypes.c_int)]
 
 
@@ -97,6 +99,7 @@ EXPORTS = {
                                              ctypes.POINTER(_WsView)]),
     "moe_decode_layer": (_I, [ctypes.POINTER(_LayerDesc), _P, _I, _P, _P, _P, _P, _P,
                               ctypes.c_size_t, _P, _P]),
+    "moe_decode_layer_launches": (_I, [ctypes.POINTER(_LayerDesc), _I, _I]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -316,6 +319,14 @@ def workspace_view(layer: LayerDesc, M: int, ws: torch.Tensor) -> dict:
         y=sl(v.y, v.max_total * H, torch.float32).view(v.max_total, H),
         y_shared=sl(v.y_shared, M * H, torch.float32).view(M, H),
         max_total=v.max_total, max_blocks=v.max_blocks, cap=v.cap)
+
+
+def moe_decode_layer_launches(layer: LayerDesc, M: int, with_logits: bool = True) -> int:
+    """Kernels one moe_decode_layer call enqueues (host only)."""
+    n = load().moe_decode_layer_launches(ctypes.pointer(layer._struct), M, int(with_logits))
+    if n < 0:
+        raise MoeError("moe_decode_layer_launches", MOE_EINVAL)
+    return n
 
 
 def moe_decode_layer(layer: LayerDesc, x: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,

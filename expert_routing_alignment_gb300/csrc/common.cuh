@@ -28,6 +28,10 @@ int check_launch();
 // make no attribute calls).
 int ensure_smem_limit(const void *func, size_t bytes);
 
+// Prefers the largest shared-memory carveout for a kernel (once per kernel
+// and device), so that kernels meant to share an SM fit together.
+int ensure_max_carveout(const void *func);
+
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
 

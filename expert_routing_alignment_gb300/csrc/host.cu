@@ -50,6 +50,24 @@ int ensure_smem_limit(const void *func, size_t bytes) {
   return MOE_OK;
 }
 
+int ensure_max_carveout(const void *func) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, bool> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ECUDA;
+  const uint64_t key = (uint64_t)(uintptr_t)func * 64u + (uint64_t)(dev & 63);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(key)) return MOE_OK;
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return MOE_ECUDA;
+  }
+  done[key] = true;
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 extern "C" const char *moe_version(void) { return "moe_gb300 0.1 sm_103a"; }

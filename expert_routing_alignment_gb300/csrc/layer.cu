@@ -16,6 +16,10 @@ int simt_down(const moe_experts *routed, const moe_experts *shared, const float 
 int launch_topk(const float *logits, int M, int E, int k, int32_t *ids, float *w, void *stream);
 int launch_blend(const float *y, const float *w, const int32_t *ttp, const float *y_sh,
                  uint16_t *out, int M, int k, int H, void *stream);
+bool fused_fits(const moe_layer_desc *L, int M, int sms);
+int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float *logits,
+                 const int32_t *ids, const float *w, uint16_t *out, void *ws,
+                 const moe_workspace_view &v, uint32_t *err, void *stream);
 
 // The expert-kernel path of a shape class.  It depends on the shapes only,
 // never on the routing, so a captured graph stays valid for every routing.
@@ -24,6 +28,7 @@ static int resolve_path(const moe_experts *routed, int M, int top_k, int path) {
   (void)M;
   (void)top_k;
   if (path == MOE_PATH_TC) return -1;   // no tensor-core kernels for this shape yet
+  if (path == MOE_PATH_SIMT_STAGED) return MOE_PATH_SIMT_STAGED;
   return MOE_PATH_SIMT;
 }
 
@@ -41,7 +46,8 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   const int E = L->routed.num_experts, k = L->top_k;
   if (M < 1 || k < 1 || k > E || L->block_size < 1) return MOE_EINVAL;
   if (M > MOE_MAX_ROWS || k > 32) return MOE_EUNSUPPORTED;
-  if (L->path != MOE_PATH_AUTO && L->path != MOE_PATH_SIMT && L->path != MOE_PATH_TC)
+  if (L->path != MOE_PATH_AUTO && L->path != MOE_PATH_SIMT && L->path != MOE_PATH_TC &&
+      L->path != MOE_PATH_SIMT_STAGED)
     return MOE_EINVAL;
   const int n = M * k;
   int max_total, max_blocks, cap;
@@ -68,6 +74,7 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   v->h_shared = take((size_t)M * Is * 4);
   v->y = take((size_t)max_total * H * 4);
   v->y_shared = take((size_t)M * H * 4);
+  v->blend_counters = take((size_t)((H + 63) / 64) * 4);
   v->total_bytes = off;
   v->max_total = max_total;
   v->max_blocks = max_blocks;
@@ -112,6 +119,15 @@ extern "C" int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int 
   return moe::layout(layer, M, view);
 }
 
+extern "C" int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logits) {
+  moe_workspace_view v;
+  if (moe::layout(layer, M, &v) != MOE_OK) return -1;
+  const int path = moe::resolve_path(&layer->routed, M, layer->top_k, layer->path);
+  if (path < 0) return -1;
+  if (path == MOE_PATH_SIMT && moe::fused_fits(layer, M, moe::sm_count())) return 2;
+  return with_logits ? 5 : 4;
+}
+
 extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,
                                 const float *router_logits, const int32_t *topk_ids,
                                 const float *topk_w, uint16_t *out, void *workspace,
@@ -131,6 +147,10 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
   auto F32 = [&](size_t o) { return reinterpret_cast<float *>(ws + o); };
   const int E = layer->routed.num_experts, k = layer->top_k, H = layer->routed.hidden;
   const moe_experts *S = layer->shared;
+
+  if (path == MOE_PATH_SIMT && moe::fused_fits(layer, M, moe::sm_count()))
+    return moe::launch_fused(layer, x, M, router_logits, topk_ids, topk_w, out, workspace, v,
+                             err_word, stream);
 
   const int32_t *ids = topk_ids;
   const float *w = topk_w;

@@ -3,6 +3,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "route.cuh"
 
 namespace moe {
 namespace {
@@ -28,56 +29,10 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_softmax_kernel(const flo
                                                                        float *w) {
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
   if (row >= M) return;
-  const float *l = logits + (size_t)row * E;
-  float v[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int e = lane + 32 * j;
-    v[j] = e < E ? __ldcg(l + e) : -INFINITY;
-  }
-  unsigned taken = 0;   // bit j: this lane's j-th value already selected
-  float mine = 0.f, vmax = 0.f;
-  int myid = 0;
-#pragma unroll 1
-  for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bid = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u) && (v[j] > bv || bid == 0x7fffffff)) {
-        bv = v[j];
-        bid = e;
-      }
-    }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-      const int oid = __shfl_xor_sync(0xffffffffu, bid, d);
-      if (oid != 0x7fffffff && (bid == 0x7fffffff || ov > bv || (ov == bv && oid < bid))) {
-        bv = ov;
-        bid = oid;
-      }
-    }
-    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-    if (r == 0) vmax = bv;
-    if (lane == r) {       // lane r keeps the r-th selection
-      mine = bv;
-      myid = bid;
-    }
-  }
-  // softmax over the selection; vmax is the row maximum
-  const float ex = lane < k ? expf(mine - vmax) : 0.f;
-  float z = ex;
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
-  if (lane < k) {
-    ids[(size_t)row * k + lane] = myid;
-    w[(size_t)row * k + lane] = ex / z;
-  }
+  topk_softmax_row<VPL>(logits + (size_t)row * E, E, k, ids + (size_t)row * k,
+                        w + (size_t)row * k);
 }
 
 // ---------------------------------------------------------------------------

@@ -49,6 +49,7 @@ extern "C" {
 
 /* ---- device error bits, ORed into *err_word ----------------------------- */
 #define MOE_ERR_BAD_ID 0x1u   /* an expert id outside [0, E): slot skipped */
+#define MOE_ERR_TIMEOUT 0x2u  /* a bounded pipeline wait gave up: outputs invalid */
 
 /* ---- formats and paths -------------------------------------------------- */
 #define MOE_FMT_FP8_B128 1  /* E4M3 codes, fp32 scale per 128x128 block      */
@@ -57,6 +58,9 @@ extern "C" {
 #define MOE_PATH_AUTO 0     /* chosen per shape class (never per routing)    */
 #define MOE_PATH_SIMT 1     /* CUDA-core kernels, in-register dequant         */
 #define MOE_PATH_TC 2       /* tcgen05 tensor-core kernels (FP8 only)         */
+#define MOE_PATH_SIMT_STAGED 3 /* moe_decode_layer only: CUDA-core kernels as the
+                                  five separate launches (router, align, gate+up,
+                                  down, blend) instead of the fused decode pair */
 
 #define MOE_MAX_EXPERTS 1024      /* experts the alignment handles            */
 #define MOE_MAX_SLOTS (1 << 20)   /* n = M * top_k the alignment handles      */
@@ -182,7 +186,8 @@ int moe_topk_softmax(const float *logits, int M, int num_experts, int top_k,
  *   h    out [max_total][I] float, rows by sorted position (padding rows
  *            untouched)
  *   h_shared out [M][S->inter] float (NULL iff shared is NULL)
- *   path     MOE_PATH_*; the grid is a function of (M, top_k, E, H, I, path).
+ *   path     MOE_PATH_AUTO / _SIMT / _TC; the grid is a function of
+ *            (M, top_k, E, H, I, path).
  * Errors: MOE_EINVAL (NULL, M < 1 or > MOE_MAX_ROWS, bad fmt/path),
  * MOE_EUNSUPPORTED (shape not admitted; TC path not available for it). */
 int moe_grouped_gate_up(const moe_experts *routed, const moe_experts *shared,
@@ -232,6 +237,7 @@ typedef struct moe_workspace_view {
     size_t active_experts, active_count;           /* [cap], [1] */
     size_t num_tokens_post_padded;                 /* [1] */
     size_t h, h_shared, y, y_shared;               /* float tables */
+    size_t blend_counters;                         /* [ceil(H/64)] int32, internal */
     size_t total_bytes;
     int max_total, max_blocks, cap;
 } moe_workspace_view;
@@ -245,11 +251,21 @@ size_t moe_decode_layer_workspace_bytes(const moe_layer_desc *layer, int max_M);
 int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int M,
                                     moe_workspace_view *view);
 
+/* Host only.  The number of kernels moe_decode_layer enqueues for M rows
+ * (2 on the fused decode path; otherwise 5 with router logits, 4 with given
+ * ids), or -1 if the call would be rejected. */
+int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logits);
+
 /* The decode MoE layer of M rows ("forward_nvfp4_grouped_decode.rs",
  * forward_nvfp4_grouped_decode): route (when router_logits is not NULL:
  * moe_topk_softmax; otherwise topk_ids [M][k] int32 and topk_w [M][k] float
  * are taken as given), moe_align, moe_grouped_gate_up, moe_grouped_down,
  * moe_blend, all enqueued on `stream` with no host read.
+ * On the CUDA-core path, when M*top_k <= 256, M <= 32, and hidden, inter and
+ * the shared inter are multiples of 128 in [256, 2048] (NVFP4: of 256), the
+ * same results come from two persistent kernels (gate+up, then down with the
+ * blend) instead of five launches; every table and intermediate is still
+ * written to the workspace.  MOE_PATH_SIMT_STAGED forces the five.
  *   x [M][H] bf16 bits; out [M][H] bf16 bits;
  *   workspace: device, >= moe_decode_layer_workspace_bytes(layer, M) bytes,
  *   256-byte aligned, used only by this call (its intermediates can be read

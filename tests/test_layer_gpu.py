@@ -124,22 +124,48 @@ def test_grouped_stages_match_oracle(moe, shape):
 
 LAYER_SHAPES = ([synth.tiny()] + [synth.decode_fp8(M) for M in (1, 2, 4, 8)]
                 + [synth.decode_nvfp4(M) for M in (1, 8, 32)])
+PATHS = {"fused": 0, "staged": 3}
 
 
+@pytest.mark.parametrize("path", list(PATHS), ids=str)
 @pytest.mark.parametrize("shape", LAYER_SHAPES, ids=lambda s: s.name)
-def test_layer_matches_oracle(moe, shape):
+def test_layer_matches_oracle(moe, shape, path):
     inp = layer_inputs(shape)
-    out, view, _ = H.gpu_layer(moe, inp)
+    out, view, (layer, _) = H.gpu_layer(moe, inp, path=PATHS[path])
+    if path == "fused":
+        assert moe.moe_decode_layer_launches(layer, shape.M) == 2
     _, ref_b, bad = H.oracle_layer(inp)
     assert bad == 0
     rl2, mx = H.compare_bf16(out, ref_b)
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
     # the layer's own tables equal the oracle's
-    rid, _ = oracle.topk_softmax(inp.logits.cpu().numpy(), shape.top_k)
+    rid, rw = oracle.topk_softmax(inp.logits.cpu().numpy(), shape.top_k)
+    np.testing.assert_array_equal(view["topk_ids"].cpu().numpy(), rid.ravel())
+    np.testing.assert_allclose(view["topk_w"].cpu().numpy(), rw.ravel(), atol=H.TOPK_W_ABS)
     tables = oracle.align(rid.ravel(), shape.E, shape.BS)
-    for key in ("sorted_token_ids", "expert_offsets", "token_to_perm", "sorted_expert_ids"):
+    for key in ("sorted_token_ids", "expert_offsets", "token_to_perm", "sorted_expert_ids",
+                "active_experts"):
         np.testing.assert_array_equal(view[key].cpu().numpy(), tables[key], err_msg=key)
     assert int(view["active_count"].item()) == int(tables["active_count"][0])
+    assert int(view["num_tokens_post_padded"].item()) == int(tables["num_tokens_post_padded"][0])
+    if shape.M <= 8:
+        # the intermediates in the workspace: h against the oracle on the same
+        # x, y against the oracle's down of the layer's own h
+        X = H.oracle_experts(inp.experts.to("cpu"))
+        S = H.oracle_experts(inp.shared.to("cpu")) if inp.shared is not None else None
+        real = tables["sorted_token_ids"] < shape.n
+        h_ref, hs_ref = oracle.grouped_gate_up(X, S, synth.bf16_bits(inp.x), shape.M,
+                                               shape.top_k, tables)
+        h_gpu = view["h"].cpu().numpy().astype(np.float64)
+        assert H.rel_l2(h_gpu[real], h_ref[real]) < H.STAGE_REL_L2
+        hs_gpu = view["h_shared"].cpu().numpy().astype(np.float64) if S else None
+        if S:
+            assert H.rel_l2(hs_gpu, hs_ref) < H.STAGE_REL_L2
+        y_ref, ys_ref = oracle.grouped_down(X, S, h_gpu, hs_gpu, shape.M, shape.top_k, tables)
+        y_gpu = view["y"].cpu().numpy().astype(np.float64)
+        assert H.rel_l2(y_gpu[real], y_ref[real]) < H.STAGE_REL_L2
+        if S:
+            assert H.rel_l2(view["y_shared"].cpu().numpy(), ys_ref) < H.STAGE_REL_L2
 
 
 def test_verify_batch_sampled_rows(moe):
@@ -165,17 +191,18 @@ def test_verify_batch_sampled_rows(moe):
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
 
 
+@pytest.mark.parametrize("path", list(PATHS), ids=str)
 @pytest.mark.parametrize("shape", [synth.decode_nvfp4(32), synth.decode_fp8(8)],
                          ids=lambda s: s.name)
-def test_row_invariance(moe, shape):
+def test_row_invariance(moe, shape, path):
     """Row 0's output bits are the same whether the batch has 1 or M rows."""
     inp = layer_inputs(shape)
-    out_m, _, _ = H.gpu_layer(moe, inp)
+    out_m, _, _ = H.gpu_layer(moe, inp, path=PATHS[path])
     one = synth.LayerInputs(
         synth.LayerShape(shape.name + "_row0", 1, shape.H, shape.I, shape.E, shape.top_k,
                          shape.BS, shape.fmt, shape.shared_I),
         inp.x[:1].contiguous(), inp.logits[:1].contiguous(), inp.experts, inp.shared)
-    out_1, _, _ = H.gpu_layer(moe, one)
+    out_1, _, _ = H.gpu_layer(moe, one, path=PATHS[path])
     assert torch.equal(out_m[:1].view(torch.int16), out_1.view(torch.int16))
 
 
@@ -205,16 +232,35 @@ def test_layer_deterministic_and_graph_replayable(moe):
         assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
 
 
-def test_layer_given_ids_with_out_of_range_id(moe):
+@pytest.mark.parametrize("path", list(PATHS), ids=str)
+def test_layer_given_ids_with_out_of_range_id(moe, path):
     shape = synth.tiny(M=4)
     inp = layer_inputs(shape)
     ids, w = oracle.topk_softmax(inp.logits.cpu().numpy(), shape.top_k)
     ids[1, 1] = shape.E + 3                        # out of range: skipped, flagged
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out, _, _ = H.gpu_layer(moe, inp, use_logits=False, ids=torch.from_numpy(ids).cuda(),
-                            w=torch.from_numpy(w.astype(np.float32)).cuda(), err=err)
-    assert int(err.item()) & moe.MOE_ERR_BAD_ID
+    out, view, _ = H.gpu_layer(moe, inp, path=PATHS[path], use_logits=False,
+                               ids=torch.from_numpy(ids).cuda(),
+                               w=torch.from_numpy(w.astype(np.float32)).cuda(), err=err)
+    assert int(err.item()) == moe.MOE_ERR_BAD_ID
     _, ref_b, bad = H.oracle_layer(inp, ids=ids, w=w)
     assert bad == 1
     rl2, mx = H.compare_bf16(out, ref_b)
+    assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS
+    tables = oracle.align(ids.ravel(), shape.E, shape.BS)
+    np.testing.assert_array_equal(view["token_to_perm"].cpu().numpy(), tables["token_to_perm"])
+    np.testing.assert_array_equal(view["sorted_token_ids"].cpu().numpy(),
+                                  tables["sorted_token_ids"])
+
+
+def test_fused_and_staged_paths_agree(moe):
+    """The fused pair and the five launches compute the same layer: equal
+    tables, outputs within the layer tolerance of each other."""
+    shape = synth.decode_nvfp4(8)
+    inp = layer_inputs(shape)
+    out_f, vf, _ = H.gpu_layer(moe, inp, path=PATHS["fused"])
+    out_s, vs, _ = H.gpu_layer(moe, inp, path=PATHS["staged"])
+    for key in ("sorted_token_ids", "expert_offsets", "token_to_perm", "topk_ids"):
+        assert torch.equal(vf[key], vs[key]), key
+    rl2, mx = H.compare_bf16(out_f, synth.bf16_bits(out_s))
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS
