@@ -60,6 +60,31 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
   return MOE_OK;
 }
 
+// launch_pdl for a grid whose CTAs wait on one another: also cooperative, so
+// the launch fails unless every CTA can be resident at once.
+template <typename... KArgs, typename... Args>
+int launch_pdl_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                    void *stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ((KArgs)args)...);
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return MOE_ECUDA;
+  }
+  return MOE_OK;
+}
+
 inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------------------------

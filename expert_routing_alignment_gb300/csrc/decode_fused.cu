@@ -1,5 +1,5 @@
-// decode_fused.cu -- the decode MoE layer (M * top_k <= 256 slots) as two
-// persistent kernels on one stream.
+// decode_fused.cu -- the decode MoE layer (M * top_k <= 256 slots) as one
+// cooperative persistent kernel.
 //
 // What ("metrale_model_layers/layers/moe/forward_nvfp4_grouped_decode.rs",
 // forward_nvfp4_grouped_decode; "fp8_moe_grouped.rs": gate+up and down over
@@ -11,35 +11,37 @@
 // moe_topk_softmax and moe_align write.
 //
 // How (GB300):
-//  * Every CTA routes the whole batch itself in shared memory from the router
-//    logits (warp top-k, then for each slot the count of smaller expert ids and
-//    of earlier equal ones: the pairwise rank of "nbxtensor/ops/moe_align.py"
-//    stage 3, cheap at n <= 256), so weight streaming starts without waiting
-//    for another kernel.  CTA 0 of the first kernel also writes the tables.
-//  * One engine serves both kernels.  The (active expert, output feature)
-//    list -- and the shared expert's features -- is split evenly over one CTA
-//    per SM.  A producer warp streams the weight rows (and NVFP4 group scales)
-//    of a stage into a shared-memory ring with cp.async.bulk (mbarrier
-//    completion, L2 evict-first).  In the eight consumer warps, a group of
-//    lanes owns one output feature of the stage and deals the row's 16-element
-//    units round-robin to its lanes; every unit is decoded once in registers
-//    and multiplied with each activation row, the unit's scale multiplies its
-//    partial sum, and an xor butterfly over the group finishes the dot product.
-//    Warps run independently through the ring; they meet only when the stage's
-//    expert changes, to stage that expert's activation rows (and FP8 block
-//    scales) in shared memory.
-//  * Kernel A (gate+up): activations are the bf16 rows of x as f16 scaled by a
-//    per-row power of two (taken from the row's largest |x| when staged); the
+//  * One CTA per SM, all co-resident (cooperative launch).  Every CTA routes
+//    the whole batch itself in shared memory from the router logits (warp
+//    top-k, then for each slot the count of smaller expert ids and of earlier
+//    equal ones: the pairwise rank of "nbxtensor/ops/moe_align.py" stage 3,
+//    cheap at n <= 256), so weight streaming starts at once.  CTA 0 also
+//    writes the tables.
+//  * The (active expert, output feature) list -- and the shared expert's
+//    features -- of each projection is split evenly over the CTAs.  A producer
+//    warp streams the CTA's gate+up weight rows, then without a pause its down
+//    weight rows (and NVFP4 group scales), into one shared-memory ring with
+//    cp.async.bulk (mbarrier completion, L2 evict-first), so the down rows are
+//    already on chip when the CTA reaches them.  In the fifteen consumer
+//    warps, a group of lanes owns one output feature of the stage and deals
+//    the row's 16-element units round-robin to its lanes; every unit is
+//    decoded once in registers and multiplied with each activation row, the
+//    unit's scale multiplies its partial sum, and an xor butterfly over the
+//    group finishes the dot product.  Warps run independently through the
+//    ring; they meet only when the stage's expert changes, to stage that
+//    expert's activation rows (and FP8 block scales) in shared memory.
+//  * gate+up: activations are the bf16 rows of x as f16 scaled by a per-row
+//    power of two (taken from the row's largest |x| when staged); the
 //    mixed-precision fma forms exact f16 x f16 products in fp32.  Epilogue:
 //    h = silu(g) * u.
-//  * Kernel B (down + blend), launched with programmatic dependent launch: its
-//    CTAs become resident while A streams, route, and fill their weight ring
-//    before waiting for A.  Activations are the fp32 h rows; weights are
-//    decoded to fp32.  Epilogue: y.  At its end a CTA adds, per 64-column
-//    tile, how many (expert, column) pairs it wrote to that tile's counter; the
-//    CTA whose addition completes a tile blends it for every token in slot
-//    order j = 0..k-1 and adds the shared expert.  The counter only decides
-//    who blends; the sum is the same whoever does it.
+//  * A grid barrier (a monotonic arrival count in the workspace) separates the
+//    last h write of any CTA from the first h read.
+//  * down: activations are the fp32 h rows; weights are decoded to fp32.
+//    Epilogue: y.  At its end a CTA adds, per 64-column tile, how many
+//    (expert, column) pairs it wrote to that tile's counter; the CTA whose
+//    addition completes a tile blends it for every token in slot order
+//    j = 0..k-1 and adds the shared expert.  The counter only decides who
+//    blends; the sum is the same whoever does it.
 // Every wait is bounded; one that gives up sets MOE_ERR_TIMEOUT.
 #include <limits.h>
 
@@ -50,9 +52,9 @@
 namespace moe {
 namespace {
 
-constexpr int kCW = 8;                    // consumer warps
+constexpr int kCW = 15;                   // consumer warps
 constexpr int kCThreads = kCW * 32;
-constexpr int kThreads = kCThreads + 32;  // + one producer warp
+constexpr int kThreads = kCThreads + 32;  // + one producer warp: 16 warps, <= 128 registers
 constexpr int kMaxN = 256;                // slots M * top_k on this path
 constexpr int kMaxM = 32;
 constexpr int kXS = 4;                    // activation rows staged in shared memory
@@ -80,10 +82,12 @@ struct FusedArgs {
   const uint16_t *x;
   int32_t *topk_ids, *sti, *sei, *off, *ttp, *act, *act_count, *ntpp;
   float *topk_w, *h, *h_sh, *y, *y_sh;
-  int32_t *tile_cnt;        // [ceil(H / kBlendTile)] blend counters, zeroed by kernel A
+  unsigned long long *grid_ctr;   // grid-barrier arrivals (monotonic; zero before first use)
+  int32_t *tile_cnt;              // [ceil(H / kBlendTile)] blend counters, zeroed each call
   uint16_t *out;
   uint32_t *err;
-  int stages[2], stage_bytes[2];   // ring of kernel A, of kernel B
+  int stages, slot_bytes;         // the weight ring
+  int rounds[2][2];               // lane-group rounds per stage: [gate+up, down][routed, shared]
 };
 
 // ---------------------------------------------------------------------------
@@ -201,8 +205,7 @@ __device__ void route_local(const Plan &P, const FusedArgs &a) {
 }
 
 // The routing and alignment tables in the workspace, as moe_topk_softmax and
-// moe_align write them; also zeroes kernel B's blend counters.  Run by the
-// first nt threads of the CTA.
+// moe_align write them.  Run by the first nt threads of the CTA.
 __device__ void write_tables(const Plan &P, const FusedArgs &a, int nt) {
   const int tid = threadIdx.x, n = a.n;
   const int A = P.hdr[kHdrA], total = P.hdr[kHdrTotal];
@@ -213,7 +216,6 @@ __device__ void write_tables(const Plan &P, const FusedArgs &a, int nt) {
     }
   for (int i = tid; i < n; i += nt) a.ttp[i] = P.pos[i];
   for (int x = tid; x < a.cap; x += nt) a.act[x] = x < A ? P.act_e[x] : -1;
-  for (int t = tid; t < (a.H + kBlendTile - 1) / kBlendTile; t += nt) a.tile_cnt[t] = 0;
   if (tid == 0) {
     *a.act_count = A;
     *a.ntpp = total;
@@ -358,7 +360,7 @@ __host__ __device__ inline int lanes_per_row(int K) {
   return units % 32 == 0 ? 32 : units % 16 == 0 ? 16 : 8;
 }
 
-// Rows of one matrix per stage: 8 warps x (32 / lanes_per_row) lane groups.
+// Rows of one matrix per lane-group round: consumer warps x (32 / lanes_per_row).
 __host__ __device__ inline int stage_feats(int K) { return kCW * (32 / lanes_per_row(K)); }
 
 // A stage: features [o0, o0 + r) of one expert's projection(s).
@@ -458,136 +460,129 @@ __device__ __forceinline__ void row_pass(const uint8_t *stage, int F, int Kb, in
   }
 }
 
-template <bool GATE_UP, int RF, int SF>
-__global__ void __maxnreg__(112) decode_expert_kernel(FusedArgs a) {
-  constexpr int kp = GATE_UP ? 0 : 1;
-  constexpr int kMats = GATE_UP ? 2 : 1;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int NS = a.stages[kp], SB = a.stage_bytes[kp];
-  // K of the routed and shared passes
-  const int Kr = GATE_UP ? a.H : a.r.I;
-  const int Ks = a.has_shared ? (GATE_UP ? a.H : a.s.I) : 0;
+// Shared-memory carve-up of the layer kernel.
+struct Smem {
+  uint8_t *ring;
+  uint64_t *full, *empty;
+  Plan P;
+  float *bscale;    // FP8 block scales of the current expert [2][256]
+  uint32_t *xmax;   // [kXS] staged-row |x| maxima
+  int *xexp;        // [kXS] their f16 exponents
+  int *misc;        // [64] tile counts / flags
+  uint8_t *xs;      // [kXS] staged activation rows
+};
+
+__host__ __device__ inline size_t xs_bytes(int H, int kd_max) {
+  const size_t g = (size_t)kXS * H * 2, d = (size_t)kXS * kd_max * 4;
+  return g > d ? g : d;
+}
+
+__device__ __forceinline__ Smem carve(uint8_t *smem, const FusedArgs &a, int kd_max) {
+  Smem S;
   size_t o = 0;
-  uint8_t *ring = smem;
-  o += (size_t)NS * SB;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + o);
-  uint64_t *empty = full + NS;
-  o += 16 * (size_t)NS;
-  const Plan P = carve_plan(smem + o, a.n);
+  S.ring = smem;
+  o += (size_t)a.stages * a.slot_bytes;
+  S.full = reinterpret_cast<uint64_t *>(smem + o);
+  S.empty = S.full + a.stages;
+  o += 16 * (size_t)a.stages;
+  S.P = carve_plan(smem + o, a.n);
   o += plan_bytes(a.n);
-  float *bscale = reinterpret_cast<float *>(smem + o);       // FP8 block scales [kMats][256]
-  o += (size_t)kMats * 256 * 4;
-  uint32_t *xmax = reinterpret_cast<uint32_t *>(smem + o);   // [kXS] staged-row |x| maxima
-  int *xexp = reinterpret_cast<int *>(xmax + kXS);           // [kXS] their f16 exponents
-  int *tiles = xexp + kXS;                                   // [32] kernel B: per-tile counts
-  o += (2 * kXS + 32 + 32) * 4;
-  uint8_t *xs = smem + o;                                    // [kXS] activation rows
+  S.bscale = reinterpret_cast<float *>(smem + o);
+  o += 2 * 256 * 4;
+  S.xmax = reinterpret_cast<uint32_t *>(smem + o);
+  S.xexp = reinterpret_cast<int *>(S.xmax + kXS);
+  S.misc = S.xexp + kXS;
+  o += (2 * kXS + 64) * 4;
+  S.xs = smem + o;
+  (void)kd_max;
+  return S;
+}
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (GATE_UP) {
-    pdl_wait();      // x and the router logits are final
-    pdl_trigger();   // kernel B may become resident and prefetch its weights
-  } else {
-    // The layer inputs (logits / ids) were final before kernel A started,
-    // and A started only after its own wait: routing from them before this
-    // kernel's wait is safe.  h is read only after pdl_wait below.
-    pdl_trigger();
-  }
-  if (tid == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kCW);
-    }
-    fence_mbar_init();
-  }
-  route_local(P, a);
+// Geometry of one phase's stage for a projection with K inputs.
+struct Geo {
+  int K, U, Kb, lpr, upl, rpw, fu, F;   // fu: features per lane-group round; F = rounds * fu
+};
 
-  const int A = P.hdr[kHdrA];
-  const int R = GATE_UP ? a.r.I : a.H;                        // features per routed expert
-  const int Rs = a.has_shared ? (GATE_UP ? a.s.I : a.H) : 0;  // features of the shared one
-  const int fs = stage_feats(Kr), fss = a.has_shared ? stage_feats(Ks) : 1;
+__device__ __forceinline__ Geo geo(int fmt, int K, int rounds) {
+  Geo g;
+  g.K = K;
+  g.U = K / 16;
+  g.Kb = (int)row_bytes(fmt, K);
+  g.lpr = lanes_per_row(K);
+  g.upl = g.U / g.lpr;
+  g.rpw = 32 / g.lpr;
+  g.fu = kCW * g.rpw;
+  g.F = rounds * g.fu;
+  return g;
+}
 
-  if (warp == kCW) {
-    // ---------------- producer ----------------
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      Iter it = make_iter(A, R, Rs, fs, fss);
-      Stage st;
-      int s = 0;
-      bool ok = true;
-      while (it.next(st)) {
-        const int slot = s % NS;
-        if (!mbar_wait(&empty[slot], ((uint32_t)(s / NS) & 1u) ^ 1u)) {
-          ok = false;
-          break;
-        }
-        const bool sh = st.a < 0;
-        const Exp &X = sh ? a.s : a.r;
-        const int fmt = sh ? SF : RF;
-        const int e = sh ? 0 : P.act_e[st.a];
-        const int K = sh ? Ks : Kr;
-        const int F = sh ? fss : fs;
-        const int rows = GATE_UP ? X.I : a.H;   // rows of each matrix
-        const size_t Kb = row_bytes(fmt, K);
-        const uint32_t wbytes = (uint32_t)(st.r * Kb);
-        const uint32_t sbytes = fmt == MOE_FMT_NVFP4_G16 ? (uint32_t)(st.r * (K / 16)) : 0u;
-        uint8_t *dst = ring + (size_t)slot * SB;
-        mbar_expect_tx(&full[slot], kMats * (wbytes + sbytes));
-#pragma unroll
-        for (int m = 0; m < kMats; ++m) {
-          const Proj &Pj = GATE_UP ? (m == 0 ? X.gate : X.up) : X.down;
-          bulk_g2s(dst + (size_t)m * F * Kb, Pj.codes + ((size_t)e * rows + st.o0) * Kb, wbytes,
-                   &full[slot], pol);
-          if (sbytes)
-            bulk_g2s(dst + (size_t)kMats * F * Kb + (size_t)m * F * (K / 16),
-                     reinterpret_cast<const uint8_t *>(Pj.scale) +
-                         ((size_t)e * rows + st.o0) * (K / 16),
-                     sbytes, &full[slot], pol);
-        }
-        ++s;
-      }
-      if (!ok) {
-        if (a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
-        for (int q = max(0, s - NS); q < s; ++q)   // the last fill of each slot lands
-          (void)mbar_wait(&full[q % NS], (uint32_t)(q / NS) & 1u);
-      }
-    }
-    return;
-  }
-
-  // ---------------- consumers ----------------
-  if (!GATE_UP) {
-    pdl_wait();   // h from kernel A is final
-    if (A == 0 && !a.has_shared) {   // every slot out of range: the blend is zero
-      const int c0 = (int)((long long)a.H * blockIdx.x / gridDim.x);
-      const int c1 = (int)((long long)a.H * (blockIdx.x + 1) / gridDim.x);
-      for (int t = tid; t < a.M * (c1 - c0); t += kCThreads)
-        a.out[(size_t)(t / (c1 - c0)) * a.H + c0 + t % (c1 - c0)] = 0;
-      return;
-    }
-  }
-  int cur_a = INT_MIN, cur_x0 = -1;
-  Iter it = make_iter(A, R, Rs, fs, fss);
+// Producer: stream one phase's stages into the ring, continuing the stage
+// counter s.  False when a wait gave up.
+template <bool GATE_UP, int RF, int SF>
+__device__ bool produce(const FusedArgs &a, const Smem &S, int A, int &s, uint64_t pol) {
+  constexpr int kMats = GATE_UP ? 2 : 1;
+  const int p = GATE_UP ? 0 : 1;
+  const int Kr = GATE_UP ? a.H : a.r.I, Ks = a.has_shared ? (GATE_UP ? a.H : a.s.I) : 0;
+  const Geo gr = geo(RF, Kr, a.rounds[p][0]);
+  const Geo gs = geo(SF, a.has_shared ? Ks : 256, a.rounds[p][1]);
+  const int R = GATE_UP ? a.r.I : a.H, Rs = a.has_shared ? (GATE_UP ? a.s.I : a.H) : 0;
+  Iter it = make_iter(A, R, Rs, gr.F, gs.F);
   Stage st;
-  int s = 0;
-  bool failed = false;
   while (it.next(st)) {
-    const int slot = s % NS;
-    const uint32_t par = (uint32_t)(s / NS) & 1u;
+    const int slot = s % a.stages;
+    if (!mbar_wait(&S.empty[slot], ((uint32_t)(s / a.stages) & 1u) ^ 1u)) return false;
     const bool sh = st.a < 0;
     const Exp &X = sh ? a.s : a.r;
     const int fmt = sh ? SF : RF;
+    const Geo &g = sh ? gs : gr;
+    const int e = sh ? 0 : S.P.act_e[st.a];
+    const int rows = GATE_UP ? X.I : a.H;   // rows of each matrix
+    const uint32_t wbytes = (uint32_t)(st.r * g.Kb);
+    const uint32_t sbytes = fmt == MOE_FMT_NVFP4_G16 ? (uint32_t)(st.r * (g.K / 16)) : 0u;
+    uint8_t *dst = S.ring + (size_t)slot * a.slot_bytes;
+    mbar_expect_tx(&S.full[slot], kMats * (wbytes + sbytes));
+#pragma unroll
+    for (int m = 0; m < kMats; ++m) {
+      const Proj &Pj = GATE_UP ? (m == 0 ? X.gate : X.up) : X.down;
+      bulk_g2s(dst + (size_t)m * g.F * g.Kb, Pj.codes + ((size_t)e * rows + st.o0) * g.Kb,
+               wbytes, &S.full[slot], pol);
+      if (sbytes)
+        bulk_g2s(dst + (size_t)kMats * g.F * g.Kb + (size_t)m * g.F * (g.K / 16),
+                 reinterpret_cast<const uint8_t *>(Pj.scale) + ((size_t)e * rows + st.o0) * (g.K / 16),
+                 sbytes, &S.full[slot], pol);
+    }
+    ++s;
+  }
+  return true;
+}
+
+// Consumers: one phase's stages, continuing the stage counter s.
+template <bool GATE_UP, int RF, int SF>
+__device__ void consume(const FusedArgs &a, const Smem &S, int A, int &s, bool &failed) {
+  constexpr int kMats = GATE_UP ? 2 : 1;
+  const int p = GATE_UP ? 0 : 1;
+  const Plan &P = S.P;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Kr = GATE_UP ? a.H : a.r.I, Ks = a.has_shared ? (GATE_UP ? a.H : a.s.I) : 0;
+  const Geo gr = geo(RF, Kr, a.rounds[p][0]);
+  const Geo gs = geo(SF, a.has_shared ? Ks : 256, a.rounds[p][1]);
+  const int R = GATE_UP ? a.r.I : a.H, Rs = a.has_shared ? (GATE_UP ? a.s.I : a.H) : 0;
+  Iter it = make_iter(A, R, Rs, gr.F, gs.F);
+  Stage st;
+  int cur_a = INT_MIN, cur_x0 = -1;
+  uint8_t *xs = S.xs;
+  while (it.next(st)) {
+    const int slot = s % a.stages;
+    const uint32_t par = (uint32_t)(s / a.stages) & 1u;
+    const bool sh = st.a < 0;
+    const Exp &X = sh ? a.s : a.r;
+    const int fmt = sh ? SF : RF;
+    const Geo &g = sh ? gs : gr;
     const int e = sh ? 0 : P.act_e[st.a];
-    const int K = sh ? Ks : Kr;
-    const int U = K / 16;
-    const int Kb = (int)row_bytes(fmt, K);
-    const int F = sh ? fss : fs;
+    const int K = g.K, U = g.U;
     const int rows = sh ? a.M : P.act_cnt[st.a];    // activation rows of this expert
     const int mrows = GATE_UP ? X.I : a.H;          // rows of each weight matrix
-    const int lpr = lanes_per_row(K), upl = U / lpr;
-    const int g = lane / lpr, j = lane % lpr;
-    const int f = warp * (32 / lpr) + g;            // this lane group's feature of the stage
-    const bool live = f < st.r;
+    const int gi = lane / g.lpr, j = lane % g.lpr;
     bool waited = false;
     for (int x0 = 0; x0 < rows; x0 += kXS) {
       const int xn = min(kXS, rows - x0);
@@ -598,44 +593,49 @@ __global__ void __maxnreg__(112) decode_expert_kernel(FusedArgs a) {
         if (GATE_UP) {
           // bf16 x rows -> f16 * 2^-s, s from the row's largest |x|, stored
           // as [row][half][unit] x 16 bytes
-          if (tid < kXS) xmax[tid] = 0u;
+          if (tid < kXS) S.xmax[tid] = 0u;
           named_sync(kCThreads);
-          uint4 held[kXS][2];
+          uint4 held[kXS];
 #pragma unroll
           for (int r = 0; r < kXS; ++r) {
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              const int k8 = (tid + v * kCThreads) * 8;
-              held[r][v] = make_uint4(0, 0, 0, 0);
-              if (r < xn && k8 < K) {
-                const int tok = sh ? x0 + r : P.rowslot[P.act_start[st.a] + x0 + r] / a.k;
-                held[r][v] =
-                    __ldcg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * a.H + k8));
-              }
+            const int k8 = tid * 8;
+            held[r] = make_uint4(0, 0, 0, 0);
+            if (r < xn && k8 < K) {
+              const int tok = sh ? x0 + r : P.rowslot[P.act_start[st.a] + x0 + r] / a.k;
+              held[r] = __ldcg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * a.H + k8));
             }
+            const uint32_t wd[4] = {held[r].x, held[r].y, held[r].z, held[r].w};
             uint32_t mx = 0;
 #pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              const uint32_t wd[4] = {held[r][v].x, held[r][v].y, held[r][v].z, held[r][v].w};
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                mx = max(mx, max(wd[i] & 0x7FFFu, (wd[i] >> 16) & 0x7FFFu));
-            }
+            for (int i = 0; i < 4; ++i) mx = max(mx, max(wd[i] & 0x7FFFu, (wd[i] >> 16) & 0x7FFFu));
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, d));
-            if (lane == 0 && r < xn) atomicMax(&xmax[r], mx);
+            if (lane == 0 && r < xn) atomicMax(&S.xmax[r], mx);
           }
+          // rows longer than the thread count: the remaining chunks
+          for (int k8 = (tid + kCThreads) * 8; k8 < K; k8 += kCThreads * 8)
+            for (int r = 0; r < xn; ++r) {
+              const int tok = sh ? x0 + r : P.rowslot[P.act_start[st.a] + x0 + r] / a.k;
+              const uint4 q = __ldcg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * a.H + k8));
+              const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+              uint32_t mx = 0;
+              for (int i = 0; i < 4; ++i) mx = max(mx, max(wd[i] & 0x7FFFu, (wd[i] >> 16) & 0x7FFFu));
+              atomicMax(&S.xmax[r], mx);
+            }
           named_sync(kCThreads);
-          if (tid < xn) xexp[tid] = max(0, (int)((xmax[tid] >> 7) & 0xFF) - 127 - 14);
+          if (tid < xn) S.xexp[tid] = max(0, (int)((S.xmax[tid] >> 7) & 0xFF) - 127 - 14);
+          for (int k8 = tid * 8; k8 < K; k8 += kCThreads * 8) {
 #pragma unroll
-          for (int r = 0; r < kXS; ++r) {
-            if (r >= xn) break;
-            const float m = pow2f(-max(0, (int)((xmax[r] >> 7) & 0xFF) - 127 - 14));
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              const int k8 = (tid + v * kCThreads) * 8;
-              if (k8 >= K) continue;
-              const uint4 q = held[r][v];
+            for (int r = 0; r < kXS; ++r) {
+              if (r >= xn) break;
+              uint4 q;
+              if (k8 == tid * 8) {
+                q = held[r];
+              } else {
+                const int tok = sh ? x0 + r : P.rowslot[P.act_start[st.a] + x0 + r] / a.k;
+                q = __ldcg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * a.H + k8));
+              }
+              const float m = pow2f(-max(0, (int)((S.xmax[r] >> 7) & 0xFF) - 127 - 14));
               uint4 hv;
               hv.x = pack_f16x2(__uint_as_float(q.x << 16) * m, __uint_as_float(q.x & 0xFFFF0000u) * m);
               hv.y = pack_f16x2(__uint_as_float(q.y << 16) * m, __uint_as_float(q.y & 0xFFFF0000u) * m);
@@ -662,7 +662,7 @@ __global__ void __maxnreg__(112) decode_expert_kernel(FusedArgs a) {
           for (int m = 0; m < kMats; ++m) {
             const Proj &Pj = GATE_UP ? (m == 0 ? X.gate : X.up) : X.down;
             const float *sp = reinterpret_cast<const float *>(Pj.scale) + (size_t)e * nb;
-            for (int v = tid; v < nb; v += kCThreads) bscale[m * 256 + v] = __ldg(sp + v);
+            for (int v = tid; v < nb; v += kCThreads) S.bscale[m * 256 + v] = __ldg(sp + v);
           }
         }
         named_sync(kCThreads);
@@ -670,131 +670,215 @@ __global__ void __maxnreg__(112) decode_expert_kernel(FusedArgs a) {
         cur_x0 = x0;
       }
       if (!waited) {
-        if (!failed && !mbar_wait(&full[slot], par)) {
+        if (!failed && !mbar_wait(&S.full[slot], par)) {
           failed = true;
           if (a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
         }
         waited = true;
       }
-      const uint8_t *stage = ring + (size_t)slot * SB;
-      const bool go = live && !failed;
-      const float gg = (fmt == MOE_FMT_NVFP4_G16 && go)
-                           ? __ldg((GATE_UP ? X.gate : X.down).glob + e) : 1.f;
-      const float gu = (GATE_UP && fmt == MOE_FMT_NVFP4_G16 && go) ? __ldg(X.up.glob + e) : 1.f;
-      for (int r0 = 0; r0 < xn; r0 += 4) {
-        const int nr = min(4, xn - r0);
-        float acc0[4], acc1[4];
-#define MOE_ROWS(F_, NR)                                                                     \
-  row_pass<GATE_UP, F_, NR>(stage, F, Kb, K, lpr, upl, xs, r0, f, j, go, st.o0, bscale, acc0, \
-                            acc1)
-        if (fmt == MOE_FMT_FP8_B128) {
-          if (nr == 1) MOE_ROWS(MOE_FMT_FP8_B128, 1);
-          else if (nr == 2) MOE_ROWS(MOE_FMT_FP8_B128, 2);
-          else MOE_ROWS(MOE_FMT_FP8_B128, 4);
-        } else {
-          if (nr == 1) MOE_ROWS(MOE_FMT_NVFP4_G16, 1);
-          else if (nr == 2) MOE_ROWS(MOE_FMT_NVFP4_G16, 2);
-          else MOE_ROWS(MOE_FMT_NVFP4_G16, 4);
-        }
+      const uint8_t *stage = S.ring + (size_t)slot * a.slot_bytes;
+      const float gg = (fmt == MOE_FMT_NVFP4_G16) ? __ldg((GATE_UP ? X.gate : X.down).glob + e) : 1.f;
+      const float gu = (GATE_UP && fmt == MOE_FMT_NVFP4_G16) ? __ldg(X.up.glob + e) : 1.f;
+      for (int q = 0; q < g.F / g.fu; ++q) {   // lane-group rounds of the stage
+        const int f = q * g.fu + warp * g.rpw + gi;   // this lane group's feature
+        const bool go = f < st.r && !failed;
+        if (q * g.fu >= st.r) break;
+        for (int r0 = 0; r0 < xn; r0 += 4) {
+          const int nr = min(4, xn - r0);
+          float acc0[4], acc1[4];
+#define MOE_ROWS(F_, NR)                                                                        \
+  row_pass<GATE_UP, F_, NR>(stage, g.F, g.Kb, K, g.lpr, g.upl, xs, r0, f, j, go, st.o0, S.bscale, \
+                            acc0, acc1)
+          if (fmt == MOE_FMT_FP8_B128) {
+            if (nr == 1) MOE_ROWS(MOE_FMT_FP8_B128, 1);
+            else if (nr == 2) MOE_ROWS(MOE_FMT_FP8_B128, 2);
+            else MOE_ROWS(MOE_FMT_FP8_B128, 4);
+          } else {
+            if (nr == 1) MOE_ROWS(MOE_FMT_NVFP4_G16, 1);
+            else if (nr == 2) MOE_ROWS(MOE_FMT_NVFP4_G16, 2);
+            else MOE_ROWS(MOE_FMT_NVFP4_G16, 4);
+          }
 #undef MOE_ROWS
-        if (j == 0 && go) {
+          if (j == 0 && go) {
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            if (r >= nr) break;
-            const int row = x0 + r0 + r;   // activation row of the expert
-            if (GATE_UP) {
-              const float mx = pow2f(xexp[r0 + r]);
-              const float hv = silu_f32(acc0[r] * gg * mx) * (acc1[r] * gu * mx);
-              if (sh)
-                a.h_sh[(size_t)row * X.I + st.o0 + f] = hv;
-              else
-                a.h[(size_t)(P.act_off[st.a] + row) * X.I + st.o0 + f] = hv;
-            } else {
-              const float yv = acc0[r] * gg;
-              if (sh)
-                a.y_sh[(size_t)row * a.H + st.o0 + f] = yv;
-              else
-                a.y[(size_t)(P.act_off[st.a] + row) * a.H + st.o0 + f] = yv;
+            for (int r = 0; r < 4; ++r) {
+              if (r >= nr) break;
+              const int row = x0 + r0 + r;   // activation row of the expert
+              if (GATE_UP) {
+                const float mx = pow2f(S.xexp[r0 + r]);
+                const float hv = silu_f32(acc0[r] * gg * mx) * (acc1[r] * gu * mx);
+                if (sh)
+                  a.h_sh[(size_t)row * X.I + st.o0 + f] = hv;
+                else
+                  a.h[(size_t)(P.act_off[st.a] + row) * X.I + st.o0 + f] = hv;
+              } else {
+                const float yv = acc0[r] * gg;
+                if (sh)
+                  a.y_sh[(size_t)row * a.H + st.o0 + f] = yv;
+                else
+                  a.y[(size_t)(P.act_off[st.a] + row) * a.H + st.o0 + f] = yv;
+              }
             }
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the stage
+    if (lane == 0) mbar_arrive(&S.empty[slot]);   // this warp is done with the stage
     ++s;
   }
+}
 
-  if (GATE_UP) {
-    if (blockIdx.x == 0) write_tables(P, a, kCThreads);
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Barrier over the consumer threads of every CTA of the (co-resident) grid.
+// The counter only grows: each CTA adds one per call, so the CTAs of a call
+// all see arrival numbers inside the same window [c*G, (c+1)*G).  False when
+// the wait gave up.
+__device__ bool grid_barrier(unsigned long long *ctr, int *flag) {
+  __threadfence();
+  named_sync(kCThreads);
+  if (threadIdx.x == 0) {
+    const unsigned long long G = gridDim.x;
+    const unsigned long long v = atomicAdd(ctr, 1ull);
+    const unsigned long long target = (v / G + 1) * G;
+    bool ok = false;
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+      if (ld_acquire_u64(ctr) >= target) {
+        ok = true;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    *flag = ok;
+  }
+  named_sync(kCThreads);
+  return *flag != 0;
+}
+
+template <int RF, int SF>
+__global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(FusedArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Smem S = carve(smem, a, 0);
+  const Plan &P = S.P;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  pdl_wait();      // x and the router logits are final
+  pdl_trigger();   // the next kernel on the stream may be scheduled
+  if (tid == 0) {
+    for (int i = 0; i < a.stages; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], kCW);
+    }
+    fence_mbar_init();
+  }
+  route_local(P, a);
+  const int A = P.hdr[kHdrA];
+
+  if (warp == kCW) {
+    // ---------------- producer: gate+up stages, then down stages ----------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int s = 0;
+      bool ok = produce<true, RF, SF>(a, S, A, s, pol);
+      if (ok) ok = produce<false, RF, SF>(a, S, A, s, pol);
+      if (!ok) {
+        if (a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
+        for (int q = max(0, s - a.stages); q < s; ++q)   // the last fill of each slot lands
+          (void)mbar_wait(&S.full[q % a.stages], (uint32_t)(q / a.stages) & 1u);
+      }
+    }
     return;
   }
 
-  // ---------------- kernel B: blend ----------------
-  // Publish how many (expert, column) pairs of each 64-column tile this CTA
-  // wrote; the CTA whose count completes a tile blends it, in slot order.
+  // ---------------- consumers ----------------
   const int ntiles = (a.H + kBlendTile - 1) / kBlendTile;
-  __threadfence();          // this thread's y writes are visible device-wide
-  if (tid < 32) tiles[tid] = 0;
-  named_sync(kCThreads);
-  if (tid == 0) {
-    Iter it2 = make_iter(A, R, Rs, fs, fss);
-    Stage s2;
-    while (it2.next(s2))
-      for (int tcol = s2.o0 / kBlendTile; tcol * kBlendTile < s2.o0 + s2.r; ++tcol)
-        tiles[tcol] += min(s2.o0 + s2.r, (tcol + 1) * kBlendTile) - max(s2.o0, tcol * kBlendTile);
+  if (blockIdx.x == 0)   // read only after the grid barrier below
+    for (int t = tid; t < ntiles; t += kCThreads) a.tile_cnt[t] = 0;
+  int s = 0;
+  bool failed = false;
+  consume<true, RF, SF>(a, S, A, s, failed);
+  // every h row of every CTA is written before any CTA reads one
+  if (!grid_barrier(a.grid_ctr, S.misc + 32)) {
+    failed = true;
+    if (tid == 0 && a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
   }
-  named_sync(kCThreads);
-  if (tid < ntiles) {
-    const int mine = tiles[tid];
-    int last = 0;
-    if (mine > 0) {
-      const int width = min(kBlendTile, a.H - tid * kBlendTile);
-      const int target = (A + (a.has_shared ? 1 : 0)) * width;
-      last = atomicAdd(&a.tile_cnt[tid], mine) + mine == target;
+  consume<false, RF, SF>(a, S, A, s, failed);
+
+  // ---------------- blend ----------------
+  int *tiles = S.misc;   // [32]
+  if (A == 0 && !a.has_shared) {   // every slot out of range: the blend is zero
+    const int c0 = (int)((long long)a.H * blockIdx.x / gridDim.x);
+    const int c1 = (int)((long long)a.H * (blockIdx.x + 1) / gridDim.x);
+    for (int t = tid; t < a.M * (c1 - c0); t += kCThreads)
+      a.out[(size_t)(t / (c1 - c0)) * a.H + c0 + t % (c1 - c0)] = 0;
+  } else {
+    // Publish how many (expert, column) pairs of each 64-column tile this CTA
+    // wrote; the CTA whose count completes a tile blends it, in slot order.
+    __threadfence();          // this thread's y writes are visible device-wide
+    if (tid < 32) tiles[tid] = 0;
+    named_sync(kCThreads);
+    if (tid == 0) {
+      const int Ks = a.has_shared ? a.s.I : 256;
+      Iter it2 = make_iter(A, a.H, a.has_shared ? a.H : 0,
+                           geo(RF, a.r.I, a.rounds[1][0]).F, geo(SF, Ks, a.rounds[1][1]).F);
+      Stage s2;
+      while (it2.next(s2))
+        for (int tcol = s2.o0 / kBlendTile; tcol * kBlendTile < s2.o0 + s2.r; ++tcol)
+          tiles[tcol] += min(s2.o0 + s2.r, (tcol + 1) * kBlendTile) - max(s2.o0, tcol * kBlendTile);
     }
-    __threadfence();
-    tiles[tid] = last;
-  }
-  named_sync(kCThreads);
-  for (int tcol = 0; tcol < ntiles; ++tcol) {
-    if (!tiles[tcol]) continue;
-    const int c0 = tcol * kBlendTile, width = min(kBlendTile, a.H - c0);
-    for (int t = tid; t < a.M * width; t += kCThreads) {
-      const int tok = t / width, cc = c0 + t % width;
-      float acc = 0.f;
-      for (int jj = 0; jj < a.k; ++jj) {
-        const int slot_j = tok * a.k + jj;
-        const int p = P.pos[slot_j];
-        if (p < 0) continue;
-        acc = fmaf(P.w[slot_j], __ldcg(a.y + (size_t)p * a.H + cc), acc);
+    named_sync(kCThreads);
+    if (tid < ntiles) {
+      const int mine = tiles[tid];
+      int last = 0;
+      if (mine > 0) {
+        const int width = min(kBlendTile, a.H - tid * kBlendTile);
+        const int target = (A + (a.has_shared ? 1 : 0)) * width;
+        last = atomicAdd(&a.tile_cnt[tid], mine) + mine == target;
       }
-      if (a.has_shared) acc += __ldcg(a.y_sh + (size_t)tok * a.H + cc);
-      a.out[(size_t)tok * a.H + cc] = float_to_bf16_rn(acc);
+      __threadfence();
+      tiles[tid] = last;
+    }
+    named_sync(kCThreads);
+    for (int tcol = 0; tcol < ntiles; ++tcol) {
+      if (!tiles[tcol]) continue;
+      const int c0 = tcol * kBlendTile, width = min(kBlendTile, a.H - c0);
+      for (int t = tid; t < a.M * width; t += kCThreads) {
+        const int tok = t / width, cc = c0 + t % width;
+        float acc = 0.f;
+        for (int jj = 0; jj < a.k; ++jj) {
+          const int slot_j = tok * a.k + jj;
+          const int pj = P.pos[slot_j];
+          if (pj < 0) continue;
+          acc = fmaf(P.w[slot_j], __ldcg(a.y + (size_t)pj * a.H + cc), acc);
+        }
+        if (a.has_shared) acc += __ldcg(a.y_sh + (size_t)tok * a.H + cc);
+        a.out[(size_t)tok * a.H + cc] = float_to_bf16_rn(acc);
+      }
     }
   }
+  if (blockIdx.x == 0) write_tables(P, a, kCThreads);
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
-// Shared memory of kernel A (gate+up, 2/3 of the bytes) and kernel B (down):
-// both fit on one SM together, so B can prefetch while A streams.
-constexpr size_t kBudgetA = 126 * 1024;
-constexpr size_t kBudgetB = 96 * 1024;
+constexpr size_t kSmemMax = 227 * 1024;
 
 struct Shape {
-  int stages[2], stage_bytes[2];
-  size_t smem[2];
+  int stages, slot_bytes, rounds[2][2];
+  size_t smem;
 };
 
-size_t fixed_bytes(bool gate_up, int n, int kmax) {
-  return plan_bytes(n) + (size_t)(gate_up ? 2 : 1) * 256 * 4 + (2 * kXS + 64) * 4 +
-         (size_t)kXS * kmax * (gate_up ? 2 : 4);
-}
-
-size_t stage_bytes_of(bool gate_up, int fmt, int K) {
+// Bytes of one lane-group round of a stage: every lane group one row of each
+// matrix (and the NVFP4 group scales of those rows).
+size_t round_bytes(bool gate_up, int fmt, int K) {
   const size_t per_row = row_bytes(fmt, K) + (fmt == MOE_FMT_NVFP4_G16 ? (size_t)K / 16 : 0);
   return (size_t)(gate_up ? 2 : 1) * stage_feats(K) * per_row;
 }
@@ -821,25 +905,25 @@ bool plan_shape(const moe_layer_desc *L, int M, int sms, Shape &sp) {
            ((uintptr_t)X->down.scale & 15) == 0;
   };
   if (!scales_ok(&R) || !scales_ok(S)) return false;
-  for (int p = 0; p < 2; ++p) {
-    const bool gu = p == 0;
-    const int kr = gu ? H : R.inter, ks = S ? (gu ? H : S->inter) : 0;
-    const int kmax = kr > ks ? kr : ks;
-    size_t sb = stage_bytes_of(gu, R.fmt, kr);
-    if (S) {
-      const size_t sbs = stage_bytes_of(gu, S->fmt, ks);
-      sb = sb > sbs ? sb : sbs;
-    }
-    sb = (sb + 127) & ~(size_t)127;
-    const size_t budget = gu ? kBudgetA : kBudgetB;
-    const size_t fixed = fixed_bytes(gu, n, kmax);
-    if (fixed + 2 * (sb + 16) > budget) return false;
-    int ns = (int)((budget - fixed) / (sb + 16));
-    if (ns > 12) ns = 12;
-    sp.stages[p] = ns;
-    sp.stage_bytes[p] = (int)sb;
-    sp.smem[p] = (size_t)ns * sb + 16 * (size_t)ns + fixed;
-  }
+  // a ring slot holds one gate+up round; down stages take as many rounds as fit
+  size_t slot = round_bytes(true, R.fmt, H);
+  if (S && round_bytes(true, S->fmt, H) > slot) slot = round_bytes(true, S->fmt, H);
+  const size_t dr = round_bytes(false, R.fmt, R.inter);
+  const size_t ds = S ? round_bytes(false, S->fmt, S->inter) : 0;
+  if (dr > slot) slot = dr;
+  if (ds > slot) slot = ds;
+  slot = (slot + 127) & ~(size_t)127;
+  sp.rounds[0][0] = sp.rounds[0][1] = 1;
+  sp.rounds[1][0] = (int)(slot / dr);
+  sp.rounds[1][1] = S ? (int)(slot / ds) : 1;
+  const int kd_max = S && S->inter > R.inter ? S->inter : R.inter;
+  const size_t fixed = plan_bytes(n) + 2 * 256 * 4 + (2 * kXS + 64) * 4 + xs_bytes(H, kd_max);
+  if (fixed + 2 * (slot + 16) > kSmemMax) return false;
+  int ns = (int)((kSmemMax - fixed) / (slot + 16));
+  if (ns > 16) ns = 16;
+  sp.stages = ns;
+  sp.slot_bytes = (int)slot;
+  sp.smem = (size_t)ns * slot + 16 * (size_t)ns + fixed;
   return true;
 }
 
@@ -902,37 +986,28 @@ int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float 
   a.h_sh = reinterpret_cast<float *>(base + v.h_shared);
   a.y = reinterpret_cast<float *>(base + v.y);
   a.y_sh = reinterpret_cast<float *>(base + v.y_shared);
-  a.tile_cnt = reinterpret_cast<int32_t *>(base + v.blend_counters);
+  a.grid_ctr = reinterpret_cast<unsigned long long *>(base + v.blend_counters);
+  a.tile_cnt = reinterpret_cast<int32_t *>(base + v.blend_counters + 8);
   a.out = out;
   a.err = err;
-  for (int p = 0; p < 2; ++p) {
-    a.stages[p] = sp.stages[p];
-    a.stage_bytes[p] = sp.stage_bytes[p];
-  }
+  a.stages = sp.stages;
+  a.slot_bytes = sp.slot_bytes;
+  for (int p = 0; p < 2; ++p)
+    for (int q = 0; q < 2; ++q) a.rounds[p][q] = sp.rounds[p][q];
   const int rf = L->routed.fmt, sf = L->shared ? L->shared->fmt : rf;
-  auto go = [&](auto ka, auto kb) -> int {
-    // both kernels ask for the largest shared-memory carveout so that they
-    // fit on one SM together
-    int st = ensure_max_carveout(reinterpret_cast<const void *>(ka));
+  auto go = [&](auto kern) -> int {
+    int st = ensure_max_carveout(reinterpret_cast<const void *>(kern));
     if (st) return st;
-    st = ensure_max_carveout(reinterpret_cast<const void *>(kb));
+    st = ensure_smem_limit(reinterpret_cast<const void *>(kern), sp.smem);
     if (st) return st;
-    st = ensure_smem_limit(reinterpret_cast<const void *>(ka), sp.smem[0]);
-    if (st) return st;
-    st = ensure_smem_limit(reinterpret_cast<const void *>(kb), sp.smem[1]);
-    if (st) return st;
-    st = launch_pdl(ka, dim3(sms), dim3(kThreads), sp.smem[0], stream, a);
-    if (st) return st;
-    return launch_pdl(kb, dim3(sms), dim3(kThreads), sp.smem[1], stream, a);
+    // cooperative: all CTAs are co-resident, which the grid barrier needs
+    return launch_pdl_coop(kern, dim3(sms), dim3(kThreads), sp.smem, stream, a);
   };
   constexpr int F8 = MOE_FMT_FP8_B128, F4 = MOE_FMT_NVFP4_G16;
-  if (rf == F8 && sf == F8)
-    return go(decode_expert_kernel<true, F8, F8>, decode_expert_kernel<false, F8, F8>);
-  if (rf == F4 && sf == F8)
-    return go(decode_expert_kernel<true, F4, F8>, decode_expert_kernel<false, F4, F8>);
-  if (rf == F8 && sf == F4)
-    return go(decode_expert_kernel<true, F8, F4>, decode_expert_kernel<false, F8, F4>);
-  return go(decode_expert_kernel<true, F4, F4>, decode_expert_kernel<false, F4, F4>);
+  if (rf == F8 && sf == F8) return go(decode_layer_kernel<F8, F8>);
+  if (rf == F4 && sf == F8) return go(decode_layer_kernel<F4, F8>);
+  if (rf == F8 && sf == F4) return go(decode_layer_kernel<F8, F4>);
+  return go(decode_layer_kernel<F4, F4>);
 }
 
 }  // namespace moe

@@ -74,7 +74,7 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   v->h_shared = take((size_t)M * Is * 4);
   v->y = take((size_t)max_total * H * 4);
   v->y_shared = take((size_t)M * H * 4);
-  v->blend_counters = take((size_t)((H + 63) / 64) * 4);
+  v->blend_counters = take(8 + (size_t)((H + 63) / 64) * 4);
   v->total_bytes = off;
   v->max_total = max_total;
   v->max_blocks = max_blocks;
@@ -124,7 +124,7 @@ extern "C" int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int
   if (moe::layout(layer, M, &v) != MOE_OK) return -1;
   const int path = moe::resolve_path(&layer->routed, M, layer->top_k, layer->path);
   if (path < 0) return -1;
-  if (path == MOE_PATH_SIMT && moe::fused_fits(layer, M, moe::sm_count())) return 2;
+  if (path == MOE_PATH_SIMT && moe::fused_fits(layer, M, moe::sm_count())) return 1;
   return with_logits ? 5 : 4;
 }
 

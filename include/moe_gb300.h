@@ -237,7 +237,7 @@ typedef struct moe_workspace_view {
     size_t active_experts, active_count;           /* [cap], [1] */
     size_t num_tokens_post_padded;                 /* [1] */
     size_t h, h_shared, y, y_shared;               /* float tables */
-    size_t blend_counters;                         /* [ceil(H/64)] int32, internal */
+    size_t blend_counters;                         /* internal: [1] uint64 + [ceil(H/64)] int32 */
     size_t total_bytes;
     int max_total, max_blocks, cap;
 } moe_workspace_view;
@@ -252,7 +252,7 @@ int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int M,
                                     moe_workspace_view *view);
 
 /* Host only.  The number of kernels moe_decode_layer enqueues for M rows
- * (2 on the fused decode path; otherwise 5 with router logits, 4 with given
+ * (1 on the fused decode path; otherwise 5 with router logits, 4 with given
  * ids), or -1 if the call would be rejected. */
 int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logits);
 
@@ -263,13 +263,17 @@ int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logit
  * moe_blend, all enqueued on `stream` with no host read.
  * On the CUDA-core path, when M*top_k <= 256, M <= 32, and hidden, inter and
  * the shared inter are multiples of 128 in [256, 2048] (NVFP4: of 256), the
- * same results come from two persistent kernels (gate+up, then down with the
- * blend) instead of five launches; every table and intermediate is still
- * written to the workspace.  MOE_PATH_SIMT_STAGED forces the five.
+ * same results come from one cooperative persistent kernel (gate+up, a grid
+ * barrier, then down with the blend) instead of five launches; every table
+ * and intermediate is still written to the workspace.  MOE_PATH_SIMT_STAGED
+ * forces the five.
  *   x [M][H] bf16 bits; out [M][H] bf16 bits;
  *   workspace: device, >= moe_decode_layer_workspace_bytes(layer, M) bytes,
  *   256-byte aligned, used only by this call (its intermediates can be read
- *   back through moe_decode_layer_workspace_view).
+ *   back through moe_decode_layer_workspace_view).  ZERO-FILL it once before
+ *   its first use: the fused path keeps a grid-barrier arrival count in it
+ *   (the blend_counters region) that every call leaves consistent for the
+ *   next.  After a call that reported MOE_ERR_TIMEOUT, zero it again.
  * Shape admission (host, nothing launched on failure):
  *   1 <= M <= MOE_MAX_ROWS, 1 <= top_k <= min(E, 32), E <= MOE_MAX_EXPERTS,
  *   block_size >= 1, and the format's hidden/inter rules.
