@@ -13,37 +13,47 @@
 // How (GB300):
 //  * One CTA per SM, all co-resident (cooperative launch).  Every CTA routes
 //    the whole batch itself in shared memory from the router logits (warp
-//    top-k, then for each slot the count of smaller expert ids and of earlier
-//    equal ones: the pairwise rank of "nbxtensor/ops/moe_align.py" stage 3,
-//    cheap at n <= 256), so weight streaming starts at once.  CTA 0 also
-//    writes the tables.
-//  * The (active expert, output feature) list -- and the shared expert's
-//    features -- of each projection is split evenly over the CTAs.  A producer
-//    warp streams the CTA's gate+up weight rows, then without a pause its down
-//    weight rows (and NVFP4 group scales), into one shared-memory ring with
-//    cp.async.bulk (mbarrier completion, L2 evict-first), so the down rows are
-//    already on chip when the CTA reaches them.  In the fifteen consumer
-//    warps, a group of lanes owns one output feature of the stage and deals
-//    the row's 16-element units round-robin to its lanes; every unit is
-//    decoded once in registers and multiplied with each activation row, the
-//    unit's scale multiplies its partial sum, and an xor butterfly over the
-//    group finishes the dot product.  Warps run independently through the
-//    ring; they meet only when the stage's expert changes, to stage that
-//    expert's activation rows (and FP8 block scales) in shared memory.
+//    top-k by redux.sync; then one warp ranks the slots of each expert in slot
+//    order with match.any and scans the per-expert counts), so weight
+//    streaming starts at once.  CTA 0 also writes the tables.
+//  * Work unit: a tile of 16 output features of one expert.  The tiles of
+//    each projection (and of the shared expert) are split evenly over the
+//    CTAs.  A stage of the weight stream is a group of tiles x a part of K,
+//    up to 32 KB of codes: one 3-D tensor copy per tile (cp.async.bulk.tensor;
+//    16 rows x the K part as 128-byte column blocks, 128-byte swizzle, L2
+//    evict-first) issued by one producer thread into a ring of stages in
+//    shared memory (mbarrier completion).  The producer streams the gate+up stages and then, without
+//    a pause, the down stages.
+//  * Sixteen consumer warps each take one (tile, K-range) item of a stage and
+//    run mma.sync m16n8k16 (f16 x f16 -> fp32) with the tile's 16 features as
+//    the MMA rows and up to 8 activation rows as its columns.  Weights are
+//    decoded in registers (E4M3 / E2M1 -> f16, exact; NVFP4 codes times their
+//    E4M3 group scale, exact in f16); the K order inside each MMA is a fixed
+//    permutation shared by both operands; the rows of a tile are taken in an
+//    order that makes the swizzled shared-memory reads conflict-free.  FP8
+//    block scales multiply each 64-wide K piece's fp32 partial sum.  After
+//    a tile group's last K part the warps' partial tiles meet in shared
+//    memory and are summed in a fixed order.
 //  * gate+up: activations are the bf16 rows of x as f16 scaled by a per-row
-//    power of two (taken from the row's largest |x| when staged); the
-//    mixed-precision fma forms exact f16 x f16 products in fp32.  Epilogue:
-//    h = silu(g) * u.
-//  * A grid barrier (a monotonic arrival count in the workspace) separates the
-//    last h write of any CTA from the first h read.
-//  * down: activations are the fp32 h rows; weights are decoded to fp32.
-//    Epilogue: y.  At its end a CTA adds, per 64-column tile, how many
-//    (expert, column) pairs it wrote to that tile's counter; the CTA whose
-//    addition completes a tile blends it for every token in slot order
-//    j = 0..k-1 and adds the shared expert.  The counter only decides who
-//    blends; the sum is the same whoever does it.
-// Every wait is bounded; one that gives up sets MOE_ERR_TIMEOUT.
+//    power of two (exact); epilogue h = silu(g) * u.  down: the fp32 h rows
+//    are split into two f16 terms (hi + lo, per-row power-of-two scale), so the
+//    product keeps about 22 bits of h; epilogue y.
+//  * Grid barriers (a monotonic arrival count in the workspace) separate the
+//    last h write of any CTA from the first h read, and the last y write from
+//    the blend.  Then every CTA blends an equal share of the M x H outputs,
+//    each in slot order j = 0..k-1 plus the shared expert, and writes a share
+//    of the tables.
+// Every result depends only on its own row's data: the K split, the order of
+// every sum and the MMA shapes are fixed by the layer's shapes, never by the
+// batch.  Every wait is bounded; one that gives up sets MOE_ERR_TIMEOUT.
 #include <limits.h>
+#include <string.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "async.cuh"
 #include "common.cuh"
@@ -52,24 +62,29 @@
 namespace moe {
 namespace {
 
-constexpr int kCW = 15;                   // consumer warps
+constexpr int kCW = 16;                   // consumer warps
 constexpr int kCThreads = kCW * 32;
-constexpr int kThreads = kCThreads + 32;  // + one producer warp: 16 warps, <= 128 registers
+constexpr int kThreads = kCThreads + 32;  // + one producer warp
 constexpr int kMaxN = 256;                // slots M * top_k on this path
 constexpr int kMaxM = 32;
-constexpr int kXS = 4;                    // activation rows staged in shared memory
-constexpr int kBlendTile = 64;            // output columns per blend tile
+constexpr int kRows = 8;                  // activation rows per pass (the MMA's n)
 constexpr int kNoKey = INT_MAX;
+constexpr int kBoxBytes = 16 * 128;       // one code box: 16 rows x 128 bytes
+constexpr int kSBoxBytes = 16 * 16;       // one NVFP4 scale box: 16 rows x 16 bytes
 
-struct Proj {
-  const uint8_t *codes;
-  const void *scale;
-  const float *glob;
+// Stage geometry of one projection (host-computed).  A half-chunk (hc) is 64
+// bytes of a weight row: FP8 64 inputs, NVFP4 128.  Each consumer warp takes
+// cpw half-chunks of one tile per stage; wpt warps share a tile; a stage holds
+// mt tiles x kr half-chunks (kr even: whole 128-byte boxes) of every matrix;
+// K is covered in nkp stages.
+struct PGeo {
+  int fmt, K, R, Kb, nhc, cpw, kr, wpt, mt, nkp, code_bytes, stage_bytes;
 };
 
 struct Exp {
   int fmt, I;
-  Proj gate, up, down;
+  const float *bscale[3];   // FP8 block scales of gate, up, down
+  const float *glob[3];     // NVFP4 global scales
 };
 
 struct FusedArgs {
@@ -83,11 +98,16 @@ struct FusedArgs {
   int32_t *topk_ids, *sti, *sei, *off, *ttp, *act, *act_count, *ntpp;
   float *topk_w, *h, *h_sh, *y, *y_sh;
   unsigned long long *grid_ctr;   // grid-barrier arrivals (monotonic; zero before first use)
-  int32_t *tile_cnt;              // [ceil(H / kBlendTile)] blend counters, zeroed each call
   uint16_t *out;
   uint32_t *err;
-  int stages, slot_bytes;         // the weight ring
-  int rounds[2][2];               // lane-group rounds per stage: [gate+up, down][routed, shared]
+  PGeo geo[2][2];                 // [gate+up, down][routed, shared]
+  int stages, slot_bytes, xs_row_bytes;
+};
+
+// Tensor maps of the weight codes and NVFP4 group scales:
+// [routed, shared][gate, up, down][codes, scales].
+struct Maps {
+  CUtensorMap m[2][3][2];
 };
 
 // ---------------------------------------------------------------------------
@@ -99,7 +119,6 @@ enum { kHdrA = 0, kHdrTotal, kHdrBad, kHdrInts = 8 };
 struct Plan {
   int *hdr;        // A, total padded rows, out-of-range slots
   int *key;        // [n] expert id of slot i, kNoKey when out of range
-  int *cnth;       // [n] rows of the expert if slot i is its first slot, else 0
   int *pos;        // [n] sorted position of slot i (token_to_perm), -1 if out of range
   float *w;        // [n] routing weight of slot i
   int *act_e;      // [n] active experts, ascending
@@ -110,7 +129,7 @@ struct Plan {
 };
 
 __host__ __device__ inline size_t plan_bytes(int n) {
-  return (((size_t)kHdrInts + 9 * (size_t)n) * 4 + 15) & ~(size_t)15;
+  return (((size_t)kHdrInts + 8 * (size_t)n) * 4 + 15) & ~(size_t)15;
 }
 
 __device__ __forceinline__ Plan carve_plan(uint8_t *base, int n) {
@@ -119,8 +138,6 @@ __device__ __forceinline__ Plan carve_plan(uint8_t *base, int n) {
   P.hdr = q;
   q += kHdrInts;
   P.key = q;
-  q += n;
-  P.cnth = q;
   q += n;
   P.pos = q;
   q += n;
@@ -141,9 +158,12 @@ __device__ __forceinline__ Plan carve_plan(uint8_t *base, int n) {
 __device__ __forceinline__ int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
 // Route every row (top-k softmax, or the given ids and weights) and align.
-__device__ void route_local(const Plan &P, const FusedArgs &a) {
-  const int tid = threadIdx.x, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  const int n = a.n;
+// scratch: 3 * E ints of shared memory, free for the duration of the call.
+__device__ void route_local(const Plan &P, const FusedArgs &a, int *scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int n = a.n, E = a.E;
+  int *cnt = scratch, *less = scratch + E, *poff = scratch + 2 * E;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
   if (a.logits) {
     for (int t = warp; t < a.M; t += nwarps)
       topk_softmax_row<32>(a.logits + (size_t)t * a.E, a.E, a.k, P.key + t * a.k, P.w + t * a.k);
@@ -154,60 +174,92 @@ __device__ void route_local(const Plan &P, const FusedArgs &a) {
     }
   }
   __syncthreads();
-  int my = kNoKey, less = 0, eqb = 0, cnt = 0;
-  if (tid < n) {
-    my = P.key[tid];
-    if (my < 0 || my >= a.E) my = kNoKey;
-  }
-  __syncthreads();
-  if (tid < n) P.key[tid] = my;
-  __syncthreads();
-  if (tid < n) {
-    for (int j = 0; j < n; ++j) {
-      const int kj = P.key[j];
-      less += kj < my;
-      eqb += (kj == my) & (j < tid);
-      cnt += kj == my;
+  if (warp == 0) {
+    // Rank of each slot among the earlier slots of its expert (slot order)
+    // and the per-expert counts: 32 slots at a time, in slot order.
+    int bad = 0;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      const int i = i0 + lane;
+      int key = kNoKey;
+      if (i < n) {
+        key = P.key[i];
+        if (key < 0 || key >= E) key = kNoKey;
+        P.key[i] = key;
+      }
+      const bool real = i < n && key != kNoKey;
+      bad += __popc(__ballot_sync(0xffffffffu, i < n && !real));
+      const unsigned grp = __match_any_sync(0xffffffffu, key);
+      const int before = __popc(grp & lanemask_lt());
+      const int base = real ? cnt[key] : 0;
+      __syncwarp();
+      if (real) {
+        P.pos[i] = base + before;   // rank for now; the sorted position below
+        if (before == 0) cnt[key] = base + __popc(grp);
+      }
+      __syncwarp();
     }
-    P.cnth[tid] = (my != kNoKey && eqb == 0) ? cnt : 0;
-  }
-  __syncthreads();
-  if (tid < n) {
-    int aidx = 0, off = 0;
-    for (int j = 0; j < n; ++j) {
-      const int c = P.cnth[j];
-      if (c > 0 && P.key[j] < my) {
-        ++aidx;
-        off += round_up(c, a.BS);
+    // Exclusive scans over the experts: rows below (less), padded rows below
+    // (poff) and active experts below; lane L owns experts [L*per, L*per+per).
+    const int per = (E + 31) / 32, e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int c = 0, na = 0, po = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int v = cnt[e];
+      c += v;
+      na += v > 0;
+      po += round_up(v, a.BS);
+    }
+    int ci = c, nai = na, poi = po;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int c2 = __shfl_up_sync(0xffffffffu, ci, d);
+      const int n2 = __shfl_up_sync(0xffffffffu, nai, d);
+      const int p2 = __shfl_up_sync(0xffffffffu, poi, d);
+      if (lane >= d) {
+        ci += c2;
+        nai += n2;
+        poi += p2;
       }
     }
-    if (my != kNoKey) {
-      P.pos[tid] = off + eqb;
-      P.rowslot[less + eqb] = tid;
-      if (eqb == 0) {
-        P.act_e[aidx] = my;
-        P.act_cnt[aidx] = cnt;
-        P.act_start[aidx] = less;
-        P.act_off[aidx] = off;
+    int cr = ci - c, ar = nai - na, pr = poi - po;
+    for (int e = e0; e < e1; ++e) {
+      const int v = cnt[e];
+      less[e] = cr;
+      poff[e] = pr;
+      if (v > 0) {
+        P.act_e[ar] = e;
+        P.act_cnt[ar] = v;
+        P.act_start[ar] = cr;
+        P.act_off[ar] = pr;
+        ++ar;
       }
+      cr += v;
+      pr += round_up(v, a.BS);
+    }
+    if (lane == 31) {
+      P.hdr[kHdrA] = nai;
+      P.hdr[kHdrTotal] = poi;
+      P.hdr[kHdrBad] = bad;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int key = P.key[i];
+    if (key == kNoKey) {
+      P.pos[i] = -1;
     } else {
-      P.pos[tid] = -1;
+      const int rank = P.pos[i];
+      P.pos[i] = poff[key] + rank;
+      P.rowslot[less[key] + rank] = i;
     }
-  }
-  const int A = __syncthreads_count(tid < n && my != kNoKey && eqb == 0);
-  const int bad = __syncthreads_count(tid < n && my == kNoKey);
-  if (tid == 0) {
-    P.hdr[kHdrA] = A;
-    P.hdr[kHdrBad] = bad;
-    P.hdr[kHdrTotal] = A > 0 ? P.act_off[A - 1] + round_up(P.act_cnt[A - 1], a.BS) : 0;
   }
   __syncthreads();
 }
 
 // The routing and alignment tables in the workspace, as moe_topk_softmax and
-// moe_align write them.  Run by the first nt threads of the CTA.
-__device__ void write_tables(const Plan &P, const FusedArgs &a, int nt) {
-  const int tid = threadIdx.x, n = a.n;
+// moe_align write them; thread tid of nt (over the whole grid: every CTA
+// holds the same plan).
+__device__ void write_tables(const Plan &P, const FusedArgs &a, int tid, int nt) {
+  const int n = a.n;
   const int A = P.hdr[kHdrA], total = P.hdr[kHdrTotal];
   if (a.logits)
     for (int i = tid; i < n; i += nt) {
@@ -265,71 +317,144 @@ __device__ void write_tables(const Plan &P, const FusedArgs &a, int nt) {
 }
 
 // ---------------------------------------------------------------------------
-// units of 16 weights
+// the stage walk: the same sequence for the producer and the consumers
 // ---------------------------------------------------------------------------
 
-template <int FMT>
-struct Unit {
-  static constexpr int kBytes = FMT == MOE_FMT_FP8_B128 ? 16 : 8;
+struct Stage {
+  int seg;        // 0 routed, 1 shared
+  int ai;         // active index (routed), -1 shared
+  int e;          // expert id (0 for the shared expert)
+  int x0, xn;     // activation rows [x0, x0 + xn) of the expert
+  int tg, nt;     // first tile within the expert, tiles in this group
+  int kp;         // K part
+  bool new_rows;  // first stage of (expert, x0): stage its activation rows
 };
 
-__host__ __device__ inline size_t row_bytes(int fmt, int K) {
-  return fmt == MOE_FMT_FP8_B128 ? (size_t)K : (size_t)K / 2;
-}
-
-// 16 weights (one unit in shared memory) -> 8 f16x2 registers, exact.
-template <int FMT>
-__device__ __forceinline__ void unit_f16(const uint8_t *src, uint32_t (&wh)[8]) {
-  if constexpr (FMT == MOE_FMT_FP8_B128) {
-    const uint4 q = *reinterpret_cast<const uint4 *>(src);
-    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      wh[2 * i] = e4m3x2_to_f16x2((uint16_t)(wd[i] & 0xFFFFu));
-      wh[2 * i + 1] = e4m3x2_to_f16x2((uint16_t)(wd[i] >> 16));
+// The CTA's stages of one projection: its share of the routed tile list (all
+// active experts' tiles, expert-major), then its share of the shared expert's
+// tiles; per expert, row passes of kRows rows, tile groups of mt tiles, K
+// parts.  fn(Stage) is called for each.
+template <class Fn>
+__device__ __forceinline__ void walk(const FusedArgs &a, const Plan &P, int A, int phase, Fn &&fn) {
+  for (int seg = 0; seg < 2; ++seg) {
+    if (seg == 1 && !a.has_shared) break;
+    const PGeo &g = a.geo[phase][seg];
+    const int RT = g.R / 16;
+    const long long T = seg == 0 ? (long long)A * RT : RT;
+    const long long t1 = T * (blockIdx.x + 1) / gridDim.x;
+    long long t = T * blockIdx.x / gridDim.x;
+    while (t < t1) {
+      const int ai = seg == 0 ? (int)(t / RT) : -1;
+      const int et0 = (int)(t % RT);
+      const long long ebase = t - et0;
+      const int et1 = (int)min((long long)RT, t1 - ebase);
+      const int rows = seg == 0 ? P.act_cnt[ai] : a.M;
+      const int e = seg == 0 ? P.act_e[ai] : 0;
+      for (int x0 = 0; x0 < rows; x0 += kRows)
+        for (int tg = et0; tg < et1; tg += g.mt)
+          for (int kp = 0; kp < g.nkp; ++kp) {
+            Stage st;
+            st.seg = seg;
+            st.ai = ai;
+            st.e = e;
+            st.x0 = x0;
+            st.xn = min(kRows, rows - x0);
+            st.tg = tg;
+            st.nt = min(g.mt, et1 - tg);
+            st.kp = kp;
+            st.new_rows = tg == et0 && kp == 0;
+            fn(st);
+          }
+      t = ebase + et1;
     }
-  } else {
-    const uint2 q = *reinterpret_cast<const uint2 *>(src);
-    const uint32_t wd[2] = {q.x, q.y};
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) wh[4 * i + b] = e2m1x2_to_f16x2((wd[i] >> (8 * b)) & 0xFFu);
   }
 }
 
-// w . x over 16 elements (x as two uint4 of f16): exact f16 x f16 products
-// accumulated in fp32; even elements and odd elements in two chains, added at
-// the end.
-__device__ __forceinline__ float dot16_mixed(const uint32_t (&w)[8], const uint4 &x0,
-                                             const uint4 &x1) {
-  const uint32_t x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-  float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    asm("{\n\t.reg .f16 wl, wh, xl, xh;\n\t"
-        "mov.b32 {wl, wh}, %2;\n\t"
-        "mov.b32 {xl, xh}, %3;\n\t"
-        "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
-        "fma.rn.f32.f16 %1, wh, xh, %1;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "r"(w[i]), "r"(x[i]));
-  return a0 + a1;
+// ---------------------------------------------------------------------------
+// producer
+// ---------------------------------------------------------------------------
+
+// One box of a 3-D tensor map (x: bytes within a 128-byte column block,
+// y: row, z: column block) into shared memory.
+__device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                       uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
+      "l"(policy)
+      : "memory");
 }
 
-// w . h over 16 elements: weights decoded to fp32, fp32 fma, even and odd
-// elements in two chains.
-__device__ __forceinline__ float dot16_f32(const uint32_t (&w)[8], const float4 (&hv)[4]) {
-  const float h[16] = {hv[0].x, hv[0].y, hv[0].z, hv[0].w, hv[1].x, hv[1].y, hv[1].z, hv[1].w,
-                       hv[2].x, hv[2].y, hv[2].z, hv[2].w, hv[3].x, hv[3].y, hv[3].z, hv[3].w};
-  float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float2 f = f16x2_to_float2(w[i]);
-    a0 = fmaf(f.x, h[2 * i], a0);
-    a1 = fmaf(f.y, h[2 * i + 1], a1);
-  }
-  return a0 + a1;
+// Stream one projection's stages into the ring, continuing the stage counter
+// s.  False when a wait gave up.
+template <int RF, int SF>
+__device__ bool produce(const FusedArgs &a, const Maps &maps, uint8_t *ring, uint64_t *full,
+                        uint64_t *empty, const Plan &P, int A, int phase, int &s,
+                        uint64_t pol) {
+  const int kMats = phase == 0 ? 2 : 1;
+  bool ok = true;
+  walk(a, P, A, phase, [&](const Stage &st) {
+    if (!ok) return;
+    const int slot = s % a.stages;
+    if (!mbar_wait(&empty[slot], ((uint32_t)(s / a.stages) & 1u) ^ 1u)) {
+      ok = false;
+      return;
+    }
+    const PGeo &g = a.geo[phase][st.seg];
+    const bool f4 = (st.seg == 0 ? RF : SF) == MOE_FMT_NVFP4_G16;
+    const int boxes = g.kr >> 1;
+    const uint32_t bytes =
+        (uint32_t)(kMats * st.nt * boxes * (kBoxBytes + (f4 ? kSBoxBytes : 0)));
+    mbar_expect_tx(&full[slot], bytes);
+    uint8_t *dst = ring + (size_t)slot * a.slot_bytes;
+    for (int m = 0; m < kMats; ++m) {
+      const int proj = phase == 0 ? m : 2;
+      const CUtensorMap *cm = &maps.m[st.seg][proj][0];
+      const CUtensorMap *sm = &maps.m[st.seg][proj][1];
+      // one copy per tile: 16 rows x kr/2 column blocks of 128 bytes (and
+      // of 16 scale bytes), column block b at b * 16 rows
+      for (int i = 0; i < st.nt; ++i) {
+        const int row = st.e * g.R + (st.tg + i) * 16;
+        const int blk = (m * g.mt + i) * boxes;
+        tma_3d(dst + (size_t)blk * kBoxBytes, cm, 0, row, st.kp * boxes, &full[slot], pol);
+        if (f4)
+          tma_3d(dst + g.code_bytes + (size_t)blk * kSBoxBytes, sm, 0, row, st.kp * boxes,
+                 &full[slot], pol);
+      }
+    }
+    ++s;
+  });
+  return ok;
+}
+
+// ---------------------------------------------------------------------------
+// consumers: MMA over a stage
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) {
+  return *reinterpret_cast<const uint4 *>(p);
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -342,391 +467,390 @@ __device__ __forceinline__ float pow2f(int e) {
   return __uint_as_float((uint32_t)(127 + e) << 23);
 }
 
-// Sum over the lg consecutive lanes of a group (xor butterfly, fixed order).
-__device__ __forceinline__ float group_sum(float v, int lg) {
-  for (int d = lg >> 1; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-  return v;
-}
-
-// ---------------------------------------------------------------------------
-// the engine
-// ---------------------------------------------------------------------------
-
-// Lanes that share one weight row: the row's K/16 units of 16 elements are
-// dealt round-robin to them (K is a multiple of 128, so K/16 is a multiple
-// of 8).
-__host__ __device__ inline int lanes_per_row(int K) {
-  const int units = K / 16;
-  return units % 32 == 0 ? 32 : units % 16 == 0 ? 16 : 8;
-}
-
-// Rows of one matrix per lane-group round: consumer warps x (32 / lanes_per_row).
-__host__ __device__ inline int stage_feats(int K) { return kCW * (32 / lanes_per_row(K)); }
-
-// A stage: features [o0, o0 + r) of one expert's projection(s).
-struct Stage {
-  int a, o0, r;   // active index (-1: shared expert), first feature, features
+// 16-byte activation pieces per lane per half-chunk: FP8 16 inputs (2), NVFP4
+// 32 inputs (4).
+template <int FMT>
+struct Frag {
+  static constexpr int kQ = FMT == MOE_FMT_FP8_B128 ? 2 : 4;
 };
 
-// The CTA's stages: its share of the routed (expert, feature) list, then its
-// share of the shared expert's features.
-struct Iter {
-  long long f, f1, sf, sf1;
-  int R, fs, fss;
-  __device__ bool next(Stage &st) {
-    if (f < f1) {
-      st.a = (int)(f / R);
-      st.o0 = (int)(f % R);
-      st.r = (int)min((long long)fs, min(f1 - f, (long long)(R - st.o0)));
-      f += st.r;
-      return true;
-    }
-    if (sf < sf1) {
-      st.a = -1;
-      st.o0 = (int)sf;
-      st.r = (int)min((long long)fss, sf1 - sf);
-      sf += st.r;
-      return true;
-    }
-    return false;
-  }
-};
-
-__device__ __forceinline__ Iter make_iter(int A, int R, int Rs, int fs, int fss) {
-  Iter it;
-  const long long T = (long long)A * R;
-  it.f = T * blockIdx.x / gridDim.x;
-  it.f1 = T * (blockIdx.x + 1) / gridDim.x;
-  it.sf = (long long)Rs * blockIdx.x / gridDim.x;
-  it.sf1 = (long long)Rs * (blockIdx.x + 1) / gridDim.x;
-  it.R = R;
-  it.fs = fs;
-  it.fss = fss;
-  return it;
+// Index (in 16-byte units) of activation piece q of lane (g, t) in half-chunk
+// hc.  The pieces a warp reads together are 512 contiguous bytes.
+__device__ __forceinline__ int xs_unit(int hc, int q, int g, int t, int kQ) {
+  return ((hc * kQ + q) * 8 + g) * 4 + t;
 }
 
-// One lane group's dot products for NR staged activation rows (r0 .. r0+NR)
-// against weight row f of the stage (gate+up: gate row f and up row F + f).
-// Lane j of the group takes units j, j + lpr, ...; per unit the weights are
-// decoded once and used for every row; the unit's scale multiplies its
-// partial sum; the group's lanes are then summed by an xor butterfly.  The
-// order of every sum is fixed and independent of NR.
-template <bool GATE_UP, int FMT, int NR>
-__device__ __forceinline__ void row_pass(const uint8_t *stage, int F, int Kb, int K, int lpr,
-                                         int upl, const uint8_t *xs, int r0, int f, int j,
-                                         bool live, int o0, const float *bscale, float (&acc0)[4],
-                                         float (&acc1)[4]) {
-  const int U = K / 16;
+// Tile rows in MMA-row order: MMA rows 2p and 2p+1 sit in tile rows p and
+// p + 4, whose 128-byte-swizzled pieces fall in opposite bank halves.
+__device__ __forceinline__ int tile_row(int mrow) {
+  const int lo = mrow & 7;
+  return ((lo >> 1) | ((lo & 1) << 2)) + (mrow & 8);
+}
+
+// One warp's item of a stage: tile ti, half-chunks [hl0, hl0 + CPW) of the
+// stage (global half-chunk hg0 + ...).  The item's weight pieces are loaded
+// into registers first and the stage released (empty barrier) before any
+// MMA, so the slot refills while the warp computes.  acc[m] accumulates
+// matrix m's 16 x 8 tile.  FP8: sc[m][0], sc[m][1] are the block scales of
+// the 128-input blocks hg0 / 2 and hg0 / 2 + 1 (CPW <= 2 spans at most two).
+template <bool GU, int FMT, int CPW>
+__device__ __forceinline__ void stage_mma(const uint8_t *stage, uint64_t *empty, const PGeo &g,
+                                          int ti, int hl0, int hg0, const uint4 *xs_hi,
+                                          const uint4 *xs_lo, bool xrow, const float (&sc)[2][2],
+                                          float (&acc)[2][4]) {
+  constexpr int kMats = GU ? 2 : 1;
+  constexpr int kQ = Frag<FMT>::kQ;
+  const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
+  const int ra = tile_row(gq);   // tile rows of MMA rows gq and gq + 8: ra, ra + 8
+  const int boxes = g.kr >> 1;
+  uint4 wa[CPW][kMats], wb[CPW][kMats];
+  uint32_t s_a[CPW][kMats], s_b[CPW][kMats];
 #pragma unroll
-  for (int r = 0; r < 4; ++r) acc0[r] = acc1[r] = 0.f;
-  if (live) {
-    const uint8_t *s16 = stage + (size_t)(GATE_UP ? 2 : 1) * F * Kb;
-#pragma unroll 4
-    for (int u = 0; u < upl; ++u) {
-      const int c = j + u * lpr;
-      uint32_t wa[8], wb[8];
-      unit_f16<FMT>(stage + (size_t)f * Kb + (size_t)c * Unit<FMT>::kBytes, wa);
-      float sa, sb = 0.f;
+  for (int c = 0; c < CPW; ++c) {
+    const int hl = hl0 + c, b = hl >> 1, half = hl & 1;
+    const int u = (((half << 2) | t) ^ (ra & 7)) << 4;   // swizzled byte offset in the row
+#pragma unroll
+    for (int m = 0; m < kMats; ++m) {
+      const int blk = (m * g.mt + ti) * boxes + b;
+      const uint8_t *box = stage + (size_t)blk * kBoxBytes;
+      wa[c][m] = lds128(box + ra * 128 + u);
+      wb[c][m] = lds128(box + (ra + 8) * 128 + u);
+      if constexpr (FMT == MOE_FMT_NVFP4_G16) {
+        const uint8_t *sbox = stage + g.code_bytes + (size_t)blk * kSBoxBytes;
+        s_a[c][m] = *reinterpret_cast<const uint16_t *>(sbox + ra * 16 + half * 8 + 2 * t);
+        s_b[c][m] = *reinterpret_cast<const uint16_t *>(sbox + (ra + 8) * 16 + half * 8 + 2 * t);
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty);   // the stage is in registers
+#pragma unroll
+  for (int c = 0; c < CPW; ++c) {
+    const int hg = hg0 + c;
+    uint4 xh[kQ], xl[kQ];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      xh[q] = make_uint4(0, 0, 0, 0);
+      xl[q] = make_uint4(0, 0, 0, 0);
+      if (xrow) {
+        xh[q] = xs_hi[xs_unit(hg, q, gq, t, kQ)];
+        if (!GU) xl[q] = xs_lo[xs_unit(hg, q, gq, t, kQ)];
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < kMats; ++m) {
+      const uint32_t wa4[4] = {wa[c][m].x, wa[c][m].y, wa[c][m].z, wa[c][m].w};
+      const uint32_t wb4[4] = {wb[c][m].x, wb[c][m].y, wb[c][m].z, wb[c][m].w};
       if constexpr (FMT == MOE_FMT_FP8_B128) {
-        sa = bscale[((o0 + f) / 128) * (K / 128) + c / 8];
-        if (GATE_UP) sb = bscale[256 + ((o0 + f) / 128) * (K / 128) + c / 8];
-      } else {
-        sa = e4m3_to_float(s16[(size_t)f * (K / 16) + c]);
-        if (GATE_UP) sb = e4m3_to_float(s16[(size_t)(F + f) * (K / 16) + c]);
-      }
-      if constexpr (GATE_UP) {
-        unit_f16<FMT>(stage + (size_t)(F + f) * Kb + (size_t)c * Unit<FMT>::kBytes, wb);
+        // 16 inputs per row: MMA j takes inputs 4j .. 4j+3 of the lane's span
+        float tmp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          const uint4 *xp = reinterpret_cast<const uint4 *>(xs) + (size_t)(r0 + r) * 2 * U + c;
-          const uint4 x0 = xp[0], x1 = xp[U];
-          acc0[r] = fmaf(dot16_mixed(wa, x0, x1), sa, acc0[r]);
-          acc1[r] = fmaf(dot16_mixed(wb, x0, x1), sb, acc1[r]);
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(wa4[j] & 0xFFFFu));
+          const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(wb4[j] & 0xFFFFu));
+          const uint32_t a2 = e4m3x2_to_f16x2((uint16_t)(wa4[j] >> 16));
+          const uint32_t a3 = e4m3x2_to_f16x2((uint16_t)(wb4[j] >> 16));
+          const uint4 &xq = xh[j >> 1];
+          mma16816(tmp, a0, a1, a2, a3, (j & 1) ? xq.z : xq.x, (j & 1) ? xq.w : xq.y);
+          if (!GU) {
+            const uint4 &lq = xl[j >> 1];
+            mma16816(tmp, a0, a1, a2, a3, (j & 1) ? lq.z : lq.x, (j & 1) ? lq.w : lq.y);
+          }
         }
-      } else {
+        const float sk = ((hg >> 1) != (hg0 >> 1)) ? sc[m][1] : sc[m][0];
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          const float4 *hp = reinterpret_cast<const float4 *>(xs) + (size_t)(r0 + r) * 4 * U + c;
-          const float4 hv[4] = {hp[0], hp[U], hp[2 * U], hp[3 * U]};
-          acc0[r] = fmaf(dot16_f32(wa, hv), sa, acc0[r]);
+        for (int r = 0; r < 4; ++r) acc[m][r] = fmaf(tmp[r], sk, acc[m][r]);
+      } else {
+        // 32 inputs per row in two 16-input groups, each with its E4M3 scale
+        const uint32_t sA = e4m3x2_to_f16x2((uint16_t)s_a[c][m]);
+        const uint32_t sB = e4m3x2_to_f16x2((uint16_t)s_b[c][m]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t sa = prmt(sA, sA, j < 4 ? 0x1010u : 0x3232u);
+          const uint32_t sb = prmt(sB, sB, j < 4 ? 0x1010u : 0x3232u);
+          const int sh = (j & 1) * 16;
+          const uint32_t wA = wa4[j >> 1] >> sh, wB = wb4[j >> 1] >> sh;
+          const uint32_t a0 = hmul2(e2m1x2_to_f16x2(wA & 0xFFu), sa);
+          const uint32_t a1 = hmul2(e2m1x2_to_f16x2(wB & 0xFFu), sb);
+          const uint32_t a2 = hmul2(e2m1x2_to_f16x2((wA >> 8) & 0xFFu), sa);
+          const uint32_t a3 = hmul2(e2m1x2_to_f16x2((wB >> 8) & 0xFFu), sb);
+          const uint4 &xq = xh[j >> 1];
+          mma16816(acc[m], a0, a1, a2, a3, (j & 1) ? xq.z : xq.x, (j & 1) ? xq.w : xq.y);
+          if (!GU) {
+            const uint4 &lq = xl[j >> 1];
+            mma16816(acc[m], a0, a1, a2, a3, (j & 1) ? lq.z : lq.x, (j & 1) ? lq.w : lq.y);
+          }
         }
       }
     }
   }
-#pragma unroll
-  for (int r = 0; r < NR; ++r) {
-    acc0[r] = group_sum(acc0[r], lpr);
-    if (GATE_UP) acc1[r] = group_sum(acc1[r], lpr);
-  }
 }
 
-// Shared-memory carve-up of the layer kernel.
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
 struct Smem {
   uint8_t *ring;
   uint64_t *full, *empty;
   Plan P;
-  float *bscale;    // FP8 block scales of the current expert [2][256]
-  uint32_t *xmax;   // [kXS] staged-row |x| maxima
-  int *xexp;        // [kXS] their f16 exponents
-  int *misc;        // [64] tile counts / flags
-  uint8_t *xs;      // [kXS] staged activation rows
+  uint8_t *xs;      // staged activation rows (permuted f16 pieces)
+  uint32_t *xmax;   // [kRows] row |max| bits
+  int *xexp;        // [kRows] row power-of-two exponents
+  float4 *red;      // [2][kCW][32] partial tiles
+  float *bsc;       // [2][256] FP8 block scales of the staged expert's matrices
+  float *gsc;       // [4] NVFP4 global scales of the staged expert's matrices
+  int *misc;        // [64] flags
 };
 
-__host__ __device__ inline size_t xs_bytes(int H, int kd_max) {
-  const size_t g = (size_t)kXS * H * 2, d = (size_t)kXS * kd_max * 4;
-  return g > d ? g : d;
+__host__ __device__ inline size_t fixed_smem(int n, int xs_row_bytes) {
+  return plan_bytes(n) + (size_t)kRows * xs_row_bytes + 2 * kRows * 4 +
+         (size_t)2 * kCW * 32 * 16 + (2 * 256 + 4) * 4 + 64 * 4;
 }
 
-__device__ __forceinline__ Smem carve(uint8_t *smem, const FusedArgs &a, int kd_max) {
+__device__ __forceinline__ Smem carve(uint8_t *smem, const FusedArgs &a) {
   Smem S;
-  size_t o = 0;
-  S.ring = smem;
-  o += (size_t)a.stages * a.slot_bytes;
-  S.full = reinterpret_cast<uint64_t *>(smem + o);
+  // the 128-byte swizzle of the code boxes wants 1024-byte aligned boxes
+  const uint32_t base = smem_addr(smem);
+  uint8_t *p = smem + ((1024u - (base & 1023u)) & 1023u);
+  S.ring = p;
+  p += (size_t)a.stages * a.slot_bytes;
+  S.full = reinterpret_cast<uint64_t *>(p);
   S.empty = S.full + a.stages;
-  o += 16 * (size_t)a.stages;
-  S.P = carve_plan(smem + o, a.n);
-  o += plan_bytes(a.n);
-  S.bscale = reinterpret_cast<float *>(smem + o);
-  o += 2 * 256 * 4;
-  S.xmax = reinterpret_cast<uint32_t *>(smem + o);
-  S.xexp = reinterpret_cast<int *>(S.xmax + kXS);
-  S.misc = S.xexp + kXS;
-  o += (2 * kXS + 64) * 4;
-  S.xs = smem + o;
-  (void)kd_max;
+  p += 16 * (size_t)a.stages;
+  S.P = carve_plan(p, a.n);
+  p += plan_bytes(a.n);
+  S.xs = p;
+  p += (size_t)kRows * a.xs_row_bytes;
+  S.xmax = reinterpret_cast<uint32_t *>(p);
+  S.xexp = reinterpret_cast<int *>(S.xmax + kRows);
+  p += 2 * kRows * 4;
+  S.red = reinterpret_cast<float4 *>(p);
+  p += (size_t)2 * kCW * 32 * 16;
+  S.bsc = reinterpret_cast<float *>(p);
+  S.gsc = S.bsc + 2 * 256;
+  p += (2 * 256 + 4) * 4;
+  S.misc = reinterpret_cast<int *>(p);
   return S;
 }
 
-// Geometry of one phase's stage for a projection with K inputs.
-struct Geo {
-  int K, U, Kb, lpr, upl, rpw, fu, F;   // fu: features per lane-group round; F = rounds * fu
-};
-
-__device__ __forceinline__ Geo geo(int fmt, int K, int rounds) {
-  Geo g;
-  g.K = K;
-  g.U = K / 16;
-  g.Kb = (int)row_bytes(fmt, K);
-  g.lpr = lanes_per_row(K);
-  g.upl = g.U / g.lpr;
-  g.rpw = 32 / g.lpr;
-  g.fu = kCW * g.rpw;
-  g.F = rounds * g.fu;
-  return g;
+// The power-of-two exponent s of a row whose largest |value| has exponent
+// field exp_field (fp32 layout): |values| * 2^-s < 2^15, the largest in
+// [2^14, 2^15).
+__device__ __forceinline__ int row_shift(uint32_t exp_field) {
+  const int s = (int)exp_field - 127 - 14;
+  return max(-100, min(100, s));
 }
 
-// Producer: stream one phase's stages into the ring, continuing the stage
-// counter s.  False when a wait gave up.
-template <bool GATE_UP, int RF, int SF>
-__device__ bool produce(const FusedArgs &a, const Smem &S, int A, int &s, uint64_t pol) {
-  constexpr int kMats = GATE_UP ? 2 : 1;
-  const int p = GATE_UP ? 0 : 1;
-  const int Kr = GATE_UP ? a.H : a.r.I, Ks = a.has_shared ? (GATE_UP ? a.H : a.s.I) : 0;
-  const Geo gr = geo(RF, Kr, a.rounds[p][0]);
-  const Geo gs = geo(SF, a.has_shared ? Ks : 256, a.rounds[p][1]);
-  const int R = GATE_UP ? a.r.I : a.H, Rs = a.has_shared ? (GATE_UP ? a.s.I : a.H) : 0;
-  Iter it = make_iter(A, R, Rs, gr.F, gs.F);
-  Stage st;
-  while (it.next(st)) {
-    const int slot = s % a.stages;
-    if (!mbar_wait(&S.empty[slot], ((uint32_t)(s / a.stages) & 1u) ^ 1u)) return false;
-    const bool sh = st.a < 0;
-    const Exp &X = sh ? a.s : a.r;
-    const int fmt = sh ? SF : RF;
-    const Geo &g = sh ? gs : gr;
-    const int e = sh ? 0 : S.P.act_e[st.a];
-    const int rows = GATE_UP ? X.I : a.H;   // rows of each matrix
-    const uint32_t wbytes = (uint32_t)(st.r * g.Kb);
-    const uint32_t sbytes = fmt == MOE_FMT_NVFP4_G16 ? (uint32_t)(st.r * (g.K / 16)) : 0u;
-    uint8_t *dst = S.ring + (size_t)slot * a.slot_bytes;
-    mbar_expect_tx(&S.full[slot], kMats * (wbytes + sbytes));
-#pragma unroll
-    for (int m = 0; m < kMats; ++m) {
-      const Proj &Pj = GATE_UP ? (m == 0 ? X.gate : X.up) : X.down;
-      bulk_g2s(dst + (size_t)m * g.F * g.Kb, Pj.codes + ((size_t)e * rows + st.o0) * g.Kb,
-               wbytes, &S.full[slot], pol);
-      if (sbytes)
-        bulk_g2s(dst + (size_t)kMats * g.F * g.Kb + (size_t)m * g.F * (g.K / 16),
-                 reinterpret_cast<const uint8_t *>(Pj.scale) + ((size_t)e * rows + st.o0) * (g.K / 16),
-                 sbytes, &S.full[slot], pol);
-    }
-    ++s;
-  }
-  return true;
-}
-
-// Consumers: one phase's stages, continuing the stage counter s.
-template <bool GATE_UP, int RF, int SF>
-__device__ void consume(const FusedArgs &a, const Smem &S, int A, int &s, bool &failed) {
-  constexpr int kMats = GATE_UP ? 2 : 1;
-  const int p = GATE_UP ? 0 : 1;
+// Stage activation rows [x0, x0 + xn) of the stage's expert as permuted f16
+// pieces.  gate+up: bf16 x rows; down: fp32 h rows as hi + lo.  All consumer
+// threads.
+template <bool GU, int FMT>
+__device__ void stage_rows(const FusedArgs &a, const Smem &S, const Stage &st, const PGeo &g) {
+  constexpr int kQ = Frag<FMT>::kQ;
+  constexpr int kMats = GU ? 2 : 1;
+  const int K = g.K;
+  const int tid = threadIdx.x;
   const Plan &P = S.P;
+  // the expert's scales, read once here rather than per stage
+  const Exp &X = st.seg == 0 ? a.r : a.s;
+  if constexpr (FMT == MOE_FMT_FP8_B128) {
+    const int nb = (g.R / 128) * (K / 128);   // <= 16 x 16
+#pragma unroll
+    for (int m = 0; m < kMats; ++m)
+      for (int v = tid; v < nb; v += kCThreads)
+        S.bsc[m * 256 + v] = __ldg(X.bscale[GU ? m : 2] + (size_t)st.e * nb + v);
+  } else {
+    if (tid < kMats) S.gsc[tid] = __ldg(X.glob[GU ? tid : 2] + st.e);
+  }
+  if (tid < kRows) S.xmax[tid] = 0u;
+  named_sync(kCThreads);
+  const int upr = K / 8;                 // 8-input units per row
+  const int units = st.xn * upr;
+  // pass 1: the rows' largest |value| (the loads are repeated in pass 2,
+  // from L2, rather than held in registers)
+  for (int v = tid; v < units; v += kCThreads) {
+    const int r = v / upr, k8 = (v % upr) * 8;
+    uint32_t mx = 0;
+    if (GU) {
+      const int tok = st.seg == 0 ? P.rowslot[P.act_start[st.ai] + st.x0 + r] / a.k : st.x0 + r;
+      const uint4 q4 = __ldcg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * a.H + k8));
+      const uint32_t wd[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) mx = max(mx, max((wd[q] & 0x7FFFu) << 16, wd[q] & 0x7FFF0000u));
+    } else {
+      const float *src = st.seg == 0 ? a.h + (size_t)(P.act_off[st.ai] + st.x0 + r) * K
+                                     : a.h_sh + (size_t)(st.x0 + r) * K;
+      const uint4 q0 = __ldcg(reinterpret_cast<const uint4 *>(src + k8));
+      const uint4 q1 = __ldcg(reinterpret_cast<const uint4 *>(src + k8 + 4));
+      const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx = max(mx, wd[q] & 0x7FFFFFFFu);
+    }
+    atomicMax(&S.xmax[r], mx);
+  }
+  named_sync(kCThreads);
+  if (tid < st.xn) S.xexp[tid] = row_shift((S.xmax[tid] >> 23) & 0xFFu);
+  named_sync(kCThreads);
+  uint4 *xs_hi = reinterpret_cast<uint4 *>(S.xs);
+  uint4 *xs_lo = xs_hi + (size_t)kRows * K / 8;
+  for (int v = tid; v < units; v += kCThreads) {
+    const int r = v / upr, k = (v % upr) * 8;
+    const float m = pow2f(-S.xexp[r]);
+    float f[8];
+    if (GU) {
+      const int tok = st.seg == 0 ? P.rowslot[P.act_start[st.ai] + st.x0 + r] / a.k : st.x0 + r;
+      const uint4 q4 = __ldcg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * a.H + k));
+      const uint32_t wd[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        f[2 * q] = __uint_as_float(wd[q] << 16) * m;
+        f[2 * q + 1] = __uint_as_float(wd[q] & 0xFFFF0000u) * m;
+      }
+    } else {
+      const float *src = st.seg == 0 ? a.h + (size_t)(P.act_off[st.ai] + st.x0 + r) * K
+                                     : a.h_sh + (size_t)(st.x0 + r) * K;
+      const uint4 q0 = __ldcg(reinterpret_cast<const uint4 *>(src + k));
+      const uint4 q1 = __ldcg(reinterpret_cast<const uint4 *>(src + k + 4));
+      const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(wd[q]) * m;
+    }
+    // piece (hc, q, t) of row r: 8 inputs starting at k
+    const int span = 8 * kQ;                      // inputs per lane per half-chunk
+    const int hc = k / (4 * span), t = (k / span) & 3, q = (k / 8) % kQ;
+    const int unit = xs_unit(hc, q, r, t, kQ);
+    uint4 hv;
+    hv.x = pack_f16x2(f[0], f[1]);
+    hv.y = pack_f16x2(f[2], f[3]);
+    hv.z = pack_f16x2(f[4], f[5]);
+    hv.w = pack_f16x2(f[6], f[7]);
+    xs_hi[unit] = hv;
+    if (!GU) {
+      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+      uint32_t lw[4];
+#pragma unroll
+      for (int q2 = 0; q2 < 4; ++q2) {
+        const float2 hf = f16x2_to_float2(hw[q2]);
+        lw[q2] = pack_f16x2(f[2 * q2] - hf.x, f[2 * q2 + 1] - hf.y);
+      }
+      xs_lo[unit] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+  }
+  named_sync(kCThreads);
+}
+
+// One projection's stages on the consumer side, continuing the stage counter s.
+template <bool GU, int RF, int SF>
+__device__ void consume(const FusedArgs &a, const Smem &S, int A, int &s, bool &failed) {
+  constexpr int kMats = GU ? 2 : 1;
+  const int phase = GU ? 0 : 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int Kr = GATE_UP ? a.H : a.r.I, Ks = a.has_shared ? (GATE_UP ? a.H : a.s.I) : 0;
-  const Geo gr = geo(RF, Kr, a.rounds[p][0]);
-  const Geo gs = geo(SF, a.has_shared ? Ks : 256, a.rounds[p][1]);
-  const int R = GATE_UP ? a.r.I : a.H, Rs = a.has_shared ? (GATE_UP ? a.s.I : a.H) : 0;
-  Iter it = make_iter(A, R, Rs, gr.F, gs.F);
-  Stage st;
-  int cur_a = INT_MIN, cur_x0 = -1;
-  uint8_t *xs = S.xs;
-  while (it.next(st)) {
+  const Plan &P = S.P;
+  float acc[2][4];
+  int cur_ai = INT_MIN, cur_seg = -1, cur_x0 = -1;
+  walk(a, P, A, phase, [&](const Stage &st) {
+    const PGeo &g = a.geo[phase][st.seg];
+    const int fmt = st.seg == 0 ? RF : SF;
+    const Exp &X = st.seg == 0 ? a.r : a.s;
     const int slot = s % a.stages;
     const uint32_t par = (uint32_t)(s / a.stages) & 1u;
-    const bool sh = st.a < 0;
-    const Exp &X = sh ? a.s : a.r;
-    const int fmt = sh ? SF : RF;
-    const Geo &g = sh ? gs : gr;
-    const int e = sh ? 0 : P.act_e[st.a];
-    const int K = g.K, U = g.U;
-    const int rows = sh ? a.M : P.act_cnt[st.a];    // activation rows of this expert
-    const int mrows = GATE_UP ? X.I : a.H;          // rows of each weight matrix
-    const int gi = lane / g.lpr, j = lane % g.lpr;
-    bool waited = false;
-    for (int x0 = 0; x0 < rows; x0 += kXS) {
-      const int xn = min(kXS, rows - x0);
-      if (st.a != cur_a || x0 != cur_x0) {
-        // stage rows x0 .. x0+xn of this expert's activations (and, on a new
-        // expert, its FP8 block scales); every consumer warp reaches here
-        named_sync(kCThreads);
-        if (GATE_UP) {
-          // bf16 x rows -> f16 * 2^-s, s from the row's largest |x|, stored
-          // as [row][half][unit] x 16 bytes
-          if (tid < kXS) S.xmax[tid] = 0u;
-          named_sync(kCThreads);
-          uint4 held[kXS];
+    if (st.seg != cur_seg || st.ai != cur_ai || st.x0 != cur_x0) {
+      named_sync(kCThreads);   // nobody still reads the previous rows
+      if (fmt == MOE_FMT_FP8_B128)
+        stage_rows<GU, MOE_FMT_FP8_B128>(a, S, st, g);
+      else
+        stage_rows<GU, MOE_FMT_NVFP4_G16>(a, S, st, g);
+      cur_seg = st.seg;
+      cur_ai = st.ai;
+      cur_x0 = st.x0;
+    }
+    if (st.kp == 0)
 #pragma unroll
-          for (int r = 0; r < kXS; ++r) {
-            const int k8 = tid * 8;
-            held[r] = make_uint4(0, 0, 0, 0);
-            if (r < xn && k8 < K) {
-              const int tok = sh ? x0 + r : P.rowslot[P.act_start[st.a] + x0 + r] / a.k;
-              held[r] = __ldcg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * a.H + k8));
-            }
-            const uint32_t wd[4] = {held[r].x, held[r].y, held[r].z, held[r].w};
-            uint32_t mx = 0;
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mx = max(mx, max(wd[i] & 0x7FFFu, (wd[i] >> 16) & 0x7FFFu));
+        for (int r = 0; r < 4; ++r) acc[m][r] = 0.f;
+    const int ti = warp / g.wpt, wi = warp % g.wpt;
+    const bool active = ti < st.nt;
+    const int hl0 = wi * g.cpw, hg0 = st.kp * g.kr + hl0;
+    float sc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
+    if (active && fmt == MOE_FMT_FP8_B128) {
+      const int nkb = g.K / 128;
+      const int fb = ((st.tg + ti) * 16) / 128, kb = hg0 / 2;
 #pragma unroll
-            for (int d = 16; d > 0; d >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, d));
-            if (lane == 0 && r < xn) atomicMax(&S.xmax[r], mx);
-          }
-          // rows longer than the thread count: the remaining chunks
-          for (int k8 = (tid + kCThreads) * 8; k8 < K; k8 += kCThreads * 8)
-            for (int r = 0; r < xn; ++r) {
-              const int tok = sh ? x0 + r : P.rowslot[P.act_start[st.a] + x0 + r] / a.k;
-              const uint4 q = __ldcg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * a.H + k8));
-              const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
-              uint32_t mx = 0;
-              for (int i = 0; i < 4; ++i) mx = max(mx, max(wd[i] & 0x7FFFu, (wd[i] >> 16) & 0x7FFFu));
-              atomicMax(&S.xmax[r], mx);
-            }
-          named_sync(kCThreads);
-          if (tid < xn) S.xexp[tid] = max(0, (int)((S.xmax[tid] >> 7) & 0xFF) - 127 - 14);
-          for (int k8 = tid * 8; k8 < K; k8 += kCThreads * 8) {
-#pragma unroll
-            for (int r = 0; r < kXS; ++r) {
-              if (r >= xn) break;
-              uint4 q;
-              if (k8 == tid * 8) {
-                q = held[r];
-              } else {
-                const int tok = sh ? x0 + r : P.rowslot[P.act_start[st.a] + x0 + r] / a.k;
-                q = __ldcg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * a.H + k8));
-              }
-              const float m = pow2f(-max(0, (int)((S.xmax[r] >> 7) & 0xFF) - 127 - 14));
-              uint4 hv;
-              hv.x = pack_f16x2(__uint_as_float(q.x << 16) * m, __uint_as_float(q.x & 0xFFFF0000u) * m);
-              hv.y = pack_f16x2(__uint_as_float(q.y << 16) * m, __uint_as_float(q.y & 0xFFFF0000u) * m);
-              hv.z = pack_f16x2(__uint_as_float(q.z << 16) * m, __uint_as_float(q.z & 0xFFFF0000u) * m);
-              hv.w = pack_f16x2(__uint_as_float(q.w << 16) * m, __uint_as_float(q.w & 0xFFFF0000u) * m);
-              const int c = k8 / 16, half = (k8 / 8) & 1;
-              reinterpret_cast<uint4 *>(xs)[((size_t)r * 2 + half) * U + c] = hv;
-            }
-          }
-        } else {
-          // fp32 h rows, stored as [row][quarter][unit] x 16 bytes
-          const float *src = sh ? a.h_sh + (size_t)x0 * K
-                                : a.h + (size_t)(P.act_off[st.a] + x0) * K;
-          for (int v = tid; v < xn * (K / 4); v += kCThreads) {
-            const int r = v / (K / 4), k4 = (v % (K / 4)) * 4;
-            const int c = k4 / 16, qd = (k4 / 4) & 3;
-            reinterpret_cast<float4 *>(xs)[((size_t)r * 4 + qd) * U + c] =
-                __ldcg(reinterpret_cast<const float4 *>(src + (size_t)r * K + k4));
-          }
-        }
-        if (fmt == MOE_FMT_FP8_B128 && st.a != cur_a) {
-          const int nb = (mrows / 128) * (K / 128);
-#pragma unroll
-          for (int m = 0; m < kMats; ++m) {
-            const Proj &Pj = GATE_UP ? (m == 0 ? X.gate : X.up) : X.down;
-            const float *sp = reinterpret_cast<const float *>(Pj.scale) + (size_t)e * nb;
-            for (int v = tid; v < nb; v += kCThreads) S.bscale[m * 256 + v] = __ldg(sp + v);
-          }
-        }
-        named_sync(kCThreads);
-        cur_a = st.a;
-        cur_x0 = x0;
+      for (int m = 0; m < kMats; ++m) {
+        sc[m][0] = S.bsc[m * 256 + fb * nkb + kb];
+        if (kb + 1 < nkb) sc[m][1] = S.bsc[m * 256 + fb * nkb + kb + 1];
       }
-      if (!waited) {
-        if (!failed && !mbar_wait(&S.full[slot], par)) {
-          failed = true;
-          if (a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
-        }
-        waited = true;
-      }
+    }
+    if (!failed && !mbar_wait(&S.full[slot], par)) {
+      failed = true;
+      if (a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
+    }
+    if (active && !failed) {
+      uint64_t *empty = &S.empty[slot];
       const uint8_t *stage = S.ring + (size_t)slot * a.slot_bytes;
-      const float gg = (fmt == MOE_FMT_NVFP4_G16) ? __ldg((GATE_UP ? X.gate : X.down).glob + e) : 1.f;
-      const float gu = (GATE_UP && fmt == MOE_FMT_NVFP4_G16) ? __ldg(X.up.glob + e) : 1.f;
-      for (int q = 0; q < g.F / g.fu; ++q) {   // lane-group rounds of the stage
-        const int f = q * g.fu + warp * g.rpw + gi;   // this lane group's feature
-        const bool go = f < st.r && !failed;
-        if (q * g.fu >= st.r) break;
-        for (int r0 = 0; r0 < xn; r0 += 4) {
-          const int nr = min(4, xn - r0);
-          float acc0[4], acc1[4];
-#define MOE_ROWS(F_, NR)                                                                        \
-  row_pass<GATE_UP, F_, NR>(stage, g.F, g.Kb, K, g.lpr, g.upl, xs, r0, f, j, go, st.o0, S.bscale, \
-                            acc0, acc1)
-          if (fmt == MOE_FMT_FP8_B128) {
-            if (nr == 1) MOE_ROWS(MOE_FMT_FP8_B128, 1);
-            else if (nr == 2) MOE_ROWS(MOE_FMT_FP8_B128, 2);
-            else MOE_ROWS(MOE_FMT_FP8_B128, 4);
-          } else {
-            if (nr == 1) MOE_ROWS(MOE_FMT_NVFP4_G16, 1);
-            else if (nr == 2) MOE_ROWS(MOE_FMT_NVFP4_G16, 2);
-            else MOE_ROWS(MOE_FMT_NVFP4_G16, 4);
-          }
-#undef MOE_ROWS
-          if (j == 0 && go) {
+      const uint4 *xh = reinterpret_cast<const uint4 *>(S.xs);
+      const uint4 *xl = xh + (size_t)kRows * g.K / 8;
+      const bool xrow = (lane >> 2) < st.xn;
+#define MOE_MMA(F_, C_) \
+  stage_mma<GU, F_, C_>(stage, empty, g, ti, hl0, hg0, xh, xl, xrow, sc, acc)
+      // gate+up items are one half-chunk of both matrices; down items one
+      // or two half-chunks of one matrix (a warp's weights in registers)
+      if (fmt == MOE_FMT_FP8_B128) {
+        if (GU || g.cpw == 1) MOE_MMA(MOE_FMT_FP8_B128, 1);
+        else MOE_MMA(MOE_FMT_FP8_B128, GU ? 1 : 2);
+      } else {
+        if (GU || g.cpw == 1) MOE_MMA(MOE_FMT_NVFP4_G16, 1);
+        else MOE_MMA(MOE_FMT_NVFP4_G16, GU ? 1 : 2);
+      }
+#undef MOE_MMA
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[slot]);   // nothing of this stage for this warp
+    }
+    ++s;
+    if (st.kp == g.nkp - 1) {
+      // the group's partial tiles -> shared memory -> fixed-order sums
+      named_sync(kCThreads);   // the previous group's sums are done
+      if (active)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              if (r >= nr) break;
-              const int row = x0 + r0 + r;   // activation row of the expert
-              if (GATE_UP) {
-                const float mx = pow2f(S.xexp[r0 + r]);
-                const float hv = silu_f32(acc0[r] * gg * mx) * (acc1[r] * gu * mx);
-                if (sh)
-                  a.h_sh[(size_t)row * X.I + st.o0 + f] = hv;
-                else
-                  a.h[(size_t)(P.act_off[st.a] + row) * X.I + st.o0 + f] = hv;
-              } else {
-                const float yv = acc0[r] * gg;
-                if (sh)
-                  a.y_sh[(size_t)row * a.H + st.o0 + f] = yv;
-                else
-                  a.y[(size_t)(P.act_off[st.a] + row) * a.H + st.o0 + f] = yv;
-              }
-            }
-          }
+        for (int m = 0; m < kMats; ++m)
+          S.red[(m * kCW + warp) * 32 + lane] =
+              make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+      named_sync(kCThreads);
+      const float g0 = fmt == MOE_FMT_NVFP4_G16 ? S.gsc[0] : 1.f;
+      const float g1 = (GU && fmt == MOE_FMT_NVFP4_G16) ? S.gsc[1] : 1.f;
+      const float *red = reinterpret_cast<const float *>(S.red);
+      for (int o = tid; o < st.nt * 128; o += kCThreads) {
+        const int i = o >> 7, mr = (o >> 3) & 15, n = o & 7;
+        if (n >= st.xn) continue;
+        const int ln = 4 * (mr & 7) + (n >> 1), rg = ((mr >> 3) << 1) | (n & 1);
+        float v0 = 0.f, v1 = 0.f;
+        for (int w2 = 0; w2 < g.wpt; ++w2) {
+          const int wv = i * g.wpt + w2;
+          v0 += red[((0 * kCW + wv) * 32 + ln) * 4 + rg];
+          if (GU) v1 += red[((1 * kCW + wv) * 32 + ln) * 4 + rg];
+        }
+        const float mx = pow2f(S.xexp[n]);
+        const int feat = (st.tg + i) * 16 + tile_row(mr);
+        const int row = st.x0 + n;
+        if (GU) {
+          const float hv = silu_f32(v0 * mx * g0) * (v1 * mx * g1);
+          if (st.seg == 0)
+            a.h[(size_t)(P.act_off[st.ai] + row) * X.I + feat] = hv;
+          else
+            a.h_sh[(size_t)row * X.I + feat] = hv;
+        } else {
+          const float yv = v0 * mx * g0;
+          if (st.seg == 0)
+            a.y[(size_t)(P.act_off[st.ai] + row) * a.H + feat] = yv;
+          else
+            a.y_sh[(size_t)row * a.H + feat] = yv;
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[slot]);   // this warp is done with the stage
-    ++s;
-  }
+  });
 }
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
@@ -762,9 +886,10 @@ __device__ bool grid_barrier(unsigned long long *ctr, int *flag) {
 }
 
 template <int RF, int SF>
-__global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(FusedArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const Smem S = carve(smem, a, 0);
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_layer_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__ Maps maps) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Smem S = carve(smem, a);
   const Plan &P = S.P;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -777,7 +902,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(FusedArgs a) 
     }
     fence_mbar_init();
   }
-  route_local(P, a);
+  // the ring is idle until the producer starts: routing scratch
+  route_local(P, a, reinterpret_cast<int *>(S.ring));
   const int A = P.hdr[kHdrA];
 
   if (warp == kCW) {
@@ -785,8 +911,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(FusedArgs a) 
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int s = 0;
-      bool ok = produce<true, RF, SF>(a, S, A, s, pol);
-      if (ok) ok = produce<false, RF, SF>(a, S, A, s, pol);
+      bool ok = produce<RF, SF>(a, maps, S.ring, S.full, S.empty, P, A, 0, s, pol);
+      if (ok) ok = produce<RF, SF>(a, maps, S.ring, S.full, S.empty, P, A, 1, s, pol);
       if (!ok) {
         if (a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
         for (int q = max(0, s - a.stages); q < s; ++q)   // the last fill of each slot lands
@@ -797,9 +923,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(FusedArgs a) 
   }
 
   // ---------------- consumers ----------------
-  const int ntiles = (a.H + kBlendTile - 1) / kBlendTile;
-  if (blockIdx.x == 0)   // read only after the grid barrier below
-    for (int t = tid; t < ntiles; t += kCThreads) a.tile_cnt[t] = 0;
   int s = 0;
   bool failed = false;
   consume<true, RF, SF>(a, S, A, s, failed);
@@ -809,60 +932,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(FusedArgs a) 
     if (tid == 0 && a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
   }
   consume<false, RF, SF>(a, S, A, s, failed);
+  // every y row is written before any CTA blends
+  if (!grid_barrier(a.grid_ctr, S.misc + 32)) {
+    failed = true;
+    if (tid == 0 && a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
+  }
 
-  // ---------------- blend ----------------
-  int *tiles = S.misc;   // [32]
-  if (A == 0 && !a.has_shared) {   // every slot out of range: the blend is zero
-    const int c0 = (int)((long long)a.H * blockIdx.x / gridDim.x);
-    const int c1 = (int)((long long)a.H * (blockIdx.x + 1) / gridDim.x);
-    for (int t = tid; t < a.M * (c1 - c0); t += kCThreads)
-      a.out[(size_t)(t / (c1 - c0)) * a.H + c0 + t % (c1 - c0)] = 0;
-  } else {
-    // Publish how many (expert, column) pairs of each 64-column tile this CTA
-    // wrote; the CTA whose count completes a tile blends it, in slot order.
-    __threadfence();          // this thread's y writes are visible device-wide
-    if (tid < 32) tiles[tid] = 0;
-    named_sync(kCThreads);
-    if (tid == 0) {
-      const int Ks = a.has_shared ? a.s.I : 256;
-      Iter it2 = make_iter(A, a.H, a.has_shared ? a.H : 0,
-                           geo(RF, a.r.I, a.rounds[1][0]).F, geo(SF, Ks, a.rounds[1][1]).F);
-      Stage s2;
-      while (it2.next(s2))
-        for (int tcol = s2.o0 / kBlendTile; tcol * kBlendTile < s2.o0 + s2.r; ++tcol)
-          tiles[tcol] += min(s2.o0 + s2.r, (tcol + 1) * kBlendTile) - max(s2.o0, tcol * kBlendTile);
-    }
-    named_sync(kCThreads);
-    if (tid < ntiles) {
-      const int mine = tiles[tid];
-      int last = 0;
-      if (mine > 0) {
-        const int width = min(kBlendTile, a.H - tid * kBlendTile);
-        const int target = (A + (a.has_shared ? 1 : 0)) * width;
-        last = atomicAdd(&a.tile_cnt[tid], mine) + mine == target;
-      }
-      __threadfence();
-      tiles[tid] = last;
-    }
-    named_sync(kCThreads);
-    for (int tcol = 0; tcol < ntiles; ++tcol) {
-      if (!tiles[tcol]) continue;
-      const int c0 = tcol * kBlendTile, width = min(kBlendTile, a.H - c0);
-      for (int t = tid; t < a.M * width; t += kCThreads) {
-        const int tok = t / width, cc = c0 + t % width;
-        float acc = 0.f;
-        for (int jj = 0; jj < a.k; ++jj) {
-          const int slot_j = tok * a.k + jj;
-          const int pj = P.pos[slot_j];
-          if (pj < 0) continue;
-          acc = fmaf(P.w[slot_j], __ldcg(a.y + (size_t)pj * a.H + cc), acc);
+  // ---------------- blend: this CTA's share of the M x H outputs ----------
+  {
+    const long long T = (long long)a.M * a.H;
+    const long long o1 = T * (blockIdx.x + 1) / gridDim.x;
+    for (long long o = T * blockIdx.x / gridDim.x + tid; o < o1; o += kCThreads) {
+      const int tok = (int)(o / a.H), cc = (int)(o % a.H);
+      const int k = a.k;
+      float acc = 0.f;
+      for (int j0 = 0; j0 < k; j0 += 8) {   // 8 loads in flight, then the fixed-order sum
+        float yv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int jj = j0 + i;
+          const int pj = jj < k ? P.pos[tok * k + jj] : -1;
+          yv[i] = pj >= 0 ? __ldcg(a.y + (size_t)pj * a.H + cc) : 0.f;
         }
-        if (a.has_shared) acc += __ldcg(a.y_sh + (size_t)tok * a.H + cc);
-        a.out[(size_t)tok * a.H + cc] = float_to_bf16_rn(acc);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int jj = j0 + i;
+          if (jj < k && P.pos[tok * k + jj] >= 0) acc = fmaf(P.w[tok * k + jj], yv[i], acc);
+        }
       }
+      if (a.has_shared) acc += __ldcg(a.y_sh + (size_t)tok * a.H + cc);
+      a.out[(size_t)tok * a.H + cc] = float_to_bf16_rn(acc);
     }
   }
-  if (blockIdx.x == 0) write_tables(P, a, kCThreads);
+  write_tables(P, a, blockIdx.x * kCThreads + tid, gridDim.x * kCThreads);
 }
 
 // ---------------------------------------------------------------------------
@@ -870,61 +972,184 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(FusedArgs a) 
 // ---------------------------------------------------------------------------
 
 constexpr size_t kSmemMax = 227 * 1024;
+constexpr int kStageCodeBytes = 32768;   // codes per stage
+
+// Stage geometry of a projection with K inputs and R outputs per expert in
+// format fmt, for kMats matrices per stage.
+PGeo make_geo(int fmt, int K, int R, int kMats) {
+  PGeo g = {};
+  g.fmt = fmt;
+  g.K = K;
+  g.R = R;
+  g.Kb = fmt == MOE_FMT_FP8_B128 ? K : K / 2;
+  g.nhc = g.Kb / 64;
+  // kr even (whole boxes) dividing nhc; cpw dividing kr, 1 for gate+up and
+  // at most 2 for down (the item's weights stay in registers); wpt = kr / cpw
+  // dividing the warp count.
+  // Largest stage with at most kStageCodeBytes of codes;
+  // among equals, the fewest tiles per group (a CTA's share of a projection
+  // may be only a few tiles).  A function of the shapes alone: it fixes the
+  // order of every sum, which must not depend on the batch.
+  int best = -1, best_mt = 0;
+  for (int kr = 2; kr <= g.nhc; kr += 2) {
+    if (g.nhc % kr) continue;
+    for (int cpw = 1; cpw <= kr && cpw <= (kMats == 2 ? 1 : 2); ++cpw) {
+      if (kr % cpw) continue;
+      const int wpt = kr / cpw;
+      if (kCW % wpt) continue;
+      const int mt = kCW / wpt;
+      const int bytes = kMats * mt * kr * 1024;
+      if (bytes > kStageCodeBytes || bytes < best || (bytes == best && mt >= best_mt)) continue;
+      best = bytes;
+      best_mt = mt;
+      g.kr = kr;
+      g.cpw = cpw;
+    }
+  }
+  g.wpt = g.kr / g.cpw;
+  g.mt = kCW / g.wpt;
+  g.nkp = g.nhc / g.kr;
+  g.code_bytes = kMats * g.mt * (g.kr / 2) * kBoxBytes;
+  g.stage_bytes =
+      g.code_bytes + (fmt == MOE_FMT_NVFP4_G16 ? kMats * g.mt * (g.kr / 2) * kSBoxBytes : 0);
+  return g;
+}
 
 struct Shape {
-  int stages, slot_bytes, rounds[2][2];
+  PGeo geo[2][2];
+  int stages, slot_bytes, xs_row_bytes;
   size_t smem;
 };
-
-// Bytes of one lane-group round of a stage: every lane group one row of each
-// matrix (and the NVFP4 group scales of those rows).
-size_t round_bytes(bool gate_up, int fmt, int K) {
-  const size_t per_row = row_bytes(fmt, K) + (fmt == MOE_FMT_NVFP4_G16 ? (size_t)K / 16 : 0);
-  return (size_t)(gate_up ? 2 : 1) * stage_feats(K) * per_row;
-}
 
 bool plan_shape(const moe_layer_desc *L, int M, int sms, Shape &sp) {
   const moe_experts &R = L->routed;
   const moe_experts *S = L->shared;
   const int n = M * L->top_k;
-  if (n > kMaxN || M > kMaxM || L->top_k > 32 || sms < 1) return false;
+  if (n > kMaxN || M > kMaxM || L->top_k > 32 || sms < 1 || R.num_experts > 1024) return false;
   const int H = R.hidden;
-  // K in [256, 2048], a multiple of 128 (at most 4 units of 16 per lane, FP8
-  // block scales of at most 16 x 16 blocks); NVFP4 group scales are copied by
-  // rows, so K/16 bytes must be a multiple of 16.
+  // K and R multiples of 128 in [256, 2048] (NVFP4: K of 256, so that a code
+  // row is whole 128-byte boxes and a scale row whole 16-byte boxes)
   auto k_ok = [](int K, int fmt) {
     return K % 128 == 0 && K >= 256 && K <= 2048 && (fmt == MOE_FMT_FP8_B128 || K % 256 == 0);
   };
   if (!k_ok(H, R.fmt) || !k_ok(R.inter, R.fmt)) return false;
   if (S && (!k_ok(H, S->fmt) || !k_ok(S->inter, S->fmt))) return false;
-  if ((H + kBlendTile - 1) / kBlendTile > 32) return false;
-  // NVFP4 group scales are bulk-copied: 16-byte aligned tables
-  auto scales_ok = [](const moe_experts *X) {
-    if (!X || X->fmt != MOE_FMT_NVFP4_G16) return true;
-    return ((uintptr_t)X->gate.scale & 15) == 0 && ((uintptr_t)X->up.scale & 15) == 0 &&
-           ((uintptr_t)X->down.scale & 15) == 0;
+  // tensor copies read 16-byte aligned tables
+  auto aligned = [](const moe_experts *X) {
+    if (!X) return true;
+    const moe_proj *p[3] = {&X->gate, &X->up, &X->down};
+    for (auto *q : p) {
+      if ((uintptr_t)q->codes & 15) return false;
+      if (X->fmt == MOE_FMT_NVFP4_G16 && ((uintptr_t)q->scale & 15)) return false;
+    }
+    return true;
   };
-  if (!scales_ok(&R) || !scales_ok(S)) return false;
-  // a ring slot holds one gate+up round; down stages take as many rounds as fit
-  size_t slot = round_bytes(true, R.fmt, H);
-  if (S && round_bytes(true, S->fmt, H) > slot) slot = round_bytes(true, S->fmt, H);
-  const size_t dr = round_bytes(false, R.fmt, R.inter);
-  const size_t ds = S ? round_bytes(false, S->fmt, S->inter) : 0;
-  if (dr > slot) slot = dr;
-  if (ds > slot) slot = ds;
-  slot = (slot + 127) & ~(size_t)127;
-  sp.rounds[0][0] = sp.rounds[0][1] = 1;
-  sp.rounds[1][0] = (int)(slot / dr);
-  sp.rounds[1][1] = S ? (int)(slot / ds) : 1;
-  const int kd_max = S && S->inter > R.inter ? S->inter : R.inter;
-  const size_t fixed = plan_bytes(n) + 2 * 256 * 4 + (2 * kXS + 64) * 4 + xs_bytes(H, kd_max);
-  if (fixed + 2 * (slot + 16) > kSmemMax) return false;
-  int ns = (int)((kSmemMax - fixed) / (slot + 16));
-  if (ns > 16) ns = 16;
+  if (!aligned(&R) || !aligned(S)) return false;
+  const moe_experts *X[2] = {&R, S};
+  int slot = 0;
+  for (int seg = 0; seg < 2; ++seg) {
+    if (!X[seg]) {
+      sp.geo[0][seg] = sp.geo[0][0];
+      sp.geo[1][seg] = sp.geo[1][0];
+      continue;
+    }
+    sp.geo[0][seg] = make_geo(X[seg]->fmt, H, X[seg]->inter, 2);
+    sp.geo[1][seg] = make_geo(X[seg]->fmt, X[seg]->inter, H, 1);
+    for (int p = 0; p < 2; ++p)
+      if (sp.geo[p][seg].stage_bytes > slot) slot = sp.geo[p][seg].stage_bytes;
+  }
+  slot = (slot + 2047) & ~2047;
+  const int kd = S && S->inter > R.inter ? S->inter : R.inter;
+  sp.xs_row_bytes = 2 * H > 4 * kd ? 2 * H : 4 * kd;
+  const size_t fixed = fixed_smem(n, sp.xs_row_bytes) + 1024;   // + alignment slack
+  if (fixed + 2 * ((size_t)slot + 16) > kSmemMax) return false;
+  int ns = (int)((kSmemMax - fixed) / ((size_t)slot + 16));
+  if (ns > 8) ns = 8;
+  if ((size_t)ns * slot < (size_t)3 * R.num_experts * 4) return false;   // routing scratch
   sp.stages = ns;
-  sp.slot_bytes = (int)slot;
+  sp.slot_bytes = slot;
   sp.smem = (size_t)ns * slot + 16 * (size_t)ns + fixed;
   return true;
+}
+
+// cuTensorMapEncodeTiled, from the driver through the runtime (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A [rows][row_bytes] u8 table seen as [row_bytes / cb][rows][cb]: column
+// blocks of cb bytes (the innermost dimension), rows, column-block index; a
+// box is 16 rows x nb column blocks, laid out column block after column
+// block in shared memory.
+int make_map(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows, uint32_t cb,
+             uint32_t nb, bool swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ECUDA;
+  const cuuint64_t dims[3] = {cb, rows, row_bytes / cb};
+  const cuuint64_t strides[2] = {row_bytes, cb};
+  const cuuint32_t box[3] = {cb, 16, nb};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_EUNSUPPORTED;
+}
+
+// Tensor maps of one expert set (cached by table address and shape: encoding
+// is host work that would otherwise repeat on every call).  nb[j]: column
+// blocks per copy of projection j (gate, up, down).
+int expert_maps(const moe_experts *X, const int (&nb)[3], CUtensorMap (&out)[3][2]) {
+  struct Key {
+    const void *p;
+    uint64_t rb, rows;
+    uint32_t cb, nb;
+    bool operator==(const Key &o) const {
+      return p == o.p && rb == o.rb && rows == o.rows && cb == o.cb && nb == o.nb;
+    }
+  };
+  struct KeyHash {
+    size_t operator()(const Key &k) const {
+      return std::hash<const void *>()(k.p) ^ (k.rb * 0x9E3779B97F4A7C15ull) ^ (k.rows << 7) ^
+             ((size_t)k.cb << 3) ^ ((size_t)k.nb << 17);
+    }
+  };
+  static std::mutex mu;
+  static std::unordered_map<Key, CUtensorMap, KeyHash> cache;
+  const moe_proj *p[3] = {&X->gate, &X->up, &X->down};
+  const int H = X->hidden, I = X->inter, E = X->num_experts;
+  const bool f4 = X->fmt == MOE_FMT_NVFP4_G16;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int j = 0; j < 3; ++j) {
+    const int K = j < 2 ? H : I, R = j < 2 ? I : H;
+    const Key kc = {p[j]->codes, (uint64_t)(f4 ? K / 2 : K), (uint64_t)E * R, 128,
+                    (uint32_t)nb[j]};
+    const Key ks = {p[j]->scale, (uint64_t)(K / 16), (uint64_t)E * R, 16, (uint32_t)nb[j]};
+    for (int w = 0; w < (f4 ? 2 : 1); ++w) {
+      const Key &k = w == 0 ? kc : ks;
+      auto it = cache.find(k);
+      if (it == cache.end()) {
+        CUtensorMap m;
+        const int st = make_map(&m, k.p, k.rb, k.rows, k.cb, k.nb, k.cb == 128);
+        if (st) return st;
+        if (cache.size() > 4096) cache.clear();
+        it = cache.emplace(k, m).first;
+      }
+      out[j][w] = it->second;
+    }
+    if (!f4) out[j][1] = out[j][0];
+  }
+  return MOE_OK;
 }
 
 }  // namespace
@@ -942,17 +1167,27 @@ int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float 
   Shape sp;
   if (!plan_shape(L, M, sms, sp)) return MOE_EUNSUPPORTED;
   FusedArgs a = {};
+  Maps maps;
+  memset(&maps, 0, sizeof(maps));
+  const int nbr[3] = {sp.geo[0][0].kr / 2, sp.geo[0][0].kr / 2, sp.geo[1][0].kr / 2};
+  const int nbs[3] = {sp.geo[0][1].kr / 2, sp.geo[0][1].kr / 2, sp.geo[1][1].kr / 2};
+  int st = expert_maps(&L->routed, nbr, maps.m[0]);
+  if (st) return st;
+  if (L->shared) {
+    st = expert_maps(L->shared, nbs, maps.m[1]);
+    if (st) return st;
+  } else {
+    memcpy(maps.m[1], maps.m[0], sizeof(maps.m[0]));
+  }
   auto conv = [](const moe_experts *X) {
     Exp d = {};
     if (!X) return d;
     d.fmt = X->fmt;
     d.I = X->inter;
     const moe_proj *src[3] = {&X->gate, &X->up, &X->down};
-    Proj *dst[3] = {&d.gate, &d.up, &d.down};
     for (int i = 0; i < 3; ++i) {
-      dst[i]->codes = reinterpret_cast<const uint8_t *>(src[i]->codes);
-      dst[i]->scale = src[i]->scale;
-      dst[i]->glob = src[i]->global_scale;
+      d.bscale[i] = reinterpret_cast<const float *>(src[i]->scale);
+      d.glob[i] = src[i]->global_scale;
     }
     return d;
   };
@@ -987,21 +1222,20 @@ int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float 
   a.y = reinterpret_cast<float *>(base + v.y);
   a.y_sh = reinterpret_cast<float *>(base + v.y_shared);
   a.grid_ctr = reinterpret_cast<unsigned long long *>(base + v.blend_counters);
-  a.tile_cnt = reinterpret_cast<int32_t *>(base + v.blend_counters + 8);
   a.out = out;
   a.err = err;
+  memcpy(a.geo, sp.geo, sizeof(a.geo));
   a.stages = sp.stages;
   a.slot_bytes = sp.slot_bytes;
-  for (int p = 0; p < 2; ++p)
-    for (int q = 0; q < 2; ++q) a.rounds[p][q] = sp.rounds[p][q];
+  a.xs_row_bytes = sp.xs_row_bytes;
   const int rf = L->routed.fmt, sf = L->shared ? L->shared->fmt : rf;
   auto go = [&](auto kern) -> int {
-    int st = ensure_max_carveout(reinterpret_cast<const void *>(kern));
-    if (st) return st;
-    st = ensure_smem_limit(reinterpret_cast<const void *>(kern), sp.smem);
-    if (st) return st;
+    int r = ensure_max_carveout(reinterpret_cast<const void *>(kern));
+    if (r) return r;
+    r = ensure_smem_limit(reinterpret_cast<const void *>(kern), sp.smem);
+    if (r) return r;
     // cooperative: all CTAs are co-resident, which the grid barrier needs
-    return launch_pdl_coop(kern, dim3(sms), dim3(kThreads), sp.smem, stream, a);
+    return launch_pdl_coop(kern, dim3(sms), dim3(kThreads), sp.smem, stream, a, maps);
   };
   constexpr int F8 = MOE_FMT_FP8_B128, F4 = MOE_FMT_NVFP4_G16;
   if (rf == F8 && sf == F8) return go(decode_layer_kernel<F8, F8>);

@@ -74,7 +74,7 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   v->h_shared = take((size_t)M * Is * 4);
   v->y = take((size_t)max_total * H * 4);
   v->y_shared = take((size_t)M * H * 4);
-  v->blend_counters = take(8 + (size_t)((H + 63) / 64) * 4);
+  v->blend_counters = take(8);
   v->total_bytes = off;
   v->max_total = max_total;
   v->max_blocks = max_blocks;

@@ -9,54 +9,60 @@
 
 namespace moe {
 
+// Order-preserving map of a float to an unsigned key (larger float, larger
+// key; -0.0 is taken as +0.0 so that the two compare equal).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t b = __float_as_uint(f + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // One warp routes one row of fp32 logits [E] ("forward_nvfp4_grouped_decode.rs",
 // grouped_route with GroupedRouting::PerRow; the workload's "softmax then
 // top-k renormalised"): the k largest logits (equal logits: lower expert id
 // first) in descending order, weights exp(l_j - l_max) / sum over the k
-// selected.  Selection compares fp32 values exactly; the weight sum runs as an
-// xor butterfly over the 32 lanes (fixed order).  ids[j] / w[j] for j < k are
-// written by lane j.  Requires E <= 32 * VPL and k <= 32.
+// selected.  Each selection round takes the warp's largest key with one
+// redux.sync and, among the lanes holding it, the lowest expert id with a
+// second.  The weight sum runs as an xor butterfly over the 32 lanes (fixed
+// order).  ids[j] / w[j] for j < k are written by lane j.  Requires
+// E <= 32 * VPL and k <= 32.
 template <int VPL>
 __device__ __forceinline__ void topk_softmax_row(const float *l, int E, int k, int32_t *ids,
                                                  float *w) {
   const int lane = threadIdx.x & 31;
   const int nv = (E + 31) / 32;   // logits per lane actually present
-  float v[VPL];
+  uint32_t key[VPL];              // 0: absent (below every real logit)
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
     const int e = lane + 32 * j;
-    v[j] = (j < nv && e < E) ? __ldcg(l + e) : -INFINITY;
+    key[j] = (j < nv && e < E) ? order_key(__ldcg(l + e)) : 0u;
   }
   unsigned taken = 0;   // bit j: this lane's j-th value already selected
   float mine = 0.f, vmax = 0.f;
   int myid = 0;
 #pragma unroll 1
   for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bid = 0x7fffffff;
+    uint32_t bk = 0;
+    int bj = -1;
 #pragma unroll
     for (int j = 0; j < VPL; ++j) {
       if (j >= nv) break;
-      const int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u) && (v[j] > bv || bid == 0x7fffffff)) {
-        bv = v[j];
-        bid = e;
+      if (!((taken >> j) & 1u) && key[j] > bk) {   // strict: the lower id wins a tie
+        bk = key[j];
+        bj = j;
       }
     }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-      const int oid = __shfl_xor_sync(0xffffffffu, bid, d);
-      if (oid != 0x7fffffff && (bid == 0x7fffffff || ov > bv || (ov == bv && oid < bid))) {
-        bv = ov;
-        bid = oid;
-      }
-    }
-    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-    if (r == 0) vmax = bv;
+    const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = (bj >= 0 && bk == wk) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+    const uint32_t wid = __reduce_min_sync(0xffffffffu, cand);
+    if ((int)(wid & 31u) == lane) taken |= 1u << (wid >> 5);
+    const float wv = key_value(wk);
+    if (r == 0) vmax = wv;
     if (lane == r) {       // lane r keeps the r-th selection
-      mine = bv;
-      myid = bid;
+      mine = wv;
+      myid = (int)wid;
     }
   }
   const float ex = lane < k ? expf(mine - vmax) : 0.f;

@@ -237,7 +237,7 @@ typedef struct moe_workspace_view {
     size_t active_experts, active_count;           /* [cap], [1] */
     size_t num_tokens_post_padded;                 /* [1] */
     size_t h, h_shared, y, y_shared;               /* float tables */
-    size_t blend_counters;                         /* internal: [1] uint64 + [ceil(H/64)] int32 */
+    size_t blend_counters;                         /* internal: [1] uint64 grid-barrier count */
     size_t total_bytes;
     int max_total, max_blocks, cap;
 } moe_workspace_view;
@@ -264,8 +264,8 @@ int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logit
  * On the CUDA-core path, when M*top_k <= 256, M <= 32, and hidden, inter and
  * the shared inter are multiples of 128 in [256, 2048] (NVFP4: of 256), the
  * same results come from one cooperative persistent kernel (gate+up, a grid
- * barrier, then down with the blend) instead of five launches; every table
- * and intermediate is still written to the workspace.  MOE_PATH_SIMT_STAGED
+ * barrier, down, a grid barrier, the blend) instead of five launches; every
+ * table and intermediate is still written to the workspace.  MOE_PATH_SIMT_STAGED
  * forces the five.
  *   x [M][H] bf16 bits; out [M][H] bf16 bits;
  *   workspace: device, >= moe_decode_layer_workspace_bytes(layer, M) bytes,
