@@ -11,9 +11,10 @@ no step finds its weights in the 129 MB L2.
 Timed regions (CUDA events on the launching stream, after W warm-up steps,
 synchronize on both sides):
   * value:    K steps captured in one CUDA graph, replayed once;
-  * roofline: the layer's kernels of K steps (on the fused path the gate+up
-              kernel with the down+blend kernel overlapping it), each call
-              bracketed by events, algorithmic bytes / mean duration;
+  * roofline: the layer kernel (one cooperative launch per layer call on the
+              fused decode path), each call bracketed by events,
+              algorithmic bytes / mean duration; DRAM traffic per launch from
+              the committed ncu summary of the same kernel source, else null;
   * e2e:      K steps through the public API with host buffers: x and logits
               copied in from pinned memory, the output copied back, per step.
 The CPU baseline is the oracle on a bounded sample of the same workload.
@@ -40,6 +41,32 @@ METRIC = ("MoE decode layer µs/tokens·s⁻¹ and weight-stream HBM GB/s "
 N_COPIES = 16
 NOMINAL_HBM_GBS = 8000.0
 SEED = 1001
+
+
+def kernel_source_digest() -> str:
+    """sha256 of the fused layer kernel's source (ties a profile to a build)."""
+    import hashlib
+    src = os.path.join(HERE, "expert_routing_alignment_gb300", "csrc", "decode_fused.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the layer kernel for `workload` from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(HERE, "profiles", "decode_layer_kernel_fp8_decode.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel source sha256") != kernel_source_digest():
+        return None
+    key = f"traffic bytes per launch ({workload})"
+    return int(fields[key]) if key in fields else None
 
 
 def measured_peaks() -> dict:
@@ -371,7 +398,7 @@ def run_gpu(args, rank: int, world: int):
     line = dict(
         metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=W,
         ms_per_step=ms_max / K, higher_is_better=True, scaling="weak", vs_baseline=None,
-        dtype="f32", data="synthetic",
+        dtype="fp8_e4m3 weights, f16 x f16 -> f32 mma", data="synthetic",
         config=dict(workload=shape.name, M=shape.M, H=shape.H, I=shape.I, E=shape.E,
                     top_k=shape.top_k, BS=shape.BS, weights="fp8_e4m3 128x128 fp32 block scales",
                     routing="fresh N(0,1) logits every step",
@@ -383,13 +410,14 @@ def run_gpu(args, rank: int, world: int):
         algorithmic_bytes_per_layer=int(r["nbytes"]),
         sweep=sweep,
         roofline=dict(bound="hbm",
-                      kernel=("fused decode pair (gate+up kernel, down+blend kernel overlapping "
-                              "it)" if r["launches"] == 2 else "layer call (5 launches)"),
+                      kernel=("decode_layer_kernel (one cooperative launch per layer call)"
+                              if r["launches"] == 1 else
+                              f"layer call ({r['launches']} launches)"),
                       achieved=round(dk_achieved, 1),
                       peak=peaks["hbm_gbs"], peak_source=f"{peaks['source']} copy bandwidth",
                       unit="GB/s", frac=round(dk_achieved / peaks["hbm_gbs"], 4),
                       bytes_per_launch=int(r["nbytes"]), us_per_launch=round(1e3 * r["dk_ms"], 3),
-                      traffic=None),
+                      traffic=profiled_traffic(shape.name)),
         e2e=dict(value=shape.M * K / (r["e2e_ms"] * 1e-3), unit="tokens/s",
                  h2d_bytes_per_step=r["h2d"], d2h_bytes_per_step=r["d2h"]),
         gpu_launches=r["launches"] * K,

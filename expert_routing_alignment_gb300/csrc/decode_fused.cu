@@ -871,7 +871,7 @@ __device__ bool grid_barrier(unsigned long long *ctr, int *flag) {
     const unsigned long long v = atomicAdd(ctr, 1ull);
     const unsigned long long target = (v / G + 1) * G;
     bool ok = false;
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    for (uint32_t i = 0; i < (1u << 24); ++i) {   // about a second at most
       if (ld_acquire_u64(ctr) >= target) {
         ok = true;
         break;
