@@ -100,6 +100,8 @@ EXPORTS = {
     "moe_decode_layer": (_I, [ctypes.POINTER(_LayerDesc), _P, _I, _P, _P, _P, _P, _P,
                               ctypes.c_size_t, _P, _P]),
     "moe_decode_layer_launches": (_I, [ctypes.POINTER(_LayerDesc), _I, _I]),
+    "moe_decode_layer_noalloc": (_I, [ctypes.POINTER(_LayerDesc), _P, _I, _P, _P, _P, _P, _P,
+                                      _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -339,3 +341,20 @@ def moe_decode_layer(layer: LayerDesc, x: torch.Tensor, out: torch.Tensor, works
         ctypes.pointer(layer._struct), _ptr(x), M, _ptr(router_logits), _ptr(topk_ids),
         _ptr(topk_w), _ptr(out), _ptr(workspace), workspace.numel(), _ptr(err_word),
         _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def moe_decode_layer_noalloc(layer: LayerDesc, x: torch.Tensor, out: torch.Tensor,
+                             router_logits: Optional[torch.Tensor] = None,
+                             topk_ids: Optional[torch.Tensor] = None,
+                             topk_w: Optional[torch.Tensor] = None,
+                             err_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """moe_decode_layer without a caller workspace, for callers that cannot
+    allocate device memory: the library's fixed device array (32 MiB, shared
+    by every call on the device) serves as the workspace."""
+    M = x.shape[0]
+    _check("moe_decode_layer_noalloc", load().moe_decode_layer_noalloc(
+        ctypes.pointer(layer._struct), _ptr(x), M, _ptr(router_logits), _ptr(topk_ids),
+        _ptr(topk_w), _ptr(out), _ptr(err_word), _stream(stream)))

@@ -283,6 +283,33 @@ int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,
                      const float *topk_w, uint16_t *out, void *workspace,
                      size_t workspace_bytes, uint32_t *err_word, void *stream);
 
+/* ---- the layer without allocation --------------------------------------- */
+
+/* Bytes of the fixed device array that moe_decode_layer_noalloc uses as its
+ * workspace (held on every GPU that loads the library until it is unloaded). */
+#define MOE_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* moe_decode_layer for callers that cannot allocate device memory when they
+ * run the layer (code running inside another framework's captured graph or
+ * stream callback, plugins whose host forbids device allocation after
+ * start-up, embedded runtimes with a device-memory budget fixed at load).
+ * The pages have no counterpart: it is the same layer, same arguments and
+ * same results as moe_decode_layer, with the workspace taken from a
+ * file-scope device array of MOE_NOALLOC_SCRATCH_BYTES instead of a caller
+ * buffer.  It calls no allocating routine.
+ *   The first call on a device looks up the array's device address (once per
+ *   device), so make that call before capturing any stream that contains it.
+ *   Every call on a device shares the array and leaves its contents there:
+ *   calls that overlap on the GPU race on it, so order them on one stream.
+ *   The intermediates are not readable through a workspace view.
+ * Errors: as moe_decode_layer, and MOE_EUNSUPPORTED when the layer's
+ * workspace for M rows (moe_decode_layer_workspace_bytes) exceeds
+ * MOE_NOALLOC_SCRATCH_BYTES; nothing is launched then. */
+int moe_decode_layer_noalloc(const moe_layer_desc *layer, const uint16_t *x, int M,
+                             const float *router_logits, const int32_t *topk_ids,
+                             const float *topk_w, uint16_t *out, uint32_t *err_word,
+                             void *stream);
+
 #ifdef __cplusplus
 }
 #endif
