@@ -76,7 +76,8 @@ class _WsView(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "topk_ids", "topk_w", "sorted_token_ids", "sorted_expert_ids", "expert_offsets",
         "token_to_perm", "active_experts", "active_count", "num_tokens_post_padded", "h",
-        "h_shared", "y", "y_shared", "blend_counters", "total_bytes")] + [
+        "h_shared", "y", "y_shared", "blend_counters", "tc_x_terms", "tc_x_scale",
+        "tc_h_terms", "tc_h_scale", "tc_done", "total_bytes")] + [
         ("max_total", ctypes.c_int), ("max_blocks", ctypes.c_int), ("cap", ctypes.c_int)]
 
 
@@ -307,6 +308,15 @@ def workspace_view(layer: LayerDesc, M: int, ws: torch.Tensor) -> dict:
         nb = count * torch.tensor([], dtype=dtype).element_size()
         return ws[off: off + nb].view(dtype)
 
+    tc = {}
+    if v.tc_x_terms:   # the tensor-core path's activation terms
+        mt = v.max_total
+        tc = dict(
+            tc_x_terms=sl(v.tc_x_terms, 2 * mt * H, torch.uint8).view(2, mt, H),
+            tc_x_scale=sl(v.tc_x_scale, mt, torch.float32),
+            tc_h_terms=sl(v.tc_h_terms, 3 * mt * I, torch.uint8).view(3, mt, I),
+            tc_h_scale=sl(v.tc_h_scale, mt * (I // 128), torch.float32).view(mt, I // 128))
+
     return dict(
         topk_ids=sl(v.topk_ids, M * k, torch.int32), topk_w=sl(v.topk_w, M * k, torch.float32),
         sorted_token_ids=sl(v.sorted_token_ids, v.max_total, torch.int32),
@@ -320,7 +330,7 @@ def workspace_view(layer: LayerDesc, M: int, ws: torch.Tensor) -> dict:
         h_shared=sl(v.h_shared, M * Is, torch.float32).view(M, Is),
         y=sl(v.y, v.max_total * H, torch.float32).view(v.max_total, H),
         y_shared=sl(v.y_shared, M * H, torch.float32).view(M, H),
-        max_total=v.max_total, max_blocks=v.max_blocks, cap=v.cap)
+        max_total=v.max_total, max_blocks=v.max_blocks, cap=v.cap, **tc)
 
 
 def moe_decode_layer_launches(layer: LayerDesc, M: int, with_logits: bool = True) -> int:

@@ -17,19 +17,50 @@ int launch_topk(const float *logits, int M, int E, int k, int32_t *ids, float *w
 int launch_blend(const float *y, const float *w, const int32_t *ttp, const float *y_sh,
                  uint16_t *out, int M, int k, int H, void *stream);
 bool fused_fits(const moe_layer_desc *L, int M, int sms);
+bool tc_fits(const moe_layer_desc *L, int M);
+void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]);
+int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *sti,
+              const int32_t *off, const int32_t *act, const int32_t *act_count,
+              const int32_t *ntpp, void *ws, const moe_workspace_view &v, uint32_t *err,
+              void *stream);
 int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float *logits,
                  const int32_t *ids, const float *w, uint16_t *out, void *ws,
                  const moe_workspace_view &v, uint32_t *err, void *stream);
 
-// The expert-kernel path of a shape class.  It depends on the shapes only,
-// never on the routing, so a captured graph stays valid for every routing.
+// The expert-kernel path of the grouped entry points.  The tensor-core
+// kernels keep their activation terms in the layer workspace, so only
+// moe_decode_layer runs them.
 static int resolve_path(const moe_experts *routed, int M, int top_k, int path) {
   (void)routed;
   (void)M;
   (void)top_k;
-  if (path == MOE_PATH_TC) return -1;   // no tensor-core kernels for this shape yet
+  if (path == MOE_PATH_TC) return -1;
   if (path == MOE_PATH_SIMT_STAGED) return MOE_PATH_SIMT_STAGED;
   return MOE_PATH_SIMT;
+}
+
+// How moe_decode_layer runs a shape class: the fused CUDA-core kernel, the
+// tensor-core kernel, or the staged CUDA-core kernels.  It depends on the
+// shapes only, never on the routing, so a captured graph stays valid for
+// every routing.
+enum { kRunFused = 0, kRunTc = 1, kRunStaged = 2 };
+
+static bool tc_allowed(const moe_layer_desc *L, int M) {
+  return (L->path == MOE_PATH_AUTO || L->path == MOE_PATH_TC) && tc_fits(L, M);
+}
+
+static int layer_run(const moe_layer_desc *L, int M) {
+  switch (L->path) {
+    case MOE_PATH_TC:
+      return tc_fits(L, M) ? kRunTc : -1;
+    case MOE_PATH_SIMT_STAGED:
+      return kRunStaged;
+    case MOE_PATH_SIMT:
+      return fused_fits(L, M, sm_count()) ? kRunFused : kRunStaged;
+    default:
+      if (fused_fits(L, M, sm_count())) return kRunFused;
+      return tc_fits(L, M) ? kRunTc : kRunStaged;
+  }
 }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -75,6 +106,16 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   v->y = take((size_t)max_total * H * 4);
   v->y_shared = take((size_t)M * H * 4);
   v->blend_counters = take(8);
+  v->tc_x_terms = v->tc_x_scale = v->tc_h_terms = v->tc_h_scale = v->tc_done = 0;
+  if (tc_allowed(L, M)) {
+    size_t b[5];
+    tc_workspace(L, max_total, cap, b);
+    v->tc_x_terms = take(b[0]);
+    v->tc_x_scale = take(b[1]);
+    v->tc_h_terms = take(b[2]);
+    v->tc_h_scale = take(b[3]);
+    v->tc_done = take(b[4]);
+  }
   v->total_bytes = off;
   v->max_total = max_total;
   v->max_blocks = max_blocks;
@@ -111,7 +152,10 @@ extern "C" int moe_grouped_down(const moe_experts *routed, const moe_experts *sh
 extern "C" size_t moe_decode_layer_workspace_bytes(const moe_layer_desc *layer, int max_M) {
   moe_workspace_view v;
   if (moe::layout(layer, max_M, &v) != MOE_OK) return 0;
-  return v.total_bytes;
+  size_t most = v.total_bytes;
+  for (int m = 1; m < max_M; ++m)
+    if (moe::layout(layer, m, &v) == MOE_OK && v.total_bytes > most) most = v.total_bytes;
+  return most;
 }
 
 extern "C" int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int M,
@@ -122,9 +166,10 @@ extern "C" int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int 
 extern "C" int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logits) {
   moe_workspace_view v;
   if (moe::layout(layer, M, &v) != MOE_OK) return -1;
-  const int path = moe::resolve_path(&layer->routed, M, layer->top_k, layer->path);
-  if (path < 0) return -1;
-  if (path == MOE_PATH_SIMT && moe::fused_fits(layer, M, moe::sm_count())) return 1;
+  const int run = moe::layer_run(layer, M);
+  if (run < 0) return -1;
+  if (run == moe::kRunFused) return 1;
+  if (run == moe::kRunTc) return with_logits ? 4 : 3;
   return with_logits ? 5 : 4;
 }
 
@@ -139,8 +184,8 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
   if (!router_logits && (!topk_ids || !topk_w)) return MOE_EINVAL;
   if (workspace_bytes < v.total_bytes || ((uintptr_t)workspace & 255)) return MOE_EINVAL;
   if (((uintptr_t)x & 15) || ((uintptr_t)out & 7)) return MOE_EINVAL;
-  const int path = moe::resolve_path(&layer->routed, M, layer->top_k, layer->path);
-  if (path < 0) return MOE_EUNSUPPORTED;
+  const int run = moe::layer_run(layer, M);
+  if (run < 0) return MOE_EUNSUPPORTED;
 
   char *ws = reinterpret_cast<char *>(workspace);
   auto I32 = [&](size_t o) { return reinterpret_cast<int32_t *>(ws + o); };
@@ -148,7 +193,7 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
   const int E = layer->routed.num_experts, k = layer->top_k, H = layer->routed.hidden;
   const moe_experts *S = layer->shared;
 
-  if (path == MOE_PATH_SIMT && moe::fused_fits(layer, M, moe::sm_count()))
+  if (run == moe::kRunFused)
     return moe::launch_fused(layer, x, M, router_logits, topk_ids, topk_w, out, workspace, v,
                              err_word, stream);
 
@@ -165,6 +210,13 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
                  I32(v.active_experts), I32(v.active_count), I32(v.num_tokens_post_padded),
                  err_word, stream);
   if (st) return st;
+  if (run == moe::kRunTc) {
+    st = moe::launch_tc(layer, x, M, I32(v.sorted_token_ids), I32(v.expert_offsets),
+                        I32(v.active_experts), I32(v.active_count),
+                        I32(v.num_tokens_post_padded), workspace, v, err_word, stream);
+    if (st) return st;
+    return moe::launch_blend(F32(v.y), w, I32(v.token_to_perm), nullptr, out, M, k, H, stream);
+  }
   st = moe::simt_gate_up(&layer->routed, S, x, M, k, I32(v.expert_offsets),
                          I32(v.sorted_token_ids), I32(v.active_experts), I32(v.active_count),
                          F32(v.h), S ? F32(v.h_shared) : nullptr, stream);

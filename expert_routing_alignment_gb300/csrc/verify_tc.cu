@@ -1,0 +1,1000 @@
+// verify_tc.cu -- the grouped expert FFN of the decode MoE layer on the
+// tensor cores (tcgen05 MMA with TMEM accumulators), for batches whose active
+// experts receive many rows each (the M = 128 verify batch).
+//
+// What it computes is the same as the CUDA-core kernels: for every active
+// expert e and every real sorted position p of its run, token t,
+//   h[p] = silu(Wg[e] . x[t]) * (Wu[e] . x[t])        (fp32)
+//   y[p] = Wd[e] . h[p]                                (fp32)
+// with w = e4m3(code) * scale[o/128][k/128] ("fp8_moe_grouped.rs",
+// moe_expert_gate_up_act_fp8_grouped / moe_expert_down_act_fp8_grouped and
+// the tensor-core twins of "metrale_model_layers/layers/ops/
+// fp8_moe_grouped.rs"; the SwiGLU product of "moe_decode_vec.py").
+//
+// How, on sm_103a:
+//  * Swap-AB.  A weight tile of 128 output rows is the MMA's M side; the
+//    expert's token rows (padded to 16, at most 64 per item) are its N side,
+//    so a ragged expert costs MMA work in proportion to its rows.
+//  * The E4M3 codes go to the tensor cores as they are (kind::f8f6f4, no
+//    dequantised copy).  The activation side is split into E4M3 terms whose
+//    sum is the value: x (bf16, 8 significant bits) = t0 + t1 exactly after a
+//    power-of-two row scale; h (fp32) = t0 + t1 + t2 to about 2^-12 relative
+//    per element, with a power-of-two scale per (row, 128-column block).
+//  * Block scales are applied exactly where they change: every 128-wide k
+//    block is accumulated alone in TMEM, then read into registers and added
+//    in fp32 times its scale (fp32 promotion of the per-block partial).
+//  * One cooperative persistent kernel, one CTA per SM, warp-specialised:
+//    warp 0 streams weight tiles (TMA, 128x128-byte boxes, 128-byte swizzle)
+//    and activation terms into a byte ring of variable-size stages; warp 1
+//    issues the MMAs from one thread; 16 warps promote, finish h (SiLU
+//    product, the three terms of the down projection's input) or y.
+//    Items are (expert row tile, 128-row gate+up tile) then (expert row
+//    tile, pair of 128-row down tiles), dealt round-robin over the CTAs; a
+//    down item waits (bounded) until every gate+up item of its expert has
+//    published its h terms through a per-expert counter.
+//  * Every wait gives up after about two seconds with MOE_ERR_TIMEOUT; the
+//    CTA then stops issuing, drains its copies and MMAs and frees its TMEM.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "async.cuh"
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kEpiWarps = 16;
+constexpr int kWarps = 2 + kEpiWarps;
+constexpr int kThreads = kWarps * 32;          // 576
+constexpr int kEpiThreads = kEpiWarps * 32;    // 512
+constexpr int kRecs = 8;                       // stage records (ring slots in flight)
+constexpr int kBufs = 4;                       // TMEM accumulator buffers
+constexpr int kRowTile = 64;                   // token rows per item (MMA N <= 64)
+constexpr int kTileBytes = 128 * 128;          // one 128-row x 128-byte weight box
+constexpr int kXTerms = 2, kHTerms = 3;
+constexpr int kMaxKB = 64;                     // k blocks of 128 (H <= 8192)
+constexpr int kMaxKBd = 32;                    // down k blocks (I <= 4096)
+constexpr uint32_t kTmemCols = 512;            // kBufs x (2 x 64 columns)
+constexpr uint64_t kWaitNs = 2000000000ull;    // a wait gives up after ~2 s
+
+struct TcArgs {
+  int M, k, n, E, H, I, cap, max_total;
+  const uint16_t *x;
+  const int32_t *sti, *off, *act, *act_count, *ntpp;
+  const float *sg, *su, *sd;                 // block scales [E][R/128][K/128]
+  uint8_t *xq;                               // x terms [2][max_total][H] E4M3
+  float *xs;                                 // 2^-s of each x row [max_total]
+  uint8_t *hq;                               // h terms [3][max_total][I] E4M3
+  float *hs;                                 // 2^-s per (row, 128-block) [max_total][I/128]
+  float *h, *y;                              // [max_total][I], [max_total][H]
+  int *done;                                 // [cap] finished gate+up items per active expert
+  unsigned long long *grid_ctr;
+  uint32_t *err;
+  uint32_t ring_bytes;
+};
+
+// Weight maps: 2-D {K bytes, E*R rows}, box {128, 128}.  Term maps: 3-D
+// {K bytes, max_total rows, terms}, box {128, 16 << b, terms} for b = 0..2.
+struct TcMaps {
+  CUtensorMap wg, wu, wd;
+  CUtensorMap xq[3], hq[3];
+};
+
+struct Smem {
+  uint8_t *ring;
+  uint64_t *full, *empty, *accf, *acce, *drain;
+  uint32_t *rec;       // [kRecs] byte offset of each stage in the ring
+  volatile int *misc;  // [0] failed, [1] TMEM base, [2] active count, [3] row tiles
+  float *sc;           // [2][kMaxKB] weight block scales of the current item
+  float *cs;           // [kMaxKBd][kRowTile] per-row factors of the current item
+  uint32_t *red;       // [4 groups][4 quadrants][16] column maxima
+  int *rtp;            // [cap + 1] row-tile prefix over the active list
+  int2 *info;          // [cap] {offset, expert | rows << 16}
+};
+
+__host__ __device__ inline size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
+
+__host__ __device__ inline size_t fixed_bytes(int cap) {
+  size_t b = 0;
+  b += al16(8 * (2 * kRecs + 2 * kBufs + 1));
+  b += al16(4 * kRecs) + al16(4 * 16);
+  b += al16(4 * 2 * kMaxKB) + al16(4 * kMaxKBd * kRowTile) + al16(4 * 4 * 4 * 16);
+  b += al16(4 * ((size_t)cap + 1)) + al16(8 * (size_t)cap);
+  return b;
+}
+
+__device__ Smem carve(uint8_t *base, const TcArgs &a) {
+  Smem S;
+  S.ring = base;
+  uint8_t *p = base + a.ring_bytes;
+  auto take = [&](size_t bytes) {
+    uint8_t *r = p;
+    p += al16(bytes);
+    return r;
+  };
+  uint64_t *bars = reinterpret_cast<uint64_t *>(take(8 * (2 * kRecs + 2 * kBufs + 1)));
+  S.full = bars;
+  S.empty = bars + kRecs;
+  S.accf = bars + 2 * kRecs;
+  S.acce = bars + 2 * kRecs + kBufs;
+  S.drain = bars + 2 * kRecs + 2 * kBufs;
+  S.rec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
+  S.misc = reinterpret_cast<volatile int *>(take(4 * 16));
+  S.sc = reinterpret_cast<float *>(take(4 * 2 * kMaxKB));
+  S.cs = reinterpret_cast<float *>(take(4 * kMaxKBd * kRowTile));
+  S.red = reinterpret_cast<uint32_t *>(take(4 * 4 * 4 * 16));
+  S.rtp = reinterpret_cast<int *>(take(4 * ((size_t)a.cap + 1)));
+  S.info = reinterpret_cast<int2 *>(take(8 * (size_t)a.cap));
+  return S;
+}
+
+// ---------------------------------------------------------------------------
+// small device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t gtime() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void fail(const Smem &S, const TcArgs &a) {
+  if (!S.misc[0]) {
+    S.misc[0] = 1;
+    if (a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
+  }
+}
+
+// Wait for the phase of `parity` of an mbarrier; false when the CTA has
+// failed meanwhile or after about two seconds.
+__device__ bool wait_bar(const Smem &S, uint64_t *bar, uint32_t parity) {
+  if (mbar_poll(bar, parity)) return true;
+  const uint64_t t0 = gtime();
+  for (uint32_t i = 1; i < (1u << 30); ++i) {
+    if (mbar_poll(bar, parity)) return true;
+    if ((i & 255) == 0 && (S.misc[0] || gtime() - t0 > kWaitNs)) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ int ld_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until *p >= target (written by other CTAs with release); bounded.
+__device__ bool wait_count(const Smem &S, const int *p, int target) {
+  const uint64_t t0 = gtime();
+  for (uint32_t i = 0; i < (1u << 26); ++i) {
+    if (ld_acquire(p) >= target) return true;
+    if (S.misc[0] || gtime() - t0 > kWaitNs) return false;
+    __nanosleep(64);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void group_sync(int g) {
+  asm volatile("bar.sync %0, 128;" ::"r"(2 + g) : "memory");
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// Power-of-two exponent s such that amax * 2^s lies in [128, 256) (0 for a
+// zero maximum), kept where 2^s and 2^-s are normal floats.
+__device__ __forceinline__ int term_shift(uint32_t amax_bits) {
+  if (amax_bits == 0) return 0;
+  const int e = (int)(amax_bits >> 23) - 127;
+  const int s = 7 - e;
+  return s < -126 ? -126 : (s > 126 ? 126 : s);
+}
+
+// Two floats -> two E4M3 bytes (first in the low byte), nearest-even,
+// saturating at 448.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05
+// ---------------------------------------------------------------------------
+
+// Shared-memory matrix descriptor of a K-major operand tile written with the
+// 128-byte swizzle (rows of 128 bytes, groups of 8 rows 1024 bytes apart).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor: E4M3 x E4M3 -> f32, both K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_e4m3(int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_e4m3(uint32_t d, uint64_t ad, uint64_t bd, uint32_t id,
+                                         uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(id), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tensor copies
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                       uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                       uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// work items
+// ---------------------------------------------------------------------------
+
+struct Item {
+  bool gu;       // gate+up (else down)
+  int a, e;      // active-list index, expert
+  int pos0;      // first sorted position of the row tile
+  int rows;      // real rows in the tile (1..64)
+  int n16;       // MMA N: rows rounded up to 16
+  int box;       // term box: 16 << box rows
+  int tile;      // gate+up: 128-row tile of I; down: pair of 128-row tiles of H
+};
+
+__device__ __forceinline__ Item decode(const Smem &S, int A, int i, int TR, int FT, int FD) {
+  Item it;
+  int rtg;
+  if (i < TR * FT) {
+    it.gu = true;
+    rtg = i / FT;
+    it.tile = i - rtg * FT;
+  } else {
+    it.gu = false;
+    const int j = i - TR * FT;
+    rtg = j / FD;
+    it.tile = j - rtg * FD;
+  }
+  int lo = 0, hi = A - 1;   // the last a with rtp[a] <= rtg
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (S.rtp[mid] <= rtg)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int2 inf = S.info[lo];
+  const int rt = rtg - S.rtp[lo];
+  const int rows_e = inf.y >> 16;
+  it.a = lo;
+  it.e = inf.y & 0xFFFF;
+  it.pos0 = inf.x + rt * kRowTile;
+  it.rows = min(kRowTile, rows_e - rt * kRowTile);
+  it.n16 = (it.rows + 15) & ~15;
+  it.box = it.n16 <= 16 ? 0 : (it.n16 <= 32 ? 1 : 2);
+  return it;
+}
+
+// ---------------------------------------------------------------------------
+// phase 0: x terms of every real sorted position
+// ---------------------------------------------------------------------------
+//
+// Row p (token t = sorted_token_ids[p] / k): s = shift putting max|x[t]| in
+// [128, 256); xs[p] = 2^-s; t0 = e4m3(x * 2^s), t1 = e4m3(x * 2^s - t0).  A
+// bf16 value has 8 significant bits and each E4M3 term 4, so t0 + t1 equals
+// x * 2^s exactly wherever the residual is not below E4M3's subnormal step
+// (elements smaller than 2^-10 of the row maximum lose bits of at most
+// 2^-18 of that maximum).
+__device__ void prep_x(const TcArgs &a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < a.cap; i += kThreads) a.done[i] = 0;
+  const int ntpp = min(__ldcg(a.ntpp), a.max_total);
+  const int nw = gridDim.x * kWarps;
+  const size_t plane = (size_t)a.max_total * a.H;
+  for (int p = blockIdx.x * kWarps + warp; p < ntpp; p += nw) {
+    const int slot = __ldcg(a.sti + p);
+    if (slot < 0 || slot >= a.n) continue;
+    const uint16_t *xr = a.x + (size_t)(slot / a.k) * a.H;
+    uint32_t mx = 0;
+    for (int c = lane * 8; c < a.H; c += 256) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + c));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mx = max(mx, (w[i] & 0x7FFFu) << 16);
+        mx = max(mx, (w[i] >> 16 & 0x7FFFu) << 16);
+      }
+    }
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    const int s = term_shift(mx);
+    const float scl = pow2f(s);
+    if (lane == 0) a.xs[p] = pow2f(-s);
+    uint8_t *q0 = a.xq + (size_t)p * a.H;
+    uint8_t *q1 = q0 + plane;
+    for (int c = lane * 8; c < a.H; c += 256) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + c));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t t0[2] = {0, 0}, t1[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float f0 = bf16_to_float((uint16_t)(w[i] & 0xFFFFu)) * scl;
+        const float f1 = bf16_to_float((uint16_t)(w[i] >> 16)) * scl;
+        const uint32_t b0 = e4m3x2(f0, f1);
+        const float2 back = f16x2_to_float2(e4m3x2_to_f16x2((uint16_t)b0));
+        const uint32_t b1 = e4m3x2(f0 - back.x, f1 - back.y);
+        t0[i >> 1] |= b0 << (16 * (i & 1));
+        t1[i >> 1] |= b1 << (16 * (i & 1));
+      }
+      *reinterpret_cast<uint2 *>(q0 + c) = make_uint2(t0[0], t0[1]);
+      *reinterpret_cast<uint2 *>(q1 + c) = make_uint2(t1[0], t1[1]);
+    }
+  }
+}
+
+__device__ bool grid_barrier(const Smem &S, unsigned long long *ctr) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned long long G = gridDim.x;
+    const unsigned long long v = atomicAdd(ctr, 1ull);
+    const unsigned long long target = (v / G + 1) * G;
+    bool ok = false;
+    const uint64_t t0 = gtime();
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+      unsigned long long c;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(c) : "l"(ctr) : "memory");
+      if (c >= target) {
+        ok = true;
+        break;
+      }
+      if (gtime() - t0 > kWaitNs) break;
+      __nanosleep(64);
+    }
+    __threadfence();
+    S.misc[4] = ok;
+  }
+  __syncthreads();
+  return S.misc[4] != 0;
+}
+
+// The active list as row tiles: info[a] = {run offset, expert | rows << 16},
+// rtp = exclusive prefix of ceil(rows / 64).  Returns the active count.
+__device__ int build_table(const TcArgs &a, const Smem &S) {
+  const int A = min(max(__ldcg(a.act_count), 0), a.cap);
+  for (int i = threadIdx.x; i < A; i += kThreads) {
+    const int e = __ldcg(a.act + i);
+    int o = 0, rows = 0;
+    if (e >= 0 && e < a.E) {
+      o = __ldcg(a.off + e);
+      int lo = o, hi = __ldcg(a.off + e + 1);   // real slots first, then the sentinel n
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldcg(a.sti + mid) < a.n)
+          lo = mid + 1;
+        else
+          hi = mid;
+      }
+      rows = min(lo - o, 0x7FFF);
+    }
+    S.info[i] = make_int2(o, (e & 0xFFFF) | (rows << 16));
+    S.rtp[i] = (rows + kRowTile - 1) / kRowTile;   // counts; scanned below
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int run = 0;
+    for (int b = 0; b < A; b += 32) {
+      const int v = b + lane < A ? S.rtp[b + lane] : 0;
+      int inc = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+        if (lane >= d) inc += t;
+      }
+      if (b + lane < A) S.rtp[b + lane] = run + inc - v;
+      run += __shfl_sync(0xFFFFFFFFu, inc, 31);
+    }
+    if (lane == 0) {
+      S.rtp[A] = run;
+      S.misc[2] = A;
+      S.misc[3] = run;
+    }
+  }
+  __syncthreads();
+  return A;
+}
+
+// ---------------------------------------------------------------------------
+// roles
+// ---------------------------------------------------------------------------
+
+__device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A, int TR,
+                         int total) {
+  const uint64_t pol = policy_evict_first();
+  const int FT = a.I / 128, FD = a.H / 256;
+  uint32_t head = 0;
+  uint32_t rsz[kRecs];
+#pragma unroll
+  for (int j = 0; j < kRecs; ++j) rsz[j] = 0;
+  int s = 0, tail = 0;
+  bool ok = true;
+  for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+    const Item it = decode(S, A, i, TR, FT, FD);
+    if (!it.gu) {
+      const int need = (S.rtp[it.a + 1] - S.rtp[it.a]) * FT;
+      if (!wait_count(S, a.done + it.a, need)) {
+        ok = false;
+        break;
+      }
+      fence_proxy_async_global();
+    }
+    const int KB = it.gu ? a.H / 128 : a.I / 128;
+    const uint32_t size =
+        2 * kTileBytes + (uint32_t)(it.gu ? kXTerms : kHTerms) * (16u << it.box) * 128u;
+    const int wrow0 = it.gu ? it.e * a.I + it.tile * 128 : it.e * a.H + it.tile * 256;
+    for (int kb = 0; kb < KB; ++kb) {
+      const uint32_t pos = head + size <= a.ring_bytes ? head : 0;
+      while (tail < s) {
+        const int d = tail % kRecs;
+        const bool clash = s - tail >= kRecs || (pos < S.rec[d] + rsz[d] && S.rec[d] < pos + size);
+        if (!clash) break;
+        if (!wait_bar(S, &S.empty[d], (uint32_t)(tail / kRecs) & 1)) {
+          ok = false;
+          break;
+        }
+        ++tail;
+      }
+      if (!ok) break;
+      const int d = s % kRecs;
+      S.rec[d] = pos;
+      rsz[d] = size;
+      uint64_t *fb = &S.full[d];
+      mbar_expect_tx(fb, size);
+      uint8_t *dst = S.ring + pos;
+      const CUtensorMap *wmap = it.gu ? &m.wg : &m.wd;
+      tma_2d(dst, wmap, kb * 128, wrow0, fb, pol);
+      tma_2d(dst + kTileBytes, it.gu ? &m.wu : &m.wd, kb * 128, it.gu ? wrow0 : wrow0 + 128, fb,
+             pol);
+      tma_3d(dst + 2 * kTileBytes, it.gu ? &m.xq[it.box] : &m.hq[it.box], kb * 128, it.pos0, 0,
+             fb);
+      head = pos + size;
+      ++s;
+    }
+  }
+  if (!ok) fail(S, a);
+  // every copy this CTA issued has landed before it moves on
+  for (int j = max(tail, s - kRecs); j < s; ++j) {
+    const uint64_t t0 = gtime();
+    while (!mbar_poll(&S.full[j % kRecs], (uint32_t)(j / kRecs) & 1))
+      if (gtime() - t0 > kWaitNs) break;
+  }
+}
+
+__device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int total,
+                           uint32_t tmem) {
+  const int FT = a.I / 128, FD = a.H / 256;
+  const uint32_t ring = smem_addr(S.ring);
+  int s = 0;
+  bool ok = true;
+  for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+    const Item it = decode(S, A, i, TR, FT, FD);
+    const int KB = it.gu ? a.H / 128 : a.I / 128;
+    const int T = it.gu ? kXTerms : kHTerms;
+    const uint32_t id = idesc_e4m3(it.n16);
+    const uint32_t tstride = (16u << it.box) * 128u;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int d = s % kRecs, buf = s % kBufs;
+      if (!wait_bar(S, &S.full[d], (uint32_t)(s / kRecs) & 1) ||
+          (s >= kBufs && !wait_bar(S, &S.acce[buf], (uint32_t)(s / kBufs + 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t base = ring + S.rec[d];
+      const uint32_t d0 = tmem + (uint32_t)buf * 128u, d1 = d0 + 64u;
+      for (int t = 0; t < T; ++t) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bd = sdesc(base + 2 * kTileBytes + t * tstride + ks * 32);
+          const uint32_t acc = (t | ks) != 0;
+          mma_e4m3(d0, sdesc(base + ks * 32), bd, id, acc);
+          mma_e4m3(d1, sdesc(base + kTileBytes + ks * 32), bd, id, acc);
+        }
+      }
+      mma_commit(&S.empty[d]);
+      mma_commit(&S.accf[buf]);
+      ++s;
+    }
+  }
+  if (!ok) fail(S, a);
+  // every MMA this thread issued has completed before TMEM is freed
+  mma_commit(S.drain);
+  const uint64_t t0 = gtime();
+  while (!mbar_poll(S.drain, 0))
+    if (gtime() - t0 > kWaitNs) break;
+}
+
+// Gate+up finish of one item: h = silu(g) * u per (row, feature), written as
+// fp32 and as three E4M3 terms with a power-of-two scale per (row, this
+// 128-feature block); then the item is published.
+__device__ void finish_gate_up(const TcArgs &a, const Smem &S, const Item &it, int grp, int q,
+                               int lane, const float (&acc0)[16], const float (&acc1)[16]) {
+  const int c0 = grp * 16, f = q * 32 + lane, o = it.tile * 128 + f;
+  const int KBd = a.I / 128;
+  float hv[16];
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) {
+    const float xi = S.cs[c0 + jj];
+    hv[jj] = silu_f32(acc0[jj] * xi) * (acc1[jj] * xi);
+    if (c0 + jj < it.rows) a.h[(size_t)(it.pos0 + c0 + jj) * a.I + o] = hv[jj];
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv[jj])));
+    if (lane == 0) S.red[(grp * 4 + q) * 16 + jj] = m;
+  }
+  group_sync(grp);
+  float scl = 1.f;
+  if (lane < 16) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) m = max(m, S.red[(grp * 4 + qq) * 16 + lane]);
+    const int s = term_shift(m);
+    scl = pow2f(s);
+    if (q == 0 && c0 + lane < it.rows)
+      a.hs[(size_t)(it.pos0 + c0 + lane) * KBd + it.tile] = pow2f(-s);
+  }
+  const size_t plane = (size_t)a.max_total * a.I;
+#pragma unroll
+  for (int jj = 0; jj < 16; jj += 2) {
+    const float v0 = hv[jj] * __shfl_sync(0xFFFFFFFFu, scl, jj);
+    const float v1 = hv[jj + 1] * __shfl_sync(0xFFFFFFFFu, scl, jj + 1);
+    const uint32_t b0 = e4m3x2(v0, v1);
+    const float2 r0 = f16x2_to_float2(e4m3x2_to_f16x2((uint16_t)b0));
+    const float u0 = v0 - r0.x, u1 = v1 - r0.y;
+    const uint32_t b1 = e4m3x2(u0, u1);
+    const float2 r1 = f16x2_to_float2(e4m3x2_to_f16x2((uint16_t)b1));
+    const uint32_t b2 = e4m3x2(u0 - r1.x, u1 - r1.y);
+    const uint32_t bb[3] = {b0, b1, b2};
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      if (c0 + jj + h2 < it.rows) {
+        uint8_t *dst = a.hq + (size_t)(it.pos0 + c0 + jj + h2) * a.I + o;
+#pragma unroll
+        for (int t = 0; t < kHTerms; ++t) dst[t * plane] = (uint8_t)(bb[t] >> (8 * h2));
+      }
+    }
+  }
+}
+
+// Barrier over the 16 epilogue warps that also ORs a flag across them, so
+// that every warp takes the same branch after it.
+__device__ __forceinline__ bool epi_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(kEpiThreads)
+      : "memory");
+  return r != 0;
+}
+
+// The 16 promotion warps.  Warp w (2..17) reads TMEM lanes 32*(w%4)..+31
+// (its quadrant q of the 128 weight rows) and columns 16*g..16*g+15 (its
+// group g = (w-2)/4 of the item's token rows).  Every decision to leave the
+// item loop is taken after a vote over all 16 warps.
+__device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int total,
+                         uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ew = warp - 2, q = warp & 3, grp = ew >> 2;
+  const int et = threadIdx.x - 64;
+  const int FT = a.I / 128, FD = a.H / 256, KBd = a.I / 128;
+  const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+  const int c0 = grp * 16;
+  int s = 0;
+  int pending = -1;   // active index of a finished gate+up item not yet published
+  bool bad = false;
+  for (int i = blockIdx.x; i < total; i += gridDim.x) {
+    const Item it = decode(S, A, i, TR, FT, FD);
+    const int KB = it.gu ? a.H / 128 : KBd;
+    fence_proxy_async_global();   // this thread's h terms before the publish
+    if (epi_sync_or(bad || S.misc[0])) {
+      bad = true;
+      break;
+    }
+    if (et == 0) {
+      if (pending >= 0) {
+        __threadfence();
+        atomicAdd(a.done + pending, 1);
+      }
+      if (!it.gu) {
+        const int need = (S.rtp[it.a + 1] - S.rtp[it.a]) * FT;
+        if (!wait_count(S, a.done + it.a, need)) fail(S, a);
+      }
+    }
+    pending = -1;
+    // the item's weight block scales and per-row factors
+    if (it.gu) {
+      const size_t sb = ((size_t)it.e * FT + it.tile) * KB;
+      for (int j = et; j < KB; j += kEpiThreads) {
+        S.sc[j] = __ldg(a.sg + sb + j);
+        S.sc[kMaxKB + j] = __ldg(a.su + sb + j);
+      }
+      for (int j = et; j < kRowTile; j += kEpiThreads)
+        S.cs[j] = j < it.rows ? __ldcg(a.xs + it.pos0 + j) : 0.f;
+    } else {
+      const size_t sb = ((size_t)it.e * (a.H / 128) + 2 * it.tile) * KB;
+      for (int j = et; j < KB; j += kEpiThreads) {
+        S.sc[j] = __ldg(a.sd + sb + j);
+        S.sc[kMaxKB + j] = __ldg(a.sd + sb + KB + j);
+      }
+    }
+    // the dependency wait is over (or failed) before any h scale is read
+    if (epi_sync_or(S.misc[0])) {
+      bad = true;
+      break;
+    }
+    if (!it.gu) {
+      for (int idx = et; idx < KB * kRowTile; idx += kEpiThreads) {
+        const int kb = idx / kRowTile, j = idx - kb * kRowTile;
+        S.cs[idx] = j < it.rows ? __ldcg(a.hs + (size_t)(it.pos0 + j) * KBd + kb) : 0.f;
+      }
+      epi_sync_or(false);
+    }
+
+    float acc0[16], acc1[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) acc0[jj] = acc1[jj] = 0.f;
+    const bool mine = c0 < it.n16;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int buf = s % kBufs;
+      // every lane of the warp takes the same branch into the aligned TMEM loads
+      if (!__all_sync(0xFFFFFFFFu, wait_bar(S, &S.accf[buf], (uint32_t)(s / kBufs) & 1))) {
+        bad = true;
+        break;
+      }
+      tc_fence_after();
+      uint32_t r0[16], r1[16];
+      if (mine) {
+        const uint32_t t = lane_base + (uint32_t)buf * 128u + (uint32_t)c0;
+        tmem_ld16(t, r0);
+        tmem_ld16(t + 64u, r1);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acce[buf]);
+      ++s;
+      if (!mine) continue;
+      const float s0 = S.sc[kb], s1 = S.sc[kMaxKB + kb];
+      if (it.gu) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          acc0[jj] = fmaf(s0, __uint_as_float(r0[jj]), acc0[jj]);
+          acc1[jj] = fmaf(s1, __uint_as_float(r1[jj]), acc1[jj]);
+        }
+      } else {
+        const float *hf = S.cs + kb * kRowTile + c0;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const float hi = hf[jj];
+          acc0[jj] = fmaf(s0 * hi, __uint_as_float(r0[jj]), acc0[jj]);
+          acc1[jj] = fmaf(s1 * hi, __uint_as_float(r1[jj]), acc1[jj]);
+        }
+      }
+    }
+    // every warp finished the item's k blocks before any finishes the item
+    if (epi_sync_or(bad)) {
+      bad = true;
+      break;
+    }
+    if (it.gu) {
+      if (mine) finish_gate_up(a, S, it, grp, q, lane, acc0, acc1);
+      pending = it.a;
+    } else if (mine) {
+      const int f = q * 32 + lane;
+      const int o0 = it.tile * 256 + f;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj)
+        if (c0 + jj < it.rows) {
+          float *yr = a.y + (size_t)(it.pos0 + c0 + jj) * a.H + o0;
+          yr[0] = acc0[jj];
+          yr[128] = acc1[jj];
+        }
+    }
+  }
+  if (bad) fail(S, a);
+  // publish the last gate+up item
+  fence_proxy_async_global();
+  epi_sync_or(false);
+  if (et == 0 && pending >= 0 && !bad) {
+    __threadfence();
+    atomicAdd(a.done + pending, 1);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    verify_ffn_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ TcMaps maps) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Smem S = carve(smem, a);
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < kRecs; ++j) {
+      mbar_init(&S.full[j], 1);
+      mbar_init(&S.empty[j], 1);
+    }
+    for (int j = 0; j < kBufs; ++j) {
+      mbar_init(&S.accf[j], 1);
+      mbar_init(&S.acce[j], kEpiWarps);
+    }
+    mbar_init(S.drain, 1);
+    for (int j = 0; j < 16; ++j) S.misc[j] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr((const void *)(S.misc + 1))),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = (uint32_t)S.misc[1];
+  // the swizzled operand tiles assume a 1024-byte aligned ring
+  if ((smem_addr(S.ring) & 1023u) != 0) fail(S, a);
+
+  pdl_wait();   // the tables of the alignment are final
+  prep_x(a);
+  fence_proxy_async_global();
+  if (!grid_barrier(S, a.grid_ctr)) fail(S, a);
+  fence_proxy_async_global();
+  const int A = build_table(a, S);
+  const int TR = S.misc[3];
+  const int total = S.misc[0] ? 0 : TR * (a.I / 128 + a.H / 256);
+
+  if (warp == 0) {
+    if ((threadIdx.x & 31) == 0) producer(a, maps, S, A, TR, total);
+    __syncwarp();
+  } else if (warp == 1) {
+    if ((threadIdx.x & 31) == 0) mma_issuer(a, S, A, TR, total, tmem);
+    __syncwarp();
+  } else {
+    epilogue(a, S, A, TR, total, tmem);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host
+// ---------------------------------------------------------------------------
+
+// cuTensorMapEncodeTiled, from the driver through the runtime (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A tiled u8 map with the 128-byte swizzle (the operand layout of the MMAs).
+int encode(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
+           const cuuint64_t *strides, const cuuint32_t *box) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ECUDA;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void *>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_EUNSUPPORTED;
+}
+
+// Maps of one call, cached by (weights, workspace, shape): encoding is host
+// work that would otherwise repeat on every call.
+int tc_maps(const moe_experts *X, uint8_t *xq, uint8_t *hq, int max_total, TcMaps *out) {
+  struct Key {
+    const void *g, *u, *d, *xq, *hq;
+    int E, H, I, mt;
+    bool operator==(const Key &o) const {
+      return g == o.g && u == o.u && d == o.d && xq == o.xq && hq == o.hq && E == o.E &&
+             H == o.H && I == o.I && mt == o.mt;
+    }
+  };
+  struct KeyHash {
+    size_t operator()(const Key &k) const {
+      size_t h = std::hash<const void *>()(k.g);
+      for (const void *p : {k.u, k.d, k.xq, k.hq}) h = h * 1000003u ^ std::hash<const void *>()(p);
+      return h ^ ((size_t)k.E << 40) ^ ((size_t)k.H << 20) ^ (size_t)k.I ^ ((size_t)k.mt << 50);
+    }
+  };
+  static std::mutex mu;
+  static std::unordered_map<Key, TcMaps, KeyHash> cache;
+  const int E = X->num_experts, H = X->hidden, I = X->inter;
+  const Key key = {X->gate.codes, X->up.codes, X->down.codes, xq, hq, E, H, I, max_total};
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return MOE_OK;
+  }
+  TcMaps m;
+  const cuuint32_t wbox[2] = {128, 128};
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)E * I};
+    const cuuint64_t str[1] = {(cuuint64_t)H};
+    int st = encode(&m.wg, X->gate.codes, 2, dims, str, wbox);
+    if (!st) st = encode(&m.wu, X->up.codes, 2, dims, str, wbox);
+    if (st) return st;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)E * H};
+    const cuuint64_t str[1] = {(cuuint64_t)I};
+    const int st = encode(&m.wd, X->down.codes, 2, dims, str, wbox);
+    if (st) return st;
+  }
+  for (int b = 0; b < 3; ++b) {
+    const cuuint32_t xbox[3] = {128, (cuuint32_t)(16 << b), (cuuint32_t)kXTerms};
+    const cuuint64_t xd[3] = {(cuuint64_t)H, (cuuint64_t)max_total, (cuuint64_t)kXTerms};
+    const cuuint64_t xs[2] = {(cuuint64_t)H, (cuuint64_t)H * max_total};
+    int st = encode(&m.xq[b], xq, 3, xd, xs, xbox);
+    if (st) return st;
+    const cuuint32_t hbox[3] = {128, (cuuint32_t)(16 << b), (cuuint32_t)kHTerms};
+    const cuuint64_t hd[3] = {(cuuint64_t)I, (cuuint64_t)max_total, (cuuint64_t)kHTerms};
+    const cuuint64_t hs[2] = {(cuuint64_t)I, (cuuint64_t)I * max_total};
+    st = encode(&m.hq[b], hq, 3, hd, hs, hbox);
+    if (st) return st;
+  }
+  if (cache.size() > 1024) cache.clear();
+  cache.emplace(key, m);
+  *out = m;
+  return MOE_OK;
+}
+
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr size_t kMaxStage = 2 * kTileBytes + kHTerms * kRowTile * 128;
+
+size_t ring_bytes_for(int cap) {
+  const size_t fixed = fixed_bytes(cap);
+  if (fixed + 2 * kMaxStage > kSmemLimit) return 0;
+  return (kSmemLimit - fixed) / 1024 * 1024;
+}
+
+}  // namespace
+
+// Shape admission of the tensor-core path (host): FP8 routed experts, no
+// shared expert, H a multiple of 256 up to 8192, I a multiple of 128 up to
+// 4096, at most 65535 experts ids and room for the ring.
+bool tc_fits(const moe_layer_desc *L, int M) {
+  const moe_experts &R = L->routed;
+  if (R.fmt != MOE_FMT_FP8_B128 || L->shared) return false;
+  if (R.hidden % 256 || R.hidden > 128 * kMaxKB || R.inter % 128 || R.inter > 128 * kMaxKBd)
+    return false;
+  const int n = M * L->top_k;
+  const int cap = n < R.num_experts ? n : R.num_experts;
+  return ring_bytes_for(cap) != 0;
+}
+
+// Workspace of the tensor-core path: the term tables, their scales and the
+// per-expert counters (byte sizes, in order).
+void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]) {
+  const size_t H = L->routed.hidden, I = L->routed.inter;
+  bytes[0] = (size_t)kXTerms * max_total * H;
+  bytes[1] = (size_t)max_total * 4;
+  bytes[2] = (size_t)kHTerms * max_total * I;
+  bytes[3] = (size_t)max_total * (I / 128) * 4;
+  bytes[4] = (size_t)cap * 4;
+}
+
+int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *sti,
+              const int32_t *off, const int32_t *act, const int32_t *act_count,
+              const int32_t *ntpp, void *ws, const moe_workspace_view &v, uint32_t *err,
+              void *stream) {
+  const moe_experts &R = L->routed;
+  char *base = static_cast<char *>(ws);
+  TcArgs a = {};
+  a.M = M;
+  a.k = L->top_k;
+  a.n = M * L->top_k;
+  a.E = R.num_experts;
+  a.H = R.hidden;
+  a.I = R.inter;
+  a.cap = v.cap;
+  a.max_total = v.max_total;
+  a.x = x;
+  a.sti = sti;
+  a.off = off;
+  a.act = act;
+  a.act_count = act_count;
+  a.ntpp = ntpp;
+  a.sg = static_cast<const float *>(R.gate.scale);
+  a.su = static_cast<const float *>(R.up.scale);
+  a.sd = static_cast<const float *>(R.down.scale);
+  a.xq = reinterpret_cast<uint8_t *>(base + v.tc_x_terms);
+  a.xs = reinterpret_cast<float *>(base + v.tc_x_scale);
+  a.hq = reinterpret_cast<uint8_t *>(base + v.tc_h_terms);
+  a.hs = reinterpret_cast<float *>(base + v.tc_h_scale);
+  a.h = reinterpret_cast<float *>(base + v.h);
+  a.y = reinterpret_cast<float *>(base + v.y);
+  a.done = reinterpret_cast<int *>(base + v.tc_done);
+  a.grid_ctr = reinterpret_cast<unsigned long long *>(base + v.blend_counters);
+  a.err = err;
+  const size_t ring = ring_bytes_for(v.cap);
+  if (!ring) return MOE_EUNSUPPORTED;
+  a.ring_bytes = (uint32_t)ring;
+  TcMaps maps;
+  int st = tc_maps(&R, a.xq, a.hq, v.max_total, &maps);
+  if (st) return st;
+  const size_t smem = ring + fixed_bytes(v.cap);
+  st = ensure_smem_limit((const void *)verify_ffn_kernel, smem);
+  if (st) return st;
+  return launch_pdl_coop(verify_ffn_kernel, dim3(sm_count()), dim3(kThreads), smem, stream, a,
+                         maps);
+}
+
+}  // namespace moe

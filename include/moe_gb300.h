@@ -189,7 +189,8 @@ int moe_topk_softmax(const float *logits, int M, int num_experts, int top_k,
  *   path     MOE_PATH_AUTO / _SIMT / _TC; the grid is a function of
  *            (M, top_k, E, H, I, path).
  * Errors: MOE_EINVAL (NULL, M < 1 or > MOE_MAX_ROWS, bad fmt/path),
- * MOE_EUNSUPPORTED (shape not admitted; TC path not available for it). */
+ * MOE_EUNSUPPORTED (shape not admitted; MOE_PATH_TC, which only
+ * moe_decode_layer serves: its activation terms live in the layer workspace). */
 int moe_grouped_gate_up(const moe_experts *routed, const moe_experts *shared,
                         const uint16_t *x, int M, int top_k,
                         const int32_t *expert_offsets,
@@ -238,12 +239,19 @@ typedef struct moe_workspace_view {
     size_t num_tokens_post_padded;                 /* [1] */
     size_t h, h_shared, y, y_shared;               /* float tables */
     size_t blend_counters;                         /* internal: [1] uint64 grid-barrier count */
+    /* tensor-core path only (all 0 on the CUDA-core path): the activation
+     * terms it multiplies, as E4M3 planes with power-of-two scales --
+     * x = (t0 + t1) * x_scale[p] per sorted row [2][max_total][H] u8 and
+     * [max_total] float; h = (t0 + t1 + t2) * h_scale[p][c/128]
+     * [3][max_total][I] u8 and [max_total][I/128] float -- and an internal
+     * [cap] int32 count per active expert. */
+    size_t tc_x_terms, tc_x_scale, tc_h_terms, tc_h_scale, tc_done;
     size_t total_bytes;
     int max_total, max_blocks, cap;
 } moe_workspace_view;
 
 /* Host only.  Workspace bytes moe_decode_layer needs for any M <= max_M
- * (0 if the descriptor is invalid). */
+ * (the largest layout over 1..max_M; 0 if the descriptor is invalid). */
 size_t moe_decode_layer_workspace_bytes(const moe_layer_desc *layer, int max_M);
 
 /* Host only.  The workspace layout for M rows.  Returns MOE_EINVAL /
@@ -252,8 +260,9 @@ int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int M,
                                     moe_workspace_view *view);
 
 /* Host only.  The number of kernels moe_decode_layer enqueues for M rows
- * (1 on the fused decode path; otherwise 5 with router logits, 4 with given
- * ids), or -1 if the call would be rejected. */
+ * (1 on the fused decode path; 4 with router logits, 3 with given ids on the
+ * tensor-core path; otherwise 5 and 4), or -1 if the call would be
+ * rejected. */
 int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logits);
 
 /* The decode MoE layer of M rows ("forward_nvfp4_grouped_decode.rs",
@@ -267,6 +276,15 @@ int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logit
  * barrier, down, a grid barrier, the blend) instead of five launches; every
  * table and intermediate is still written to the workspace.  MOE_PATH_SIMT_STAGED
  * forces the five.
+ * On the tensor-core path (MOE_PATH_TC, or MOE_PATH_AUTO when the fused path
+ * does not serve the call and the routed experts are FP8 with hidden a
+ * multiple of 256 up to 8192, inter a multiple of 128 up to 4096 and no
+ * shared expert) gate+up and down run as one cooperative persistent kernel
+ * of tcgen05 MMAs between the alignment and the blend ("fp8_moe_grouped.rs",
+ * the tensor-core twins of the grouped launchers): E4M3 weight codes times
+ * exact E4M3 splits of x and h, each 128-wide k block promoted to fp32 times
+ * its block scale.  Its h and y are the same quantities as on the CUDA-core
+ * path, within the layer tolerance.
  *   x [M][H] bf16 bits; out [M][H] bf16 bits;
  *   workspace: device, >= moe_decode_layer_workspace_bytes(layer, M) bytes,
  *   256-byte aligned, used only by this call (its intermediates can be read

@@ -110,6 +110,38 @@ def test_workspace_layout_host_only():
     assert moe.workspace_bytes(layer, 1) < nb < moe.workspace_bytes(layer, 128)
 
 
+def test_tensor_core_workspace_host_only():
+    """FP8 routed experts without a shared expert get the tensor-core term
+    tables appended to the workspace: [2][max_total][H] and [3][max_total][I]
+    E4M3 planes, their float scales and a per-active-expert count."""
+    lib = moe.load()
+    layer = moe.LayerDesc(top_k=8, block_size=64, routed=_fake_experts(E=256, H=4096, I=1536))
+    v = moe._WsView()
+    assert lib.moe_decode_layer_workspace_view(ctypes.pointer(layer._struct), 128,
+                                               ctypes.byref(v)) == 0
+    mt, _, cap = oracle.align_sizes(1024, 256, 64)
+    offs = [v.blend_counters, v.tc_x_terms, v.tc_x_scale, v.tc_h_terms, v.tc_h_scale, v.tc_done]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert v.tc_x_scale - v.tc_x_terms >= 2 * mt * 4096
+    assert v.tc_h_terms - v.tc_x_scale >= mt * 4
+    assert v.tc_h_scale - v.tc_h_terms >= 3 * mt * 1536
+    assert v.tc_done - v.tc_h_scale >= mt * 12 * 4
+    assert v.total_bytes - v.tc_done >= cap * 4
+    assert moe.workspace_bytes(layer, 128) == v.total_bytes
+    # the tensor-core run is 4 launches with router logits, 3 with given ids
+    assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 1) == 4
+    assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 0) == 3
+    # not for NVFP4 experts, nor when the CUDA-core path is forced
+    for lay in (moe.LayerDesc(top_k=8, block_size=64,
+                              routed=_fake_experts(fmt=moe.FMT_NVFP4_G16, E=256, H=4096,
+                                                   I=1536)),
+                moe.LayerDesc(top_k=8, block_size=64, path=moe.PATH_SIMT_STAGED,
+                              routed=_fake_experts(E=256, H=4096, I=1536))):
+        assert lib.moe_decode_layer_workspace_view(ctypes.pointer(lay._struct), 128,
+                                                   ctypes.byref(v)) == 0
+        assert v.tc_x_terms == v.tc_h_terms == v.tc_done == 0
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(fmt=moe.FMT_FP8_B128, H=2000), moe.MOE_EUNSUPPORTED),   # FP8 needs H % 128
     (dict(fmt=moe.FMT_NVFP4_G16, I=784), moe.MOE_EUNSUPPORTED),   # NVFP4 needs I % 32

@@ -1,0 +1,182 @@
+"""The tensor-core (tcgen05) expert path of the decode MoE layer against the
+oracle.
+
+The path multiplies the E4M3 weight codes by E4M3 splits of the activations
+(x = t0 + t1 exactly, h = t0 + t1 + t2 to 12 significant bits, each with a
+power-of-two scale) and promotes every 128-wide k block to fp32 times its
+block scale.  Checked here: the layer output within the workload's tolerance
+on the tiny, decode and verify shapes; h against the oracle's gate+up on the
+same x; y against the oracle's down of the layer's own h; the split of x exact
+and the split of h within its bound; ragged row tiles (16/17 rows, a full
+64-row tile plus one row, two tiles of one expert); run-to-run bit equality and
+CUDA-graph replay."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+TC = 2
+STAGED = 3
+
+# h: exact x and weight codes, fp32 promotion of each 128-wide k block; the
+# same fp32 accumulation error as the CUDA-core path (see helpers).
+TC_H_REL_L2 = H.STAGE_REL_L2
+# y: its input h is carried as three E4M3 terms, at most 2^-12 relative plus
+# 2^-10 of the (row, block) scale per element, so y's relative L2 error is at
+# most about 2.4e-4; 5e-4 leaves 2x margin.
+TC_Y_REL_L2 = 5e-4
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import expert_routing_alignment_gb300 as m
+    m.load()
+    return m
+
+
+def _shape(name, M, H_, I, E, k, BS):
+    return synth.LayerShape(name, M, H_, I, E, k, BS, synth.FMT_FP8)
+
+
+SHAPES = [synth.tiny(), synth.decode_fp8(1), synth.decode_fp8(8),
+          _shape("decode_h2048_i768_e128_k8_fp8_m64", 64, 2048, 768, 128, 8, 16)]
+
+
+def _tables_and_real(view, shape):
+    tables = oracle.align(view["topk_ids"].cpu().numpy(), shape.E, shape.BS)
+    return tables, tables["sorted_token_ids"] < shape.n
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
+def test_tc_layer_matches_oracle(moe, shape):
+    inp = synth.make_layer(shape, 1000, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, view, (layer, _) = H.gpu_layer(moe, inp, path=TC, err=err)
+    assert moe.moe_decode_layer_launches(layer, shape.M) == 4
+    assert int(err.item()) == 0
+    _, ref_b, bad = H.oracle_layer(inp)
+    assert bad == 0
+    rl2, mx = H.compare_bf16(out, ref_b)
+    assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
+
+    tables, real = _tables_and_real(view, shape)
+    for key in ("sorted_token_ids", "expert_offsets", "token_to_perm"):
+        np.testing.assert_array_equal(view[key].cpu().numpy(), tables[key], err_msg=key)
+    X = H.oracle_experts(inp.experts.to("cpu"))
+    h_ref, _ = oracle.grouped_gate_up(X, None, synth.bf16_bits(inp.x), shape.M, shape.top_k,
+                                      tables)
+    h_gpu = view["h"].cpu().numpy().astype(np.float64)
+    assert H.rel_l2(h_gpu[real], h_ref[real]) < TC_H_REL_L2
+    y_ref, _ = oracle.grouped_down(X, None, h_gpu, None, shape.M, shape.top_k, tables)
+    y_gpu = view["y"].cpu().numpy().astype(np.float64)
+    assert H.rel_l2(y_gpu[real], y_ref[real]) < TC_Y_REL_L2
+
+
+def _e4m3(t: torch.Tensor) -> torch.Tensor:
+    return t.contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+
+
+def test_tc_x_terms_exact_and_h_terms_bounded(moe):
+    shape = synth.decode_fp8(8)
+    inp = synth.make_layer(shape, 321, device="cuda")
+    _, view, _ = H.gpu_layer(moe, inp, path=TC)
+    tables, real = _tables_and_real(view, shape)
+    pos = np.nonzero(real)[0]
+    tok = tables["sorted_token_ids"][pos] // shape.top_k
+    pos_t = torch.as_tensor(pos, device="cuda")
+
+    # x: (t0 + t1) * xs == x exactly where |x| * 2^s >= 2^-2, and within 2^-10
+    # of the scale elsewhere; the row maximum lands in [128, 256)
+    xq = view["tc_x_terms"][:, pos_t]
+    xs = view["tc_x_scale"][pos_t].to(torch.float64)[:, None]
+    rec = (_e4m3(xq[0]) + _e4m3(xq[1])) * xs
+    x = inp.x[torch.as_tensor(tok, device="cuda")].to(torch.float64)
+    scaled = x.abs() / xs
+    big = scaled >= 0.25
+    assert bool((rec[big] == x[big]).all())
+    assert bool(((rec - x).abs() <= xs * 2.0 ** -10).all())
+    mx = scaled.amax(dim=1)
+    assert bool(((mx >= 128) & (mx < 256)).all())
+
+    # h: |sum of three terms * hs - h| <= 2^-12 |h| + 2^-10 hs per (row, block)
+    I = shape.I
+    hq = view["tc_h_terms"][:, pos_t]
+    hs = view["tc_h_scale"][pos_t].to(torch.float64).repeat_interleave(128, dim=1)
+    rec = (_e4m3(hq[0]) + _e4m3(hq[1]) + _e4m3(hq[2])) * hs
+    h = view["h"][pos_t].to(torch.float64)
+    assert rec.shape == h.shape == (len(pos), I)
+    assert bool(((rec - h).abs() <= h.abs() * 2.0 ** -12 + hs * 2.0 ** -10).all())
+    bmax = (h.abs() / hs).reshape(len(pos), I // 128, 128).amax(dim=2)
+    assert bool(((bmax >= 128) & (bmax < 256)).all())
+
+
+@pytest.mark.parametrize("rows", [(16, 17), (64, 1), (65, 63), (128,)], ids=str)
+def test_tc_row_tile_edges(moe, rows):
+    """Given ids (top_k = 1): expert 3 takes rows[0] tokens, expert 5 the next
+    rows[1], and so on -- item boundaries at 16-row MMA steps and 64-row tiles."""
+    M = sum(rows)
+    shape = _shape(f"tc_edges_m{M}", M, 256, 512, 8, 1, 16)
+    inp = synth.make_layer(shape, 55, device="cuda")
+    ids = np.concatenate([np.full(r, e, np.int32) for r, e in zip(rows, (3, 5, 6))])[:, None]
+    w = np.ones((M, 1), np.float32)
+    ids_t = torch.as_tensor(ids, device="cuda")
+    w_t = torch.as_tensor(w, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, view, _ = H.gpu_layer(moe, inp, path=TC, use_logits=False, ids=ids_t, w=w_t, err=err)
+    assert int(err.item()) == 0
+    _, ref_b, bad = H.oracle_layer(inp, ids=ids, w=w.astype(np.float64))
+    assert bad == 0
+    rl2, mx = H.compare_bf16(out, ref_b)
+    assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
+
+
+def test_tc_deterministic_and_graph_replayable(moe):
+    shape = _shape("decode_h2048_i768_e128_k8_fp8_m32", 32, 2048, 768, 128, 8, 16)
+    inp = synth.make_layer(shape, 9, device="cuda")
+    out1, _, (layer, ws) = H.gpu_layer(moe, inp, path=TC)
+    out2 = torch.empty_like(out1)
+    moe.moe_decode_layer(layer, inp.x, out2, ws, router_logits=inp.logits)
+    torch.cuda.synchronize()
+    assert bool((out1.view(torch.int16) == out2.view(torch.int16)).all())
+    # one captured graph, replayed on fresh logits, equals direct calls
+    lg = inp.logits.clone()
+    out3 = torch.empty_like(out1)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        moe.moe_decode_layer(layer, inp.x, out3, ws, router_logits=lg)
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        moe.moe_decode_layer(layer, inp.x, out3, ws, router_logits=lg)
+    lg.copy_(synth.make_logits(shape.M, shape.E, 77, device="cuda"))
+    with torch.cuda.stream(st):
+        g.replay()
+    st.synchronize()
+    ref = torch.empty_like(out1)
+    moe.moe_decode_layer(layer, inp.x, ref, ws, router_logits=lg)
+    torch.cuda.synchronize()
+    assert bool((out3.view(torch.int16) == ref.view(torch.int16)).all())
+
+
+def test_tc_verify_batch_matches_staged_path(moe):
+    """The M = 128 verify batch (E = 256, H = 4096, I = 1536, BS = 64, Zipf
+    bias) takes the tensor-core path by default; its output agrees with the
+    CUDA-core staged path's within the layer tolerance on every row (the
+    oracle checks sampled rows in test_layer_gpu)."""
+    shape = synth.verify_fp8(128)
+    inp = synth.make_layer(shape, 1000, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out_tc, view, (layer, _) = H.gpu_layer(moe, inp, err=err)
+    assert moe.moe_decode_layer_launches(layer, shape.M) == 4
+    assert int(err.item()) == 0
+    assert "tc_x_terms" in view
+    out_st, _, _ = H.gpu_layer(moe, inp, path=STAGED)
+    rl2, mx = H.compare_bf16(out_tc, synth.bf16_bits(out_st))
+    assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
