@@ -19,10 +19,10 @@ int launch_blend(const float *y, const float *w, const int32_t *ttp, const float
 bool fused_fits(const moe_layer_desc *L, int M, int sms);
 bool tc_fits(const moe_layer_desc *L, int M);
 void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]);
-int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *sti,
-              const int32_t *off, const int32_t *act, const int32_t *act_count,
-              const int32_t *ntpp, void *ws, const moe_workspace_view &v, uint32_t *err,
-              void *stream);
+int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *ids,
+              const float *w, const int32_t *ttp, const int32_t *off, const int32_t *act,
+              const int32_t *act_count, uint16_t *out, void *ws, const moe_workspace_view &v,
+              uint32_t *err, void *stream);
 int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float *logits,
                  const int32_t *ids, const float *w, uint16_t *out, void *ws,
                  const moe_workspace_view &v, uint32_t *err, void *stream);
@@ -169,7 +169,7 @@ extern "C" int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int
   const int run = moe::layer_run(layer, M);
   if (run < 0) return -1;
   if (run == moe::kRunFused) return 1;
-  if (run == moe::kRunTc) return with_logits ? 4 : 3;
+  if (run == moe::kRunTc) return with_logits ? 3 : 2;
   return with_logits ? 5 : 4;
 }
 
@@ -210,13 +210,10 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
                  I32(v.active_experts), I32(v.active_count), I32(v.num_tokens_post_padded),
                  err_word, stream);
   if (st) return st;
-  if (run == moe::kRunTc) {
-    st = moe::launch_tc(layer, x, M, I32(v.sorted_token_ids), I32(v.expert_offsets),
-                        I32(v.active_experts), I32(v.active_count),
-                        I32(v.num_tokens_post_padded), workspace, v, err_word, stream);
-    if (st) return st;
-    return moe::launch_blend(F32(v.y), w, I32(v.token_to_perm), nullptr, out, M, k, H, stream);
-  }
+  if (run == moe::kRunTc)
+    return moe::launch_tc(layer, x, M, ids, w, I32(v.token_to_perm), I32(v.expert_offsets),
+                          I32(v.active_experts), I32(v.active_count), out, workspace, v,
+                          err_word, stream);
   st = moe::simt_gate_up(&layer->routed, S, x, M, k, I32(v.expert_offsets),
                          I32(v.sorted_token_ids), I32(v.active_experts), I32(v.active_count),
                          F32(v.h), S ? F32(v.h_shared) : nullptr, stream);

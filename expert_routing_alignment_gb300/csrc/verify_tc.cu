@@ -62,7 +62,10 @@ constexpr uint64_t kWaitNs = 2000000000ull;    // a wait gives up after ~2 s
 struct TcArgs {
   int M, k, n, E, H, I, cap, max_total;
   const uint16_t *x;
-  const int32_t *sti, *off, *act, *act_count, *ntpp;
+  const int32_t *ids;                        // [n] expert of each slot
+  const float *w;                            // [n] routing weight of each slot
+  const int32_t *ttp, *off, *act, *act_count;   // the alignment's tables
+  uint16_t *out;                             // [M][H] bf16
   const float *sg, *su, *sd;                 // block scales [E][R/128][K/128]
   uint8_t *xq;                               // x terms [2][max_total][H] E4M3
   float *xs;                                 // 2^-s of each x row [max_total]
@@ -75,10 +78,11 @@ struct TcArgs {
   uint32_t ring_bytes;
 };
 
-// Weight maps: 2-D {K bytes, E*R rows}, box {128, 128}.  Term maps: 3-D
-// {K bytes, max_total rows, terms}, box {128, 16 << b, terms} for b = 0..2.
+// Weight maps: 3-D {128, E*R rows, K/128 column blocks}, box {128, 128, nb}
+// for nb = 1, 2 (w[projection][nb-1]).  Term maps: 3-D {K bytes, max_total
+// rows, terms}, box {128, 16 << b, terms} for b = 0..2.
 struct TcMaps {
-  CUtensorMap wg, wu, wd;
+  CUtensorMap w[3][2];
   CUtensorMap xq[3], hq[3];
 };
 
@@ -259,12 +263,13 @@ __device__ __forceinline__ void tmem_wait_ld() {
 // tensor copies
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                       uint64_t *bar, uint64_t policy) {
+__device__ __forceinline__ void tma_3d_hint(void *dst, const CUtensorMap *map, int x, int y,
+                                            int z, uint64_t *bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
+      "l"(policy)
       : "memory");
 }
 
@@ -288,6 +293,7 @@ struct Item {
   int rows;      // real rows in the tile (1..64)
   int n16;       // MMA N: rows rounded up to 16
   int box;       // term box: 16 << box rows
+  int kps;       // k blocks per stage: 2 for up to 32 rows, else 1
   int tile;      // gate+up: 128-row tile of I; down: pair of 128-row tiles of H
 };
 
@@ -321,38 +327,47 @@ __device__ __forceinline__ Item decode(const Smem &S, int A, int i, int TR, int 
   it.rows = min(kRowTile, rows_e - rt * kRowTile);
   it.n16 = (it.rows + 15) & ~15;
   it.box = it.n16 <= 16 ? 0 : (it.n16 <= 32 ? 1 : 2);
+  it.kps = it.n16 <= 32 ? 2 : 1;
   return it;
 }
 
 // ---------------------------------------------------------------------------
-// phase 0: x terms of every real sorted position
+// phase 0: x terms of every routed slot
 // ---------------------------------------------------------------------------
 //
-// Row p (token t = sorted_token_ids[p] / k): s = shift putting max|x[t]| in
-// [128, 256); xs[p] = 2^-s; t0 = e4m3(x * 2^s), t1 = e4m3(x * 2^s - t0).  A
-// bf16 value has 8 significant bits and each E4M3 term 4, so t0 + t1 equals
-// x * 2^s exactly wherever the residual is not below E4M3's subnormal step
-// (elements smaller than 2^-10 of the row maximum lose bits of at most
-// 2^-18 of that maximum).
+// Slot i (token t = i / k) at sorted position p = token_to_perm[i]: s = shift
+// putting max|x[t]| in [128, 256); xs[p] = 2^-s; t0 = e4m3(x * 2^s),
+// t1 = e4m3(x * 2^s - t0).  A bf16 value has 8 significant bits and each E4M3
+// term 4, so t0 + t1 equals x * 2^s exactly wherever the residual is not
+// below E4M3's subnormal step (elements smaller than 2^-10 of the row maximum
+// lose bits of at most 2^-18 of that maximum).  One warp per slot, its
+// row's loads in flight together (16 per lane for H = 4096).
 __device__ void prep_x(const TcArgs &a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < a.cap; i += kThreads) a.done[i] = 0;
-  const int ntpp = min(__ldcg(a.ntpp), a.max_total);
   const int nw = gridDim.x * kWarps;
   const size_t plane = (size_t)a.max_total * a.H;
-  for (int p = blockIdx.x * kWarps + warp; p < ntpp; p += nw) {
-    const int slot = __ldcg(a.sti + p);
-    if (slot < 0 || slot >= a.n) continue;
-    const uint16_t *xr = a.x + (size_t)(slot / a.k) * a.H;
+  for (int i = blockIdx.x * kWarps + warp; i < a.n; i += nw) {
+    const int p = __ldcg(a.ttp + i);
+    if (p < 0 || p >= a.max_total) continue;
+    const uint16_t *xr = a.x + (size_t)(i / a.k) * a.H;
     uint32_t mx = 0;
-    for (int c = lane * 8; c < a.H; c += 256) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + c));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int c0 = 0; c0 < a.H; c0 += 16 * 256) {
+      uint4 v[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        mx = max(mx, (w[i] & 0x7FFFu) << 16);
-        mx = max(mx, (w[i] >> 16 & 0x7FFFu) << 16);
+      for (int j = 0; j < 16; ++j) {
+        const int c = c0 + j * 256 + lane * 8;
+        v[j] = c < a.H ? __ldg(reinterpret_cast<const uint4 *>(xr + c)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          mx = max(mx, (w[h] & 0x7FFFu) << 16);
+          mx = max(mx, (w[h] >> 16 & 0x7FFFu) << 16);
+        }
       }
     }
     mx = __reduce_max_sync(0xFFFFFFFFu, mx);
@@ -361,19 +376,20 @@ __device__ void prep_x(const TcArgs &a) {
     if (lane == 0) a.xs[p] = pow2f(-s);
     uint8_t *q0 = a.xq + (size_t)p * a.H;
     uint8_t *q1 = q0 + plane;
+#pragma unroll 4
     for (int c = lane * 8; c < a.H; c += 256) {
       const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + c));
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t t0[2] = {0, 0}, t1[2] = {0, 0};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float f0 = bf16_to_float((uint16_t)(w[i] & 0xFFFFu)) * scl;
-        const float f1 = bf16_to_float((uint16_t)(w[i] >> 16)) * scl;
+      for (int h = 0; h < 4; ++h) {
+        const float f0 = bf16_to_float((uint16_t)(w[h] & 0xFFFFu)) * scl;
+        const float f1 = bf16_to_float((uint16_t)(w[h] >> 16)) * scl;
         const uint32_t b0 = e4m3x2(f0, f1);
         const float2 back = f16x2_to_float2(e4m3x2_to_f16x2((uint16_t)b0));
         const uint32_t b1 = e4m3x2(f0 - back.x, f1 - back.y);
-        t0[i >> 1] |= b0 << (16 * (i & 1));
-        t1[i >> 1] |= b1 << (16 * (i & 1));
+        t0[h >> 1] |= b0 << (16 * (h & 1));
+        t1[h >> 1] |= b1 << (16 * (h & 1));
       }
       *reinterpret_cast<uint2 *>(q0 + c) = make_uint2(t0[0], t0[1]);
       *reinterpret_cast<uint2 *>(q1 + c) = make_uint2(t1[0], t1[1]);
@@ -408,23 +424,25 @@ __device__ bool grid_barrier(const Smem &S, unsigned long long *ctr) {
 }
 
 // The active list as row tiles: info[a] = {run offset, expert | rows << 16},
-// rtp = exclusive prefix of ceil(rows / 64).  Returns the active count.
+// rtp = exclusive prefix of ceil(rows / 64).  An expert's rows are its slot
+// count, taken here from the ids (a shared-memory histogram in the ring,
+// which is not in use yet).  Returns the active count.
 __device__ int build_table(const TcArgs &a, const Smem &S) {
+  int *cnt = reinterpret_cast<int *>(S.ring);
+  for (int e = threadIdx.x; e < a.E; e += kThreads) cnt[e] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < a.n; i += kThreads) {
+    const int e = __ldcg(a.ids + i);
+    if (e >= 0 && e < a.E) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
   const int A = min(max(__ldcg(a.act_count), 0), a.cap);
   for (int i = threadIdx.x; i < A; i += kThreads) {
     const int e = __ldcg(a.act + i);
     int o = 0, rows = 0;
     if (e >= 0 && e < a.E) {
       o = __ldcg(a.off + e);
-      int lo = o, hi = __ldcg(a.off + e + 1);   // real slots first, then the sentinel n
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldcg(a.sti + mid) < a.n)
-          lo = mid + 1;
-        else
-          hi = mid;
-      }
-      rows = min(lo - o, 0x7FFF);
+      rows = min(cnt[e], 0x7FFF);
     }
     S.info[i] = make_int2(o, (e & 0xFFFF) | (rows << 16));
     S.rtp[i] = (rows + kRowTile - 1) / kRowTile;   // counts; scanned below
@@ -479,16 +497,27 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
       fence_proxy_async_global();
     }
     const int KB = it.gu ? a.H / 128 : a.I / 128;
-    const uint32_t size =
-        2 * kTileBytes + (uint32_t)(it.gu ? kXTerms : kHTerms) * (16u << it.box) * 128u;
+    const uint32_t bterm = (uint32_t)(it.gu ? kXTerms : kHTerms) * (16u << it.box) * 128u;
+    const uint32_t abytes = (uint32_t)it.kps * kTileBytes;
+    const uint32_t size = 2 * abytes + (uint32_t)it.kps * bterm;
     const int wrow0 = it.gu ? it.e * a.I + it.tile * 128 : it.e * a.H + it.tile * 256;
-    for (int kb = 0; kb < KB; ++kb) {
+    const CUtensorMap *w0 = it.gu ? &m.w[0][it.kps - 1] : &m.w[2][it.kps - 1];
+    const CUtensorMap *w1 = it.gu ? &m.w[1][it.kps - 1] : w0;
+    const int wrow1 = it.gu ? wrow0 : wrow0 + 128;
+    const CUtensorMap *bmap = it.gu ? &m.xq[it.box] : &m.hq[it.box];
+    for (int kb = 0; kb < KB; kb += it.kps) {
+      // Stages are freed oldest first; after two wraps an in-flight stage
+      // other than the oldest can cover the new range, so every in-flight
+      // stage is checked and the oldest retired until none overlaps.
       const uint32_t pos = head + size <= a.ring_bytes ? head : 0;
       while (tail < s) {
-        const int d = tail % kRecs;
-        const bool clash = s - tail >= kRecs || (pos < S.rec[d] + rsz[d] && S.rec[d] < pos + size);
+        bool clash = s - tail >= kRecs;
+        for (int j = tail; j < s && !clash; ++j) {
+          const int dj = j % kRecs;
+          clash = pos < S.rec[dj] + rsz[dj] && S.rec[dj] < pos + size;
+        }
         if (!clash) break;
-        if (!wait_bar(S, &S.empty[d], (uint32_t)(tail / kRecs) & 1)) {
+        if (!wait_bar(S, &S.empty[tail % kRecs], (uint32_t)(tail / kRecs) & 1)) {
           ok = false;
           break;
         }
@@ -501,12 +530,10 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
       uint64_t *fb = &S.full[d];
       mbar_expect_tx(fb, size);
       uint8_t *dst = S.ring + pos;
-      const CUtensorMap *wmap = it.gu ? &m.wg : &m.wd;
-      tma_2d(dst, wmap, kb * 128, wrow0, fb, pol);
-      tma_2d(dst + kTileBytes, it.gu ? &m.wu : &m.wd, kb * 128, it.gu ? wrow0 : wrow0 + 128, fb,
-             pol);
-      tma_3d(dst + 2 * kTileBytes, it.gu ? &m.xq[it.box] : &m.hq[it.box], kb * 128, it.pos0, 0,
-             fb);
+      tma_3d_hint(dst, w0, 0, wrow0, kb, fb, pol);
+      tma_3d_hint(dst + abytes, w1, 0, wrow1, kb, fb, pol);
+      for (int j = 0; j < it.kps; ++j)
+        tma_3d(dst + 2 * abytes + j * bterm, bmap, (kb + j) * 128, it.pos0, 0, fb);
       head = pos + size;
       ++s;
     }
@@ -524,7 +551,8 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
                            uint32_t tmem) {
   const int FT = a.I / 128, FD = a.H / 256;
   const uint32_t ring = smem_addr(S.ring);
-  int s = 0;
+  int s = 0;   // stages
+  int q = 0;   // k blocks (TMEM buffer uses)
   bool ok = true;
   for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
     const Item it = decode(S, A, i, TR, FT, FD);
@@ -532,27 +560,37 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
     const int T = it.gu ? kXTerms : kHTerms;
     const uint32_t id = idesc_e4m3(it.n16);
     const uint32_t tstride = (16u << it.box) * 128u;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int d = s % kRecs, buf = s % kBufs;
-      if (!wait_bar(S, &S.full[d], (uint32_t)(s / kRecs) & 1) ||
-          (s >= kBufs && !wait_bar(S, &S.acce[buf], (uint32_t)(s / kBufs + 1) & 1))) {
+    const uint32_t abytes = (uint32_t)it.kps * kTileBytes;
+    for (int kb = 0; kb < KB && ok; kb += it.kps) {
+      const int d = s % kRecs;
+      if (!wait_bar(S, &S.full[d], (uint32_t)(s / kRecs) & 1)) {
         ok = false;
         break;
       }
-      tc_fence_after();
       const uint32_t base = ring + S.rec[d];
-      const uint32_t d0 = tmem + (uint32_t)buf * 128u, d1 = d0 + 64u;
-      for (int t = 0; t < T; ++t) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = sdesc(base + 2 * kTileBytes + t * tstride + ks * 32);
-          const uint32_t acc = (t | ks) != 0;
-          mma_e4m3(d0, sdesc(base + ks * 32), bd, id, acc);
-          mma_e4m3(d1, sdesc(base + kTileBytes + ks * 32), bd, id, acc);
+      for (int j = 0; j < it.kps; ++j) {
+        const int buf = q % kBufs;
+        if (q >= kBufs && !wait_bar(S, &S.acce[buf], (uint32_t)(q / kBufs + 1) & 1)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        const uint32_t a0 = base + j * kTileBytes, a1 = a0 + abytes;
+        const uint32_t b0 = base + 2 * abytes + j * T * tstride;
+        const uint32_t d0 = tmem + (uint32_t)buf * 128u, d1 = d0 + 64u;
+        for (int t = 0; t < T; ++t) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = sdesc(b0 + t * tstride + ks * 32);
+            const uint32_t acc = (t | ks) != 0;
+            mma_e4m3(d0, sdesc(a0 + ks * 32), bd, id, acc);
+            mma_e4m3(d1, sdesc(a1 + ks * 32), bd, id, acc);
+          }
+        }
+        mma_commit(&S.accf[buf]);
+        ++q;
       }
       mma_commit(&S.empty[d]);
-      mma_commit(&S.accf[buf]);
       ++s;
     }
   }
@@ -821,6 +859,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(kTmemCols)
                  : "memory");
   }
+
+  // ---- blend: every y row is written before any CTA blends its share ------
+  //   out[t][c] = bf16_rn(sum_j w[t][j] * y[token_to_perm[t*k+j]][c]), fp32,
+  //   j ascending ("fp8_moe_grouped.rs", moe_weighted_sum_blend_fp8_grouped)
+  if (!grid_barrier(S, a.grid_ctr) || S.misc[0]) {
+    if (threadIdx.x == 0 && a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
+    return;
+  }
+  const long long T4 = (long long)a.M * a.H / 4;
+  const long long o1 = T4 * (blockIdx.x + 1) / gridDim.x;
+  for (long long o = T4 * blockIdx.x / gridDim.x + threadIdx.x; o < o1; o += kThreads) {
+    const int t = (int)(o * 4 / a.H), c = (int)(o * 4 % a.H);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < a.k; ++j) {
+      const int p = __ldcg(a.ttp + (size_t)t * a.k + j);
+      if (p < 0) continue;
+      const float wj = __ldcg(a.w + (size_t)t * a.k + j);
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.y + (size_t)p * a.H + c));
+      acc.x = fmaf(wj, v.x, acc.x);
+      acc.y = fmaf(wj, v.y, acc.y);
+      acc.z = fmaf(wj, v.z, acc.z);
+      acc.w = fmaf(wj, v.w, acc.w);
+    }
+    const uint32_t lo =
+        (uint32_t)float_to_bf16_rn(acc.x) | ((uint32_t)float_to_bf16_rn(acc.y) << 16);
+    const uint32_t hi =
+        (uint32_t)float_to_bf16_rn(acc.z) | ((uint32_t)float_to_bf16_rn(acc.w) << 16);
+    *reinterpret_cast<uint2 *>(a.out + (size_t)t * a.H + c) = make_uint2(lo, hi);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -884,19 +951,17 @@ int tc_maps(const moe_experts *X, uint8_t *xq, uint8_t *hq, int max_total, TcMap
     return MOE_OK;
   }
   TcMaps m;
-  const cuuint32_t wbox[2] = {128, 128};
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)E * I};
-    const cuuint64_t str[1] = {(cuuint64_t)H};
-    int st = encode(&m.wg, X->gate.codes, 2, dims, str, wbox);
-    if (!st) st = encode(&m.wu, X->up.codes, 2, dims, str, wbox);
-    if (st) return st;
-  }
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)E * H};
-    const cuuint64_t str[1] = {(cuuint64_t)I};
-    const int st = encode(&m.wd, X->down.codes, 2, dims, str, wbox);
-    if (st) return st;
+  const void *codes[3] = {X->gate.codes, X->up.codes, X->down.codes};
+  for (int j = 0; j < 3; ++j) {
+    const int K = j < 2 ? H : I, R = j < 2 ? I : H;
+    // [E*R][K] seen as {128 bytes, rows, K/128 column blocks}
+    const cuuint64_t dims[3] = {128, (cuuint64_t)E * R, (cuuint64_t)K / 128};
+    const cuuint64_t str[2] = {(cuuint64_t)K, 128};
+    for (int nb = 1; nb <= 2; ++nb) {
+      const cuuint32_t box[3] = {128, 128, (cuuint32_t)nb};
+      const int st = encode(&m.w[j][nb - 1], codes[j], 3, dims, str, box);
+      if (st) return st;
+    }
   }
   for (int b = 0; b < 3; ++b) {
     const cuuint32_t xbox[3] = {128, (cuuint32_t)(16 << b), (cuuint32_t)kXTerms};
@@ -917,7 +982,9 @@ int tc_maps(const moe_experts *X, uint8_t *xq, uint8_t *hq, int max_total, TcMap
 }
 
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr size_t kMaxStage = 2 * kTileBytes + kHTerms * kRowTile * 128;
+// the largest stage: two k blocks of two weight tiles and of 32 rows of h
+// terms, or one k block with 64 rows
+constexpr size_t kMaxStage = 4 * kTileBytes + 2 * kHTerms * 32 * 128;
 
 size_t ring_bytes_for(int cap) {
   const size_t fixed = fixed_bytes(cap);
@@ -928,12 +995,12 @@ size_t ring_bytes_for(int cap) {
 }  // namespace
 
 // Shape admission of the tensor-core path (host): FP8 routed experts, no
-// shared expert, H a multiple of 256 up to 8192, I a multiple of 128 up to
-// 4096, at most 65535 experts ids and room for the ring.
+// shared expert, H and I multiples of 256 (H up to 8192, I up to 4096) and
+// room for the ring.
 bool tc_fits(const moe_layer_desc *L, int M) {
   const moe_experts &R = L->routed;
   if (R.fmt != MOE_FMT_FP8_B128 || L->shared) return false;
-  if (R.hidden % 256 || R.hidden > 128 * kMaxKB || R.inter % 128 || R.inter > 128 * kMaxKBd)
+  if (R.hidden % 256 || R.hidden > 128 * kMaxKB || R.inter % 256 || R.inter > 128 * kMaxKBd)
     return false;
   const int n = M * L->top_k;
   const int cap = n < R.num_experts ? n : R.num_experts;
@@ -951,10 +1018,10 @@ void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&byte
   bytes[4] = (size_t)cap * 4;
 }
 
-int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *sti,
-              const int32_t *off, const int32_t *act, const int32_t *act_count,
-              const int32_t *ntpp, void *ws, const moe_workspace_view &v, uint32_t *err,
-              void *stream) {
+int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *ids,
+              const float *w, const int32_t *ttp, const int32_t *off, const int32_t *act,
+              const int32_t *act_count, uint16_t *out, void *ws, const moe_workspace_view &v,
+              uint32_t *err, void *stream) {
   const moe_experts &R = L->routed;
   char *base = static_cast<char *>(ws);
   TcArgs a = {};
@@ -967,11 +1034,13 @@ int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *
   a.cap = v.cap;
   a.max_total = v.max_total;
   a.x = x;
-  a.sti = sti;
+  a.ids = ids;
+  a.w = w;
+  a.ttp = ttp;
   a.off = off;
   a.act = act;
   a.act_count = act_count;
-  a.ntpp = ntpp;
+  a.out = out;
   a.sg = static_cast<const float *>(R.gate.scale);
   a.su = static_cast<const float *>(R.up.scale);
   a.sd = static_cast<const float *>(R.down.scale);

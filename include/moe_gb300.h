@@ -260,7 +260,7 @@ int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int M,
                                     moe_workspace_view *view);
 
 /* Host only.  The number of kernels moe_decode_layer enqueues for M rows
- * (1 on the fused decode path; 4 with router logits, 3 with given ids on the
+ * (1 on the fused decode path; 3 with router logits, 2 with given ids on the
  * tensor-core path; otherwise 5 and 4), or -1 if the call would be
  * rejected. */
 int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logits);
@@ -278,9 +278,9 @@ int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logit
  * forces the five.
  * On the tensor-core path (MOE_PATH_TC, or MOE_PATH_AUTO when the fused path
  * does not serve the call and the routed experts are FP8 with hidden a
- * multiple of 256 up to 8192, inter a multiple of 128 up to 4096 and no
- * shared expert) gate+up and down run as one cooperative persistent kernel
- * of tcgen05 MMAs between the alignment and the blend ("fp8_moe_grouped.rs",
+ * multiple of 256 up to 8192, inter a multiple of 256 up to 4096 and no
+ * shared expert) gate+up, down and the blend run as one cooperative
+ * persistent kernel of tcgen05 MMAs after the alignment ("fp8_moe_grouped.rs",
  * the tensor-core twins of the grouped launchers): E4M3 weight codes times
  * exact E4M3 splits of x and h, each 128-wide k block promoted to fp32 times
  * its block scale.  Its h and y are the same quantities as on the CUDA-core

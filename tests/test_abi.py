@@ -128,9 +128,9 @@ def test_tensor_core_workspace_host_only():
     assert v.tc_done - v.tc_h_scale >= mt * 12 * 4
     assert v.total_bytes - v.tc_done >= cap * 4
     assert moe.workspace_bytes(layer, 128) == v.total_bytes
-    # the tensor-core run is 4 launches with router logits, 3 with given ids
-    assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 1) == 4
-    assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 0) == 3
+    # the tensor-core run is 3 launches with router logits, 2 with given ids
+    assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 1) == 3
+    assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 0) == 2
     # not for NVFP4 experts, nor when the CUDA-core path is forced
     for lay in (moe.LayerDesc(top_k=8, block_size=64,
                               routed=_fake_experts(fmt=moe.FMT_NVFP4_G16, E=256, H=4096,

@@ -59,7 +59,7 @@ def test_tc_layer_matches_oracle(moe, shape):
     inp = synth.make_layer(shape, 1000, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, view, (layer, _) = H.gpu_layer(moe, inp, path=TC, err=err)
-    assert moe.moe_decode_layer_launches(layer, shape.M) == 4
+    assert moe.moe_decode_layer_launches(layer, shape.M) == 3
     assert int(err.item()) == 0
     _, ref_b, bad = H.oracle_layer(inp)
     assert bad == 0
@@ -174,7 +174,7 @@ def test_tc_verify_batch_matches_staged_path(moe):
     inp = synth.make_layer(shape, 1000, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out_tc, view, (layer, _) = H.gpu_layer(moe, inp, err=err)
-    assert moe.moe_decode_layer_launches(layer, shape.M) == 4
+    assert moe.moe_decode_layer_launches(layer, shape.M) == 3
     assert int(err.item()) == 0
     assert "tc_x_terms" in view
     out_st, _, _ = H.gpu_layer(moe, inp, path=STAGED)
