@@ -50,13 +50,13 @@ constexpr int kWarps = 2 + kEpiWarps;
 constexpr int kThreads = kWarps * 32;          // 576
 constexpr int kEpiThreads = kEpiWarps * 32;    // 512
 constexpr int kRecs = 8;                       // stage records (ring slots in flight)
-constexpr int kBufs = 4;                       // TMEM accumulator buffers
+constexpr int kAccs = 8;                       // k-block accumulators in flight (TMEM)
 constexpr int kRowTile = 64;                   // token rows per item (MMA N <= 64)
 constexpr int kTileBytes = 128 * 128;          // one 128-row x 128-byte weight box
 constexpr int kXTerms = 2, kHTerms = 3;
 constexpr int kMaxKB = 64;                     // k blocks of 128 (H <= 8192)
 constexpr int kMaxKBd = 32;                    // down k blocks (I <= 4096)
-constexpr uint32_t kTmemCols = 512;            // kBufs x (2 x 64 columns)
+constexpr uint32_t kTmemCols = 512;            // the circular accumulator range
 constexpr uint64_t kWaitNs = 2000000000ull;    // a wait gives up after ~2 s
 
 struct TcArgs {
@@ -90,6 +90,8 @@ struct Smem {
   uint8_t *ring;
   uint64_t *full, *empty, *accf, *acce, *drain;
   uint32_t *rec;       // [kRecs] byte offset of each stage in the ring
+  uint32_t *rlen;      // [kRecs] its size
+  uint32_t *trec;      // [kAccs] TMEM column | count << 16 of each accumulator
   volatile int *misc;  // [0] failed, [1] TMEM base, [2] active count, [3] row tiles
   float *sc;           // [2][kMaxKB] weight block scales of the current item
   float *cs;           // [kMaxKBd][kRowTile] per-row factors of the current item
@@ -102,8 +104,8 @@ __host__ __device__ inline size_t al16(size_t v) { return (v + 15) & ~size_t(15)
 
 __host__ __device__ inline size_t fixed_bytes(int cap) {
   size_t b = 0;
-  b += al16(8 * (2 * kRecs + 2 * kBufs + 1));
-  b += al16(4 * kRecs) + al16(4 * 16);
+  b += al16(8 * (2 * kRecs + 2 * kAccs + 1));
+  b += al16(4 * kRecs) + al16(4 * kRecs) + al16(4 * kAccs) + al16(4 * 16);
   b += al16(4 * 2 * kMaxKB) + al16(4 * kMaxKBd * kRowTile) + al16(4 * 4 * 4 * 16);
   b += al16(4 * ((size_t)cap + 1)) + al16(8 * (size_t)cap);
   return b;
@@ -118,13 +120,15 @@ __device__ Smem carve(uint8_t *base, const TcArgs &a) {
     p += al16(bytes);
     return r;
   };
-  uint64_t *bars = reinterpret_cast<uint64_t *>(take(8 * (2 * kRecs + 2 * kBufs + 1)));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(take(8 * (2 * kRecs + 2 * kAccs + 1)));
   S.full = bars;
   S.empty = bars + kRecs;
   S.accf = bars + 2 * kRecs;
-  S.acce = bars + 2 * kRecs + kBufs;
-  S.drain = bars + 2 * kRecs + 2 * kBufs;
+  S.acce = bars + 2 * kRecs + kAccs;
+  S.drain = bars + 2 * kRecs + 2 * kAccs;
   S.rec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
+  S.rlen = reinterpret_cast<uint32_t *>(take(4 * kRecs));
+  S.trec = reinterpret_cast<uint32_t *>(take(4 * kAccs));
   S.misc = reinterpret_cast<volatile int *>(take(4 * 16));
   S.sc = reinterpret_cast<float *>(take(4 * 2 * kMaxKB));
   S.cs = reinterpret_cast<float *>(take(4 * kMaxKBd * kRowTile));
@@ -151,16 +155,36 @@ __device__ __forceinline__ void fail(const Smem &S, const TcArgs &a) {
   }
 }
 
+// One potentially blocking test of an mbarrier phase: the hardware may park
+// the thread until the phase completes or a short time limit passes, so
+// waiting warps leave the issue slots to the MMA and copy threads.
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `parity` of an mbarrier; false when the CTA has
 // failed meanwhile or after about two seconds.
-__device__ bool wait_bar(const Smem &S, uint64_t *bar, uint32_t parity) {
-  if (mbar_poll(bar, parity)) return true;
+__device__ __forceinline__ bool wait_bar(const Smem &S, uint64_t *bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = gtime();
-  for (uint32_t i = 1; i < (1u << 30); ++i) {
-    if (mbar_poll(bar, parity)) return true;
-    if ((i & 255) == 0 && (S.misc[0] || gtime() - t0 > kWaitNs)) return false;
+  for (uint32_t i = 1; i < (1u << 28); ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 15) == 0 && (S.misc[0] || gtime() - t0 > kWaitNs)) return false;
   }
   return false;
+}
+
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(n)
+               : "memory");
 }
 
 __device__ __forceinline__ int ld_acquire(const int *p) {
@@ -331,6 +355,21 @@ __device__ __forceinline__ Item decode(const Smem &S, int A, int i, int TR, int 
   return it;
 }
 
+// TMEM columns of one k block's accumulators: the two weight tiles, each
+// against the item's terms stacked along N (term t of row j in column
+// t * nt + j), so one MMA per tile and 32-wide k step reads the weights once.
+__device__ __forceinline__ uint32_t acc_cols(const Item &it) {
+  return 2u * (uint32_t)(it.gu ? kXTerms : kHTerms) * (16u << it.box);
+}
+
+// Where the next k block's accumulators go in the circular TMEM column range
+// (the MMA thread and the promotion warps run the same sequence).
+__device__ __forceinline__ uint32_t tmem_place(uint32_t &head, uint32_t cols) {
+  const uint32_t pos = head + cols <= kTmemCols ? head : 0u;
+  head = pos + cols;
+  return pos;
+}
+
 // ---------------------------------------------------------------------------
 // phase 0: x terms of every routed slot
 // ---------------------------------------------------------------------------
@@ -481,9 +520,6 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
   const uint64_t pol = policy_evict_first();
   const int FT = a.I / 128, FD = a.H / 256;
   uint32_t head = 0;
-  uint32_t rsz[kRecs];
-#pragma unroll
-  for (int j = 0; j < kRecs; ++j) rsz[j] = 0;
   int s = 0, tail = 0;
   bool ok = true;
   for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
@@ -506,27 +542,29 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
     const int wrow1 = it.gu ? wrow0 : wrow0 + 128;
     const CUtensorMap *bmap = it.gu ? &m.xq[it.box] : &m.hq[it.box];
     for (int kb = 0; kb < KB; kb += it.kps) {
-      // Stages are freed oldest first; after two wraps an in-flight stage
-      // other than the oldest can cover the new range, so every in-flight
-      // stage is checked and the oldest retired until none overlaps.
-      const uint32_t pos = head + size <= a.ring_bytes ? head : 0;
+      // Ring placement.  Stages are placed in order and freed oldest first.
+      // When the stage does not fit before the end, the ring wraps: the
+      // stages still lying in the skipped end [head, end) are the oldest and
+      // are waited for first.  Then only the oldest stage can overlap the new
+      // range, so stages are retired oldest first until it does not.
+      bool wrap = head + size > a.ring_bytes;
       while (tail < s) {
-        bool clash = s - tail >= kRecs;
-        for (int j = tail; j < s && !clash; ++j) {
-          const int dj = j % kRecs;
-          clash = pos < S.rec[dj] + rsz[dj] && S.rec[dj] < pos + size;
-        }
-        if (!clash) break;
-        if (!wait_bar(S, &S.empty[tail % kRecs], (uint32_t)(tail / kRecs) & 1)) {
+        const int dt = tail % kRecs;
+        const uint32_t tp = S.rec[dt], tl = S.rlen[dt];
+        const uint32_t at = wrap ? 0u : head;
+        const bool busy = s - tail >= kRecs || (wrap && tp >= head) || (at < tp + tl && tp < at + size);
+        if (!busy) break;
+        if (!wait_bar(S, &S.empty[dt], (uint32_t)(tail / kRecs) & 1)) {
           ok = false;
           break;
         }
         ++tail;
       }
       if (!ok) break;
+      const uint32_t pos = wrap ? 0u : head;
       const int d = s % kRecs;
       S.rec[d] = pos;
-      rsz[d] = size;
+      S.rlen[d] = size;
       uint64_t *fb = &S.full[d];
       mbar_expect_tx(fb, size);
       uint8_t *dst = S.ring + pos;
@@ -551,15 +589,18 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
                            uint32_t tmem) {
   const int FT = a.I / 128, FD = a.H / 256;
   const uint32_t ring = smem_addr(S.ring);
-  int s = 0;   // stages
-  int q = 0;   // k blocks (TMEM buffer uses)
+  int s = 0;      // stages
+  int q = 0;      // k blocks (accumulators)
+  int qtail = 0;  // oldest accumulator not yet known to be released
+  uint32_t thead = 0;
   bool ok = true;
   for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
     const Item it = decode(S, A, i, TR, FT, FD);
     const int KB = it.gu ? a.H / 128 : a.I / 128;
     const int T = it.gu ? kXTerms : kHTerms;
-    const uint32_t id = idesc_e4m3(it.n16);
-    const uint32_t tstride = (16u << it.box) * 128u;
+    const uint32_t nt = 16u << it.box;
+    const uint32_t id = idesc_e4m3(T * (int)nt);
+    const uint32_t cols = acc_cols(it);
     const uint32_t abytes = (uint32_t)it.kps * kTileBytes;
     for (int kb = 0; kb < KB && ok; kb += it.kps) {
       const int d = s % kRecs;
@@ -569,25 +610,34 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
       }
       const uint32_t base = ring + S.rec[d];
       for (int j = 0; j < it.kps; ++j) {
-        const int buf = q % kBufs;
-        if (q >= kBufs && !wait_bar(S, &S.acce[buf], (uint32_t)(q / kBufs + 1) & 1)) {
-          ok = false;
-          break;
+        // the same placement rule as the stage ring, in TMEM columns
+        const bool wrap = thead + cols > kTmemCols;
+        while (qtail < q) {
+          const uint32_t r = S.trec[qtail % kAccs], tp = r & 0xFFFFu, tl = r >> 16;
+          const uint32_t at = wrap ? 0u : thead;
+          const bool busy =
+              q - qtail >= kAccs || (wrap && tp >= thead) || (at < tp + tl && tp < at + cols);
+          if (!busy) break;
+          if (!wait_bar(S, &S.acce[qtail % kAccs], (uint32_t)(qtail / kAccs) & 1)) {
+            ok = false;
+            break;
+          }
+          ++qtail;
         }
+        if (!ok) break;
+        const uint32_t pos = tmem_place(thead, cols);
+        S.trec[q % kAccs] = pos | (cols << 16);
         tc_fence_after();
         const uint32_t a0 = base + j * kTileBytes, a1 = a0 + abytes;
-        const uint32_t b0 = base + 2 * abytes + j * T * tstride;
-        const uint32_t d0 = tmem + (uint32_t)buf * 128u, d1 = d0 + 64u;
-        for (int t = 0; t < T; ++t) {
+        const uint32_t b0 = base + 2 * abytes + j * (uint32_t)T * nt * 128u;
+        const uint32_t d0 = tmem + pos, d1 = d0 + (uint32_t)T * nt;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = sdesc(b0 + t * tstride + ks * 32);
-            const uint32_t acc = (t | ks) != 0;
-            mma_e4m3(d0, sdesc(a0 + ks * 32), bd, id, acc);
-            mma_e4m3(d1, sdesc(a1 + ks * 32), bd, id, acc);
-          }
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bd = sdesc(b0 + ks * 32);
+          mma_e4m3(d0, sdesc(a0 + ks * 32), bd, id, ks != 0);
+          mma_e4m3(d1, sdesc(a1 + ks * 32), bd, id, ks != 0);
         }
-        mma_commit(&S.accf[buf]);
+        mma_commit(&S.accf[q % kAccs]);
         ++q;
       }
       mma_commit(&S.empty[d]);
@@ -652,6 +702,32 @@ __device__ void finish_gate_up(const TcArgs &a, const Smem &S, const Item &it, i
   }
 }
 
+// acc += scale * (sum of the T term partials of this warp's 16 columns),
+// times the per-row factor hf[j] of the down projection when hf is given.
+__device__ __forceinline__ void promote(uint32_t col, uint32_t nt, int T, float scale,
+                                        const float *hf, float (&acc)[16]) {
+  uint32_t r[16], r2[16];
+  tmem_ld16(col, r);
+  tmem_ld16(col + nt, r2);
+  tmem_wait_ld();
+  float part[16];
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) part[jj] = __uint_as_float(r[jj]) + __uint_as_float(r2[jj]);
+  if (T == 3) {
+    tmem_ld16(col + 2 * nt, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) part[jj] += __uint_as_float(r[jj]);
+  }
+  if (hf == nullptr) {
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) acc[jj] = fmaf(scale, part[jj], acc[jj]);
+  } else {
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) acc[jj] = fmaf(scale * hf[jj], part[jj], acc[jj]);
+  }
+}
+
 // Barrier over the 16 epilogue warps that also ORs a flag across them, so
 // that every warp takes the same branch after it.
 __device__ __forceinline__ bool epi_sync_or(bool v) {
@@ -677,7 +753,8 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
   const int FT = a.I / 128, FD = a.H / 256, KBd = a.I / 128;
   const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
   const int c0 = grp * 16;
-  int s = 0;
+  int s = 0;            // k blocks
+  uint32_t thead = 0;   // accumulator placement, as in the MMA thread
   int pending = -1;   // active index of a finished gate+up item not yet published
   bool bad = false;
   for (int i = blockIdx.x; i < total; i += gridDim.x) {
@@ -731,43 +808,33 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
     float acc0[16], acc1[16];
 #pragma unroll
     for (int jj = 0; jj < 16; ++jj) acc0[jj] = acc1[jj] = 0.f;
+    // Only the warps whose columns hold rows of the item read TMEM; the first
+    // of them also arrives for the others, and the rest skip the k blocks.
     const bool mine = c0 < it.n16;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int buf = s % kBufs;
+    const uint32_t arrivals = ew == 0 ? (uint32_t)(kEpiWarps - (it.n16 / 16) * 4 + 1) : 1u;
+    const int T = it.gu ? kXTerms : kHTerms;
+    const uint32_t nt = 16u << it.box, cols = acc_cols(it);
+    if (!mine) {
+      for (int kb = 0; kb < KB; ++kb) tmem_place(thead, cols);
+      s += KB;
+    }
+    for (int kb = 0; kb < KB && mine; ++kb) {
+      const uint32_t pos = tmem_place(thead, cols);
+      const int slot = s % kAccs;
       // every lane of the warp takes the same branch into the aligned TMEM loads
-      if (!__all_sync(0xFFFFFFFFu, wait_bar(S, &S.accf[buf], (uint32_t)(s / kBufs) & 1))) {
+      if (!__all_sync(0xFFFFFFFFu, wait_bar(S, &S.accf[slot], (uint32_t)(s / kAccs) & 1))) {
         bad = true;
         break;
       }
       tc_fence_after();
-      uint32_t r0[16], r1[16];
-      if (mine) {
-        const uint32_t t = lane_base + (uint32_t)buf * 128u + (uint32_t)c0;
-        tmem_ld16(t, r0);
-        tmem_ld16(t + 64u, r1);
-        tmem_wait_ld();
-      }
+      const uint32_t col = lane_base + pos + (uint32_t)c0;
+      const float *hf = it.gu ? nullptr : S.cs + kb * kRowTile + c0;
+      promote(col, nt, T, S.sc[kb], hf, acc0);
+      promote(col + (uint32_t)T * nt, nt, T, S.sc[kMaxKB + kb], hf, acc1);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.acce[buf]);
+      if (lane == 0) mbar_arrive_n(&S.acce[slot], arrivals);
       ++s;
-      if (!mine) continue;
-      const float s0 = S.sc[kb], s1 = S.sc[kMaxKB + kb];
-      if (it.gu) {
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          acc0[jj] = fmaf(s0, __uint_as_float(r0[jj]), acc0[jj]);
-          acc1[jj] = fmaf(s1, __uint_as_float(r1[jj]), acc1[jj]);
-        }
-      } else {
-        const float *hf = S.cs + kb * kRowTile + c0;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const float hi = hf[jj];
-          acc0[jj] = fmaf(s0 * hi, __uint_as_float(r0[jj]), acc0[jj]);
-          acc1[jj] = fmaf(s1 * hi, __uint_as_float(r1[jj]), acc1[jj]);
-        }
-      }
     }
     // every warp finished the item's k blocks before any finishes the item
     if (epi_sync_or(bad)) {
@@ -810,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.full[j], 1);
       mbar_init(&S.empty[j], 1);
     }
-    for (int j = 0; j < kBufs; ++j) {
+    for (int j = 0; j < kAccs; ++j) {
       mbar_init(&S.accf[j], 1);
       mbar_init(&S.acce[j], kEpiWarps);
     }
