@@ -19,6 +19,12 @@ synchronize on both sides):
               copied in from pinned memory, the output copied back, per step.
 The CPU baseline is the oracle on a bounded sample of the same workload.
 
+The same line carries `verify_batch`: the M=128 verify batch (H=4096,
+I=1536, E=256, top_k=8, BS=64, router logits with a Zipf(s=1.1) per-expert
+bias, fresh noise every step) on the tensor-core path, K graph-replayed steps
+over 2 weight copies of 4.8 GB, with its weight-stream GB/s against the
+measured HBM peak.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
 from __future__ import annotations
@@ -179,6 +185,61 @@ def layer_bytes(shape, base, n_active: int) -> int:
     return (n_active * per_expert + shape.M * shape.H * 2 * 2 + shape.M * shape.E * 4 + tables)
 
 
+def run_verify(moe, stream, K: int, W: int, peaks: dict) -> dict:
+    """The M=128 verify batch: K steps in one CUDA graph, fresh logits each."""
+    import synth
+    shape = synth.verify_fp8(128)
+    base = synth.make_experts(shape.E, shape.H, shape.I, shape.fmt, SEED + 4, "cuda")
+    copies = [base, _clone_experts(base)]
+    x = synth.make_x(shape.M, shape.H, SEED + 6, "cuda")
+    logits = torch.stack([synth.make_logits(shape.M, shape.E, SEED + 300 + s, "cuda",
+                                            shape.zipf_s, shape.zipf_scale) for s in range(K)])
+    layers = [moe.LayerDesc(top_k=shape.top_k, block_size=shape.BS,
+                            routed=moe.Experts.from_synth(c)) for c in copies]
+    ws = moe.alloc_workspace(layers[0], shape.M)
+    out = torch.empty(shape.M, shape.H, dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(stream):
+        for s in range(W):
+            moe.moe_decode_layer(layers[s % 2], x, out, ws, router_logits=logits[s % K])
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for s in range(K):
+            moe.moe_decode_layer(layers[s % 2], x, out, ws, router_logits=logits[s])
+    g.replay()
+    stream.synchronize()
+    times = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = float(np.median(times))
+    n_act = active_expert_counts(logits, shape.top_k)
+    ids = torch.topk(logits, shape.top_k, dim=-1).indices
+    max_rows = max(int(torch.bincount(ids[s].flatten(), minlength=shape.E).max())
+                   for s in range(K))
+    nbytes = float(np.mean([layer_bytes(shape, base, a) for a in n_act]))
+    us = 1e3 * ms / K
+    gbs = nbytes / (us * 1e-6) / 1e9
+    launches = moe.moe_decode_layer_launches(layers[0], shape.M)
+    res = dict(workload=shape.name, M=shape.M, H=shape.H, I=shape.I, E=shape.E,
+               top_k=shape.top_k, BS=shape.BS, steps=K, us_per_layer=round(us, 3),
+               tokens_per_s=round(shape.M / (us * 1e-6), 1), weight_stream_gbs=round(gbs, 1),
+               pct_of_measured_hbm=round(100 * gbs / peaks["hbm_gbs"], 1),
+               mean_active_experts=round(float(np.mean(n_act)), 2), max_rows_per_expert=max_rows,
+               algorithmic_bytes_per_layer=int(nbytes), launches_per_layer=launches,
+               path=("tensor cores: verify_ffn_kernel (tcgen05 kind::f8f6f4, TMEM accumulators)"
+                     if launches == 3 else f"{launches} launches"),
+               l2="2 weight copies of 4.8 GB; each step streams ~1.2 GB")
+    del g, copies, layers, base, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 # --------------------------------------------------------------------------
 # timed regions
 # --------------------------------------------------------------------------
@@ -336,6 +397,29 @@ def run_reference(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_verify(args):
+    """A small case of the verify-batch kernel for ncu: the verify shape with
+    E=64 experts (1.2 GB of weights, ~40 active per step, ~0.75 GB streamed
+    per layer, above the L2), W+K direct layer calls, no graph."""
+    import dataclasses
+    import synth
+    import expert_routing_alignment_gb300 as moe
+    moe.load()
+    shape = dataclasses.replace(synth.verify_fp8(128), E=64,
+                                name="verify_h4096_i1536_e64_k8_fp8_zipf_m128")
+    base = synth.make_experts(shape.E, shape.H, shape.I, shape.fmt, SEED + 4, "cuda")
+    x = synth.make_x(shape.M, shape.H, SEED + 6, "cuda")
+    layer = moe.LayerDesc(top_k=shape.top_k, block_size=shape.BS, routed=moe.Experts.from_synth(base))
+    ws = moe.alloc_workspace(layer, shape.M)
+    out = torch.empty(shape.M, shape.H, dtype=torch.bfloat16, device="cuda")
+    for s in range(args.warmup + args.steps):
+        lg = synth.make_logits(shape.M, shape.E, SEED + 300 + s, "cuda", shape.zipf_s,
+                               shape.zipf_scale)
+        moe.moe_decode_layer(layer, x, out, ws, router_logits=lg)
+    torch.cuda.synchronize()
+    print(json.dumps(dict(profile_verify=shape.name, steps=args.warmup + args.steps)), flush=True)
+
+
 def run_gpu(args, rank: int, world: int):
     import expert_routing_alignment_gb300 as moe
     moe.load()
@@ -384,6 +468,7 @@ def run_gpu(args, rank: int, world: int):
         if rank == 0:
             print(json.dumps(dict(profile=True, sweep=sweep)), flush=True)
         return
+    verify = None if args.no_verify else run_verify(moe, stream, min(K, 16), 3, peaks)
     # max over ranks
     ms_t = torch.tensor([results["ms"]], device="cuda")
     if world > 1:
@@ -409,6 +494,7 @@ def run_gpu(args, rank: int, world: int):
         pct_of_8tbs=round(100 * r["gbs"] / NOMINAL_HBM_GBS, 1),
         algorithmic_bytes_per_layer=int(r["nbytes"]),
         sweep=sweep,
+        verify_batch=verify,
         roofline=dict(bound="hbm",
                       kernel=("decode_layer_kernel (one cooperative launch per layer call)"
                               if r["launches"] == 1 else
@@ -436,6 +522,10 @@ def main():
     ap.add_argument("--m", type=int, default=8, help="rows of the headline workload")
     ap.add_argument("--sweep", type=int, nargs="*", default=[1, 2, 4, 8])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-verify", action="store_true",
+                    help="skip the M=128 verify-batch measurement")
+    ap.add_argument("--profile-verify", action="store_true",
+                    help="only run a small case of the verify-batch kernel (for ncu)")
     ap.add_argument("--copies", type=int, default=16,
                     help="weight copies the steps rotate over (16 keeps weights out of L2)")
     ap.add_argument("--profile", action="store_true",
@@ -455,6 +545,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.profile_verify:
+            run_profile_verify(args)
         else:
             run_gpu(args, rank, world)
     finally:
