@@ -50,7 +50,8 @@ constexpr int kWarps = 2 + kEpiWarps;
 constexpr int kThreads = kWarps * 32;          // 576
 constexpr int kEpiThreads = kEpiWarps * 32;    // 512
 constexpr int kRecs = 8;                       // stage records (ring slots in flight)
-constexpr int kAccs = 8;                       // k-block accumulators in flight (TMEM)
+constexpr int kAccs = 16;                      // k-block accumulator barriers (TMEM)
+constexpr int kTfree = 16;                     // per-stage TMEM release barriers
 constexpr int kRowTile = 64;                   // token rows per item (MMA N <= 64)
 constexpr int kTileBytes = 128 * 128;          // one 128-row x 128-byte weight box
 constexpr int kXTerms = 2, kHTerms = 3;
@@ -88,10 +89,11 @@ struct TcMaps {
 
 struct Smem {
   uint8_t *ring;
-  uint64_t *full, *empty, *accf, *acce, *drain;
+  uint64_t *full, *empty, *accf, *tfree, *drain;
   uint32_t *rec;       // [kRecs] byte offset of each stage in the ring
   uint32_t *rlen;      // [kRecs] its size
-  uint32_t *trec;      // [kAccs] TMEM column | count << 16 of each accumulator
+  uint32_t *trec;      // [kRecs] its accumulators: TMEM column | count << 16
+  int *twait;          // [kRecs] the stage whose TMEM release it waits for (-1: none)
   volatile int *misc;  // [0] failed, [1] TMEM base, [2] active count, [3] row tiles
   float *sc;           // [2][kMaxKB] weight block scales of the current item
   float *cs;           // [kMaxKBd][kRowTile] per-row factors of the current item
@@ -104,8 +106,8 @@ __host__ __device__ inline size_t al16(size_t v) { return (v + 15) & ~size_t(15)
 
 __host__ __device__ inline size_t fixed_bytes(int cap) {
   size_t b = 0;
-  b += al16(8 * (2 * kRecs + 2 * kAccs + 1));
-  b += al16(4 * kRecs) + al16(4 * kRecs) + al16(4 * kAccs) + al16(4 * 16);
+  b += al16(8 * (2 * kRecs + kAccs + kTfree + 1));
+  b += 4 * al16(4 * kRecs) + al16(4 * 16);
   b += al16(4 * 2 * kMaxKB) + al16(4 * kMaxKBd * kRowTile) + al16(4 * 4 * 4 * 16);
   b += al16(4 * ((size_t)cap + 1)) + al16(8 * (size_t)cap);
   return b;
@@ -120,15 +122,16 @@ __device__ Smem carve(uint8_t *base, const TcArgs &a) {
     p += al16(bytes);
     return r;
   };
-  uint64_t *bars = reinterpret_cast<uint64_t *>(take(8 * (2 * kRecs + 2 * kAccs + 1)));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(take(8 * (2 * kRecs + kAccs + kTfree + 1)));
   S.full = bars;
   S.empty = bars + kRecs;
   S.accf = bars + 2 * kRecs;
-  S.acce = bars + 2 * kRecs + kAccs;
-  S.drain = bars + 2 * kRecs + 2 * kAccs;
+  S.tfree = bars + 2 * kRecs + kAccs;
+  S.drain = bars + 2 * kRecs + kAccs + kTfree;
   S.rec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.rlen = reinterpret_cast<uint32_t *>(take(4 * kRecs));
-  S.trec = reinterpret_cast<uint32_t *>(take(4 * kAccs));
+  S.trec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
+  S.twait = reinterpret_cast<int *>(take(4 * kRecs));
   S.misc = reinterpret_cast<volatile int *>(take(4 * 16));
   S.sc = reinterpret_cast<float *>(take(4 * 2 * kMaxKB));
   S.cs = reinterpret_cast<float *>(take(4 * kMaxKBd * kRowTile));
@@ -173,7 +176,7 @@ __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
 // Wait for the phase of `parity` of an mbarrier; false when the CTA has
 // failed meanwhile or after about two seconds.
 __device__ __forceinline__ bool wait_bar(const Smem &S, uint64_t *bar, uint32_t parity) {
-  if (mbar_try(bar, parity)) return true;
+  if (mbar_poll(bar, parity)) return true;
   const uint64_t t0 = gtime();
   for (uint32_t i = 1; i < (1u << 28); ++i) {
     if (mbar_try(bar, parity)) return true;
@@ -362,12 +365,20 @@ __device__ __forceinline__ uint32_t acc_cols(const Item &it) {
   return 2u * (uint32_t)(it.gu ? kXTerms : kHTerms) * (16u << it.box);
 }
 
-// Where the next k block's accumulators go in the circular TMEM column range
-// (the MMA thread and the promotion warps run the same sequence).
-__device__ __forceinline__ uint32_t tmem_place(uint32_t &head, uint32_t cols) {
-  const uint32_t pos = head + cols <= kTmemCols ? head : 0u;
-  head = pos + cols;
+// Placement of the next range of `len` units in a ring of `cap` units: at
+// the head, or at 0 when it does not fit before the end.  Ranges depend only
+// on the sequence of lengths, so every role computes the same positions.
+__device__ __forceinline__ uint32_t ring_place(uint32_t &head, uint32_t len, uint32_t cap) {
+  const uint32_t pos = head + len <= cap ? head : 0u;
+  head = pos + len;
   return pos;
+}
+
+// Bytes of one stage of an item: kps k blocks of the two weight tiles and of
+// the item's activation terms.
+__device__ __forceinline__ uint32_t stage_bytes(const Item &it) {
+  return 2u * (uint32_t)it.kps * kTileBytes +
+         (uint32_t)it.kps * (uint32_t)(it.gu ? kXTerms : kHTerms) * (16u << it.box) * 128u;
 }
 
 // ---------------------------------------------------------------------------
@@ -519,8 +530,9 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
                          int total) {
   const uint64_t pol = policy_evict_first();
   const int FT = a.I / 128, FD = a.H / 256;
-  uint32_t head = 0;
+  uint32_t head = 0, thead = 0;   // shared-memory and TMEM ring heads
   int s = 0, tail = 0;
+  int ttail = 0;                   // oldest stage that may still hold TMEM
   bool ok = true;
   for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
     const Item it = decode(S, A, i, TR, FT, FD);
@@ -535,24 +547,43 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
     const int KB = it.gu ? a.H / 128 : a.I / 128;
     const uint32_t bterm = (uint32_t)(it.gu ? kXTerms : kHTerms) * (16u << it.box) * 128u;
     const uint32_t abytes = (uint32_t)it.kps * kTileBytes;
-    const uint32_t size = 2 * abytes + (uint32_t)it.kps * bterm;
+    const uint32_t size = stage_bytes(it);
+    const uint32_t tcols = (uint32_t)it.kps * acc_cols(it);
     const int wrow0 = it.gu ? it.e * a.I + it.tile * 128 : it.e * a.H + it.tile * 256;
     const CUtensorMap *w0 = it.gu ? &m.w[0][it.kps - 1] : &m.w[2][it.kps - 1];
     const CUtensorMap *w1 = it.gu ? &m.w[1][it.kps - 1] : w0;
     const int wrow1 = it.gu ? wrow0 : wrow0 + 128;
     const CUtensorMap *bmap = it.gu ? &m.xq[it.box] : &m.hq[it.box];
     for (int kb = 0; kb < KB; kb += it.kps) {
-      // Ring placement.  Stages are placed in order and freed oldest first.
-      // When the stage does not fit before the end, the ring wraps: the
-      // stages still lying in the skipped end [head, end) are the oldest and
-      // are waited for first.  Then only the oldest stage can overlap the new
-      // range, so stages are retired oldest first until it does not.
-      bool wrap = head + size > a.ring_bytes;
+      // Ring placement.  A stage holds a range of the shared-memory ring (its
+      // copies, freed when its MMAs complete) and a range of the TMEM ring
+      // (its accumulators, freed when the promotion warps have read them).
+      // Ranges are placed in order and freed oldest first.  When a range does
+      // not fit before the end, its ring wraps: the stages still lying in the
+      // skipped end [head, end) are the oldest and go first.  Then only the
+      // oldest stage can overlap the new range, so stages are retired oldest
+      // first until it does not.  The copies wait here for shared memory; the
+      // TMEM retirement is only computed here and waited for by the MMA
+      // thread, which needs the columns (twait: the newest stage to retire).
+      int need_t = -1;
+      {
+        const bool twrap = thead + tcols > kTmemCols;
+        const uint32_t ct = twrap ? 0u : thead;
+        while (ttail < s) {
+          const uint32_t tr = S.trec[ttail % kRecs], cp = tr & 0xFFFFu, cl = tr >> 16;
+          const bool busy = s - ttail >= kTfree / 2 || (twrap && cp >= thead) ||
+                            (ct < cp + cl && cp < ct + tcols);
+          if (!busy) break;
+          need_t = ttail++;
+        }
+      }
+      const bool wrap = head + size > a.ring_bytes;
       while (tail < s) {
         const int dt = tail % kRecs;
         const uint32_t tp = S.rec[dt], tl = S.rlen[dt];
         const uint32_t at = wrap ? 0u : head;
-        const bool busy = s - tail >= kRecs || (wrap && tp >= head) || (at < tp + tl && tp < at + size);
+        const bool busy =
+            s - tail >= kRecs || (wrap && tp >= head) || (at < tp + tl && tp < at + size);
         if (!busy) break;
         if (!wait_bar(S, &S.empty[dt], (uint32_t)(tail / kRecs) & 1)) {
           ok = false;
@@ -561,10 +592,13 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
         ++tail;
       }
       if (!ok) break;
-      const uint32_t pos = wrap ? 0u : head;
+      const uint32_t pos = ring_place(head, size, a.ring_bytes);
+      const uint32_t tpos = ring_place(thead, tcols, kTmemCols);
       const int d = s % kRecs;
       S.rec[d] = pos;
       S.rlen[d] = size;
+      S.trec[d] = tpos | (tcols << 16);
+      S.twait[d] = need_t;
       uint64_t *fb = &S.full[d];
       mbar_expect_tx(fb, size);
       uint8_t *dst = S.ring + pos;
@@ -572,7 +606,6 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
       tma_3d_hint(dst + abytes, w1, 0, wrow1, kb, fb, pol);
       for (int j = 0; j < it.kps; ++j)
         tma_3d(dst + 2 * abytes + j * bterm, bmap, (kb + j) * 128, it.pos0, 0, fb);
-      head = pos + size;
       ++s;
     }
   }
@@ -589,10 +622,10 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
                            uint32_t tmem) {
   const int FT = a.I / 128, FD = a.H / 256;
   const uint32_t ring = smem_addr(S.ring);
-  int s = 0;      // stages
-  int q = 0;      // k blocks (accumulators)
-  int qtail = 0;  // oldest accumulator not yet known to be released
-  uint32_t thead = 0;
+  uint32_t head = 0, thead = 0;   // the copy thread's placement, recomputed
+  int s = 0;                      // stages
+  int q = 0;                      // k blocks
+  int tdone = -1;                 // newest stage whose TMEM release was seen
   bool ok = true;
   for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
     const Item it = decode(S, A, i, TR, FT, FD);
@@ -602,35 +635,28 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
     const uint32_t id = idesc_e4m3(T * (int)nt);
     const uint32_t cols = acc_cols(it);
     const uint32_t abytes = (uint32_t)it.kps * kTileBytes;
-    for (int kb = 0; kb < KB && ok; kb += it.kps) {
+    const uint32_t size = stage_bytes(it), tcols = (uint32_t)it.kps * cols;
+    for (int kb = 0; kb < KB; kb += it.kps) {
+      const uint32_t base = ring + ring_place(head, size, a.ring_bytes);
+      const uint32_t tbase = tmem + ring_place(thead, tcols, kTmemCols);
       const int d = s % kRecs;
       if (!wait_bar(S, &S.full[d], (uint32_t)(s / kRecs) & 1)) {
         ok = false;
         break;
       }
-      const uint32_t base = ring + S.rec[d];
-      for (int j = 0; j < it.kps; ++j) {
-        // the same placement rule as the stage ring, in TMEM columns
-        const bool wrap = thead + cols > kTmemCols;
-        while (qtail < q) {
-          const uint32_t r = S.trec[qtail % kAccs], tp = r & 0xFFFFu, tl = r >> 16;
-          const uint32_t at = wrap ? 0u : thead;
-          const bool busy =
-              q - qtail >= kAccs || (wrap && tp >= thead) || (at < tp + tl && tp < at + cols);
-          if (!busy) break;
-          if (!wait_bar(S, &S.acce[qtail % kAccs], (uint32_t)(qtail / kAccs) & 1)) {
-            ok = false;
-            break;
-          }
-          ++qtail;
+      const int tw = S.twait[d];
+      if (tw > tdone) {   // the columns are free once that stage is released
+        if (!wait_bar(S, &S.tfree[tw % kTfree], (uint32_t)(tw / kTfree) & 1)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        const uint32_t pos = tmem_place(thead, cols);
-        S.trec[q % kAccs] = pos | (cols << 16);
-        tc_fence_after();
+        tdone = tw;
+      }
+      tc_fence_after();
+      for (int j = 0; j < it.kps; ++j) {
         const uint32_t a0 = base + j * kTileBytes, a1 = a0 + abytes;
         const uint32_t b0 = base + 2 * abytes + j * (uint32_t)T * nt * 128u;
-        const uint32_t d0 = tmem + pos, d1 = d0 + (uint32_t)T * nt;
+        const uint32_t d0 = tbase + (uint32_t)j * cols, d1 = d0 + (uint32_t)T * nt;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t bd = sdesc(b0 + ks * 32);
@@ -754,7 +780,8 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
   const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
   const int c0 = grp * 16;
   int s = 0;            // k blocks
-  uint32_t thead = 0;   // accumulator placement, as in the MMA thread
+  int st = 0;           // stages
+  uint32_t thead = 0;   // the copy thread's TMEM placement, recomputed
   int pending = -1;   // active index of a finished gate+up item not yet published
   bool bad = false;
   for (int i = blockIdx.x; i < total; i += gridDim.x) {
@@ -813,13 +840,17 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
     const bool mine = c0 < it.n16;
     const uint32_t arrivals = ew == 0 ? (uint32_t)(kEpiWarps - (it.n16 / 16) * 4 + 1) : 1u;
     const int T = it.gu ? kXTerms : kHTerms;
-    const uint32_t nt = 16u << it.box, cols = acc_cols(it);
+    const uint32_t nt = 16u << it.box, cols = acc_cols(it), tcols = (uint32_t)it.kps * cols;
     if (!mine) {
-      for (int kb = 0; kb < KB; ++kb) tmem_place(thead, cols);
+      for (int kb = 0; kb < KB; kb += it.kps) ring_place(thead, tcols, kTmemCols);
       s += KB;
+      st += KB / it.kps;
     }
+    uint32_t tbase = 0;
     for (int kb = 0; kb < KB && mine; ++kb) {
-      const uint32_t pos = tmem_place(thead, cols);
+      const int j = kb % it.kps;
+      if (j == 0) tbase = ring_place(thead, tcols, kTmemCols);
+      const uint32_t pos = tbase + (uint32_t)j * cols;
       const int slot = s % kAccs;
       // every lane of the warp takes the same branch into the aligned TMEM loads
       if (!__all_sync(0xFFFFFFFFu, wait_bar(S, &S.accf[slot], (uint32_t)(s / kAccs) & 1))) {
@@ -831,10 +862,13 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
       const float *hf = it.gu ? nullptr : S.cs + kb * kRowTile + c0;
       promote(col, nt, T, S.sc[kb], hf, acc0);
       promote(col + (uint32_t)T * nt, nt, T, S.sc[kMaxKB + kb], hf, acc1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_n(&S.acce[slot], arrivals);
       ++s;
+      if (j == it.kps - 1) {   // the stage's accumulators are free
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_n(&S.tfree[st % kTfree], arrivals);
+        ++st;
+      }
     }
     // every warp finished the item's k blocks before any finishes the item
     if (epi_sync_or(bad)) {
@@ -875,12 +909,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int j = 0; j < kRecs; ++j) {
       mbar_init(&S.full[j], 1);
-      mbar_init(&S.empty[j], 1);
+      mbar_init(&S.empty[j], 1);   // the stage's MMAs have completed
     }
-    for (int j = 0; j < kAccs; ++j) {
-      mbar_init(&S.accf[j], 1);
-      mbar_init(&S.acce[j], kEpiWarps);
-    }
+    for (int j = 0; j < kAccs; ++j) mbar_init(&S.accf[j], 1);
+    for (int j = 0; j < kTfree; ++j) mbar_init(&S.tfree[j], kEpiWarps);
     mbar_init(S.drain, 1);
     for (int j = 0; j < 16; ++j) S.misc[j] = 0;
     fence_mbar_init();
