@@ -11,8 +11,8 @@ no step finds its weights in the 129 MB L2.
 Timed regions (CUDA events on the launching stream, after W warm-up steps,
 synchronize on both sides):
   * value:    K steps captured in one CUDA graph, replayed once;
-  * roofline: the layer kernel (one cooperative launch per layer call on the
-              fused decode path), each call bracketed by events,
+  * roofline: the layer call (the tensor-core kernel after the router and the
+              alignment on the FP8 decode shapes), each call bracketed by events,
               algorithmic bytes / mean duration; DRAM traffic per launch from
               the committed ncu summary of the same kernel source, else null;
   * e2e:      K steps through the public API with host buffers: x and logits
@@ -49,18 +49,29 @@ NOMINAL_HBM_GBS = 8000.0
 SEED = 1001
 
 
-def kernel_source_digest() -> str:
-    """sha256 of the fused layer kernel's source (ties a profile to a build)."""
+# The layer's dominant kernel on each path: its source file and the ncu
+# summary that holds its DRAM traffic on the decode workload.
+KERNELS = {
+    "fused": ("decode_layer_kernel (one cooperative launch per layer call)", "decode_fused.cu",
+              "decode_layer_kernel_fp8_decode.md"),
+    "tc": ("verify_ffn_kernel (tcgen05; after moe_topk_softmax and moe_align)", "verify_tc.cu",
+           "verify_ffn_kernel_fp8_decode.md"),
+}
+
+
+def kernel_source_digest(src_name: str) -> str:
+    """sha256 of a kernel's source file (ties a profile to a build)."""
     import hashlib
-    src = os.path.join(HERE, "expert_routing_alignment_gb300", "csrc", "decode_fused.cu")
+    src = os.path.join(HERE, "expert_routing_alignment_gb300", "csrc", src_name)
     with open(src, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the layer kernel for `workload` from the
+def profiled_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of the path's layer kernel for `workload` from the
     committed ncu summary, if it was taken on the current kernel source."""
-    path = os.path.join(HERE, "profiles", "decode_layer_kernel_fp8_decode.md")
+    _, src_name, prof = KERNELS[kernel]
+    path = os.path.join(HERE, "profiles", prof)
     if not os.path.exists(path):
         return None
     fields = {}
@@ -69,7 +80,7 @@ def profiled_traffic(workload: str):
             if line.startswith("- ") and ":" in line:
                 k, v = line[2:].split(":", 1)
                 fields[k.strip()] = v.strip().strip("`")
-    if fields.get("kernel source sha256") != kernel_source_digest():
+    if fields.get("kernel source sha256") != kernel_source_digest(src_name):
         return None
     key = f"traffic bytes per launch ({workload})"
     return int(fields[key]) if key in fields else None
@@ -281,9 +292,9 @@ def time_graph(moe, layers, x, logits, out, ws, K: int, W: int, stream,
 
 def time_layer_launches(moe, layers, x, logits, out, ws, K: int, W: int, stream) -> float:
     """Mean duration (ms) of one layer call's kernels, each call bracketed by
-    events on the launching stream.  On the fused decode path the call is the
-    gate+up kernel with the down+blend kernel overlapping its tail, which no
-    event can split; the brackets also stop one step from overlapping the
+    events on the launching stream: the one cooperative kernel on the fused
+    CUDA-core path; the router, the alignment and the tensor-core kernel on
+    the tensor-core path.  The brackets stop one step from overlapping the
     next, so this is slower than the graph replay."""
     pairs = []
     with torch.cuda.stream(stream):
@@ -460,6 +471,7 @@ def run_gpu(args, rank: int, world: int):
                                         K, W, stream)
             results = dict(shape=shape, base=base, x=x, logits=logits, ms=ms, us=us, gbs=gbs,
                            nbytes=nbytes, dk_ms=dk_ms, launches=launches, e2e_ms=e2e_ms,
+                           kernel="fused" if launches == 1 else "tc",
                            h2d=h2d, d2h=d2h, clocks=sampler.summary())
         del copies, layers, base, ws
         torch.cuda.empty_cache()
@@ -483,7 +495,9 @@ def run_gpu(args, rank: int, world: int):
     line = dict(
         metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=W,
         ms_per_step=ms_max / K, higher_is_better=True, scaling="weak", vs_baseline=None,
-        dtype="fp8_e4m3 weights, f16 x f16 -> f32 mma", data="synthetic",
+        dtype=("fp8_e4m3 weights, f16 x f16 -> f32 mma" if r["kernel"] == "fused" else
+               "fp8_e4m3 weights x e4m3 activation terms -> f32 (tcgen05 kind::f8f6f4)"),
+        data="synthetic",
         config=dict(workload=shape.name, M=shape.M, H=shape.H, I=shape.I, E=shape.E,
                     top_k=shape.top_k, BS=shape.BS, weights="fp8_e4m3 128x128 fp32 block scales",
                     routing="fresh N(0,1) logits every step",
@@ -496,14 +510,12 @@ def run_gpu(args, rank: int, world: int):
         sweep=sweep,
         verify_batch=verify,
         roofline=dict(bound="hbm",
-                      kernel=("decode_layer_kernel (one cooperative launch per layer call)"
-                              if r["launches"] == 1 else
-                              f"layer call ({r['launches']} launches)"),
+                      kernel=KERNELS[r["kernel"]][0],
                       achieved=round(dk_achieved, 1),
                       peak=peaks["hbm_gbs"], peak_source=f"{peaks['source']} copy bandwidth",
                       unit="GB/s", frac=round(dk_achieved / peaks["hbm_gbs"], 4),
                       bytes_per_launch=int(r["nbytes"]), us_per_launch=round(1e3 * r["dk_ms"], 3),
-                      traffic=profiled_traffic(shape.name)),
+                      traffic=profiled_traffic(shape.name, r["kernel"])),
         e2e=dict(value=shape.M * K / (r["e2e_ms"] * 1e-3), unit="tokens/s",
                  h2d_bytes_per_step=r["h2d"], d2h_bytes_per_step=r["d2h"]),
         gpu_launches=r["launches"] * K,

@@ -57,9 +57,9 @@ static int layer_run(const moe_layer_desc *L, int M) {
       return kRunStaged;
     case MOE_PATH_SIMT:
       return fused_fits(L, M, sm_count()) ? kRunFused : kRunStaged;
-    default:
-      if (fused_fits(L, M, sm_count())) return kRunFused;
-      return tc_fits(L, M) ? kRunTc : kRunStaged;
+    default:   // the tensor cores for every FP8 shape they admit, else CUDA cores
+      if (tc_fits(L, M)) return kRunTc;
+      return fused_fits(L, M, sm_count()) ? kRunFused : kRunStaged;
   }
 }
 

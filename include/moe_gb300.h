@@ -276,10 +276,10 @@ int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logit
  * barrier, down, a grid barrier, the blend) instead of five launches; every
  * table and intermediate is still written to the workspace.  MOE_PATH_SIMT_STAGED
  * forces the five.
- * On the tensor-core path (MOE_PATH_TC, or MOE_PATH_AUTO when the fused path
- * does not serve the call and the routed experts are FP8 with hidden a
- * multiple of 256 up to 8192, inter a multiple of 256 up to 4096 and no
- * shared expert) gate+up, down and the blend run as one cooperative
+ * On the tensor-core path (MOE_PATH_TC, and MOE_PATH_AUTO whenever the routed
+ * experts are FP8 with hidden a multiple of 256 up to 8192, inter a multiple
+ * of 256 up to 4096 and there is no shared expert; MOE_PATH_SIMT keeps such a
+ * layer on the CUDA cores) gate+up, down and the blend run as one cooperative
  * persistent kernel of tcgen05 MMAs after the alignment ("fp8_moe_grouped.rs",
  * the tensor-core twins of the grouped launchers): E4M3 weight codes times
  * exact E4M3 splits of x and h, each 128-wide k block promoted to fp32 times

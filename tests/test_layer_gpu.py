@@ -124,7 +124,11 @@ def test_grouped_stages_match_oracle(moe, shape):
 
 LAYER_SHAPES = ([synth.tiny()] + [synth.decode_fp8(M) for M in (1, 2, 4, 8)]
                 + [synth.decode_nvfp4(M) for M in (1, 8, 32)])
-PATHS = {"fused": 0, "staged": 3}
+# "auto" takes the tensor cores for the FP8 shapes, "fused" (MOE_PATH_SIMT)
+# keeps every shape on the CUDA cores' one-launch kernel, "staged" forces the
+# five CUDA-core launches.
+PATHS = {"auto": 0, "fused": 1, "staged": 3}
+TC_Y_REL_L2 = 5e-4   # y from h carried as three E4M3 terms (see test_tc_gpu)
 
 
 @pytest.mark.parametrize("path", list(PATHS), ids=str)
@@ -163,7 +167,8 @@ def test_layer_matches_oracle(moe, shape, path):
             assert H.rel_l2(hs_gpu, hs_ref) < H.STAGE_REL_L2
         y_ref, ys_ref = oracle.grouped_down(X, S, h_gpu, hs_gpu, shape.M, shape.top_k, tables)
         y_gpu = view["y"].cpu().numpy().astype(np.float64)
-        assert H.rel_l2(y_gpu[real], y_ref[real]) < H.STAGE_REL_L2
+        y_tol = TC_Y_REL_L2 if "tc_x_terms" in view else H.STAGE_REL_L2
+        assert H.rel_l2(y_gpu[real], y_ref[real]) < y_tol
         if S:
             assert H.rel_l2(view["y_shared"].cpu().numpy(), ys_ref) < H.STAGE_REL_L2
 

@@ -66,9 +66,16 @@ def test_tc_layer_matches_oracle(moe, shape):
     rl2, mx = H.compare_bf16(out, ref_b)
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
 
+    # the kernel's own routing and alignment tables equal the oracle's
+    rid, rw = oracle.topk_softmax(inp.logits.cpu().numpy(), shape.top_k)
+    np.testing.assert_array_equal(view["topk_ids"].cpu().numpy(), rid.ravel())
+    np.testing.assert_allclose(view["topk_w"].cpu().numpy(), rw.ravel(), atol=H.TOPK_W_ABS)
     tables, real = _tables_and_real(view, shape)
-    for key in ("sorted_token_ids", "expert_offsets", "token_to_perm"):
+    for key in ("sorted_token_ids", "expert_offsets", "token_to_perm", "sorted_expert_ids",
+                "active_experts"):
         np.testing.assert_array_equal(view[key].cpu().numpy(), tables[key], err_msg=key)
+    assert int(view["active_count"].item()) == int(tables["active_count"][0])
+    assert int(view["num_tokens_post_padded"].item()) == int(tables["num_tokens_post_padded"][0])
     X = H.oracle_experts(inp.experts.to("cpu"))
     h_ref, _ = oracle.grouped_gate_up(X, None, synth.bf16_bits(inp.x), shape.M, shape.top_k,
                                       tables)
@@ -180,3 +187,20 @@ def test_tc_verify_batch_matches_staged_path(moe):
     out_st, _, _ = H.gpu_layer(moe, inp, path=STAGED)
     rl2, mx = H.compare_bf16(out_tc, synth.bf16_bits(out_st))
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
+
+
+@pytest.mark.parametrize("shape", [synth.decode_fp8(8),
+                                   _shape("decode_h2048_i768_e128_k8_fp8_m64", 64, 2048, 768,
+                                          128, 8, 16)], ids=lambda s: s.name)
+def test_tc_row_invariance(moe, shape):
+    """On the tensor-core path row 0's output bits are the same whether the
+    batch has 1 or M rows: each row has its own x scale, every MMA column is
+    one row, and promotion, SiLU, the h scales and the blend are per row."""
+    inp = synth.make_layer(shape, 1000, device="cuda")
+    out_m, _, _ = H.gpu_layer(moe, inp, path=TC)
+    one = synth.LayerInputs(
+        synth.LayerShape(shape.name + "_row0", 1, shape.H, shape.I, shape.E, shape.top_k,
+                         shape.BS, shape.fmt),
+        inp.x[:1].contiguous(), inp.logits[:1].contiguous(), inp.experts)
+    out_1, _, _ = H.gpu_layer(moe, one, path=TC)
+    assert torch.equal(out_m[:1].view(torch.int16), out_1.view(torch.int16))
