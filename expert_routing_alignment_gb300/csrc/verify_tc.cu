@@ -393,12 +393,12 @@ __device__ __forceinline__ uint32_t stage_bytes(const Item &it) {
 // lose bits of at most 2^-18 of that maximum).  One warp per slot, its
 // row's loads in flight together (16 per lane for H = 4096).
 __device__ void prep_x(const TcArgs &a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ew = (threadIdx.x >> 5) - 2, lane = threadIdx.x & 31, et = threadIdx.x - 64;
   if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < a.cap; i += kThreads) a.done[i] = 0;
-  const int nw = gridDim.x * kWarps;
+    for (int i = et; i < a.cap; i += kEpiThreads) a.done[i] = 0;
+  const int nw = gridDim.x * kEpiWarps;
   const size_t plane = (size_t)a.max_total * a.H;
-  for (int i = blockIdx.x * kWarps + warp; i < a.n; i += nw) {
+  for (int i = blockIdx.x * kEpiWarps + ew; i < a.n; i += nw) {
     const int p = __ldcg(a.ttp + i);
     if (p < 0 || p >= a.max_total) continue;
     const uint16_t *xr = a.x + (size_t)(i / a.k) * a.H;
@@ -445,6 +445,35 @@ __device__ void prep_x(const TcArgs &a) {
       *reinterpret_cast<uint2 *>(q1 + c) = make_uint2(t1[0], t1[1]);
     }
   }
+}
+
+// Grid barrier among the promotion warps of every CTA (named barrier 1 in the
+// CTA, then one thread's arrival on the monotonic count); true when all CTAs
+// arrived within the wait limit.
+__device__ bool epi_grid_barrier(const Smem &S, unsigned long long *ctr) {
+  __threadfence();
+  asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+  if (threadIdx.x == 64) {
+    const unsigned long long G = gridDim.x;
+    const unsigned long long v = atomicAdd(ctr, 1ull);
+    const unsigned long long target = (v / G + 1) * G;
+    bool ok = false;
+    const uint64_t t0 = gtime();
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+      unsigned long long c;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(c) : "l"(ctr) : "memory");
+      if (c >= target) {
+        ok = true;
+        break;
+      }
+      if (gtime() - t0 > kWaitNs) break;
+      __nanosleep(64);
+    }
+    __threadfence();
+    S.misc[5] = ok;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+  return S.misc[5] != 0;
 }
 
 __device__ bool grid_barrier(const Smem &S, unsigned long long *ctr) {
@@ -531,6 +560,7 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
   const uint64_t pol = policy_evict_first();
   const int FT = a.I / 128, FD = a.H / 256;
   uint32_t head = 0, thead = 0;   // shared-memory and TMEM ring heads
+  bool x_ready = false;            // the grid's x terms are visible
   int s = 0, tail = 0;
   int ttail = 0;                   // oldest stage that may still hold TMEM
   bool ok = true;
@@ -604,6 +634,19 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
       uint8_t *dst = S.ring + pos;
       tma_3d_hint(dst, w0, 0, wrow0, kb, fb, pol);
       tma_3d_hint(dst + abytes, w1, 0, wrow1, kb, fb, pol);
+      if (!x_ready) {   // the weights above do not wait for the x terms
+        const uint64_t t0 = gtime();
+        while (!S.misc[6]) {
+          if (S.misc[0] || gtime() - t0 > kWaitNs) {
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+        }
+        __threadfence();
+        fence_proxy_async_global();
+        x_ready = true;
+      }
       for (int j = 0; j < it.kps; ++j)
         tma_3d(dst + 2 * abytes + j * bterm, bmap, (kb + j) * 128, it.pos0, 0, fb);
       ++s;
@@ -784,6 +827,19 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
   uint32_t thead = 0;   // the copy thread's TMEM placement, recomputed
   int pending = -1;   // active index of a finished gate+up item not yet published
   bool bad = false;
+  // the x terms of this CTA's share of the slots, then the grid barrier that
+  // makes all of them (and the zeroed counters) visible to the copies
+  prep_x(a);
+  fence_proxy_async_global();
+  if (!epi_grid_barrier(S, a.grid_ctr)) {
+    bad = true;
+    fail(S, a);
+  }
+  if (et == 0) {
+    fence_proxy_async_global();
+    __threadfence();
+    S.misc[6] = 1;
+  }
   for (int i = blockIdx.x; i < total; i += gridDim.x) {
     const Item it = decode(S, A, i, TR, FT, FD);
     const int KB = it.gu ? a.H / 128 : KBd;
@@ -932,10 +988,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if ((smem_addr(S.ring) & 1023u) != 0) fail(S, a);
 
   pdl_wait();   // the tables of the alignment are final
-  prep_x(a);
-  fence_proxy_async_global();
-  if (!grid_barrier(S, a.grid_ctr)) fail(S, a);
-  fence_proxy_async_global();
+  // The item table first (it needs only the alignment's tables); the x terms
+  // are written by the promotion warps while the copy warp already streams
+  // weight tiles, which do not depend on them (misc[6]: x terms ready).
   const int A = build_table(a, S);
   const int TR = S.misc[3];
   const int total = S.misc[0] ? 0 : TR * (a.I / 128 + a.H / 256);
