@@ -65,10 +65,14 @@ extern "C" int moe_decode_layer_noalloc(const moe_layer_desc *layer, const uint1
   void *ws = nullptr;
   st = scratch_address(&ws);
   if (st) return st;
-  // The layer's grid-barrier count must start the call consistent: clear it
-  // (the rest of the workspace is fully written before it is read).
-  const cudaError_t e = cudaMemsetAsync(static_cast<char *>(ws) + v.blend_counters, 0, 8,
-                                        (cudaStream_t)stream);
+  // The layer's grid-barrier count and the tensor-core path's item counters
+  // must start the call consistent: clear them (the rest of the workspace is
+  // fully written before it is read).
+  cudaError_t e = cudaMemsetAsync(static_cast<char *>(ws) + v.blend_counters, 0, 8,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess && v.tc_done)
+    e = cudaMemsetAsync(static_cast<char *>(ws) + v.tc_done, 0, ((size_t)v.cap + 1) * 4,
+                        (cudaStream_t)stream);
   if (e != cudaSuccess) {
     moe::set_last_cuda_error(e);
     return MOE_ECUDA;

@@ -52,6 +52,7 @@ constexpr int kEpiThreads = kEpiWarps * 32;    // 512
 constexpr int kRecs = 8;                       // stage records (ring slots in flight)
 constexpr int kAccs = 16;                      // k-block accumulator barriers (TMEM)
 constexpr int kTfree = 16;                     // per-stage TMEM release barriers
+constexpr int kIQ = 32;                        // item queue (copy thread -> MMA, promotion)
 constexpr int kRowTile = 64;                   // token rows per item (MMA N <= 64)
 constexpr int kTileBytes = 128 * 128;          // one 128-row x 128-byte weight box
 constexpr int kXTerms = 2, kHTerms = 3;
@@ -74,6 +75,7 @@ struct TcArgs {
   float *hs;                                 // 2^-s per (row, 128-block) [max_total][I/128]
   float *h, *y;                              // [max_total][I], [max_total][H]
   int *done;                                 // [cap] finished gate+up items per active expert
+  int *work;                                 // [1] next item to take (zero between calls)
   unsigned long long *grid_ctr;
   uint32_t *err;
   uint32_t ring_bytes;
@@ -89,7 +91,8 @@ struct TcMaps {
 
 struct Smem {
   uint8_t *ring;
-  uint64_t *full, *empty, *accf, *tfree, *drain;
+  uint64_t *full, *empty, *accf, *tfree, *iqbar, *drain;
+  volatile int *iq;    // [kIQ] the CTA's items in the order it takes them
   uint32_t *rec;       // [kRecs] byte offset of each stage in the ring
   uint32_t *rlen;      // [kRecs] its size
   uint32_t *trec;      // [kRecs] its accumulators: TMEM column | count << 16
@@ -106,8 +109,8 @@ __host__ __device__ inline size_t al16(size_t v) { return (v + 15) & ~size_t(15)
 
 __host__ __device__ inline size_t fixed_bytes(int cap) {
   size_t b = 0;
-  b += al16(8 * (2 * kRecs + kAccs + kTfree + 1));
-  b += 4 * al16(4 * kRecs) + al16(4 * 16);
+  b += al16(8 * (2 * kRecs + kAccs + kTfree + kIQ + 1));
+  b += 4 * al16(4 * kRecs) + al16(4 * kIQ) + al16(4 * 16);
   b += al16(4 * 2 * kMaxKB) + al16(4 * kMaxKBd * kRowTile) + al16(4 * 4 * 4 * 16);
   b += al16(4 * ((size_t)cap + 1)) + al16(8 * (size_t)cap);
   return b;
@@ -122,16 +125,18 @@ __device__ Smem carve(uint8_t *base, const TcArgs &a) {
     p += al16(bytes);
     return r;
   };
-  uint64_t *bars = reinterpret_cast<uint64_t *>(take(8 * (2 * kRecs + kAccs + kTfree + 1)));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(take(8 * (2 * kRecs + kAccs + kTfree + kIQ + 1)));
   S.full = bars;
   S.empty = bars + kRecs;
   S.accf = bars + 2 * kRecs;
   S.tfree = bars + 2 * kRecs + kAccs;
-  S.drain = bars + 2 * kRecs + kAccs + kTfree;
+  S.iqbar = bars + 2 * kRecs + kAccs + kTfree;
+  S.drain = bars + 2 * kRecs + kAccs + kTfree + kIQ;
   S.rec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.rlen = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.trec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.twait = reinterpret_cast<int *>(take(4 * kRecs));
+  S.iq = reinterpret_cast<volatile int *>(take(4 * kIQ));
   S.misc = reinterpret_cast<volatile int *>(take(4 * 16));
   S.sc = reinterpret_cast<float *>(take(4 * 2 * kMaxKB));
   S.cs = reinterpret_cast<float *>(take(4 * kMaxKBd * kRowTile));
@@ -394,8 +399,6 @@ __device__ __forceinline__ uint32_t stage_bytes(const Item &it) {
 // row's loads in flight together (16 per lane for H = 4096).
 __device__ void prep_x(const TcArgs &a) {
   const int ew = (threadIdx.x >> 5) - 2, lane = threadIdx.x & 31, et = threadIdx.x - 64;
-  if (blockIdx.x == 0)
-    for (int i = et; i < a.cap; i += kEpiThreads) a.done[i] = 0;
   const int nw = gridDim.x * kEpiWarps;
   const size_t plane = (size_t)a.max_total * a.H;
   for (int i = blockIdx.x * kEpiWarps + ew; i < a.n; i += nw) {
@@ -554,6 +557,18 @@ __device__ int build_table(const TcArgs &a, const Smem &S) {
 // ---------------------------------------------------------------------------
 // roles
 // ---------------------------------------------------------------------------
+//
+// Items are taken dynamically: CTA b starts with item b; after issuing an
+// item's copies its copy thread takes the next index of the grid-wide order
+// (gate+up items, then down items) from a counter, and passes each index to
+// the MMA thread and the promotion warps through a small queue.  Indices are taken in increasing order, so a down
+// item's gate+up items have all been taken by running CTAs before it is.
+
+// The j-th item of this CTA (total: no more items), or -1 when the wait gave up.
+__device__ __forceinline__ int next_item(const Smem &S, int j) {
+  if (!wait_bar(S, &S.iqbar[j % kIQ], (uint32_t)(j / kIQ) & 1)) return -1;
+  return S.iq[j % kIQ];
+}
 
 __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A, int TR,
                          int total) {
@@ -564,7 +579,13 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
   int s = 0, tail = 0;
   int ttail = 0;                   // oldest stage that may still hold TMEM
   bool ok = true;
-  for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+  int jq = 0;                      // items passed to the queue
+  int i = blockIdx.x;              // the first item is the CTA's own
+  if (i >= total) i = total;
+  while (i < total && ok) {
+    S.iq[jq % kIQ] = i;
+    mbar_arrive(&S.iqbar[jq % kIQ]);
+    ++jq;
     const Item it = decode(S, A, i, TR, FT, FD);
     if (!it.gu) {
       const int need = (S.rtp[it.a + 1] - S.rtp[it.a]) * FT;
@@ -651,7 +672,12 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
         tma_3d(dst + 2 * abytes + j * bterm, bmap, (kb + j) * 128, it.pos0, 0, fb);
       ++s;
     }
+    // the next item, taken once this one's copies are all issued (taken any
+    // earlier, a CTA would hold two items while another has none)
+    i = (int)gridDim.x + atomicAdd(a.work, 1);
   }
+  S.iq[jq % kIQ] = total;   // no more items
+  mbar_arrive(&S.iqbar[jq % kIQ]);
   if (!ok) fail(S, a);
   // every copy this CTA issued has landed before it moves on
   for (int j = max(tail, s - kRecs); j < s; ++j) {
@@ -670,7 +696,10 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
   int q = 0;                      // k blocks
   int tdone = -1;                 // newest stage whose TMEM release was seen
   bool ok = true;
-  for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+  for (int jq = 0; ok; ++jq) {
+    const int i = next_item(S, jq);
+    if (i < 0) ok = false;
+    if (i < 0 || i >= total) break;
     const Item it = decode(S, A, i, TR, FT, FD);
     const int KB = it.gu ? a.H / 128 : a.I / 128;
     const int T = it.gu ? kXTerms : kHTerms;
@@ -840,7 +869,15 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
     __threadfence();
     S.misc[6] = 1;
   }
-  for (int i = blockIdx.x; i < total; i += gridDim.x) {
+  for (int jq = 0;; ++jq) {
+    // every lane of every promotion warp takes the same item
+    int i = next_item(S, jq);
+    i = __shfl_sync(0xFFFFFFFFu, i, 0);
+    if (epi_sync_or(i < 0)) {
+      bad = true;
+      break;
+    }
+    if (i >= total) break;
     const Item it = decode(S, A, i, TR, FT, FD);
     const int KB = it.gu ? a.H / 128 : KBd;
     fence_proxy_async_global();   // this thread's h terms before the publish
@@ -969,6 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int j = 0; j < kAccs; ++j) mbar_init(&S.accf[j], 1);
     for (int j = 0; j < kTfree; ++j) mbar_init(&S.tfree[j], kEpiWarps);
+    for (int j = 0; j < kIQ; ++j) mbar_init(&S.iqbar[j], 1);
     mbar_init(S.drain, 1);
     for (int j = 0; j < 16; ++j) S.misc[j] = 0;
     fence_mbar_init();
@@ -1021,6 +1059,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
     return;
   }
+  // every item of every CTA is done: the counters start the next call at zero
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= a.cap; i += kThreads) a.done[i] = 0;
   const long long T4 = (long long)a.M * a.H / 4;
   const long long o1 = T4 * (blockIdx.x + 1) / gridDim.x;
   for (long long o = T4 * blockIdx.x / gridDim.x + threadIdx.x; o < o1; o += kThreads) {
@@ -1169,7 +1210,7 @@ void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&byte
   bytes[1] = (size_t)max_total * 4;
   bytes[2] = (size_t)kHTerms * max_total * I;
   bytes[3] = (size_t)max_total * (I / 128) * 4;
-  bytes[4] = (size_t)cap * 4;
+  bytes[4] = ((size_t)cap + 1) * 4;
 }
 
 int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *ids,
@@ -1205,6 +1246,7 @@ int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *
   a.h = reinterpret_cast<float *>(base + v.h);
   a.y = reinterpret_cast<float *>(base + v.y);
   a.done = reinterpret_cast<int *>(base + v.tc_done);
+  a.work = a.done + v.cap;
   a.grid_ctr = reinterpret_cast<unsigned long long *>(base + v.blend_counters);
   a.err = err;
   const size_t ring = ring_bytes_for(v.cap);

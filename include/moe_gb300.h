@@ -243,8 +243,9 @@ typedef struct moe_workspace_view {
      * terms it multiplies, as E4M3 planes with power-of-two scales --
      * x = (t0 + t1) * x_scale[p] per sorted row [2][max_total][H] u8 and
      * [max_total] float; h = (t0 + t1 + t2) * h_scale[p][c/128]
-     * [3][max_total][I] u8 and [max_total][I/128] float -- and an internal
-     * [cap] int32 count per active expert. */
+     * [3][max_total][I] u8 and [max_total][I/128] float -- and internal
+     * int32 counters ([cap] per active expert, then the item counter), which
+     * every call leaves at zero. */
     size_t tc_x_terms, tc_x_scale, tc_h_terms, tc_h_scale, tc_done;
     size_t total_bytes;
     int max_total, max_blocks, cap;
