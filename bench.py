@@ -160,7 +160,7 @@ class ClockSampler:
 # workload
 # --------------------------------------------------------------------------
 
-def build_workload(M: int, steps: int, device: str):
+def build_workload(M: int, steps: int, device: str, path: int = 0):
     import synth
     import expert_routing_alignment_gb300 as moe
     shape = synth.decode_fp8(M)
@@ -171,7 +171,7 @@ def build_workload(M: int, steps: int, device: str):
     logits = torch.stack([synth.make_logits(M, shape.E, SEED + 100 + s, device)
                           for s in range(steps)])
     layers = [moe.LayerDesc(top_k=shape.top_k, block_size=shape.BS,
-                            routed=moe.Experts.from_synth(c)) for c in copies]
+                            routed=moe.Experts.from_synth(c), path=path) for c in copies]
     return shape, base, copies, layers, x, logits
 
 
@@ -442,7 +442,7 @@ def run_gpu(args, rank: int, world: int):
     results = {}
     sweep = []
     for M in args.sweep:
-        shape, base, copies, layers, x, logits = build_workload(M, K, "cuda")
+        shape, base, copies, layers, x, logits = build_workload(M, K, "cuda", args.path)
         ws = moe.alloc_workspace(layers[0], M)
         out = torch.empty(M, shape.H, dtype=torch.bfloat16, device="cuda")
         head = M == args.m and not args.profile
@@ -538,6 +538,9 @@ def main():
                     help="skip the M=128 verify-batch measurement")
     ap.add_argument("--profile-verify", action="store_true",
                     help="only run a small case of the verify-batch kernel (for ncu)")
+    ap.add_argument("--path", type=int, default=0,
+                    help="MOE_PATH_* of the decode workloads (0 auto: tensor cores for FP8; "
+                         "1: the CUDA cores' fused kernel)")
     ap.add_argument("--copies", type=int, default=16,
                     help="weight copies the steps rotate over (16 keeps weights out of L2)")
     ap.add_argument("--profile", action="store_true",
