@@ -757,14 +757,19 @@ __device__ void finish_gate_up(const TcArgs &a, const Smem &S, const Item &it, i
                                int lane, const float (&acc0)[16], const float (&acc1)[16]) {
   const int c0 = grp * 16, f = q * 32 + lane, o = it.tile * 128 + f;
   const int KBd = a.I / 128;
+  // only the item's real rows are finished (the condition is the same for the
+  // whole warp; at decode sizes most of a warp's 16 columns are padding)
   float hv[16];
 #pragma unroll
   for (int jj = 0; jj < 16; ++jj) {
-    const float xi = S.cs[c0 + jj];
-    hv[jj] = silu_f32(acc0[jj] * xi) * (acc1[jj] * xi);
-    if (c0 + jj < it.rows) a.h[(size_t)(it.pos0 + c0 + jj) * a.I + o] = hv[jj];
-    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv[jj])));
-    if (lane == 0) S.red[(grp * 4 + q) * 16 + jj] = m;
+    hv[jj] = 0.f;
+    if (c0 + jj < it.rows) {
+      const float xi = S.cs[c0 + jj];
+      hv[jj] = silu_f32(acc0[jj] * xi) * (acc1[jj] * xi);
+      a.h[(size_t)(it.pos0 + c0 + jj) * a.I + o] = hv[jj];
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv[jj])));
+      if (lane == 0) S.red[(grp * 4 + q) * 16 + jj] = m;
+    }
   }
   group_sync(grp);
   float scl = 1.f;
@@ -780,6 +785,7 @@ __device__ void finish_gate_up(const TcArgs &a, const Smem &S, const Item &it, i
   const size_t plane = (size_t)a.max_total * a.I;
 #pragma unroll
   for (int jj = 0; jj < 16; jj += 2) {
+    if (c0 + jj >= it.rows) break;
     const float v0 = hv[jj] * __shfl_sync(0xFFFFFFFFu, scl, jj);
     const float v1 = hv[jj + 1] * __shfl_sync(0xFFFFFFFFu, scl, jj + 1);
     const uint32_t b0 = e4m3x2(v0, v1);
