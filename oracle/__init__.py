@@ -73,6 +73,8 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_bf16_rne.argtypes = [ctypes.c_double]
     L.oracle_bf16_value.restype = ctypes.c_double
     L.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+    L.oracle_router_logits.restype = None
+    L.oracle_router_logits.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     L.oracle_topk_softmax.restype = None
     L.oracle_topk_softmax.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P]
     L.oracle_align_sizes.restype = None
@@ -135,6 +137,18 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 # --------------------------------------------------------------------------
 # routing and alignment
 # --------------------------------------------------------------------------
+
+def router_logits(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """float64 [M, E] logits of bf16 rows x [M, H] against bf16 router weights [E, H]."""
+    x = _c(x_bits, np.uint16)
+    W = _c(w_bits, np.uint16)
+    M, H = x.shape
+    E = W.shape[0]
+    assert W.shape[1] == H
+    out = np.empty((M, E), np.float64)
+    lib().oracle_router_logits(_ptr(x), _ptr(W), M, H, E, _ptr(out))
+    return out
+
 
 def topk_softmax(logits: np.ndarray, k: int):
     """ids int32 [M, k] (descending logit, ties to the lower id), w float64 [M, k]."""

@@ -25,6 +25,8 @@
  *            (page 2): forward_nvfp4_grouped_decode (route -> sort -> gate+up
  *            -> down -> blend; NVFP4 tables = packed codes, per-16 scales and
  *            one fp32 global scale per projection).
+ *   [ROUTER] the same page: the router matrix-vector product named in
+ *            nvfp4_grouped_decode_ok (router_gemv_batchm) ahead of grouped_route.
  *   [VEC]    "nbxtensor/ops/moe_decode_vec.py" (page 1): the SwiGLU epilogue
  *            h = silu(g) * u in pure fp32 (here: double), fixed-order
  *            combine of the router-weighted expert outputs.
@@ -103,6 +105,29 @@ double oracle_bf16_value(uint16_t bits)
     float f;
     memcpy(&f, &b, 4);
     return (double)f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Router logits: the matrix-vector product ahead of the top-k              */
+/* ------------------------------------------------------------------------ */
+
+/* logits[t][e] = sum_c x[t][c] * W[e][c], in double, for M rows of bf16 x
+ * [M][H] and bf16 router weights W [E][H] (row-major).  The pages name the
+ * kernel (forward_nvfp4_grouped_decode: nvfp4_grouped_decode_ok requires
+ * router_gemv_batchm; grouped_route takes the hidden input) but print no
+ * arithmetic; this is the plainest reading of a router that maps hidden
+ * states to one logit per expert: no bias, no normalisation. */
+void oracle_router_logits(const uint16_t *x, const uint16_t *W, int M, int H, int E,
+                          double *logits)
+{
+    for (int t = 0; t < M; ++t)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int c = 0; c < H; ++c)
+                acc += oracle_bf16_value(x[(size_t)t * H + c]) *
+                       oracle_bf16_value(W[(size_t)e * H + c]);
+            logits[(size_t)t * E + e] = acc;
+        }
 }
 
 /* ------------------------------------------------------------------------ */

@@ -131,6 +131,41 @@ def test_dequant_nvfp4_matches_table_and_torch():
 # routing
 # --------------------------------------------------------------------------
 
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_router_logits_match_torch_matmul():
+    """The router's logits equal a float64 matmul of the bf16 values (library
+    routine), for several shapes including the decode and verify widths."""
+    g = torch.Generator().manual_seed(3)
+    for M, H, E in [(1, 64, 8), (4, 256, 8), (8, 2048, 128), (3, 4096, 256)]:
+        x = torch.randn(M, H, generator=g).to(torch.bfloat16)
+        W = (torch.randn(E, H, generator=g) * 0.02).to(torch.bfloat16)
+        got = oracle.router_logits(_bits(x), _bits(W))
+        ref = (x.double() @ W.double().T).numpy()
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_router_logits_closed_form():
+    """Exact cases: one-hot rows pick out a weight column; small-integer
+    operands give exact integer dot products; the order of the rows and of
+    the experts is kept (a transposed operand would fail)."""
+    M, H, E = 3, 40, 5
+    x = np.zeros((M, H), np.float32)
+    x[0, 7] = 1.0
+    x[1, 0] = 2.0
+    x[2] = np.arange(H) % 5 - 2
+    W = (np.arange(E * H).reshape(E, H) % 7 - 3).astype(np.float32)
+    xb = _bits(torch.from_numpy(x).to(torch.bfloat16))
+    Wb = _bits(torch.from_numpy(W).to(torch.bfloat16))
+    got = oracle.router_logits(xb, Wb)
+    np.testing.assert_array_equal(got[0], W[:, 7])
+    np.testing.assert_array_equal(got[1], 2.0 * W[:, 0])
+    want2 = [sum(int(x[2, c]) * int(W[e, c]) for c in range(H)) for e in range(E)]
+    np.testing.assert_array_equal(got[2], np.array(want2, np.float64))
+
+
 def test_topk_softmax_matches_torch():
     g = torch.Generator().manual_seed(3)
     lg = torch.randn(64, 128, generator=g)
