@@ -19,6 +19,11 @@ synchronize on both sides):
               copied in from pinned memory, the output copied back, per step.
 The CPU baseline is the oracle on a bounded sample of the same workload.
 
+The line also carries `router_logits`: the router matrix-vector product ahead of the
+top-k (bf16 x times bf16 router weights) at the decode and verify widths, timed over
+weight copies that keep it out of L2; and `hidden_in`: the headline decode layer given
+x alone, its logits computed from router weights inside the layer call.
+
 The same line carries `verify_batch`: the M=128 verify batch (H=4096,
 I=1536, E=256, top_k=8, BS=64, router logits with a Zipf(s=1.1) per-expert
 bias, fresh noise every step) on the tensor-core path, K graph-replayed steps
@@ -246,6 +251,90 @@ def run_verify(moe, stream, K: int, W: int, peaks: dict) -> dict:
                path=("tensor cores: verify_ffn_kernel (tcgen05 kind::f8f6f4, TMEM accumulators)"
                      if launches == 3 else f"{launches} launches"),
                l2="2 weight copies of 4.8 GB; each step streams ~1.2 GB")
+    del g, copies, layers, base, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_router(moe, stream, peaks: dict) -> list:
+    """The router logits (bf16 x times bf16 router weights) at the decode and
+    verify widths: 64 calls in one CUDA graph, rotating over enough weight
+    copies (256 MB in all) that no call finds its weights in L2."""
+    res = []
+    for M, H, E in ((8, 2048, 128), (128, 4096, 256)):
+        g = torch.Generator(device="cuda").manual_seed(SEED + 7)
+        x = torch.randn(M, H, generator=g, device="cuda").to(torch.bfloat16)
+        per = E * H * 2
+        n_w = max(2, (256 << 20) // per)
+        Ws = (torch.randn(E, H, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+        Ws = Ws.unsqueeze(0).repeat(n_w, 1, 1).contiguous()
+        out = torch.empty(M, E, dtype=torch.float32, device="cuda")
+        calls = 64
+        with torch.cuda.stream(stream):
+            for i in range(8):
+                moe.moe_router_logits(x, Ws[i % n_w], out)
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(calls):
+                moe.moe_router_logits(x, Ws[(i * 7) % n_w], out)
+        times = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                gr.replay()
+                b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        us = 1e3 * float(np.median(times)) / calls
+        nbytes = per + M * H * 2 + M * E * 4
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res.append(dict(M=M, H=H, E=E, us_per_call=round(us, 3), bytes_per_call=nbytes,
+                        gbs=round(gbs, 1), pct_of_measured_hbm=round(100 * gbs / peaks["hbm_gbs"], 1),
+                        kernel="router_logits_kernel (k split over 256 threads, fixed-order sums)"))
+        del gr, Ws
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_hidden_in(moe, stream, M: int, K: int, W: int, path: int) -> dict:
+    """The decode layer given x alone: the layer computes its logits from its
+    router weights (one launch more).  K steps in one CUDA graph over the 16
+    weight copies (each with its own router weights) and fresh x every step."""
+    import synth
+    shape, base, copies, layers, _, _ = build_workload(M, 1, "cuda", path)
+    ws_r = [synth.make_router_weight(shape.E, shape.H, SEED + 500 + i, "cuda")
+            for i in range(N_COPIES)]
+    layers = [moe.LayerDesc(top_k=shape.top_k, block_size=shape.BS, routed=lay.routed,
+                            path=path, router_weight=w) for lay, w in zip(layers, ws_r)]
+    xs = torch.stack([synth.make_x(M, shape.H, SEED + 600 + s, "cuda") for s in range(K)])
+    ws = moe.alloc_workspace(layers[0], M)
+    out = torch.empty(M, shape.H, dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(stream):
+        for s in range(W):
+            moe.moe_decode_layer(layers[s % N_COPIES], xs[s % K], out, ws)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for s in range(K):
+            moe.moe_decode_layer(layers[s % N_COPIES], xs[s], out, ws)
+    g.replay()
+    stream.synchronize()
+    times = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    us = 1e3 * float(np.median(times)) / K
+    res = dict(workload=shape.name, M=M, steps=K, us_per_layer=round(us, 3),
+               tokens_per_s=round(M / (us * 1e-6), 1),
+               launches_per_layer=moe.moe_decode_layer_launches(layers[0], M, 2),
+               input="x alone; logits from bf16 router weights [E, H], one set per weight copy")
     del g, copies, layers, base, ws
     torch.cuda.empty_cache()
     return res
@@ -481,6 +570,8 @@ def run_gpu(args, rank: int, world: int):
             print(json.dumps(dict(profile=True, sweep=sweep)), flush=True)
         return
     verify = None if args.no_verify else run_verify(moe, stream, min(K, 16), 3, peaks)
+    router = None if args.no_verify else run_router(moe, stream, peaks)
+    hidden_in = None if args.no_verify else run_hidden_in(moe, stream, args.m, K, W, args.path)
     # max over ranks
     ms_t = torch.tensor([results["ms"]], device="cuda")
     if world > 1:
@@ -509,6 +600,8 @@ def run_gpu(args, rank: int, world: int):
         algorithmic_bytes_per_layer=int(r["nbytes"]),
         sweep=sweep,
         verify_batch=verify,
+        router_logits=router,
+        hidden_in=hidden_in,
         roofline=dict(bound="hbm",
                       kernel=KERNELS[r["kernel"]][0],
                       achieved=round(dk_achieved, 1),

@@ -69,14 +69,15 @@ class _Experts(ctypes.Structure):
 
 class _LayerDesc(ctypes.Structure):
     _fields_ = [("top_k", ctypes.c_int), ("block_size", ctypes.c_int), ("path", ctypes.c_int),
-                ("routed", _Experts), ("shared", ctypes.POINTER(_Experts))]
+                ("routed", _Experts), ("shared", ctypes.POINTER(_Experts)),
+                ("router_weight", ctypes.c_void_p)]
 
 
 class _WsView(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "topk_ids", "topk_w", "sorted_token_ids", "sorted_expert_ids", "expert_offsets",
         "token_to_perm", "active_experts", "active_count", "num_tokens_post_padded", "h",
-        "h_shared", "y", "y_shared", "blend_counters", "tc_x_terms", "tc_x_scale",
+        "h_shared", "y", "y_shared", "blend_counters", "router_logits", "tc_x_terms", "tc_x_scale",
         "tc_h_terms", "tc_h_scale", "tc_done", "total_bytes")] + [
         ("max_total", ctypes.c_int), ("max_blocks", ctypes.c_int), ("cap", ctypes.c_int)]
 
@@ -90,6 +91,7 @@ EXPORTS = {
     "moe_align_sizes": (_I, [_I, _I, _I, _P, _P, _P]),
     "moe_align": (_I, [_P, _I, _I, _I, _I] + [_P] * 9),
     "moe_topk_softmax": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_router_logits": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_grouped_gate_up": (_I, [ctypes.POINTER(_Experts), ctypes.POINTER(_Experts), _P, _I, _I,
                                  _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_grouped_down": (_I, [ctypes.POINTER(_Experts), ctypes.POINTER(_Experts), _P, _P, _I, _I,
@@ -182,11 +184,14 @@ class LayerDesc:
     routed: Experts
     shared: Optional[Experts] = None
     path: int = PATH_AUTO
+    # bf16 [E, H] on the device: lets moe_decode_layer take x alone (hidden in)
+    router_weight: Optional[torch.Tensor] = None
     _struct: _LayerDesc = field(init=False, repr=False)
 
     def __post_init__(self):
         sh = ctypes.pointer(self.shared._struct) if self.shared is not None else None
-        self._struct = _LayerDesc(self.top_k, self.block_size, self.path, self.routed._struct, sh)
+        self._struct = _LayerDesc(self.top_k, self.block_size, self.path, self.routed._struct, sh,
+                                  _ptr(self.router_weight))
 
     @property
     def num_experts(self) -> int:
@@ -248,6 +253,18 @@ def moe_topk_softmax(logits: torch.Tensor, top_k: int, ids: Optional[torch.Tenso
     _check("moe_topk_softmax", load().moe_topk_softmax(_ptr(logits), M, E, top_k, _ptr(ids),
                                                        _ptr(w), _stream(stream)))
     return ids, w
+
+
+def moe_router_logits(x: torch.Tensor, router_weight: torch.Tensor,
+                      logits: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """fp32 logits [M, E] = x [M, H] (bf16) times router_weight [E, H] (bf16) transposed."""
+    M, H = x.shape
+    E = router_weight.shape[0]
+    if logits is None:
+        logits = torch.empty(M, E, dtype=torch.float32, device=x.device)
+    _check("moe_router_logits", load().moe_router_logits(_ptr(x), _ptr(router_weight), M, H, E,
+                                                         _ptr(logits), _stream(stream)))
+    return logits
 
 
 def _sp(x: Optional[Experts]):
@@ -330,11 +347,13 @@ def workspace_view(layer: LayerDesc, M: int, ws: torch.Tensor) -> dict:
         h_shared=sl(v.h_shared, M * Is, torch.float32).view(M, Is),
         y=sl(v.y, v.max_total * H, torch.float32).view(v.max_total, H),
         y_shared=sl(v.y_shared, M * H, torch.float32).view(M, H),
+        router_logits=sl(v.router_logits, M * E, torch.float32).view(M, E),
         max_total=v.max_total, max_blocks=v.max_blocks, cap=v.cap, **tc)
 
 
-def moe_decode_layer_launches(layer: LayerDesc, M: int, with_logits: bool = True) -> int:
-    """Kernels one moe_decode_layer call enqueues (host only)."""
+def moe_decode_layer_launches(layer: LayerDesc, M: int, with_logits: int = 1) -> int:
+    """Kernels one moe_decode_layer call enqueues (host only); with_logits 0:
+    ids given, 1: logits given, 2: logits computed from x (hidden in)."""
     n = load().moe_decode_layer_launches(ctypes.pointer(layer._struct), M, int(with_logits))
     if n < 0:
         raise MoeError("moe_decode_layer_launches", MOE_EINVAL)

@@ -14,6 +14,8 @@ int simt_down(const moe_experts *routed, const moe_experts *shared, const float 
               const float *h_sh, int M, int top_k, const int32_t *off, const int32_t *sti,
               const int32_t *act, const int32_t *act_count, float *y, float *y_sh, void *stream);
 int launch_topk(const float *logits, int M, int E, int k, int32_t *ids, float *w, void *stream);
+int launch_router(const uint16_t *x, const uint16_t *W, int M, int H, int E, float *logits,
+                  void *stream);
 int launch_blend(const float *y, const float *w, const int32_t *ttp, const float *y_sh,
                  uint16_t *out, int M, int k, int H, void *stream);
 bool fused_fits(const moe_layer_desc *L, int M, int sms);
@@ -106,6 +108,7 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   v->y = take((size_t)max_total * H * 4);
   v->y_shared = take((size_t)M * H * 4);
   v->blend_counters = take(8);
+  v->router_logits = take((size_t)M * E * 4);
   v->tc_x_terms = v->tc_x_scale = v->tc_h_terms = v->tc_h_scale = v->tc_done = 0;
   if (tc_allowed(L, M)) {
     size_t b[5];
@@ -168,9 +171,11 @@ extern "C" int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int
   if (moe::layout(layer, M, &v) != MOE_OK) return -1;
   const int run = moe::layer_run(layer, M);
   if (run < 0) return -1;
-  if (run == moe::kRunFused) return 1;
-  if (run == moe::kRunTc) return with_logits ? 3 : 2;
-  return with_logits ? 5 : 4;
+  if (with_logits == 2 && !layer->router_weight) return -1;
+  const int router = with_logits == 2;   // the logits kernel ahead of the route
+  if (run == moe::kRunFused) return 1 + router;
+  if (run == moe::kRunTc) return (with_logits ? 3 : 2) + router;
+  return (with_logits ? 5 : 4) + router;
 }
 
 extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,
@@ -181,7 +186,10 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
   int st = moe::layout(layer, M, &v);
   if (st) return st;
   if (!x || !out || !workspace) return MOE_EINVAL;
-  if (!router_logits && (!topk_ids || !topk_w)) return MOE_EINVAL;
+  // hidden in: the logits come from x and the layer's router weights
+  const bool hidden_in = !router_logits && !topk_ids && layer->router_weight;
+  if (!router_logits && !hidden_in && (!topk_ids || !topk_w)) return MOE_EINVAL;
+  if (hidden_in && ((uintptr_t)layer->router_weight & 15)) return MOE_EINVAL;
   if (workspace_bytes < v.total_bytes || ((uintptr_t)workspace & 255)) return MOE_EINVAL;
   if (((uintptr_t)x & 15) || ((uintptr_t)out & 7)) return MOE_EINVAL;
   const int run = moe::layer_run(layer, M);
@@ -193,6 +201,11 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
   const int E = layer->routed.num_experts, k = layer->top_k, H = layer->routed.hidden;
   const moe_experts *S = layer->shared;
 
+  if (hidden_in) {
+    st = moe::launch_router(x, layer->router_weight, M, H, E, F32(v.router_logits), stream);
+    if (st) return st;
+    router_logits = F32(v.router_logits);
+  }
   if (run == moe::kRunFused)
     return moe::launch_fused(layer, x, M, router_logits, topk_ids, topk_w, out, workspace, v,
                              err_word, stream);

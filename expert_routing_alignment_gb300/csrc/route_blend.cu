@@ -36,6 +36,129 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_softmax_kernel(const flo
 }
 
 // ---------------------------------------------------------------------------
+// router logits: the k dimension split over a block's threads
+// ---------------------------------------------------------------------------
+//
+// What (the router matrix-vector product ahead of the top-k; the pages name
+// router_gemv_batchm in nvfp4_grouped_decode_ok of
+// "forward_nvfp4_grouped_decode.rs"): logits[t][e] = sum_c x[t][c] * W[e][c]
+// for bf16 x [M][H] and bf16 W [E][H], fp32 result.
+// How: a block owns RE (1, 2 or 4) expert rows and 8 x rows.  Thread i of the block takes
+// the 16-byte chunks i, i + 256, ... of every row, so each row of W is read
+// once per 8 x rows, in whole-block coalesced lines, and x comes from L2.
+// Each thread keeps RE x 8 fp32 partial sums (fmaf in chunk order, elements
+// ascending); a warp ends them with a reduce-scatter butterfly (xor 16, 8, 4,
+// 2, 1: the pairing tree of a plain butterfly, so every sum is added in the
+// same tree) and the 8 warps' sums are added in warp order.  The order of
+// every addition depends on H alone: a row's logits are the same bits for
+// every M, every RE and every run.  Products of two bf16 values are exact in
+// fp32.
+
+constexpr int kRouterThreads = 256;
+constexpr int kRouterRows = 8;   // x rows per block
+
+template <int RE>   // expert rows per block
+__global__ void __launch_bounds__(kRouterThreads)
+    router_logits_kernel(const uint16_t *x, const uint16_t *W, int M, int H, int E,
+                         float *logits) {
+  constexpr int N = RE * kRouterRows;   // partial sums per thread, index re * 8 + r
+  __shared__ float red[kRouterThreads / 32][N];
+  pdl_wait();
+  pdl_trigger();
+  const int e0 = blockIdx.x * RE, t0 = blockIdx.y * kRouterRows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chunks = H / 8;   // 16-byte chunks per row
+  float acc[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) acc[i] = 0.f;
+  // U chunks' loads are issued before any is used (the decode widths are
+  // bound by load latency); the sums still take the chunks in ascending order
+  constexpr int U = RE == 1 ? 4 : RE == 2 ? 2 : 1;
+  for (int c0 = tid; c0 < chunks; c0 += U * kRouterThreads) {
+    uint4 wv[U][RE], xv[U][kRouterRows];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * kRouterThreads;
+#pragma unroll
+      for (int re = 0; re < RE; ++re)
+        wv[u][re] = c < chunks && e0 + re < E
+                        ? ld_stream16(reinterpret_cast<const uint4 *>(W + (size_t)(e0 + re) * H) + c)
+                        : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int r = 0; r < kRouterRows; ++r)
+        xv[u][r] = c < chunks && t0 + r < M
+                       ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + r) * H) + c)
+                       : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (c0 + u * kRouterThreads >= chunks) break;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float wl[RE], wh[RE], xl[kRouterRows], xh[kRouterRows];
+#pragma unroll
+        for (int re = 0; re < RE; ++re) {
+          const uint4 q = wv[u][re];
+          const uint32_t v = h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w;
+          wl[re] = __uint_as_float(v << 16);
+          wh[re] = __uint_as_float(v & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int r = 0; r < kRouterRows; ++r) {
+          const uint4 q = xv[u][r];
+          const uint32_t v = h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w;
+          xl[r] = __uint_as_float(v << 16);
+          xh[r] = __uint_as_float(v & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int re = 0; re < RE; ++re)
+#pragma unroll
+          for (int r = 0; r < kRouterRows; ++r) {
+            float &v = acc[re * kRouterRows + r];
+            v = fmaf(wl[re], xl[r], v);
+            v = fmaf(wh[re], xh[r], v);
+          }
+      }
+    }
+  }
+  // reduce-scatter: while a lane holds more than one sum it keeps half of them
+  // (the upper half where its lane bit is set) and adds the partner's copy
+  int idx = 0;   // the first sum this lane ends with
+  int cnt = N;
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) {
+    if (cnt > 1) {
+      const bool up = lane & m;
+      const int half = cnt / 2;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < half) {
+          const float send = up ? acc[i] : acc[i + half];
+          const float keep = up ? acc[i + half] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, m);
+        }
+      }
+      if (up) idx += half;
+      cnt = half;
+    } else {
+      acc[0] += __shfl_xor_sync(0xFFFFFFFFu, acc[0], m);
+    }
+  }
+  // lanes that hold the same sums (N < 32) wrote equal values; one writes
+  if ((lane & (32 * cnt / N - 1)) == 0)
+#pragma unroll
+    for (int i = 0; i < (N >= 32 ? N / 32 : 1); ++i) red[warp][idx + i] = acc[i];
+  __syncthreads();
+  if (tid < N) {
+    float v = red[0][tid];
+#pragma unroll
+    for (int w = 1; w < kRouterThreads / 32; ++w) v += red[w][tid];
+    const int re = tid / kRouterRows, r = tid - re * kRouterRows;
+    if (e0 + re < E && t0 + r < M) logits[(size_t)(t0 + r) * E + e0 + re] = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // blend
 // ---------------------------------------------------------------------------
 //
@@ -94,6 +217,25 @@ int launch_blend(const float *y, const float *w, const int32_t *ttp, const float
   return launch_pdl(blend_kernel, grid, dim3(256), 0, stream, y, w, ttp, y_sh, out, M, k, H);
 }
 
+// Expert rows per block: the most (up to 4, for the fewest re-reads of x; 8
+// holds too many registers for two blocks per SM) that still leave two blocks
+// per SM; 1 when even that is too few blocks.
+int launch_router(const uint16_t *x, const uint16_t *W, int M, int H, int E, float *logits,
+                  void *stream) {
+  const int row_blocks = (M + kRouterRows - 1) / kRouterRows;
+  const int want = 2 * sm_count();
+  auto blocks = [&](int re) { return ((E + re - 1) / re) * row_blocks; };
+  const dim3 block(kRouterThreads);
+  if (blocks(4) >= want)
+    return launch_pdl(router_logits_kernel<4>, dim3((E + 3) / 4, row_blocks), block, 0, stream, x,
+                      W, M, H, E, logits);
+  if (blocks(2) >= want)
+    return launch_pdl(router_logits_kernel<2>, dim3((E + 1) / 2, row_blocks), block, 0, stream, x,
+                      W, M, H, E, logits);
+  return launch_pdl(router_logits_kernel<1>, dim3(E, row_blocks), block, 0, stream, x, W, M, H, E,
+                    logits);
+}
+
 }  // namespace moe
 
 extern "C" int moe_topk_softmax(const float *logits, int M, int num_experts, int top_k,
@@ -103,6 +245,15 @@ extern "C" int moe_topk_softmax(const float *logits, int M, int num_experts, int
     return MOE_EINVAL;
   if (num_experts > MOE_MAX_EXPERTS || top_k > 32) return MOE_EUNSUPPORTED;
   return moe::launch_topk(logits, M, num_experts, top_k, topk_ids, topk_w, stream);
+}
+
+extern "C" int moe_router_logits(const uint16_t *x, const uint16_t *router_weight, int M,
+                                 int hidden, int num_experts, float *logits, void *stream) {
+  if (!x || !router_weight || !logits || M < 1 || hidden < 1 || num_experts < 1)
+    return MOE_EINVAL;
+  if (hidden % 8 || ((uintptr_t)x & 15) || ((uintptr_t)router_weight & 15))
+    return MOE_EUNSUPPORTED;
+  return moe::launch_router(x, router_weight, M, hidden, num_experts, logits, stream);
 }
 
 extern "C" int moe_blend(const float *y, const float *topk_w, const int32_t *token_to_perm,

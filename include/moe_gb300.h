@@ -103,6 +103,11 @@ typedef struct moe_layer_desc {
     int path;                    /* MOE_PATH_* */
     moe_experts routed;
     const moe_experts *shared;   /* host pointer to a descriptor, or NULL */
+    /* Router weights [num_experts][hidden] bf16 bits on the device, 16-byte
+     * aligned, or NULL.  With them, a moe_decode_layer call given neither
+     * router logits nor top-k ids computes the logits from x itself
+     * (moe_router_logits) into the workspace's router_logits region. */
+    const uint16_t *router_weight;
 } moe_layer_desc;
 
 /* ---- library information ------------------------------------------------ */
@@ -168,6 +173,20 @@ int moe_align(const void *topk_ids, int ids_is_int64, int n, int num_experts,
  * MOE_EUNSUPPORTED (E > MOE_MAX_EXPERTS, top_k > 32). */
 int moe_topk_softmax(const float *logits, int M, int num_experts, int top_k,
                      int32_t *topk_ids, float *topk_w, void *stream);
+
+/* Router logits, the matrix-vector product ahead of the top-k
+ * ("forward_nvfp4_grouped_decode.rs": the router_gemv_batchm kernel that
+ * nvfp4_grouped_decode_ok requires; grouped_route takes the hidden input).
+ * The pages print no arithmetic; the plain reading, with no bias:
+ *   logits[t][e] = sum_c x[t][c] * router_weight[e][c]
+ * accumulated in fp32 in an order that depends on hidden alone: run to run,
+ * and for every M, a row's logits are the same bits.
+ *   x [M][hidden] bf16 bits; router_weight [num_experts][hidden] bf16 bits,
+ *   both 16-byte aligned; logits out [M][num_experts] float.
+ * Errors: MOE_EINVAL (NULL, M, hidden or num_experts < 1), MOE_EUNSUPPORTED
+ * (hidden not a multiple of 8, x or weights misaligned). */
+int moe_router_logits(const uint16_t *x, const uint16_t *router_weight, int M,
+                      int hidden, int num_experts, float *logits, void *stream);
 
 /* ---- grouped expert FFN ------------------------------------------------- */
 
@@ -239,6 +258,8 @@ typedef struct moe_workspace_view {
     size_t num_tokens_post_padded;                 /* [1] */
     size_t h, h_shared, y, y_shared;               /* float tables */
     size_t blend_counters;                         /* internal: [1] uint64 grid-barrier count */
+    size_t router_logits;                          /* [M][E] float: the logits of a call that
+                                                      computed them from x (else unwritten) */
     /* tensor-core path only (all 0 on the CUDA-core path): the activation
      * terms it multiplies, as E4M3 planes with power-of-two scales --
      * x = (t0 + t1) * x_scale[p] per sorted row [2][max_total][H] u8 and
@@ -263,14 +284,18 @@ int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int M,
 /* Host only.  The number of kernels moe_decode_layer enqueues for M rows
  * (1 on the fused decode path; 3 with router logits, 2 with given ids on the
  * tensor-core path; otherwise 5 and 4), or -1 if the call would be
- * rejected. */
+ * rejected.  with_logits: 0 ids given, 1 logits given, 2 logits computed from
+ * x and the layer's router_weight (one launch more than 1). */
 int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logits);
 
 /* The decode MoE layer of M rows ("forward_nvfp4_grouped_decode.rs",
  * forward_nvfp4_grouped_decode): route (when router_logits is not NULL:
- * moe_topk_softmax; otherwise topk_ids [M][k] int32 and topk_w [M][k] float
- * are taken as given), moe_align, moe_grouped_gate_up, moe_grouped_down,
- * moe_blend, all enqueued on `stream` with no host read.
+ * moe_topk_softmax; when both router_logits and topk_ids are NULL and the
+ * layer has router_weight: moe_router_logits of x into the workspace, then
+ * moe_topk_softmax -- grouped_route's hidden input; otherwise topk_ids [M][k]
+ * int32 and topk_w [M][k] float are taken as given), moe_align,
+ * moe_grouped_gate_up, moe_grouped_down, moe_blend, all enqueued on `stream`
+ * with no host read.
  * On the CUDA-core path, when M*top_k <= 256, M <= 32, and hidden, inter and
  * the shared inter are multiples of 128 in [256, 2048] (NVFP4: of 256), the
  * same results come from one cooperative persistent kernel (gate+up, a grid

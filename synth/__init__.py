@@ -16,6 +16,8 @@ Workloads (no dataset or checkpoint exists; these shapes stand in):
                FP8 shared expert of inter 512 applied to every row
   * verify:    M=128, H=4096, I=1536, E=256, top_k=8, BS=64, FP8, router
                logits skewed by a Zipf(s=1.1) per-expert bias
+  * router:    bf16 router weights [E, H] for the layer's hidden-in form
+               (x alone, the logits computed on the device)
   * align:     ids only, n = 8*M, M in {1, 64, 1024, 4096}, E in
                {64, 256, 1024}, BS in {16, 64, 128}; uniform, Zipf(s=1.2)
                or all one expert
@@ -221,6 +223,16 @@ def make_logits(M: int, E: int, seed: int, device="cpu", zipf_s: Optional[float]
     if zipf_s is not None:
         lg = lg + zipf_bias(E, zipf_s, zipf_scale, bias_seed).to(device)
     return lg
+
+
+def make_router_weight(E: int, H: int, seed: int, device="cpu") -> torch.Tensor:
+    """bf16 [E, H] router weights, normal with standard deviation 1/sqrt(H):
+    with make_x's unit-normal x the logits have unit variance, like
+    make_logits' draws."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    w = torch.randn(E, H, generator=gen, device=device, dtype=torch.float32)
+    return (w * H ** -0.5).to(torch.bfloat16)
 
 
 def align_ids(n: int, E: int, dist: str, seed: int, expert: int = 0) -> np.ndarray:

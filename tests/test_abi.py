@@ -12,6 +12,7 @@ import pytest
 
 import expert_routing_alignment_gb300 as moe
 import oracle
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -171,3 +172,25 @@ def test_layer_rejects_rows_and_topk():
     fake = ctypes.c_void_p(256)
     assert lib.moe_decode_layer(p, fake, 8, fake, None, None, fake, fake, 16, None,
                                 None) == moe.MOE_EINVAL
+
+
+def test_hidden_in_launch_counts_and_logits_region():
+    """A layer with router weights can take x alone: the logits kernel runs
+    ahead of the route (one launch more than with given logits) and writes
+    the [M][E] float router_logits region of the workspace."""
+    lib = moe.load()
+    fake_w = torch.zeros(16, dtype=torch.int64)   # a host address; nothing is launched
+    for path, with_l in ((moe.PATH_AUTO, 3), (moe.PATH_SIMT_STAGED, 5)):
+        plain = moe.LayerDesc(top_k=8, block_size=64, path=path,
+                              routed=_fake_experts(E=256, H=4096, I=1536))
+        assert lib.moe_decode_layer_launches(ctypes.pointer(plain._struct), 128, 2) == -1
+        layer = moe.LayerDesc(top_k=8, block_size=64, path=path, router_weight=fake_w,
+                              routed=_fake_experts(E=256, H=4096, I=1536))
+        assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 1) == with_l
+        assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 2) == with_l + 1
+        v = moe._WsView()
+        assert lib.moe_decode_layer_workspace_view(ctypes.pointer(layer._struct), 128,
+                                                   ctypes.byref(v)) == 0
+        assert v.router_logits % 256 == 0 and v.router_logits > v.blend_counters
+        nxt = [o for o in (v.tc_x_terms, v.total_bytes) if o > v.router_logits]
+        assert min(nxt) - v.router_logits >= 128 * 256 * 4
