@@ -91,10 +91,12 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_grouped_down.argtypes = [ex, ex, _P, _P, ctypes.c_int, ctypes.c_int,
                                       _P, _P, _P, ctypes.c_int, _P, _P]
     L.oracle_blend.restype = None
-    L.oracle_blend.argtypes = [_P, _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+    L.oracle_shared_gate.restype = None
+    L.oracle_shared_gate.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int, _P]
+    L.oracle_blend.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                _P, _P]
     L.oracle_moe_layer.restype = ctypes.c_int
-    L.oracle_moe_layer.argtypes = [ex, ex, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+    L.oracle_moe_layer.argtypes = [ex, ex, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    _P, _P, _P, _P, _P]
 
 
@@ -147,6 +149,18 @@ def router_logits(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
     assert W.shape[1] == H
     out = np.empty((M, E), np.float64)
     lib().oracle_router_logits(_ptr(x), _ptr(W), M, H, E, _ptr(out))
+    return out
+
+
+def shared_gate(x_bits: np.ndarray, gate_bits: np.ndarray) -> np.ndarray:
+    """float64 [M] gates sigmoid(x[t] . gate_w) of bf16 rows x [M, H] and a
+    bf16 gate weight [H]."""
+    x = _c(x_bits, np.uint16)
+    g = _c(gate_bits, np.uint16).ravel()
+    M, H = x.shape
+    assert g.shape == (H,)
+    out = np.empty(M, np.float64)
+    lib().oracle_shared_gate(_ptr(x), _ptr(g), M, H, _ptr(out))
     return out
 
 
@@ -274,22 +288,25 @@ def grouped_down(X: Experts, S: Optional[Experts], h: np.ndarray, h_sh: Optional
 
 
 def blend(y: np.ndarray, w: np.ndarray, token_to_perm: np.ndarray, y_sh: Optional[np.ndarray],
-          M: int, top_k: int, H: int):
+          M: int, top_k: int, H: int, gate: Optional[np.ndarray] = None):
+    """gate: float64 [M] shared-expert gates, or None (ungated)."""
     y = _c(y, np.float64)
     w = _c(w, np.float64)
     ttp = _c(token_to_perm, np.int32)
     y_sh = None if y_sh is None else _c(y_sh, np.float64)
+    gate = None if gate is None else _c(gate, np.float64)
     out_d = np.empty((M, H), np.float64)
     out_b = np.empty((M, H), np.uint16)
-    lib().oracle_blend(_ptr(y), _ptr(w), _ptr(ttp), _ptr(y_sh), M, top_k, H, _ptr(out_d),
-                       _ptr(out_b))
+    lib().oracle_blend(_ptr(y), _ptr(w), _ptr(ttp), _ptr(y_sh), _ptr(gate), M, top_k, H,
+                       _ptr(out_d), _ptr(out_b))
     return out_d, out_b
 
 
 def moe_layer(X: Experts, S: Optional[Experts], x_bits: np.ndarray, M: int, top_k: int, BS: int,
               logits: Optional[np.ndarray] = None, ids: Optional[np.ndarray] = None,
-              w: Optional[np.ndarray] = None):
-    """The whole layer; returns (out float64 [M, H], out bf16 bits [M, H], bad ids)."""
+              w: Optional[np.ndarray] = None, shared_gate_bits: Optional[np.ndarray] = None):
+    """The whole layer; returns (out float64 [M, H], out bf16 bits [M, H], bad ids).
+    shared_gate_bits: bf16 [H] gate weight of the shared expert, or None."""
     x = _c(x_bits, np.uint16)
     lg = None if logits is None else _c(logits, np.float32)
     ids_c = None if ids is None else _c(ids, np.int32)
@@ -298,6 +315,7 @@ def moe_layer(X: Experts, S: Optional[Experts], x_bits: np.ndarray, M: int, top_
     out_b = np.empty((M, X.H), np.uint16)
     _xs, xp = _exp_ptr(X)
     _ss, sp = _exp_ptr(S)
-    bad = lib().oracle_moe_layer(xp, sp, _ptr(x), M, top_k, BS, _ptr(lg), _ptr(ids_c), _ptr(w_c),
+    gw = None if shared_gate_bits is None else _c(shared_gate_bits, np.uint16).ravel()
+    bad = lib().oracle_moe_layer(xp, sp, _ptr(gw), _ptr(x), M, top_k, BS, _ptr(lg), _ptr(ids_c), _ptr(w_c),
                                  _ptr(out_d), _ptr(out_b))
     return out_d, out_b, bad

@@ -27,6 +27,9 @@
  *            one fp32 global scale per projection).
  *   [ROUTER] the same page: the router matrix-vector product named in
  *            nvfp4_grouped_decode_ok (router_gemv_batchm) ahead of grouped_route.
+ *   [GATE]   the same page and moe_weighted_sum_blend_fp8_grouped of page 3:
+ *            the blend takes the layer input and shared_expert_gate.weight
+ *            (NULL: ungated shared expert).
  *   [VEC]    "nbxtensor/ops/moe_decode_vec.py" (page 1): the SwiGLU epilogue
  *            h = silu(g) * u in pure fp32 (here: double), fixed-order
  *            combine of the router-weighted expert outputs.
@@ -447,14 +450,30 @@ void oracle_grouped_down(const oracle_experts *X, const oracle_experts *S,
     }
 }
 
+/* [GATE] The shared expert's gate per token.  The pages pass the layer
+ * input and shared_expert_gate.weight to the blend and print no formula; the
+ * plain reading of a one-output gate layer: g[t] = sigmoid(sum_c x[t][c] *
+ * gate_w[c]) with bf16 x [M][H] and bf16 gate_w [H], no bias,
+ * sigmoid(z) = 1 / (1 + exp(-z)). */
+void oracle_shared_gate(const uint16_t *x, const uint16_t *gate_w, int M, int H, double *g)
+{
+    for (int t = 0; t < M; ++t) {
+        double z = 0.0;
+        for (int c = 0; c < H; ++c)
+            z += oracle_bf16_value(x[(size_t)t * H + c]) * oracle_bf16_value(gate_w[c]);
+        g[t] = 1.0 / (1.0 + exp(-z));
+    }
+}
+
 /* [SORT moe_weighted_sum_blend_fp8_grouped; VEC fixed-order combine]
  * out[t][c] = bf16( sum_{j=0..k-1} w[t][j] * y[token_to_perm[t*k+j]][c]
- *                   + y_sh[t][c] ), j in increasing order, one rounding to
- * bf16 at the end.  Slots with token_to_perm = -1 (an out-of-range id)
- * contribute nothing.  y_sh may be NULL (no shared expert; the shared gate
- * is absent: ungated).  out_d keeps the unrounded double. */
+ *                   + gate[t] * y_sh[t][c] ), j in increasing order, one
+ * rounding to bf16 at the end.  Slots with token_to_perm = -1 (an
+ * out-of-range id) contribute nothing.  y_sh may be NULL (no shared expert);
+ * gate may be NULL (an ungated shared expert: gate[t] = 1).  out_d keeps the
+ * unrounded double. */
 void oracle_blend(const double *y, const double *w, const int32_t *token_to_perm,
-                  const double *y_sh, int M, int top_k, int H,
+                  const double *y_sh, const double *gate, int M, int top_k, int H,
                   double *out_d, uint16_t *out_bf16)
 {
     for (int t = 0; t < M; ++t)
@@ -467,7 +486,7 @@ void oracle_blend(const double *y, const double *w, const int32_t *token_to_perm
                 acc += w[(size_t)t * top_k + j] * y[(size_t)p * H + c];
             }
             if (y_sh)
-                acc += y_sh[(size_t)t * H + c];
+                acc += (gate ? gate[t] : 1.0) * y_sh[(size_t)t * H + c];
             if (out_d)
                 out_d[(size_t)t * H + c] = acc;
             if (out_bf16)
@@ -477,8 +496,10 @@ void oracle_blend(const double *y, const double *w, const int32_t *token_to_perm
 
 /* [LAYER forward_nvfp4_grouped_decode] the whole layer: route (when logits
  * are given; else the caller's ids and weights), align, gate+up, down,
- * blend.  Returns the number of out-of-range ids the alignment skipped. */
+ * blend.  shared_gate_w ([H] bf16, or NULL: ungated) gates the shared
+ * expert.  Returns the number of out-of-range ids the alignment skipped. */
 int oracle_moe_layer(const oracle_experts *X, const oracle_experts *S,
+                     const uint16_t *shared_gate_w,
                      const uint16_t *x, int M, int top_k, int BS,
                      const float *logits, const int32_t *ids_in, const double *w_in,
                      double *out_d, uint16_t *out_bf16)
@@ -506,15 +527,19 @@ int oracle_moe_layer(const oracle_experts *X, const oracle_experts *S,
     int bad = oracle_align(ids, n, E, BS, sti, sei, off, ttp, act, &count, &ntpp, NULL);
     double *h = (double *)calloc((size_t)max_total * I + 1, sizeof(double));
     double *y = (double *)calloc((size_t)max_total * H + 1, sizeof(double));
-    double *h_sh = NULL, *y_sh = NULL;
+    double *h_sh = NULL, *y_sh = NULL, *gate = NULL;
     if (S) {
         h_sh = (double *)calloc((size_t)M * S->I, sizeof(double));
         y_sh = (double *)calloc((size_t)M * H, sizeof(double));
+        if (shared_gate_w) {
+            gate = (double *)malloc(sizeof(double) * (size_t)M);
+            oracle_shared_gate(x, shared_gate_w, M, H, gate);
+        }
     }
     oracle_grouped_gate_up(X, S, x, M, top_k, sti, off, act, count, h, h_sh);
     oracle_grouped_down(X, S, h, h_sh, M, top_k, sti, off, act, count, y, y_sh);
-    oracle_blend(y, w, ttp, y_sh, M, top_k, H, out_d, out_bf16);
+    oracle_blend(y, w, ttp, y_sh, gate, M, top_k, H, out_d, out_bf16);
     free(ids32); free(w); free(ids); free(sti); free(sei); free(off); free(ttp);
-    free(act); free(h); free(y); free(h_sh); free(y_sh);
+    free(act); free(h); free(y); free(h_sh); free(y_sh); free(gate);
     return bad;
 }

@@ -18,6 +18,8 @@ Workloads (no dataset or checkpoint exists; these shapes stand in):
                logits skewed by a Zipf(s=1.1) per-expert bias
   * router:    bf16 router weights [E, H] for the layer's hidden-in form
                (x alone, the logits computed on the device)
+  * gate:      a bf16 [H] gate weight for the shared expert (the nvfp4
+               shape's shared expert, gated)
   * align:     ids only, n = 8*M, M in {1, 64, 1024, 4096}, E in
                {64, 256, 1024}, BS in {16, 64, 128}; uniform, Zipf(s=1.2)
                or all one expert
@@ -232,6 +234,16 @@ def make_router_weight(E: int, H: int, seed: int, device="cpu") -> torch.Tensor:
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     w = torch.randn(E, H, generator=gen, device=device, dtype=torch.float32)
+    return (w * H ** -0.5).to(torch.bfloat16)
+
+
+def make_shared_gate(H: int, seed: int, device="cpu") -> torch.Tensor:
+    """bf16 [H] gate weight of the shared expert, normal with standard
+    deviation 1/sqrt(H): with make_x's unit-normal x the gate's argument has
+    unit variance, so the gates spread over about (0.1, 0.9)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    w = torch.randn(H, generator=gen, device=device, dtype=torch.float32)
     return (w * H ** -0.5).to(torch.bfloat16)
 
 

@@ -70,8 +70,10 @@ def torch_route(logits: torch.Tensor, k: int):
     return ids, w / w.sum(dim=-1, keepdim=True)
 
 
-def torch_layer(inp: synth.LayerInputs, ids=None, w=None) -> torch.Tensor:
-    """out[t] = sum_j w[t, j] * FFN_{ids[t, j]}(x[t]) + shared(x[t]), float64."""
+def torch_layer(inp: synth.LayerInputs, ids=None, w=None, gate=None) -> torch.Tensor:
+    """out[t] = sum_j w[t, j] * FFN_{ids[t, j]}(x[t]) + g[t] * shared(x[t]),
+    float64; g[t] = torch.sigmoid(x[t] . gate) for a bf16 gate weight [H],
+    else 1."""
     x = inp.x.cpu().to(torch.float64)
     if ids is None:
         ids, w = torch_route(inp.logits.cpu(), inp.shape.top_k)
@@ -80,7 +82,10 @@ def torch_layer(inp: synth.LayerInputs, ids=None, w=None) -> torch.Tensor:
         for j in range(ids.shape[1]):
             out[t] += float(w[t, j]) * torch_ffn(inp.experts, int(ids[t, j]), x[t: t + 1])[0]
     if inp.shared is not None:
-        out += torch_ffn(inp.shared, 0, x)
+        sh = torch_ffn(inp.shared, 0, x)
+        if gate is not None:
+            sh = torch.sigmoid(x @ gate.cpu().to(torch.float64))[:, None] * sh
+        out += sh
     return out
 
 

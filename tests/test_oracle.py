@@ -434,3 +434,64 @@ def test_blend_skips_bad_slots_and_is_weighted_sum():
     out, _ = oracle.blend(y, w, ttp, y_sh, 2, 2, 3)
     np.testing.assert_array_equal(out[0], 0.25 * y[2] + 0.75 * y[0] + 1)
     np.testing.assert_array_equal(out[1], 0.5 * y[3] + 1)
+
+
+# ---- the shared expert's gate: sigmoid(x . gate_w), on the shared term only ----
+
+def test_shared_gate_special_values_and_symmetry():
+    rng = np.random.default_rng(5)
+    H = 64
+    x = synth.bf16_bits(torch.tensor(rng.standard_normal((3, H)), dtype=torch.bfloat16))
+    zero = np.zeros(H, np.uint16)
+    np.testing.assert_array_equal(oracle.shared_gate(x, zero), [0.5, 0.5, 0.5])
+    ones = synth.bf16_bits(torch.ones(1, H, dtype=torch.bfloat16))
+    g1 = synth.bf16_bits(torch.ones(H, dtype=torch.bfloat16))
+    assert oracle.shared_gate(ones, g1)[0] == 1.0                   # sigmoid(64)
+    assert 0.0 < oracle.shared_gate(ones, g1 | 0x8000)[0] < 1e-27   # sigmoid(-64)
+    g = synth.bf16_bits(torch.tensor(rng.standard_normal(H) / 8, dtype=torch.bfloat16))
+    np.testing.assert_allclose(oracle.shared_gate(x, g) + oracle.shared_gate(x, g ^ 0x8000),
+                               1.0, rtol=0, atol=1e-15)
+
+
+def test_shared_gate_matches_library_sigmoid_of_the_dot():
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(6)
+    M, H = 5, 256
+    xt = torch.tensor(rng.standard_normal((M, H)), dtype=torch.bfloat16)
+    gt = torch.tensor(rng.standard_normal(H) / 16, dtype=torch.bfloat16)
+    z = (xt.to(torch.float64) @ gt.to(torch.float64)).numpy()
+    np.testing.assert_allclose(oracle.shared_gate(synth.bf16_bits(xt), synth.bf16_bits(gt)),
+                               special.expit(z), rtol=1e-14, atol=0)
+
+
+def test_blend_gate_scales_only_the_shared_term():
+    # the worked blend above with gates 0.5 and 0.25 on the shared term
+    y = np.arange(12, dtype=np.float64).reshape(4, 3)
+    w = np.array([[0.25, 0.75], [1.0, 0.5]])
+    ttp = np.array([2, 0, -1, 3], np.int32)
+    y_sh = np.ones((2, 3))
+    out, _ = oracle.blend(y, w, ttp, y_sh, 2, 2, 3, gate=np.array([0.5, 0.25]))
+    np.testing.assert_array_equal(out[0], 0.25 * y[2] + 0.75 * y[0] + 0.5)
+    np.testing.assert_array_equal(out[1], 0.5 * y[3] + 0.25)
+    ungated, _ = oracle.blend(y, w, ttp, y_sh, 2, 2, 3)
+    ones, _ = oracle.blend(y, w, ttp, y_sh, 2, 2, 3, gate=np.ones(2))
+    np.testing.assert_array_equal(ungated, ones)
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_FP8, synth.FMT_NVFP4])
+def test_layer_gated_shared_expert_matches_torch(fmt):
+    inp = _small_inputs(fmt, True, M=5, seed=66)
+    s = inp.shape
+    gate = synth.make_shared_gate(s.H, 67)
+    X = helpers.oracle_experts(inp.experts)
+    S = helpers.oracle_experts(inp.shared)
+    out_d, _, bad = oracle.moe_layer(X, S, synth.bf16_bits(inp.x), s.M, s.top_k, s.BS,
+                                     logits=inp.logits.numpy(),
+                                     shared_gate_bits=synth.bf16_bits(gate))
+    assert bad == 0
+    ref = helpers.torch_layer(inp, gate=gate).numpy()
+    np.testing.assert_allclose(out_d, ref, rtol=1e-10, atol=1e-12)
+    # and the gate matters: the ungated layer differs
+    plain, _, _ = oracle.moe_layer(X, S, synth.bf16_bits(inp.x), s.M, s.top_k, s.BS,
+                                   logits=inp.logits.numpy())
+    assert np.abs(plain - out_d).max() > 1e-3
