@@ -22,7 +22,8 @@ The CPU baseline is the oracle on a bounded sample of the same workload.
 The line also carries `router_logits`: the router matrix-vector product ahead of the
 top-k (bf16 x times bf16 router weights) at the decode and verify widths, timed over
 weight copies that keep it out of L2; and `hidden_in`: the headline decode layer given
-x alone, its logits computed from router weights inside the layer call.
+x alone, its logits computed from router weights inside the layer call; and
+`gated_shared`: the NVFP4 layer with an FP8 shared expert, ungated and gated.
 
 The same line carries `verify_batch`: the M=128 verify batch (H=4096,
 I=1536, E=256, top_k=8, BS=64, router logits with a Zipf(s=1.1) per-expert
@@ -295,6 +296,63 @@ def run_router(moe, stream, peaks: dict) -> list:
                         kernel="router_logits_kernel (k split over 256 threads, fixed-order sums)"))
         del gr, Ws
         torch.cuda.empty_cache()
+    return res
+
+
+def run_gated_shared(moe, stream, M: int, K: int, W: int, peaks: dict) -> dict:
+    """The NVFP4 layer with an FP8 shared expert of inter 512 (M rows, fresh
+    logits every step), its shared term ungated and gated by
+    sigmoid(x . gate_w): K steps in one CUDA graph over 4 weight copies of
+    340 MB."""
+    import synth
+    shape = synth.decode_nvfp4(M)
+    base = synth.make_experts(shape.E, shape.H, shape.I, shape.fmt, SEED + 8, "cuda")
+    sh = synth.make_experts(1, shape.H, shape.shared_I, synth.FMT_FP8, SEED + 9, "cuda")
+    copies = [base] + [_clone_experts(base) for _ in range(3)]
+    gate = synth.make_shared_gate(shape.H, SEED + 10, "cuda")
+    x = synth.make_x(M, shape.H, SEED + 11, "cuda")
+    logits = torch.stack([synth.make_logits(M, shape.E, SEED + 700 + s, "cuda")
+                          for s in range(K)])
+    shared = moe.Experts.from_synth(sh)
+    res = dict(workload=shape.name, M=M, steps=K)
+    for name, g in (("ungated", None), ("gated", gate)):
+        layers = [moe.LayerDesc(top_k=shape.top_k, block_size=shape.BS,
+                                routed=moe.Experts.from_synth(c), shared=shared, shared_gate=g)
+                  for c in copies]
+        ws = moe.alloc_workspace(layers[0], M)
+        out = torch.empty(M, shape.H, dtype=torch.bfloat16, device="cuda")
+        with torch.cuda.stream(stream):
+            for s in range(W):
+                moe.moe_decode_layer(layers[s % 4], x, out, ws, router_logits=logits[s % K])
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for s in range(K):
+                moe.moe_decode_layer(layers[s % 4], x, out, ws, router_logits=logits[s])
+        gr.replay()
+        stream.synchronize()
+        times = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                gr.replay()
+                b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        us = 1e3 * float(np.median(times)) / K
+        res[f"us_per_layer_{name}"] = round(us, 3)
+        res[f"launches_{name}"] = moe.moe_decode_layer_launches(layers[0], M)
+        del gr, layers, ws
+    n_act = active_expert_counts(logits, shape.top_k)
+    nbytes = float(np.mean([layer_bytes(shape, base, a) for a in n_act])) + \
+        sh.bytes_per_expert()
+    res["algorithmic_bytes_per_layer"] = int(nbytes)
+    res["weight_stream_gbs_gated"] = round(nbytes / (res["us_per_layer_gated"] * 1e-6) / 1e9, 1)
+    res["pct_of_measured_hbm_gated"] = round(
+        100 * res["weight_stream_gbs_gated"] / peaks["hbm_gbs"], 1)
+    del copies, base, sh
+    torch.cuda.empty_cache()
     return res
 
 
@@ -572,6 +630,7 @@ def run_gpu(args, rank: int, world: int):
     verify = None if args.no_verify else run_verify(moe, stream, min(K, 16), 3, peaks)
     router = None if args.no_verify else run_router(moe, stream, peaks)
     hidden_in = None if args.no_verify else run_hidden_in(moe, stream, args.m, K, W, args.path)
+    gated = None if args.no_verify else run_gated_shared(moe, stream, 8, min(K, 16), 3, peaks)
     # max over ranks
     ms_t = torch.tensor([results["ms"]], device="cuda")
     if world > 1:
@@ -602,6 +661,7 @@ def run_gpu(args, rank: int, world: int):
         verify_batch=verify,
         router_logits=router,
         hidden_in=hidden_in,
+        gated_shared=gated,
         roofline=dict(bound="hbm",
                       kernel=KERNELS[r["kernel"]][0],
                       achieved=round(dk_achieved, 1),

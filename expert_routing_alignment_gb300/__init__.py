@@ -70,14 +70,14 @@ class _Experts(ctypes.Structure):
 class _LayerDesc(ctypes.Structure):
     _fields_ = [("top_k", ctypes.c_int), ("block_size", ctypes.c_int), ("path", ctypes.c_int),
                 ("routed", _Experts), ("shared", ctypes.POINTER(_Experts)),
-                ("router_weight", ctypes.c_void_p)]
+                ("shared_gate", ctypes.c_void_p), ("router_weight", ctypes.c_void_p)]
 
 
 class _WsView(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "topk_ids", "topk_w", "sorted_token_ids", "sorted_expert_ids", "expert_offsets",
         "token_to_perm", "active_experts", "active_count", "num_tokens_post_padded", "h",
-        "h_shared", "y", "y_shared", "blend_counters", "router_logits", "tc_x_terms", "tc_x_scale",
+        "h_shared", "y", "y_shared", "blend_counters", "router_logits", "shared_gate", "tc_x_terms", "tc_x_scale",
         "tc_h_terms", "tc_h_scale", "tc_done", "total_bytes")] + [
         ("max_total", ctypes.c_int), ("max_blocks", ctypes.c_int), ("cap", ctypes.c_int)]
 
@@ -96,7 +96,7 @@ EXPORTS = {
                                  _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_grouped_down": (_I, [ctypes.POINTER(_Experts), ctypes.POINTER(_Experts), _P, _P, _I, _I,
                               _P, _P, _P, _P, _P, _P, _I, _P]),
-    "moe_blend": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "moe_blend": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "moe_decode_layer_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(_LayerDesc), _I]),
     "moe_decode_layer_workspace_view": (_I, [ctypes.POINTER(_LayerDesc), _I,
                                              ctypes.POINTER(_WsView)]),
@@ -186,12 +186,14 @@ class LayerDesc:
     path: int = PATH_AUTO
     # bf16 [E, H] on the device: lets moe_decode_layer take x alone (hidden in)
     router_weight: Optional[torch.Tensor] = None
+    # bf16 [H] on the device: gates the shared expert, sigmoid(x . shared_gate)
+    shared_gate: Optional[torch.Tensor] = None
     _struct: _LayerDesc = field(init=False, repr=False)
 
     def __post_init__(self):
         sh = ctypes.pointer(self.shared._struct) if self.shared is not None else None
         self._struct = _LayerDesc(self.top_k, self.block_size, self.path, self.routed._struct, sh,
-                                  _ptr(self.router_weight))
+                                  _ptr(self.shared_gate), _ptr(self.router_weight))
 
     @property
     def num_experts(self) -> int:
@@ -294,10 +296,14 @@ def moe_grouped_down(routed: Experts, shared: Optional[Experts], h: torch.Tensor
 
 def moe_blend(y: torch.Tensor, topk_w: torch.Tensor, token_to_perm: torch.Tensor,
               y_shared: Optional[torch.Tensor], out: torch.Tensor, top_k: int,
+              x: Optional[torch.Tensor] = None, shared_gate: Optional[torch.Tensor] = None,
               stream=None) -> None:
+    """shared_gate (bf16 [H]) with x (bf16 [M, H]) gates the shared term by
+    sigmoid(x[t] . shared_gate)."""
     M, H = out.shape
     _check("moe_blend", load().moe_blend(_ptr(y), _ptr(topk_w), _ptr(token_to_perm),
-                                         _ptr(y_shared), _ptr(out), M, top_k, H, _stream(stream)))
+                                         _ptr(y_shared), _ptr(x), _ptr(shared_gate), _ptr(out),
+                                         M, top_k, H, _stream(stream)))
 
 
 def workspace_bytes(layer: LayerDesc, max_M: int) -> int:
@@ -348,6 +354,7 @@ def workspace_view(layer: LayerDesc, M: int, ws: torch.Tensor) -> dict:
         y=sl(v.y, v.max_total * H, torch.float32).view(v.max_total, H),
         y_shared=sl(v.y_shared, M * H, torch.float32).view(M, H),
         router_logits=sl(v.router_logits, M * E, torch.float32).view(M, E),
+        shared_gate=sl(v.shared_gate, M, torch.float32),
         max_total=v.max_total, max_blocks=v.max_blocks, cap=v.cap, **tc)
 
 

@@ -41,8 +41,9 @@
 //  * Grid barriers (a monotonic arrival count in the workspace) separate the
 //    last h write of any CTA from the first h read, and the last y write from
 //    the blend.  Then every CTA blends an equal share of the M x H outputs,
-//    each in slot order j = 0..k-1 plus the shared expert, and writes a share
-//    of the tables.
+//    each in slot order j = 0..k-1 plus the shared expert (times its gate
+//    when gated: CTA t computes token t's gate before the barrier), and
+//    writes a share of the tables.
 // Every result depends only on its own row's data: the K split, the order of
 // every sum and the MMA shapes are fixed by the layer's shapes, never by the
 // batch.  Every wait is bounded; one that gives up sets MOE_ERR_TIMEOUT.
@@ -95,6 +96,8 @@ struct FusedArgs {
   const int32_t *ids_in;
   const float *w_in;
   const uint16_t *x;
+  const uint16_t *gate_w;   // the shared expert's gate weight [H], or NULL (ungated)
+  float *gate_vals;         // [M] the shared expert's gates (workspace)
   int32_t *topk_ids, *sti, *sei, *off, *ttp, *act, *act_count, *ntpp;
   float *topk_w, *h, *h_sh, *y, *y_sh;
   unsigned long long *grid_ctr;   // grid-barrier arrivals (monotonic; zero before first use)
@@ -932,7 +935,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0 && a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
   }
   consume<false, RF, SF>(a, S, A, s, failed);
-  // every y row is written before any CTA blends
+  // the shared expert's gates: token t by warp 0 of CTA t (mod the grid)
+  if (a.gate_w && warp == 0)
+    for (int t = blockIdx.x; t < a.M; t += gridDim.x) {
+      const float g = shared_gate_warp(a.x + (size_t)t * a.H, a.gate_w, a.H);
+      if (lane == 0) a.gate_vals[t] = g;
+    }
+  // every y row (and gate) is written before any CTA blends
   if (!grid_barrier(a.grid_ctr, S.misc + 32)) {
     failed = true;
     if (tid == 0 && a.err) atomicOr(a.err, MOE_ERR_TIMEOUT);
@@ -960,7 +969,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (jj < k && P.pos[tok * k + jj] >= 0) acc = fmaf(P.w[tok * k + jj], yv[i], acc);
         }
       }
-      if (a.has_shared) acc += __ldcg(a.y_sh + (size_t)tok * a.H + cc);
+      if (a.has_shared) {
+        const float ysh = __ldcg(a.y_sh + (size_t)tok * a.H + cc);
+        acc = a.gate_w ? fmaf(__ldcg(a.gate_vals + tok), ysh, acc) : acc + ysh;
+      }
       a.out[(size_t)tok * a.H + cc] = float_to_bf16_rn(acc);
     }
   }
@@ -1207,7 +1219,9 @@ int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float 
   a.ids_in = ids;
   a.w_in = w;
   a.x = x;
+  a.gate_w = L->shared ? L->shared_gate : nullptr;
   char *base = reinterpret_cast<char *>(ws);
+  a.gate_vals = reinterpret_cast<float *>(base + v.shared_gate);
   a.topk_ids = reinterpret_cast<int32_t *>(base + v.topk_ids);
   a.topk_w = reinterpret_cast<float *>(base + v.topk_w);
   a.sti = reinterpret_cast<int32_t *>(base + v.sorted_token_ids);

@@ -17,7 +17,8 @@ int launch_topk(const float *logits, int M, int E, int k, int32_t *ids, float *w
 int launch_router(const uint16_t *x, const uint16_t *W, int M, int H, int E, float *logits,
                   void *stream);
 int launch_blend(const float *y, const float *w, const int32_t *ttp, const float *y_sh,
-                 uint16_t *out, int M, int k, int H, void *stream);
+                 const uint16_t *x, const uint16_t *gate_w, uint16_t *out, int M, int k, int H,
+                 void *stream);
 bool fused_fits(const moe_layer_desc *L, int M, int sms);
 bool tc_fits(const moe_layer_desc *L, int M);
 void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]);
@@ -76,6 +77,7 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
     if (st) return st;
     if (L->shared->hidden != L->routed.hidden) return MOE_EINVAL;
   }
+  if (L->shared_gate && (!L->shared || ((uintptr_t)L->shared_gate & 15))) return MOE_EINVAL;
   const int E = L->routed.num_experts, k = L->top_k;
   if (M < 1 || k < 1 || k > E || L->block_size < 1) return MOE_EINVAL;
   if (M > MOE_MAX_ROWS || k > 32) return MOE_EUNSUPPORTED;
@@ -109,6 +111,7 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   v->y_shared = take((size_t)M * H * 4);
   v->blend_counters = take(8);
   v->router_logits = take((size_t)M * E * 4);
+  v->shared_gate = take((size_t)M * 4);
   v->tc_x_terms = v->tc_x_scale = v->tc_h_terms = v->tc_h_scale = v->tc_done = 0;
   if (tc_allowed(L, M)) {
     size_t b[5];
@@ -235,6 +238,6 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
                       I32(v.expert_offsets), I32(v.sorted_token_ids), I32(v.active_experts),
                       I32(v.active_count), F32(v.y), S ? F32(v.y_shared) : nullptr, stream);
   if (st) return st;
-  return moe::launch_blend(F32(v.y), w, I32(v.token_to_perm), S ? F32(v.y_shared) : nullptr, out,
-                           M, k, H, stream);
+  return moe::launch_blend(F32(v.y), w, I32(v.token_to_perm), S ? F32(v.y_shared) : nullptr, x,
+                           S ? layer->shared_gate : nullptr, out, M, k, H, stream);
 }

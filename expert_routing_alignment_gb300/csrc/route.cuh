@@ -75,4 +75,30 @@ __device__ __forceinline__ void topk_softmax_row(const float *l, int E, int k, i
   }
 }
 
+// The shared expert's gate of one token, by one warp ("fp8_moe_grouped.rs":
+// moe_weighted_sum_blend_fp8_grouped takes the layer input and
+// shared_expert_gate.weight; read as a one-output gate layer):
+// sigmoid(sum_c x[c] * g[c]) over bf16 x [H] and bf16 g [H], H % 8 == 0, both
+// 16-byte aligned.  Lane l sums the 16-byte chunks l, l + 32, ... with fmaf
+// (elements ascending), an xor butterfly ends the sum, so the blend kernel and
+// the fused kernel get the same bits.  Every lane returns the gate.
+__device__ __forceinline__ float shared_gate_warp(const uint16_t *x, const uint16_t *g, int H) {
+  const int lane = threadIdx.x & 31;
+  float z = 0.f;
+#pragma unroll 4
+  for (int c = lane; c < H / 8; c += 32) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(x) + c);
+    const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(g) + c);
+    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, gs[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      z = fmaf(__uint_as_float(xs[i] << 16), __uint_as_float(gs[i] << 16), z);
+      z = fmaf(__uint_as_float(xs[i] & 0xFFFF0000u), __uint_as_float(gs[i] & 0xFFFF0000u), z);
+    }
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
+  return 1.f / (1.f + expf(-z));
+}
+
 }  // namespace moe

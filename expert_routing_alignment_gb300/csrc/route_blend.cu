@@ -164,16 +164,27 @@ __global__ void __launch_bounds__(kRouterThreads)
 //
 // What ("fp8_moe_grouped.rs", moe_weighted_sum_blend_fp8_grouped; the fixed
 // order of "moe_decode_vec.py"'s combine): out[t][c] = bf16_rn(sum_j w[t][j] *
-// y[token_to_perm[t*k+j]][c] + y_sh[t][c]), fp32, j ascending, then the shared
-// term.  How: grid (ceil(H/1024), M), each thread 4 consecutive columns with
-// 16-byte loads; no atomics.
+// y[token_to_perm[t*k+j]][c] + g[t] * y_sh[t][c]), fp32, j ascending, then the
+// shared term; g[t] = sigmoid(x[t] . gate_w) when the shared expert is gated
+// (shared_gate_warp), else the term is added as it is.  How: grid
+// (ceil(H/1024), M), each thread 4 consecutive columns with 16-byte loads; no
+// atomics.  Warp 0 of each block computes its token's gate.
 
 __global__ void __launch_bounds__(256) blend_kernel(const float *y, const float *w,
                                                     const int32_t *ttp, const float *y_sh,
+                                                    const uint16_t *x, const uint16_t *gate_w,
                                                     uint16_t *out, int M, int k, int H) {
+  __shared__ float gate_s;
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.y;
+  if (gate_w) {
+    if (threadIdx.x < 32) {
+      const float g = shared_gate_warp(x + (size_t)t * H, gate_w, H);
+      if (threadIdx.x == 0) gate_s = g;
+    }
+    __syncthreads();
+  }
   const int c = (blockIdx.x * 256 + threadIdx.x) * 4;
   if (c >= H) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -189,10 +200,18 @@ __global__ void __launch_bounds__(256) blend_kernel(const float *y, const float 
   }
   if (y_sh) {
     const float4 v = __ldcg(reinterpret_cast<const float4 *>(y_sh + (size_t)t * H + c));
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
+    if (gate_w) {
+      const float g = gate_s;
+      acc.x = fmaf(g, v.x, acc.x);
+      acc.y = fmaf(g, v.y, acc.y);
+      acc.z = fmaf(g, v.z, acc.z);
+      acc.w = fmaf(g, v.w, acc.w);
+    } else {
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
   }
   const uint32_t lo = (uint32_t)float_to_bf16_rn(acc.x) | ((uint32_t)float_to_bf16_rn(acc.y) << 16);
   const uint32_t hi = (uint32_t)float_to_bf16_rn(acc.z) | ((uint32_t)float_to_bf16_rn(acc.w) << 16);
@@ -212,9 +231,11 @@ int launch_topk(const float *logits, int M, int E, int k, int32_t *ids, float *w
 }
 
 int launch_blend(const float *y, const float *w, const int32_t *ttp, const float *y_sh,
-                 uint16_t *out, int M, int k, int H, void *stream) {
+                 const uint16_t *x, const uint16_t *gate_w, uint16_t *out, int M, int k, int H,
+                 void *stream) {
   const dim3 grid((H / 4 + 255) / 256, M);
-  return launch_pdl(blend_kernel, grid, dim3(256), 0, stream, y, w, ttp, y_sh, out, M, k, H);
+  return launch_pdl(blend_kernel, grid, dim3(256), 0, stream, y, w, ttp, y_sh, x, gate_w, out, M,
+                    k, H);
 }
 
 // Expert rows per block: the most (up to 4, for the fewest re-reads of x; 8
@@ -257,12 +278,16 @@ extern "C" int moe_router_logits(const uint16_t *x, const uint16_t *router_weigh
 }
 
 extern "C" int moe_blend(const float *y, const float *topk_w, const int32_t *token_to_perm,
-                         const float *y_shared, uint16_t *out, int M, int top_k, int hidden,
-                         void *stream) {
+                         const float *y_shared, const uint16_t *x, const uint16_t *shared_gate,
+                         uint16_t *out, int M, int top_k, int hidden, void *stream) {
   if (!y || !topk_w || !token_to_perm || !out || M < 1 || top_k < 1 || hidden < 1)
     return MOE_EINVAL;
+  if (shared_gate && (!y_shared || !x)) return MOE_EINVAL;
   if (hidden % 4 != 0 || ((uintptr_t)y & 15) || ((uintptr_t)out & 7) ||
       (y_shared && ((uintptr_t)y_shared & 15)))
     return MOE_EUNSUPPORTED;
-  return moe::launch_blend(y, topk_w, token_to_perm, y_shared, out, M, top_k, hidden, stream);
+  if (shared_gate && (hidden % 8 != 0 || ((uintptr_t)x & 15) || ((uintptr_t)shared_gate & 15)))
+    return MOE_EUNSUPPORTED;
+  return moe::launch_blend(y, topk_w, token_to_perm, y_shared, x, shared_gate, out, M, top_k,
+                           hidden, stream);
 }

@@ -103,6 +103,10 @@ typedef struct moe_layer_desc {
     int path;                    /* MOE_PATH_* */
     moe_experts routed;
     const moe_experts *shared;   /* host pointer to a descriptor, or NULL */
+    /* The shared expert's gate weight [hidden] bf16 bits on the device,
+     * 16-byte aligned, or NULL (ungated); only with a shared expert.  The
+     * blend scales the shared term by sigmoid(x[t] . shared_gate). */
+    const uint16_t *shared_gate;
     /* Router weights [num_experts][hidden] bf16 bits on the device, 16-byte
      * aligned, or NULL.  With them, a moe_decode_layer call given neither
      * router logits nor top-k ids computes the logits from x itself
@@ -237,14 +241,20 @@ int moe_grouped_down(const moe_experts *routed, const moe_experts *shared,
  * moe_weighted_sum_blend_fp8_grouped; fixed-order combine of
  * "moe_decode_vec.py"):
  *   out[t][c] = bf16_rn( sum_{j=0..top_k-1} topk_w[t][j] *
- *                        y[token_to_perm[t*top_k+j]][c]  + y_shared[t][c] )
- * accumulated in fp32, j ascending, then y_shared; slots with
- * token_to_perm = -1 contribute nothing.  y_shared may be NULL.
- *   out [M][H] bf16 bits.
- * Errors: MOE_EINVAL (NULL, M < 1, top_k < 1, H < 1). */
+ *                        y[token_to_perm[t*top_k+j]][c]  + g[t] * y_shared[t][c] )
+ * accumulated in fp32, j ascending, then the shared term; slots with
+ * token_to_perm = -1 contribute nothing.  y_shared may be NULL.  The blend
+ * takes the layer input and the shared expert's gate weight, as the pages'
+ * blend does: with shared_gate ([H] bf16, 16-byte aligned) the shared term
+ * is gated, g[t] = sigmoid(x[t] . shared_gate) in fp32 (the pages print no
+ * formula: the plain reading of a one-output gate layer, no bias); with
+ * shared_gate NULL it is added as it is (x may then be NULL).
+ *   x [M][H] bf16 bits; out [M][H] bf16 bits.
+ * Errors: MOE_EINVAL (NULL, M < 1, top_k < 1, H < 1, a gate without
+ * y_shared or x), MOE_EUNSUPPORTED (H % 4, misaligned; gated: H % 8). */
 int moe_blend(const float *y, const float *topk_w, const int32_t *token_to_perm,
-              const float *y_shared, uint16_t *out, int M, int top_k,
-              int hidden, void *stream);
+              const float *y_shared, const uint16_t *x, const uint16_t *shared_gate,
+              uint16_t *out, int M, int top_k, int hidden, void *stream);
 
 /* ---- the layer ---------------------------------------------------------- */
 
@@ -260,6 +270,8 @@ typedef struct moe_workspace_view {
     size_t blend_counters;                         /* internal: [1] uint64 grid-barrier count */
     size_t router_logits;                          /* [M][E] float: the logits of a call that
                                                       computed them from x (else unwritten) */
+    size_t shared_gate;                            /* [M] float: the shared expert's gates
+                                                      (fused path, gated layers; else unwritten) */
     /* tensor-core path only (all 0 on the CUDA-core path): the activation
      * terms it multiplies, as E4M3 planes with power-of-two scales --
      * x = (t0 + t1) * x_scale[p] per sorted row [2][max_total][H] u8 and

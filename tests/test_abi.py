@@ -194,3 +194,13 @@ def test_hidden_in_launch_counts_and_logits_region():
         assert v.router_logits % 256 == 0 and v.router_logits > v.blend_counters
         nxt = [o for o in (v.tc_x_terms, v.total_bytes) if o > v.router_logits]
         assert min(nxt) - v.router_logits >= 128 * 256 * 4
+
+
+def test_shared_gate_needs_a_shared_expert():
+    lib = moe.load()
+    gate = torch.zeros(2048, dtype=torch.int16)   # a host address; nothing is launched
+    lay = moe.LayerDesc(top_k=8, block_size=16, routed=_fake_experts(E=128, H=2048, I=768),
+                        shared_gate=gate)
+    v = moe._WsView()
+    assert lib.moe_decode_layer_workspace_view(ctypes.pointer(lay._struct), 8,
+                                               ctypes.byref(v)) == moe.MOE_EINVAL
