@@ -578,6 +578,22 @@ def run_profile_verify(args):
     print(json.dumps(dict(profile_verify=shape.name, steps=args.warmup + args.steps)), flush=True)
 
 
+def run_profile_router(args):
+    """The router logits kernel for ncu: W+K direct calls at the decode width
+    (M=8, H=2048, E=128) and then at the verify width (M=128, H=4096, E=256)."""
+    import synth
+    import expert_routing_alignment_gb300 as moe
+    moe.load()
+    for M, H, E in ((8, 2048, 128), (128, 4096, 256)):
+        x = synth.make_x(M, H, SEED + 12, "cuda")
+        Wr = synth.make_router_weight(E, H, SEED + 13, "cuda")
+        out = torch.empty(M, E, dtype=torch.float32, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            moe.moe_router_logits(x, Wr, out)
+    torch.cuda.synchronize()
+    print(json.dumps(dict(profile_router=True, calls=2 * (args.warmup + args.steps))), flush=True)
+
+
 def run_gpu(args, rank: int, world: int):
     import expert_routing_alignment_gb300 as moe
     moe.load()
@@ -691,6 +707,8 @@ def main():
                     help="skip the M=128 verify-batch measurement")
     ap.add_argument("--profile-verify", action="store_true",
                     help="only run a small case of the verify-batch kernel (for ncu)")
+    ap.add_argument("--profile-router", action="store_true",
+                    help="only run the router logits kernel at two widths (for ncu)")
     ap.add_argument("--path", type=int, default=0,
                     help="MOE_PATH_* of the decode workloads (0 auto: tensor cores for FP8; "
                          "1: the CUDA cores' fused kernel)")
@@ -715,6 +733,8 @@ def main():
             run_reference(args, rank, world)
         elif args.profile_verify:
             run_profile_verify(args)
+        elif args.profile_router:
+            run_profile_router(args)
         else:
             run_gpu(args, rank, world)
     finally:
