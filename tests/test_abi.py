@@ -204,3 +204,34 @@ def test_shared_gate_needs_a_shared_expert():
     v = moe._WsView()
     assert lib.moe_decode_layer_workspace_view(ctypes.pointer(lay._struct), 8,
                                                ctypes.byref(v)) == moe.MOE_EINVAL
+
+
+def test_header_is_plain_c_and_struct_layouts_match_the_binding(tmp_path):
+    """The header compiles as C99, and the binding's ctypes mirrors have the
+    header's sizes and field offsets (a C program prints them)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    structs = {"moe_layer_desc": moe._LayerDesc, "moe_workspace_view": moe._WsView,
+               "moe_experts": moe._Experts, "moe_proj": moe._Proj}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "moe_gb300.h"',
+             "int main(void) {"]
+    for cname, cty in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in cty._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = {tuple(l.split()[:-1]): int(l.split()[-1]) for l in out.splitlines()}
+    for cname, cty in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cty), cname
+        for fname, _ in cty._fields_:
+            assert got[(cname, fname)] == getattr(cty, fname).offset, (cname, fname)
