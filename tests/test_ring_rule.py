@@ -12,7 +12,7 @@ and freed oldest first.  Before placing a range the kernel retires stages:
 The claim the kernel relies on: after this, the new range overlaps no
 in-flight range at all, although only the oldest one was compared.  This is
 the rule restated on the host and checked against every in-flight range over
-random sequences of the stage sizes the kernel uses (a checker of the rule,
+random sequences of the stage sizes the kernel uses (a check of the rule,
 not of the device code)."""
 from __future__ import annotations
 
@@ -70,9 +70,9 @@ def test_no_overlap_over_random_sequences(ring, sizes):
         assert place_all(seq, ring) is None
 
 
-def test_checker_catches_the_rule_without_the_wrap_step():
+def test_overlap_scan_catches_the_rule_without_the_wrap_step():
     """Without retiring the skipped end on a wrap, the oldest-only comparison
-    lets a new range overlap a newer in-flight one; the checker finds it."""
+    lets a new range overlap a newer in-flight one; the overlap scan finds it."""
     def naive(sizes, ring):
         head, tail, rec = 0, 0, {}
         for s, size in enumerate(sizes):
