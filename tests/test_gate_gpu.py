@@ -72,7 +72,8 @@ def _fp8_shared(M):
 
 
 GATED = [(synth.decode_nvfp4(1), 0), (synth.decode_nvfp4(8), 0), (synth.decode_nvfp4(32), 0),
-         (synth.decode_nvfp4(8), 3), (_fp8_shared(8), 0), (_fp8_shared(8), 3)]
+         (synth.decode_nvfp4(8), 3), (synth.decode_nvfp4(32), 3), (_fp8_shared(8), 0),
+         (_fp8_shared(8), 3)]
 
 
 @pytest.mark.parametrize("shape,path", GATED, ids=lambda v: getattr(v, "name", str(v)))

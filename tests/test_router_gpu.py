@@ -29,7 +29,7 @@ def _bits(t: torch.Tensor) -> np.ndarray:
 
 
 SHAPES = [(4, 256, 8), (1, 2048, 128), (8, 2048, 128), (128, 4096, 256), (3, 264, 33),
-          (17, 8192, 64), (200, 1024, 157), (2, 16384, 16)]
+          (17, 8192, 64), (200, 1024, 157), (2, 16384, 16), (1, 8, 1), (5, 16, 3)]
 
 
 @pytest.mark.parametrize("M,H,E", SHAPES, ids=lambda v: str(v))
@@ -85,7 +85,8 @@ def test_router_rejects_unsupported_shapes(moe):
     assert exc.value.status == moe.MOE_EUNSUPPORTED
 
 
-HIDDEN_IN = [(synth.decode_fp8(8), 0), (synth.decode_fp8(8), 1), (synth.decode_fp8(8), 3),
+HIDDEN_IN = [(synth.decode_fp8(1), 0), (synth.decode_fp8(8), 0), (synth.decode_fp8(8), 1),
+             (synth.decode_fp8(8), 3),
              (synth.decode_nvfp4(8), 0), (synth.verify_fp8(128), 0)]
 
 
