@@ -235,3 +235,58 @@ def test_header_is_plain_c_and_struct_layouts_match_the_binding(tmp_path):
         assert got[(cname, "size")] == ctypes.sizeof(cty), cname
         for fname, _ in cty._fields_:
             assert got[(cname, fname)] == getattr(cty, fname).offset, (cname, fname)
+
+
+def test_a_c_program_links_the_library_and_gets_the_bindings_answers(tmp_path):
+    """The library is usable from plain C: a C99 program includes the header,
+    links the shared library and calls the host-only entry points; its
+    answers equal the Python binding's (and the oracle's sizes)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    so = moe.load()._name
+    src = tmp_path / "use.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "moe_gb300.h"
+static unsigned char codes[256] __attribute__((aligned(256)));
+static float scales[64] __attribute__((aligned(256)));
+int main(void) {
+    int mt = 0, mb = 0, cap = 0;
+    if (moe_align_sizes(64, 128, 16, &mt, &mb, &cap) != MOE_OK) return 2;
+    printf("sizes %d %d %d\n", mt, mb, cap);
+    printf("einval %s\n", moe_status_string(MOE_EINVAL));
+    moe_layer_desc L = {0};
+    L.top_k = 8;
+    L.block_size = 16;
+    L.path = MOE_PATH_AUTO;
+    L.routed.fmt = MOE_FMT_FP8_B128;
+    L.routed.num_experts = 128;
+    L.routed.hidden = 2048;
+    L.routed.inter = 768;
+    moe_proj p = {codes, scales, NULL};
+    L.routed.gate = p;
+    L.routed.up = p;
+    L.routed.down = p;
+    printf("ws %zu\n", moe_decode_layer_workspace_bytes(&L, 8));
+    printf("launches %d %d\n", moe_decode_layer_launches(&L, 8, 1),
+           moe_decode_layer_launches(&L, 8, 0));
+    return 0;
+}
+''')
+    exe = tmp_path / "use"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                    str(src), so, "-Wl,-rpath," + os.path.dirname(so), "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = dict(l.split(" ", 1) for l in
+               subprocess.run([str(exe)], check=True, capture_output=True,
+                              text=True).stdout.splitlines())
+    assert tuple(map(int, out["sizes"].split())) == tuple(oracle.align_sizes(64, 128, 16))
+    assert out["einval"] == moe.load().moe_status_string(moe.MOE_EINVAL).decode()
+    layer = moe.LayerDesc(top_k=8, block_size=16, routed=_fake_experts())
+    assert int(out["ws"]) == moe.workspace_bytes(layer, 8)
+    assert out["launches"].split() == [str(moe.moe_decode_layer_launches(layer, 8, 1)),
+                                       str(moe.moe_decode_layer_launches(layer, 8, 0))]
