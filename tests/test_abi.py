@@ -290,3 +290,33 @@ int main(void) {
     assert int(out["ws"]) == moe.workspace_bytes(layer, 8)
     assert out["launches"].split() == [str(moe.moe_decode_layer_launches(layer, 8, 1)),
                                        str(moe.moe_decode_layer_launches(layer, 8, 0))]
+
+
+def test_router_blend_and_noalloc_reject_before_launch():
+    """Host checks of the router, the gated blend and the no-alloc layer:
+    each rejection returns before anything is launched (fake addresses)."""
+    lib = moe.load()
+    f = ctypes.c_void_p(4096)        # 16-byte aligned
+    odd = ctypes.c_void_p(4096 + 8)  # 8-byte aligned only
+    # router: NULL / sizes, hidden % 8, misaligned operands
+    assert lib.moe_router_logits(None, f, 2, 256, 8, f, None) == moe.MOE_EINVAL
+    assert lib.moe_router_logits(f, f, 0, 256, 8, f, None) == moe.MOE_EINVAL
+    assert lib.moe_router_logits(f, f, 2, 100, 8, f, None) == moe.MOE_EUNSUPPORTED
+    assert lib.moe_router_logits(odd, f, 2, 256, 8, f, None) == moe.MOE_EUNSUPPORTED
+    assert lib.moe_router_logits(f, odd, 2, 256, 8, f, None) == moe.MOE_EUNSUPPORTED
+    # blend: a gate needs the shared term and x; gated needs hidden % 8 and alignment
+    assert lib.moe_blend(f, f, f, None, f, f, f, 2, 1, 256, None) == moe.MOE_EINVAL
+    assert lib.moe_blend(f, f, f, f, None, f, f, 2, 1, 256, None) == moe.MOE_EINVAL
+    assert lib.moe_blend(f, f, f, f, f, f, f, 2, 1, 260, None) == moe.MOE_EUNSUPPORTED
+    assert lib.moe_blend(f, f, f, f, f, odd, f, 2, 1, 256, None) == moe.MOE_EUNSUPPORTED
+    # no-alloc layer: a workspace above the fixed array is rejected (verify batch)
+    layer = moe.LayerDesc(top_k=8, block_size=64, routed=_fake_experts(E=256, H=4096, I=1536))
+    assert moe.workspace_bytes(layer, 128) > moe.NOALLOC_SCRATCH_BYTES
+    assert lib.moe_decode_layer_noalloc(ctypes.pointer(layer._struct), f, 128, f, None, None,
+                                        f, None, None) == moe.MOE_EUNSUPPORTED
+    # the layer: hidden in with misaligned router weights
+    bad = moe.LayerDesc(top_k=8, block_size=16, routed=_fake_experts(),
+                        router_weight=_FakeTensor(4096 + 8))
+    ws = ctypes.c_void_p(1 << 20)
+    assert lib.moe_decode_layer(ctypes.pointer(bad._struct), f, 8, None, None, None, f, ws,
+                                moe.workspace_bytes(bad, 8), None, None) == moe.MOE_EINVAL
