@@ -257,13 +257,23 @@ def moe_topk_softmax(logits: torch.Tensor, top_k: int, ids: Optional[torch.Tenso
     return ids, w
 
 
+def _dense(name: str, t: torch.Tensor, dtype: torch.dtype, shape: tuple) -> None:
+    """The C entry points read plain row-major buffers: refuse anything else."""
+    if t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != shape:
+        raise ValueError(f"{name}: want a contiguous {dtype} tensor of shape {shape}, "
+                         f"got {t.dtype} {tuple(t.shape)}")
+
+
 def moe_router_logits(x: torch.Tensor, router_weight: torch.Tensor,
                       logits: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """fp32 logits [M, E] = x [M, H] (bf16) times router_weight [E, H] (bf16) transposed."""
     M, H = x.shape
     E = router_weight.shape[0]
+    _dense("x", x, torch.bfloat16, (M, H))
+    _dense("router_weight", router_weight, torch.bfloat16, (E, H))
     if logits is None:
         logits = torch.empty(M, E, dtype=torch.float32, device=x.device)
+    _dense("logits", logits, torch.float32, (M, E))
     _check("moe_router_logits", load().moe_router_logits(_ptr(x), _ptr(router_weight), M, H, E,
                                                          _ptr(logits), _stream(stream)))
     return logits
@@ -301,6 +311,11 @@ def moe_blend(y: torch.Tensor, topk_w: torch.Tensor, token_to_perm: torch.Tensor
     """shared_gate (bf16 [H]) with x (bf16 [M, H]) gates the shared term by
     sigmoid(x[t] . shared_gate)."""
     M, H = out.shape
+    if shared_gate is not None:
+        if x is None:
+            raise ValueError("shared_gate: x is required to compute the gate")
+        _dense("x", x, torch.bfloat16, (M, H))
+        _dense("shared_gate", shared_gate, torch.bfloat16, (H,))
     _check("moe_blend", load().moe_blend(_ptr(y), _ptr(topk_w), _ptr(token_to_perm),
                                          _ptr(y_shared), _ptr(x), _ptr(shared_gate), _ptr(out),
                                          M, top_k, H, _stream(stream)))

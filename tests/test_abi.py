@@ -320,3 +320,30 @@ def test_router_blend_and_noalloc_reject_before_launch():
     ws = ctypes.c_void_p(1 << 20)
     assert lib.moe_decode_layer(ctypes.pointer(bad._struct), f, 8, None, None, None, f, ws,
                                 moe.workspace_bytes(bad, 8), None, None) == moe.MOE_EINVAL
+
+
+def test_binding_refuses_buffers_the_c_abi_cannot_read():
+    """The Python wrappers refuse wrong dtypes, shapes and strided views before
+    any call into the library."""
+    x = torch.zeros(4, 256, dtype=torch.bfloat16)
+    w = torch.zeros(8, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        moe.moe_router_logits(x.float(), w)
+    with pytest.raises(ValueError):
+        moe.moe_router_logits(x, w[:, :128])
+    with pytest.raises(ValueError):
+        moe.moe_router_logits(torch.zeros(4, 512, dtype=torch.bfloat16)[:, ::2], w)
+    with pytest.raises(ValueError):
+        moe.moe_router_logits(x, w, torch.zeros(4, 8, dtype=torch.float64))
+    y = torch.zeros(8, 256)
+    out = torch.zeros(4, 256, dtype=torch.bfloat16)
+    ttp = torch.zeros(4, dtype=torch.int32)
+    tw = torch.ones(4, 1)
+    with pytest.raises(ValueError):
+        moe.moe_blend(y, tw, ttp, y[:4], out, 1, x=None, shared_gate=torch.zeros(256))
+    with pytest.raises(ValueError):
+        moe.moe_blend(y, tw, ttp, y[:4], out, 1, x=x,
+                      shared_gate=torch.zeros(256, dtype=torch.float32))
+    with pytest.raises(ValueError):
+        moe.moe_blend(y, tw, ttp, y[:4], out, 1, x=x,
+                      shared_gate=torch.zeros(128, dtype=torch.bfloat16))
