@@ -347,3 +347,69 @@ def test_binding_refuses_buffers_the_c_abi_cannot_read():
     with pytest.raises(ValueError):
         moe.moe_blend(y, tw, ttp, y[:4], out, 1, x=x,
                       shared_gate=torch.zeros(128, dtype=torch.bfloat16))
+
+
+def _header_params(fn: str) -> list:
+    """Parameter names of fn's declaration in the header, in order."""
+    text = open(os.path.join(ROOT, "include", "moe_gb300.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    m = re.search(r"\b" + fn + r"\s*\(([^;]*?)\)\s*;", text, flags=re.S)
+    assert m, fn
+    return [re.findall(r"\w+", p)[-1] for p in m.group(1).split(",")]
+
+
+class _Recorder:
+    """Stands in for the library: records each call's arguments."""
+
+    def __init__(self):
+        self.calls = {}
+
+    def __getattr__(self, name):
+        def call(*args):
+            self.calls[name] = args
+            return 0
+        return call
+
+
+def _val(a):
+    return a.value if isinstance(a, ctypes.c_void_p) else a
+
+
+@pytest.mark.parametrize("fn", ["moe_router_logits", "moe_blend", "moe_topk_softmax",
+                                "moe_decode_layer"])
+def test_binding_passes_arguments_in_the_headers_order(monkeypatch, fn):
+    rec = _Recorder()
+    monkeypatch.setattr(moe, "_lib", rec)
+    M, H, E, k = 4, 256, 8, 2
+    x = torch.zeros(M, H, dtype=torch.bfloat16)
+    if fn == "moe_router_logits":
+        W = torch.zeros(E, H, dtype=torch.bfloat16)
+        lg = torch.zeros(M, E)
+        moe.moe_router_logits(x, W, lg, stream=7)
+        want = dict(x=x, router_weight=W, M=M, hidden=H, num_experts=E, logits=lg)
+    elif fn == "moe_blend":
+        y, w, ttp = torch.zeros(16, H), torch.zeros(M, k), torch.zeros(M * k, dtype=torch.int32)
+        ysh, g = torch.zeros(M, H), torch.zeros(H, dtype=torch.bfloat16)
+        out = torch.zeros(M, H, dtype=torch.bfloat16)
+        moe.moe_blend(y, w, ttp, ysh, out, k, x=x, shared_gate=g, stream=7)
+        want = dict(y=y, topk_w=w, token_to_perm=ttp, y_shared=ysh, x=x, shared_gate=g,
+                    out=out, M=M, top_k=k, hidden=H)
+    elif fn == "moe_topk_softmax":
+        lg = torch.zeros(M, E)
+        ids, w = moe.moe_topk_softmax(lg, k, stream=7)
+        want = dict(logits=lg, M=M, num_experts=E, top_k=k, topk_ids=ids, topk_w=w)
+    else:
+        layer = moe.LayerDesc(top_k=k, block_size=16, routed=_fake_experts(E=E, H=H, I=256))
+        out = torch.zeros(M, H, dtype=torch.bfloat16)
+        ws = torch.zeros(1024, dtype=torch.uint8)
+        lg, err = torch.zeros(M, E), torch.zeros(1, dtype=torch.int32)
+        moe.moe_decode_layer(layer, x, out, ws, router_logits=lg, err_word=err, stream=7)
+        want = dict(x=x, M=M, router_logits=lg, topk_ids=None, topk_w=None, out=out,
+                    workspace=ws, workspace_bytes=1024, err_word=err)
+    names = _header_params(fn)
+    got = dict(zip(names, rec.calls[fn]))
+    assert len(rec.calls[fn]) == len(names)
+    assert _val(got["stream"]) == 7
+    for name, v in want.items():
+        exp = v.data_ptr() if isinstance(v, torch.Tensor) else v
+        assert _val(got[name]) == exp, name
