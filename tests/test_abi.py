@@ -376,7 +376,8 @@ def _val(a):
 
 
 @pytest.mark.parametrize("fn", ["moe_router_logits", "moe_blend", "moe_topk_softmax",
-                                "moe_decode_layer"])
+                                "moe_decode_layer", "moe_decode_layer_noalloc", "moe_align",
+                                "moe_grouped_gate_up", "moe_grouped_down"])
 def test_binding_passes_arguments_in_the_headers_order(monkeypatch, fn):
     rec = _Recorder()
     monkeypatch.setattr(moe, "_lib", rec)
@@ -398,7 +399,7 @@ def test_binding_passes_arguments_in_the_headers_order(monkeypatch, fn):
         lg = torch.zeros(M, E)
         ids, w = moe.moe_topk_softmax(lg, k, stream=7)
         want = dict(logits=lg, M=M, num_experts=E, top_k=k, topk_ids=ids, topk_w=w)
-    else:
+    elif fn == "moe_decode_layer":
         layer = moe.LayerDesc(top_k=k, block_size=16, routed=_fake_experts(E=E, H=H, I=256))
         out = torch.zeros(M, H, dtype=torch.bfloat16)
         ws = torch.zeros(1024, dtype=torch.uint8)
@@ -406,6 +407,39 @@ def test_binding_passes_arguments_in_the_headers_order(monkeypatch, fn):
         moe.moe_decode_layer(layer, x, out, ws, router_logits=lg, err_word=err, stream=7)
         want = dict(x=x, M=M, router_logits=lg, topk_ids=None, topk_w=None, out=out,
                     workspace=ws, workspace_bytes=1024, err_word=err)
+    elif fn == "moe_decode_layer_noalloc":
+        layer = moe.LayerDesc(top_k=k, block_size=16, routed=_fake_experts(E=E, H=H, I=256))
+        out = torch.zeros(M, H, dtype=torch.bfloat16)
+        ids, w = torch.zeros(M, k, dtype=torch.int32), torch.zeros(M, k)
+        err = torch.zeros(1, dtype=torch.int32)
+        moe.moe_decode_layer_noalloc(layer, x, out, topk_ids=ids, topk_w=w, err_word=err,
+                                     stream=7)
+        want = dict(x=x, M=M, router_logits=None, topk_ids=ids, topk_w=w, out=out, err_word=err)
+    elif fn == "moe_align":
+        ids = torch.zeros(M * k, dtype=torch.int64)
+        err = torch.zeros(1, dtype=torch.int32)
+        t = moe.moe_align(ids, E, 16, err_word=err, stream=7)
+        want = dict(topk_ids=ids, ids_is_int64=1, n=M * k, num_experts=E, block_size=16,
+                    err_word=err, **{key: t[key] for key in (
+                        "sorted_token_ids", "sorted_expert_ids", "expert_offsets",
+                        "token_to_perm", "active_experts", "active_count",
+                        "num_tokens_post_padded")})
+    else:
+        routed = _fake_experts(E=E, H=H, I=256)
+        mt, _, cap = oracle.align_sizes(M * k, E, 16)
+        i32 = dict(dtype=torch.int32)
+        t = dict(expert_offsets=torch.zeros(E + 1, **i32), sorted_token_ids=torch.zeros(mt, **i32),
+                 active_experts=torch.zeros(cap, **i32), active_count=torch.zeros(1, **i32))
+        tabs = dict(t)
+        h, y = torch.zeros(mt, 256), torch.zeros(mt, H)
+        if fn == "moe_grouped_gate_up":
+            moe.moe_grouped_gate_up(routed, None, x, k, t, h, None, path=moe.PATH_SIMT, stream=7)
+            want = dict(x=x, M=M, top_k=k, h=h, h_shared=None, path=moe.PATH_SIMT, **tabs)
+        else:
+            moe.moe_grouped_down(routed, None, h, None, M, k, t, y, None, path=moe.PATH_SIMT,
+                                 stream=7)
+            want = dict(h=h, h_shared=None, M=M, top_k=k, y=y, y_shared=None,
+                        path=moe.PATH_SIMT, **tabs)
     names = _header_params(fn)
     got = dict(zip(names, rec.calls[fn]))
     assert len(rec.calls[fn]) == len(names)
