@@ -11,13 +11,22 @@ no step finds its weights in the 129 MB L2.
 Timed regions (CUDA events on the launching stream, after W warm-up steps,
 synchronize on both sides):
   * value:    K steps captured in one CUDA graph, replayed once;
-  * roofline: the layer call (the tensor-core kernel after the router and the
-              alignment on the FP8 decode shapes), each call bracketed by events,
-              algorithmic bytes / mean duration; DRAM traffic per launch from
-              the committed ncu summary of the same kernel source, else null;
+  * roofline: the layer's dominant kernel alone (the tensor-core expert kernel
+              on the FP8 decode shapes): K launches of moe_decode_experts in one
+              CUDA graph, each on routing and alignment tables prepared in its
+              own workspace beforehand, so only that kernel runs in the timed
+              region; algorithmic bytes / mean duration per launch; DRAM
+              traffic per launch from the committed ncu summary of the same
+              kernel source, else null;
   * e2e:      K steps through the public API with host buffers: x and logits
               copied in from pinned memory, the output copied back, per step.
-The CPU baseline is the oracle on a bounded sample of the same workload.
+The CPU baseline is the oracle on a bounded sample of the same workload, on one
+host core and on all of them (threads over the rows of the layer calls).
+
+The line also carries `align_grid`: µs per moe_align call over the alignment
+stress grid (n = 8·{1, 64, 1024, 4096}, E in {64, 256, 1024}, BS in {16, 64, 128},
+uniform ids); `nvfp4_decode`: the NVFP4 layer with its FP8 shared expert at
+M in {1, 8, 32} (the fused CUDA-core kernel) and at M=64 (the staged kernels).
 
 The line also carries `router_logits`: the router matrix-vector product ahead of the
 top-k (bf16 x times bf16 router weights) at the decode and verify widths, timed over
@@ -200,6 +209,12 @@ def layer_bytes(shape, base, n_active: int) -> int:
     mt = shape.n + min(shape.n, shape.E) * (shape.BS - 1)
     tables = 4 * (mt + n + shape.E)
     return (n_active * per_expert + shape.M * shape.H * 2 * 2 + shape.M * shape.E * 4 + tables)
+
+
+def expert_kernel_bytes(shape, base, n_active: int) -> int:
+    """Algorithmic bytes of one launch of the expert kernel: the layer's bytes
+    without the router logits (the routing and alignment ran before it)."""
+    return layer_bytes(shape, base, n_active) - shape.M * shape.E * 4
 
 
 def run_verify(moe, stream, K: int, W: int, peaks: dict) -> dict:
@@ -398,6 +413,95 @@ def run_hidden_in(moe, stream, M: int, K: int, W: int, path: int) -> dict:
     return res
 
 
+def _graph_ms(stream, K: int, body) -> float:
+    """Median over 3 replays of a CUDA graph of body(s) for s < K, in ms per
+    step (one untimed replay first)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for s in range(K):
+            body(s)
+    g.replay()
+    stream.synchronize()
+    times = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b) / K)
+    del g
+    return float(np.median(times))
+
+
+def run_nvfp4_decode(moe, stream, K: int, W: int, peaks: dict) -> dict:
+    """The NVFP4 layer with its FP8 shared expert (inter 512) at M in {1, 8, 32}
+    and 64: K graph-replayed steps over 4 weight copies of 340 MB, fresh
+    logits every step, ungated.  M <= 32 runs the fused CUDA-core kernel; M=64
+    the staged CUDA-core kernels (the shapes outside the fused admission)."""
+    import synth
+    shape0 = synth.decode_nvfp4(1)
+    base = synth.make_experts(shape0.E, shape0.H, shape0.I, shape0.fmt, SEED + 8, "cuda")
+    sh = synth.make_experts(1, shape0.H, shape0.shared_I, synth.FMT_FP8, SEED + 9, "cuda")
+    copies = [base] + [_clone_experts(base) for _ in range(3)]
+    shared = moe.Experts.from_synth(sh)
+    layers = [moe.LayerDesc(top_k=shape0.top_k, block_size=shape0.BS,
+                            routed=moe.Experts.from_synth(c), shared=shared) for c in copies]
+    rows = []
+    for M in (1, 8, 32, 64):
+        shape = synth.decode_nvfp4(M)
+        x = synth.make_x(M, shape.H, SEED + 11, "cuda")
+        logits = torch.stack([synth.make_logits(M, shape.E, SEED + 800 + s, "cuda")
+                              for s in range(K)])
+        ws = moe.alloc_workspace(layers[0], M)
+        out = torch.empty(M, shape.H, dtype=torch.bfloat16, device="cuda")
+        with torch.cuda.stream(stream):
+            for s in range(W):
+                moe.moe_decode_layer(layers[s % 4], x, out, ws, router_logits=logits[s % K])
+        stream.synchronize()
+        ms = _graph_ms(stream, K, lambda s: moe.moe_decode_layer(layers[s % 4], x, out, ws,
+                                                                 router_logits=logits[s]))
+        n_act = active_expert_counts(logits, shape.top_k)
+        nbytes = float(np.mean([layer_bytes(shape, base, a) for a in n_act])) + \
+            sh.bytes_per_expert()
+        us = 1e3 * ms
+        gbs = nbytes / (us * 1e-6) / 1e9
+        launches = moe.moe_decode_layer_launches(layers[0], M)
+        rows.append(dict(M=M, us_per_layer=round(us, 3), tokens_per_s=round(M / (us * 1e-6), 1),
+                         weight_stream_gbs=round(gbs, 1),
+                         pct_of_measured_hbm=round(100 * gbs / peaks["hbm_gbs"], 1),
+                         launches_per_layer=launches,
+                         mean_active_experts=round(float(np.mean(n_act)), 2),
+                         algorithmic_bytes_per_layer=int(nbytes)))
+        del ws
+    del copies, layers, base, sh
+    torch.cuda.empty_cache()
+    return dict(workload="decode_h2048_i768_e128_k8_nvfp4_shared512", steps=K, rows=rows)
+
+
+def run_align_grid(moe, stream) -> list:
+    """µs per moe_align call over the alignment stress grid (uniform int64
+    ids): 32 calls in one CUDA graph, rotating over 4 id sets."""
+    import synth
+    res = []
+    for M in (1, 64, 1024, 4096):
+        n = 8 * M
+        for E in (64, 256, 1024):
+            for BS in (16, 64, 128):
+                ids = [torch.from_numpy(synth.align_ids(n, E, "uniform", SEED + 40 + j)).cuda()
+                       for j in range(4)]
+                outs = [moe.alloc_align_outputs(n, E, BS) for _ in range(4)]
+                for j in range(4):
+                    moe.moe_align(ids[j], E, BS, out=outs[j], stream=stream)
+                stream.synchronize()
+                ms = _graph_ms(stream, 32, lambda s: moe.moe_align(ids[s % 4], E, BS,
+                                                                   out=outs[s % 4],
+                                                                   stream=stream))
+                res.append(dict(n=n, E=E, BS=BS, us_per_align=round(1e3 * ms, 3)))
+    return res
+
+
 # --------------------------------------------------------------------------
 # timed regions
 # --------------------------------------------------------------------------
@@ -437,24 +541,41 @@ def time_graph(moe, layers, x, logits, out, ws, K: int, W: int, stream,
     return start.elapsed_time(end)
 
 
-def time_layer_launches(moe, layers, x, logits, out, ws, K: int, W: int, stream) -> float:
-    """Mean duration (ms) of one layer call's kernels, each call bracketed by
-    events on the launching stream: the one cooperative kernel on the fused
-    CUDA-core path; the router, the alignment and the tensor-core kernel on
-    the tensor-core path.  The brackets stop one step from overlapping the
-    next, so this is slower than the graph replay."""
-    pairs = []
+def time_expert_kernel(moe, layers, x, logits, out, K: int, W: int, stream):
+    """Mean duration (ms) of one launch of the layer's expert kernel alone.
+
+    Each of the N_COPIES weight copies gets its own workspace, and one layer
+    call on it (untimed) leaves that step's routing and alignment tables
+    there; then K launches of moe_decode_experts (the expert half of the layer:
+    one kernel on the tensor-core and fused paths) run back to back from one
+    CUDA graph, launch s on copy s % N_COPIES with its tables, and the graph is
+    timed with events on the launching stream."""
+    M = x.shape[0]
+    n = min(N_COPIES, K)
+    wss = [moe.alloc_workspace(layers[c], M) for c in range(n)]
     with torch.cuda.stream(stream):
-        for s in range(W + K):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            moe.moe_decode_layer(layers[s % N_COPIES], x, out, ws, router_logits=logits[s % K])
-            b.record(stream)
-            if s >= W:
-                pairs.append((a, b))
+        for c in range(n):
+            moe.moe_decode_layer(layers[c], x, out, wss[c], router_logits=logits[c % K])
+        for s in range(W):
+            moe.moe_decode_experts(layers[s % n], x, out, wss[s % n])
     stream.synchronize()
-    return float(np.mean([a.elapsed_time(b) for a, b in pairs]))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for s in range(K):
+            moe.moe_decode_experts(layers[s % n], x, out, wss[s % n])
+    g.replay()
+    stream.synchronize()
+    times = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b) / K)
+    del g, wss
+    return float(np.median(times))
 
 
 def time_e2e(moe, shape, layer, x_host, logits_host, out_host, ws, K: int, W: int, stream):
@@ -494,24 +615,59 @@ def oracle_experts(d):
     return oracle.Experts(d.E, d.H, d.I, P(d.gate), P(d.up), P(d.down))
 
 
-def cpu_baseline(shape, base, x, logits, budget_s: float = 15.0) -> dict:
-    """The oracle on the host cores: whole layer calls of the workload at M
-    rows, as many as fit in the time budget (at least one)."""
+def _oracle_rows(X, xb, lg, M: int, top_k: int, BS: int, threads: int, budget_s: float,
+                 max_calls: int):
+    """Whole layer calls of M rows on the oracle, `threads` host threads at a
+    time, for about budget_s seconds (at least one call).  A call's rows go to
+    the threads one row each (a row's output depends only on its own x and
+    logits, so each is the oracle's layer on that row alone); ctypes drops
+    the interpreter lock during the C call, so the threads run in parallel.
+    Returns (calls, seconds)."""
+    import concurrent.futures as cf
     import oracle
+    t0 = time.perf_counter()
+    calls = 0
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        while True:
+            lgc = lg[calls % len(lg)]
+            if threads == 1:
+                oracle.moe_layer(X, None, xb, M, top_k, BS, logits=lgc)
+            else:
+                list(ex.map(lambda r: oracle.moe_layer(X, None, xb[r:r + 1], 1, top_k, BS,
+                                                       logits=lgc[r:r + 1]), range(M)))
+            calls += 1
+            if time.perf_counter() - t0 > budget_s or calls >= max_calls:
+                break
+    return calls, time.perf_counter() - t0
+
+
+def cpu_baseline(shape, base, x, logits, budget_s: float = 8.0) -> dict:
+    """The oracle on the host cores: whole layer calls of the workload at M
+    rows, as many as fit in the time budget, on all host cores (threads over
+    the rows) and on one core."""
     X = oracle_experts(base)
     xb = x.cpu().view(torch.int16).numpy().view(np.uint16)
     lg = logits.cpu().numpy()
-    t0 = time.perf_counter()
-    calls = 0
-    while True:
-        oracle.moe_layer(X, None, xb, shape.M, shape.top_k, shape.BS, logits=lg[calls % len(lg)])
-        calls += 1
-        if time.perf_counter() - t0 > budget_s or calls >= len(lg):
-            break
-    dt = time.perf_counter() - t0
-    return dict(value=shape.M * calls / dt, unit="tokens/s", cores=1, kind="oracle",
-                sample=f"{calls} whole layer calls of {shape.name} ({shape.M} rows each), "
-                       f"single-threaded C oracle in double, {dt:.1f} s")
+    threads = max(1, min(os.cpu_count() or 1, shape.M))
+    calls, dt = _oracle_rows(X, xb, lg, shape.M, shape.top_k, shape.BS, threads, budget_s,
+                             len(lg))
+    calls1, dt1 = _oracle_rows(X, xb, lg, shape.M, shape.top_k, shape.BS, 1, budget_s, len(lg))
+    return dict(value=shape.M * calls / dt, unit="tokens/s", cores=threads, kind="oracle",
+                host_cpus=os.cpu_count(),
+                sample=f"{calls} whole layer calls of {shape.name} ({shape.M} rows each, one "
+                       f"row per thread on {threads} threads), C oracle in double, {dt:.1f} s",
+                single_thread=dict(value=shape.M * calls1 / dt1, unit="tokens/s", cores=1,
+                                   sample=f"{calls1} whole layer calls on one thread, "
+                                          f"{dt1:.1f} s"))
+
+
+def workload_config(shape, world: int) -> dict:
+    """The `config` object of the headline line (both arms carry the same)."""
+    return dict(workload=shape.name, M=shape.M, H=shape.H, I=shape.I, E=shape.E,
+                top_k=shape.top_k, BS=shape.BS, weights="fp8_e4m3 128x128 fp32 block scales",
+                routing="fresh N(0,1) logits every step",
+                l2="inputs larger than L2: steps rotate over 16 weight copies of 604 MB",
+                parallelism=f"replicas x{world}")
 
 
 # --------------------------------------------------------------------------
@@ -519,38 +675,36 @@ def cpu_baseline(shape, base, x, logits, budget_s: float = 15.0) -> dict:
 # --------------------------------------------------------------------------
 
 def run_reference(args, rank: int, world: int):
-    """The oracle as the reference arm: each step is one layer call of the
-    workload on the host cores (a bounded sample: 2 of the M rows)."""
+    """The oracle as the reference arm: each step is one whole layer call of the
+    headline workload (all M rows) on the host cores, one row per thread."""
     if rank != 0:
         return
     import synth
-    import oracle
     M = args.m
     shape = synth.decode_fp8(M)
     base = synth.make_experts(shape.E, shape.H, shape.I, shape.fmt, SEED, "cpu")
     X = oracle_experts(base)
     x = synth.make_x(M, shape.H, SEED + 2, "cpu")
-    rows = 2
-    xb = x[:rows].contiguous().view(torch.int16).numpy().view(np.uint16)
-    for s in range(args.warmup):
-        lg = synth.make_logits(M, shape.E, SEED + 100 + s, "cpu")[:rows].numpy()
-        oracle.moe_layer(X, None, xb, rows, shape.top_k, shape.BS, logits=lg)
-    lgs = [synth.make_logits(M, shape.E, SEED + 100 + s, "cpu")[:rows].numpy()
-           for s in range(args.steps)]
-    t0 = time.perf_counter()
-    for s in range(args.steps):
-        oracle.moe_layer(X, None, xb, rows, shape.top_k, shape.BS, logits=lgs[s])
-    dt = time.perf_counter() - t0
-    value = rows * args.steps / dt
+    xb = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+    threads = max(1, min(os.cpu_count() or 1, M))
+    lg_w = np.stack([synth.make_logits(M, shape.E, SEED + 100 + s, "cpu").numpy()
+                     for s in range(args.warmup)])
+    _oracle_rows(X, xb, lg_w, M, shape.top_k, shape.BS, threads, 0.0, args.warmup)
+    lgs = np.stack([synth.make_logits(M, shape.E, SEED + 100 + s, "cpu").numpy()
+                    for s in range(args.steps)])
+    calls, dt = _oracle_rows(X, xb, lgs, M, shape.top_k, shape.BS, threads, float("inf"),
+                             args.steps)
+    value = M * calls / dt
     line = dict(
         impl="reference", metric=METRIC, value=value, unit="tokens/s", n_gpus=world,
         steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * dt / args.steps,
         higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-        config=dict(workload=shape.name, M=M, H=shape.H, I=shape.I, E=shape.E,
-                    top_k=shape.top_k, BS=shape.BS),
-        cpu_baseline=dict(value=value, unit="tokens/s", cores=1, kind="oracle",
-                          sample=f"each step: the oracle on {rows} of the {M} rows of one "
-                                 f"layer call of {shape.name}"),
+        config=workload_config(shape, world),
+        cpu_baseline=dict(value=value, unit="tokens/s", cores=threads, kind="oracle",
+                          host_cpus=os.cpu_count(),
+                          sample=f"each step: one whole layer call of {shape.name} ({M} rows, "
+                                 f"one row per thread on {threads} threads), C oracle in "
+                                 f"double"),
         e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
 
@@ -625,7 +779,11 @@ def run_gpu(args, rank: int, world: int):
                           pct_of_8tbs=round(100 * gbs / NOMINAL_HBM_GBS, 1),
                           mean_active_experts=round(float(np.mean(n_act)), 2)))
         if head:
-            dk_ms = time_layer_launches(moe, layers, x, logits, out, ws, K, W, stream)
+            dk_ms = time_expert_kernel(moe, layers, x, logits, out, K, W, stream)
+            n_kern = min(N_COPIES, K)
+            kbytes = float(np.mean([expert_kernel_bytes(shape, base, a)
+                                    for a in active_expert_counts(logits[:n_kern],
+                                                                  shape.top_k)]))
             launches = moe.moe_decode_layer_launches(layers[0], M)
             x_host = x.cpu().pin_memory()
             lg_host = logits.cpu().pin_memory()
@@ -633,7 +791,8 @@ def run_gpu(args, rank: int, world: int):
             e2e_ms, h2d, d2h = time_e2e(moe, shape, layers[0], x_host, lg_host, out_host, ws,
                                         K, W, stream)
             results = dict(shape=shape, base=base, x=x, logits=logits, ms=ms, us=us, gbs=gbs,
-                           nbytes=nbytes, dk_ms=dk_ms, launches=launches, e2e_ms=e2e_ms,
+                           nbytes=nbytes, dk_ms=dk_ms, kbytes=kbytes, launches=launches,
+                           e2e_ms=e2e_ms,
                            kernel="fused" if launches == 1 else "tc",
                            h2d=h2d, d2h=d2h, clocks=sampler.summary())
         del copies, layers, base, ws
@@ -647,6 +806,8 @@ def run_gpu(args, rank: int, world: int):
     router = None if args.no_verify else run_router(moe, stream, peaks)
     hidden_in = None if args.no_verify else run_hidden_in(moe, stream, args.m, K, W, args.path)
     gated = None if args.no_verify else run_gated_shared(moe, stream, 8, min(K, 16), 3, peaks)
+    nvfp4 = None if args.no_verify else run_nvfp4_decode(moe, stream, min(K, 16), 3, peaks)
+    align_grid = None if args.no_verify else run_align_grid(moe, stream)
     # max over ranks
     ms_t = torch.tensor([results["ms"]], device="cuda")
     if world > 1:
@@ -657,18 +818,14 @@ def run_gpu(args, rank: int, world: int):
     r = results
     shape = r["shape"]
     value = world * shape.M * K / (ms_max * 1e-3)
-    dk_achieved = r["nbytes"] / (r["dk_ms"] * 1e-3) / 1e9
+    dk_achieved = r["kbytes"] / (r["dk_ms"] * 1e-3) / 1e9
     line = dict(
         metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K, warmup=W,
         ms_per_step=ms_max / K, higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype=("fp8_e4m3 weights, f16 x f16 -> f32 mma" if r["kernel"] == "fused" else
                "fp8_e4m3 weights x e4m3 activation terms -> f32 (tcgen05 kind::f8f6f4)"),
         data="synthetic",
-        config=dict(workload=shape.name, M=shape.M, H=shape.H, I=shape.I, E=shape.E,
-                    top_k=shape.top_k, BS=shape.BS, weights="fp8_e4m3 128x128 fp32 block scales",
-                    routing="fresh N(0,1) logits every step",
-                    l2="inputs larger than L2: steps rotate over 16 weight copies of 604 MB",
-                    parallelism=f"replicas x{world}"),
+        config=workload_config(shape, world),
         us_per_layer=round(r["us"], 3), weight_stream_gbs=round(r["gbs"], 1),
         pct_of_measured_hbm=round(100 * r["gbs"] / peaks["hbm_gbs"], 1),
         pct_of_8tbs=round(100 * r["gbs"] / NOMINAL_HBM_GBS, 1),
@@ -678,12 +835,16 @@ def run_gpu(args, rank: int, world: int):
         router_logits=router,
         hidden_in=hidden_in,
         gated_shared=gated,
+        nvfp4_decode=nvfp4,
+        align_grid=align_grid,
         roofline=dict(bound="hbm",
                       kernel=KERNELS[r["kernel"]][0],
                       achieved=round(dk_achieved, 1),
                       peak=peaks["hbm_gbs"], peak_source=f"{peaks['source']} copy bandwidth",
                       unit="GB/s", frac=round(dk_achieved / peaks["hbm_gbs"], 4),
-                      bytes_per_launch=int(r["nbytes"]), us_per_launch=round(1e3 * r["dk_ms"], 3),
+                      bytes_per_launch=int(r["kbytes"]), us_per_launch=round(1e3 * r["dk_ms"], 3),
+                      timed="the kernel alone: K launches of moe_decode_experts from one CUDA "
+                            "graph on prepared tables, CUDA events on the launching stream",
                       traffic=profiled_traffic(shape.name, r["kernel"])),
         e2e=dict(value=shape.M * K / (r["e2e_ms"] * 1e-3), unit="tokens/s",
                  h2d_bytes_per_step=r["h2d"], d2h_bytes_per_step=r["d2h"]),

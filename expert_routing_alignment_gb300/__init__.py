@@ -105,6 +105,8 @@ EXPORTS = {
     "moe_decode_layer_launches": (_I, [ctypes.POINTER(_LayerDesc), _I, _I]),
     "moe_decode_layer_noalloc": (_I, [ctypes.POINTER(_LayerDesc), _P, _I, _P, _P, _P, _P, _P,
                                       _P]),
+    "moe_decode_experts": (_I, [ctypes.POINTER(_LayerDesc), _P, _I, _P, _P, ctypes.c_size_t, _P,
+                                _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -392,6 +394,19 @@ def moe_decode_layer(layer: LayerDesc, x: torch.Tensor, out: torch.Tensor, works
         ctypes.pointer(layer._struct), _ptr(x), M, _ptr(router_logits), _ptr(topk_ids),
         _ptr(topk_w), _ptr(out), _ptr(workspace), workspace.numel(), _ptr(err_word),
         _stream(stream)))
+
+
+def moe_decode_experts(layer: LayerDesc, x: torch.Tensor, out: torch.Tensor,
+                       workspace: torch.Tensor, err_word: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """The expert half of moe_decode_layer (grouped gate+up, down, blend) on
+    the routing and alignment tables the workspace already holds for these
+    rows (see workspace_view: moe_topk_softmax and moe_align can write them
+    there, or an earlier moe_decode_layer call left them)."""
+    M = x.shape[0]
+    _check("moe_decode_experts", load().moe_decode_experts(
+        ctypes.pointer(layer._struct), _ptr(x), M, _ptr(out), _ptr(workspace),
+        workspace.numel(), _ptr(err_word), _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -30,6 +30,10 @@ int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float 
                  const int32_t *ids, const float *w, uint16_t *out, void *ws,
                  const moe_workspace_view &v, uint32_t *err, void *stream);
 
+int run_experts(const moe_layer_desc *layer, int run, const uint16_t *x, int M,
+                const int32_t *ids, const float *w, uint16_t *out, void *workspace,
+                const moe_workspace_view &v, uint32_t *err_word, void *stream);
+
 // The expert-kernel path of the grouped entry points.  The tensor-core
 // kernels keep their activation terms in the layer workspace, so only
 // moe_decode_layer runs them.
@@ -96,6 +100,15 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
     off = align_up(off + bytes, 256);
     return at;
   };
+  // The counters that persist from call to call come first, at offsets and
+  // sizes that do not depend on M, so that one workspace serves every M up to
+  // the one it was sized for: the grid-barrier count at 0, then the
+  // tensor-core path's counters (sized by the layer alone).
+  v->blend_counters = take(8);
+  const bool tc = tc_allowed(L, M);
+  size_t tcb[5] = {0, 0, 0, 0, 0};
+  if (tc) tc_workspace(L, max_total, cap, tcb);
+  v->tc_done = tc ? take(tcb[4]) : 0;
   v->topk_ids = take((size_t)n * 4);
   v->topk_w = take((size_t)n * 4);
   v->sorted_token_ids = take((size_t)max_total * 4);
@@ -109,18 +122,14 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   v->h_shared = take((size_t)M * Is * 4);
   v->y = take((size_t)max_total * H * 4);
   v->y_shared = take((size_t)M * H * 4);
-  v->blend_counters = take(8);
   v->router_logits = take((size_t)M * E * 4);
   v->shared_gate = take((size_t)M * 4);
-  v->tc_x_terms = v->tc_x_scale = v->tc_h_terms = v->tc_h_scale = v->tc_done = 0;
-  if (tc_allowed(L, M)) {
-    size_t b[5];
-    tc_workspace(L, max_total, cap, b);
-    v->tc_x_terms = take(b[0]);
-    v->tc_x_scale = take(b[1]);
-    v->tc_h_terms = take(b[2]);
-    v->tc_h_scale = take(b[3]);
-    v->tc_done = take(b[4]);
+  v->tc_x_terms = v->tc_x_scale = v->tc_h_terms = v->tc_h_scale = 0;
+  if (tc) {
+    v->tc_x_terms = take(tcb[0]);
+    v->tc_x_scale = take(tcb[1]);
+    v->tc_h_terms = take(tcb[2]);
+    v->tc_h_scale = take(tcb[3]);
   }
   v->total_bytes = off;
   v->max_total = max_total;
@@ -181,28 +190,44 @@ extern "C" int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int
   return (with_logits ? 5 : 4) + router;
 }
 
+namespace moe {
+
+// Every host check of a moe_decode_layer call except those on the workspace:
+// the descriptor and M (through the layout, returned in *v), the inputs, the
+// output, and that a path admits the shape.  MOE_OK or the status to return.
+int check_layer_call(const moe_layer_desc *layer, const uint16_t *x, int M,
+                     const float *router_logits, const int32_t *topk_ids, const float *topk_w,
+                     const uint16_t *out, moe_workspace_view *v) {
+  int st = layout(layer, M, v);
+  if (st) return st;
+  if (!x || !out) return MOE_EINVAL;
+  // hidden in: the logits come from x and the layer's router weights
+  const bool hidden_in = !router_logits && !topk_ids && layer->router_weight;
+  if (!router_logits && !hidden_in && (!topk_ids || !topk_w)) return MOE_EINVAL;
+  if (hidden_in && ((uintptr_t)layer->router_weight & 15)) return MOE_EINVAL;
+  if (((uintptr_t)x & 15) || ((uintptr_t)out & 7)) return MOE_EINVAL;
+  if (layer_run(layer, M) < 0) return MOE_EUNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace moe
+
 extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,
                                 const float *router_logits, const int32_t *topk_ids,
                                 const float *topk_w, uint16_t *out, void *workspace,
                                 size_t workspace_bytes, uint32_t *err_word, void *stream) {
   moe_workspace_view v;
-  int st = moe::layout(layer, M, &v);
+  int st = moe::check_layer_call(layer, x, M, router_logits, topk_ids, topk_w, out, &v);
   if (st) return st;
-  if (!x || !out || !workspace) return MOE_EINVAL;
-  // hidden in: the logits come from x and the layer's router weights
-  const bool hidden_in = !router_logits && !topk_ids && layer->router_weight;
-  if (!router_logits && !hidden_in && (!topk_ids || !topk_w)) return MOE_EINVAL;
-  if (hidden_in && ((uintptr_t)layer->router_weight & 15)) return MOE_EINVAL;
+  if (!workspace) return MOE_EINVAL;
   if (workspace_bytes < v.total_bytes || ((uintptr_t)workspace & 255)) return MOE_EINVAL;
-  if (((uintptr_t)x & 15) || ((uintptr_t)out & 7)) return MOE_EINVAL;
+  const bool hidden_in = !router_logits && !topk_ids && layer->router_weight;
   const int run = moe::layer_run(layer, M);
-  if (run < 0) return MOE_EUNSUPPORTED;
 
   char *ws = reinterpret_cast<char *>(workspace);
   auto I32 = [&](size_t o) { return reinterpret_cast<int32_t *>(ws + o); };
   auto F32 = [&](size_t o) { return reinterpret_cast<float *>(ws + o); };
   const int E = layer->routed.num_experts, k = layer->top_k, H = layer->routed.hidden;
-  const moe_experts *S = layer->shared;
 
   if (hidden_in) {
     st = moe::launch_router(x, layer->router_weight, M, H, E, F32(v.router_logits), stream);
@@ -226,18 +251,55 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
                  I32(v.active_experts), I32(v.active_count), I32(v.num_tokens_post_padded),
                  err_word, stream);
   if (st) return st;
-  if (run == moe::kRunTc)
-    return moe::launch_tc(layer, x, M, ids, w, I32(v.token_to_perm), I32(v.expert_offsets),
-                          I32(v.active_experts), I32(v.active_count), out, workspace, v,
-                          err_word, stream);
-  st = moe::simt_gate_up(&layer->routed, S, x, M, k, I32(v.expert_offsets),
-                         I32(v.sorted_token_ids), I32(v.active_experts), I32(v.active_count),
-                         F32(v.h), S ? F32(v.h_shared) : nullptr, stream);
+  return moe::run_experts(layer, run, x, M, ids, w, out, workspace, v, err_word, stream);
+}
+
+namespace moe {
+
+// The expert half of a layer call, after the routing and the alignment
+// tables are in the workspace: the tensor-core kernel, or the staged
+// gate+up, down and blend.
+int run_experts(const moe_layer_desc *layer, int run, const uint16_t *x, int M,
+                const int32_t *ids, const float *w, uint16_t *out, void *workspace,
+                const moe_workspace_view &v, uint32_t *err_word, void *stream) {
+  char *ws = reinterpret_cast<char *>(workspace);
+  auto I32 = [&](size_t o) { return reinterpret_cast<int32_t *>(ws + o); };
+  auto F32 = [&](size_t o) { return reinterpret_cast<float *>(ws + o); };
+  const int k = layer->top_k, H = layer->routed.hidden;
+  const moe_experts *S = layer->shared;
+  if (run == kRunTc)
+    return launch_tc(layer, x, M, ids, w, I32(v.token_to_perm), I32(v.expert_offsets),
+                     I32(v.active_experts), I32(v.active_count), out, workspace, v, err_word,
+                     stream);
+  int st = simt_gate_up(&layer->routed, S, x, M, k, I32(v.expert_offsets),
+                        I32(v.sorted_token_ids), I32(v.active_experts), I32(v.active_count),
+                        F32(v.h), S ? F32(v.h_shared) : nullptr, stream);
   if (st) return st;
-  st = moe::simt_down(&layer->routed, S, F32(v.h), S ? F32(v.h_shared) : nullptr, M, k,
-                      I32(v.expert_offsets), I32(v.sorted_token_ids), I32(v.active_experts),
-                      I32(v.active_count), F32(v.y), S ? F32(v.y_shared) : nullptr, stream);
+  st = simt_down(&layer->routed, S, F32(v.h), S ? F32(v.h_shared) : nullptr, M, k,
+                 I32(v.expert_offsets), I32(v.sorted_token_ids), I32(v.active_experts),
+                 I32(v.active_count), F32(v.y), S ? F32(v.y_shared) : nullptr, stream);
   if (st) return st;
-  return moe::launch_blend(F32(v.y), w, I32(v.token_to_perm), S ? F32(v.y_shared) : nullptr, x,
-                           S ? layer->shared_gate : nullptr, out, M, k, H, stream);
+  return launch_blend(F32(v.y), w, I32(v.token_to_perm), S ? F32(v.y_shared) : nullptr, x,
+                      S ? layer->shared_gate : nullptr, out, M, k, H, stream);
+}
+
+}  // namespace moe
+
+extern "C" int moe_decode_experts(const moe_layer_desc *layer, const uint16_t *x, int M,
+                                  uint16_t *out, void *workspace, size_t workspace_bytes,
+                                  uint32_t *err_word, void *stream) {
+  moe_workspace_view v;
+  int st = moe::layout(layer, M, &v);
+  if (st) return st;
+  if (!x || !out || !workspace) return MOE_EINVAL;
+  if (((uintptr_t)x & 15) || ((uintptr_t)out & 7)) return MOE_EINVAL;
+  if (workspace_bytes < v.total_bytes || ((uintptr_t)workspace & 255)) return MOE_EINVAL;
+  const int run = moe::layer_run(layer, M);
+  if (run < 0) return MOE_EUNSUPPORTED;
+  char *ws = reinterpret_cast<char *>(workspace);
+  const int32_t *ids = reinterpret_cast<const int32_t *>(ws + v.topk_ids);
+  const float *w = reinterpret_cast<const float *>(ws + v.topk_w);
+  if (run == moe::kRunFused)   // it aligns the given ids again, to the same tables
+    return moe::launch_fused(layer, x, M, nullptr, ids, w, out, workspace, v, err_word, stream);
+  return moe::run_experts(layer, run, x, M, ids, w, out, workspace, v, err_word, stream);
 }

@@ -14,9 +14,17 @@
 // device uses the same array, so calls that overlap on the GPU (on different
 // streams, or from different host threads without ordering) race on it: order
 // them on one stream.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
+
+namespace moe {
+int check_layer_call(const moe_layer_desc *layer, const uint16_t *x, int M,
+                     const float *router_logits, const int32_t *topk_ids, const float *topk_w,
+                     const uint16_t *out, moe_workspace_view *v);
+}
 
 namespace {
 
@@ -25,11 +33,43 @@ static __device__ __align__(256) unsigned char g_layer_scratch[MOE_NOALLOC_SCRAT
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void *g_scratch[kMaxDevices];   // device address of g_layer_scratch, per device
+struct Slot {
+  unsigned long long ctx_id;   // the context the address belongs to (0: none yet)
+  void *addr;                  // device address of g_layer_scratch in it
+};
+Slot g_scratch[kMaxDevices];
 
-// The array's device address on the current device, looked up once per device
-// (the first call on a device does this, so it should come before any stream
-// capture that contains the call).
+// The unique id of the calling thread's current context (0 if it cannot be
+// read): a context created after cudaDeviceReset gets a new id, and the
+// module, with the array, may then sit at a new address.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx &&
+      get_id(ctx, &id) == CUDA_SUCCESS)
+    return id;
+  return 0;
+}
+
+// The array's device address on the current device.  It is looked up with
+// cudaGetSymbolAddress the first time a device (more precisely, a context of
+// it) calls, and cached: that first call should come before any stream
+// capture that contains the entry point.  A call from a new context of the
+// device (after cudaDeviceReset) looks the address up again.
 int scratch_address(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -38,17 +78,22 @@ int scratch_address(void **out) {
     return MOE_ECUDA;
   }
   if (dev < 0 || dev >= kMaxDevices) return MOE_EUNSUPPORTED;
+  // 0 when no context is current yet: the lookup below then makes the
+  // device's primary context current
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch[dev]) {
+  Slot &slot = g_scratch[dev];
+  if (!slot.addr || ctx == 0 || slot.ctx_id != ctx) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_layer_scratch);
     if (e != cudaSuccess || !p) {
       moe::set_last_cuda_error(e);
       return MOE_ECUDA;
     }
-    g_scratch[dev] = p;
+    slot.addr = p;
+    slot.ctx_id = ctx;
   }
-  *out = g_scratch[dev];
+  *out = slot.addr;
   return MOE_OK;
 }
 
@@ -58,21 +103,22 @@ extern "C" int moe_decode_layer_noalloc(const moe_layer_desc *layer, const uint1
                                         const float *router_logits, const int32_t *topk_ids,
                                         const float *topk_w, uint16_t *out, uint32_t *err_word,
                                         void *stream) {
+  // every host check first: a rejected call enqueues nothing
   moe_workspace_view v;
-  int st = moe_decode_layer_workspace_view(layer, M, &v);
+  int st = moe::check_layer_call(layer, x, M, router_logits, topk_ids, topk_w, out, &v);
   if (st) return st;
   if (v.total_bytes > MOE_NOALLOC_SCRATCH_BYTES) return MOE_EUNSUPPORTED;   // too large for it
   void *ws = nullptr;
   st = scratch_address(&ws);
   if (st) return st;
-  // The layer's grid-barrier count and the tensor-core path's item counters
-  // must start the call consistent: clear them (the rest of the workspace is
-  // fully written before it is read).
+  // The layer's grid-barrier count and the tensor-core path's counters must
+  // start the call consistent: clear them (the rest of the workspace is fully
+  // written before it is read).
   cudaError_t e = cudaMemsetAsync(static_cast<char *>(ws) + v.blend_counters, 0, 8,
                                   (cudaStream_t)stream);
   if (e == cudaSuccess && v.tc_done)
-    e = cudaMemsetAsync(static_cast<char *>(ws) + v.tc_done, 0, ((size_t)v.cap + 1) * 4,
-                        (cudaStream_t)stream);
+    e = cudaMemsetAsync(static_cast<char *>(ws) + v.tc_done, 0,
+                        ((size_t)layer->routed.num_experts + 1) * 4, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     moe::set_last_cuda_error(e);
     return MOE_ECUDA;

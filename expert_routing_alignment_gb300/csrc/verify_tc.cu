@@ -1066,8 +1066,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   // every item of every CTA is done: the counters start the next call at zero
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i <= a.cap; i += kThreads) a.done[i] = 0;
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < a.cap; i += kThreads) a.done[i] = 0;
+    if (threadIdx.x == 0) *a.work = 0;
+  }
   const long long T4 = (long long)a.M * a.H / 4;
   const long long o1 = T4 * (blockIdx.x + 1) / gridDim.x;
   for (long long o = T4 * blockIdx.x / gridDim.x + threadIdx.x; o < o1; o += kThreads) {
@@ -1216,7 +1218,10 @@ void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&byte
   bytes[1] = (size_t)max_total * 4;
   bytes[2] = (size_t)kHTerms * max_total * I;
   bytes[3] = (size_t)max_total * (I / 128) * 4;
-  bytes[4] = ((size_t)cap + 1) * 4;
+  // counters: one per active-list index (at most E), then the item counter;
+  // sized by the layer alone so that their place does not move with M
+  (void)cap;
+  bytes[4] = ((size_t)L->routed.num_experts + 1) * 4;
 }
 
 int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *ids,
@@ -1252,7 +1257,7 @@ int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *
   a.h = reinterpret_cast<float *>(base + v.h);
   a.y = reinterpret_cast<float *>(base + v.y);
   a.done = reinterpret_cast<int *>(base + v.tc_done);
-  a.work = a.done + v.cap;
+  a.work = a.done + a.E;
   a.grid_ctr = reinterpret_cast<unsigned long long *>(base + v.blend_counters);
   a.err = err;
   const size_t ring = ring_bytes_for(v.cap);

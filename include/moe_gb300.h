@@ -267,7 +267,8 @@ typedef struct moe_workspace_view {
     size_t active_experts, active_count;           /* [cap], [1] */
     size_t num_tokens_post_padded;                 /* [1] */
     size_t h, h_shared, y, y_shared;               /* float tables */
-    size_t blend_counters;                         /* internal: [1] uint64 grid-barrier count */
+    size_t blend_counters;                         /* internal: [1] uint64 grid-barrier count,
+                                                      always at offset 0 */
     size_t router_logits;                          /* [M][E] float: the logits of a call that
                                                       computed them from x (else unwritten) */
     size_t shared_gate;                            /* [M] float: the shared expert's gates
@@ -277,15 +278,18 @@ typedef struct moe_workspace_view {
      * x = (t0 + t1) * x_scale[p] per sorted row [2][max_total][H] u8 and
      * [max_total] float; h = (t0 + t1 + t2) * h_scale[p][c/128]
      * [3][max_total][I] u8 and [max_total][I/128] float -- and internal
-     * int32 counters ([cap] per active expert, then the item counter), which
-     * every call leaves at zero. */
+     * int32 counters (tc_done: [E] per active-list index, then the item
+     * counter), which every call leaves at zero.  tc_done is always at offset
+     * 256: the counters that persist between calls sit where M does not move
+     * them, so one workspace serves every M up to the one it was sized for. */
     size_t tc_x_terms, tc_x_scale, tc_h_terms, tc_h_scale, tc_done;
     size_t total_bytes;
     int max_total, max_blocks, cap;
 } moe_workspace_view;
 
 /* Host only.  Workspace bytes moe_decode_layer needs for any M <= max_M
- * (the largest layout over 1..max_M; 0 if the descriptor is invalid). */
+ * (the largest layout over 1..max_M; 0 if the descriptor is invalid).  One
+ * workspace of this size serves calls at any M <= max_M, in any order. */
 size_t moe_decode_layer_workspace_bytes(const moe_layer_desc *layer, int max_M);
 
 /* Host only.  The workspace layout for M rows.  Returns MOE_EINVAL /
@@ -338,6 +342,23 @@ int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,
                      const float *router_logits, const int32_t *topk_ids,
                      const float *topk_w, uint16_t *out, void *workspace,
                      size_t workspace_bytes, uint32_t *err_word, void *stream);
+
+/* The expert half of moe_decode_layer ("fp8_moe_grouped.rs": the grouped
+ * gate+up and down launchers and moe_weighted_sum_blend_fp8_grouped, which
+ * run after moe_fp8_grouped_sort): the same grouped gate+up, down and blend,
+ * on routing and alignment tables that the workspace already holds for these
+ * M rows -- topk_ids, topk_w, token_to_perm, expert_offsets, active_experts,
+ * active_count and sorted_token_ids at the offsets of
+ * moe_decode_layer_workspace_view, as moe_topk_softmax and moe_align write
+ * them or as an earlier moe_decode_layer call left them.  The kernels and the
+ * results are those of moe_decode_layer on the same tables: one launch on
+ * the tensor-core path and on the fused CUDA-core path (which aligns the
+ * given ids again, to the same tables), three on the staged path (gate+up,
+ * down, blend).  The workspace rules are moe_decode_layer's.
+ * Errors: MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA (as moe_decode_layer). */
+int moe_decode_experts(const moe_layer_desc *layer, const uint16_t *x, int M,
+                       uint16_t *out, void *workspace, size_t workspace_bytes,
+                       uint32_t *err_word, void *stream);
 
 /* ---- the layer without allocation --------------------------------------- */
 

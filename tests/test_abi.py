@@ -121,14 +121,22 @@ def test_tensor_core_workspace_host_only():
     assert lib.moe_decode_layer_workspace_view(ctypes.pointer(layer._struct), 128,
                                                ctypes.byref(v)) == 0
     mt, _, cap = oracle.align_sizes(1024, 256, 64)
-    offs = [v.blend_counters, v.tc_x_terms, v.tc_x_scale, v.tc_h_terms, v.tc_h_scale, v.tc_done]
+    offs = [v.blend_counters, v.tc_done, v.tc_x_terms, v.tc_x_scale, v.tc_h_terms, v.tc_h_scale]
     assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    # the counters that persist between calls come first: [0, 8) and 256.. (E + 1 ints)
+    assert v.blend_counters == 0 and v.tc_done == 256
+    assert v.topk_ids - v.tc_done >= (256 + 1) * 4
     assert v.tc_x_scale - v.tc_x_terms >= 2 * mt * 4096
     assert v.tc_h_terms - v.tc_x_scale >= mt * 4
     assert v.tc_h_scale - v.tc_h_terms >= 3 * mt * 1536
-    assert v.tc_done - v.tc_h_scale >= mt * 12 * 4
-    assert v.total_bytes - v.tc_done >= cap * 4
+    assert v.total_bytes - v.tc_h_scale >= mt * 12 * 4
     assert moe.workspace_bytes(layer, 128) == v.total_bytes
+    # ... at offsets that do not move with M, so one workspace serves every M
+    for M in (1, 8, 64):
+        w = moe._WsView()
+        assert lib.moe_decode_layer_workspace_view(ctypes.pointer(layer._struct), M,
+                                                   ctypes.byref(w)) == 0
+        assert (w.blend_counters, w.tc_done) == (0, 256)
     # the tensor-core run is 3 launches with router logits, 2 with given ids
     assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 1) == 3
     assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 0) == 2
@@ -377,7 +385,8 @@ def _val(a):
 
 @pytest.mark.parametrize("fn", ["moe_router_logits", "moe_blend", "moe_topk_softmax",
                                 "moe_decode_layer", "moe_decode_layer_noalloc", "moe_align",
-                                "moe_grouped_gate_up", "moe_grouped_down"])
+                                "moe_grouped_gate_up", "moe_grouped_down",
+                                "moe_decode_experts"])
 def test_binding_passes_arguments_in_the_headers_order(monkeypatch, fn):
     rec = _Recorder()
     monkeypatch.setattr(moe, "_lib", rec)
@@ -407,6 +416,13 @@ def test_binding_passes_arguments_in_the_headers_order(monkeypatch, fn):
         moe.moe_decode_layer(layer, x, out, ws, router_logits=lg, err_word=err, stream=7)
         want = dict(x=x, M=M, router_logits=lg, topk_ids=None, topk_w=None, out=out,
                     workspace=ws, workspace_bytes=1024, err_word=err)
+    elif fn == "moe_decode_experts":
+        layer = moe.LayerDesc(top_k=k, block_size=16, routed=_fake_experts(E=E, H=H, I=256))
+        out = torch.zeros(M, H, dtype=torch.bfloat16)
+        ws = torch.zeros(1024, dtype=torch.uint8)
+        err = torch.zeros(1, dtype=torch.int32)
+        moe.moe_decode_experts(layer, x, out, ws, err_word=err, stream=7)
+        want = dict(x=x, M=M, out=out, workspace=ws, workspace_bytes=1024, err_word=err)
     elif fn == "moe_decode_layer_noalloc":
         layer = moe.LayerDesc(top_k=k, block_size=16, routed=_fake_experts(E=E, H=H, I=256))
         out = torch.zeros(M, H, dtype=torch.bfloat16)

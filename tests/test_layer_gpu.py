@@ -269,3 +269,57 @@ def test_fused_and_staged_paths_agree(moe):
         assert torch.equal(vf[key], vs[key]), key
     rl2, mx = H.compare_bf16(out_f, synth.bf16_bits(out_s))
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS
+
+
+@pytest.mark.parametrize("path", [0, 1], ids=["auto", "simt"])
+def test_one_workspace_serves_alternating_rows(moe, path):
+    """A workspace sized for M=8 serves calls at M=8, then M=1, then M=8: each
+    output is the bits of the same call on a fresh zeroed workspace (the
+    counters that persist between calls sit where M does not move them)."""
+    shape8 = synth.decode_fp8(8)
+    ex = synth.make_experts(shape8.E, shape8.H, shape8.I, shape8.fmt, 3100, "cuda")
+    layer = moe.LayerDesc(top_k=shape8.top_k, block_size=shape8.BS,
+                          routed=moe.Experts.from_synth(ex), path=path)
+    shared_ws = moe.alloc_workspace(layer, 8)
+    for call, M in enumerate((8, 1, 8, 1)):
+        x = synth.make_x(M, shape8.H, 3200 + call, "cuda")
+        lg = synth.make_logits(M, shape8.E, 3300 + call, "cuda")
+        fresh = torch.empty(M, shape8.H, dtype=torch.bfloat16, device="cuda")
+        moe.moe_decode_layer(layer, x, fresh, moe.alloc_workspace(layer, M), router_logits=lg)
+        out = torch.full((M, shape8.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        moe.moe_decode_layer(layer, x, out, shared_ws, router_logits=lg, err_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, (call, M)
+        assert torch.equal(out.view(torch.int16), fresh.view(torch.int16)), (call, M)
+
+
+@pytest.mark.parametrize("path", [0, 1, 3], ids=["auto", "simt", "staged"])
+def test_decode_experts_on_tables_in_the_workspace(moe, path):
+    """moe_decode_experts runs the expert half of the layer on the tables the
+    workspace holds: those a moe_decode_layer call left, and those written
+    there by moe_topk_softmax and moe_align; the output is the layer's bits."""
+    shape = synth.decode_fp8(4)
+    inp = synth.make_layer(shape, 5150, device="cuda")
+    out, view, (layer, ws) = H.gpu_layer(moe, inp, path=path)
+    again = torch.full_like(out, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_decode_experts(layer, inp.x, again, ws, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+    # tables written by the stand-alone routing and alignment entry points
+    ws2 = moe.alloc_workspace(layer, shape.M)
+    v2 = moe.workspace_view(layer, shape.M, ws2)
+    moe.moe_topk_softmax(inp.logits, shape.top_k, ids=v2["topk_ids"].view(shape.M, shape.top_k),
+                         w=v2["topk_w"].view(shape.M, shape.top_k))
+    moe.moe_align(v2["topk_ids"], shape.E, shape.BS,
+                  out={key: v2[key] for key in ("sorted_token_ids", "sorted_expert_ids",
+                                                 "expert_offsets", "token_to_perm",
+                                                 "active_experts", "active_count",
+                                                 "num_tokens_post_padded")})
+    third = torch.full_like(out, float("nan"))
+    moe.moe_decode_experts(layer, inp.x, third, ws2, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(third.view(torch.int16), out.view(torch.int16))

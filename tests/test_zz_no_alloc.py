@@ -5,6 +5,10 @@ fixed device budget).  It takes its workspace from the library's fixed device
 array instead of a caller buffer; its output must match moe_decode_layer's on
 the same inputs, call after call.
 
+Both calls run the same kernels on the same inputs, so the output must be
+the same bits, not merely within the layer tolerance: a stale counter or a
+misplaced region of the shared array would show as a few changed values.
+
 This file is collected last on purpose, so that a run stopping at the first
 failure has run every other test before it; it also passes alone in a fresh
 process."""
@@ -50,6 +54,29 @@ def test_noalloc_matches_decode_layer_two_calls_in_a_row(moe, shape):
         assert int(err.item()) == 0, call
         rel, mx = compare_bf16(out, ref_bits)
         assert rel <= LAYER_REL_L2 and mx <= LAYER_MAX_ABS, (call, rel, mx)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), call
+
+
+@pytest.mark.parametrize("path", [0, 1], ids=["auto", "simt"])
+def test_noalloc_alternating_rows_share_the_array(moe, path):
+    # M = 8, then 1, then 8 again through the one shared array: each call's
+    # output is the bits of moe_decode_layer on a fresh workspace
+    outs = {}
+    for M in (8, 1, 8):
+        shape = synth.decode_fp8(M)
+        inp = synth.make_layer(shape, 9000 + M, device="cuda")
+        layer = _layer(moe, inp, path)
+        if M not in outs:
+            ws = moe.alloc_workspace(layer, M)
+            ref = torch.empty(M, shape.H, dtype=torch.bfloat16, device="cuda")
+            moe.moe_decode_layer(layer, inp.x, ref, ws, router_logits=inp.logits)
+            outs[M] = ref
+        out = torch.full((M, shape.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        moe.moe_decode_layer_noalloc(layer, inp.x, out, router_logits=inp.logits, err_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, M
+        assert torch.equal(out.view(torch.int16), outs[M].view(torch.int16)), M
 
 
 def test_noalloc_given_ids_matches_decode_layer(moe):
@@ -66,6 +93,7 @@ def test_noalloc_given_ids_matches_decode_layer(moe):
         torch.cuda.synchronize()
         rel, mx = compare_bf16(out, synth.bf16_bits(ref))
         assert rel <= LAYER_REL_L2 and mx <= LAYER_MAX_ABS
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
 
 
 def test_noalloc_rejects_a_workspace_beyond_its_array(moe):
