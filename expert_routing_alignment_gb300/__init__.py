@@ -79,7 +79,8 @@ class _WsView(ctypes.Structure):
         "token_to_perm", "active_experts", "active_count", "num_tokens_post_padded", "h",
         "h_shared", "y", "y_shared", "blend_counters", "router_logits", "shared_gate", "tc_x_terms", "tc_x_scale",
         "tc_h_terms", "tc_h_scale", "tc_done", "total_bytes")] + [
-        ("max_total", ctypes.c_int), ("max_blocks", ctypes.c_int), ("cap", ctypes.c_int)]
+        ("max_total", ctypes.c_int), ("max_blocks", ctypes.c_int), ("cap", ctypes.c_int),
+        ("tc_items", ctypes.c_size_t), ("tc_part", ctypes.c_size_t)]
 
 
 _P = ctypes.c_void_p
@@ -349,13 +350,17 @@ def workspace_view(layer: LayerDesc, M: int, ws: torch.Tensor) -> dict:
         return ws[off: off + nb].view(dtype)
 
     tc = {}
-    if v.tc_x_terms:   # the tensor-core path's activation terms
-        mt = v.max_total
+    mt = v.max_total
+    if v.tc_h_terms:   # the tensor-core paths' h terms and the active table
         tc = dict(
-            tc_x_terms=sl(v.tc_x_terms, 2 * mt * H, torch.uint8).view(2, mt, H),
-            tc_x_scale=sl(v.tc_x_scale, mt, torch.float32),
             tc_h_terms=sl(v.tc_h_terms, 3 * mt * I, torch.uint8).view(3, mt, I),
-            tc_h_scale=sl(v.tc_h_scale, mt * (I // 128), torch.float32).view(mt, I // 128))
+            tc_h_scale=sl(v.tc_h_scale, mt * (I // 128), torch.float32).view(mt, I // 128),
+            tc_items=sl(v.tc_items, 4 * v.cap, torch.int32).view(v.cap, 4))
+    if v.tc_x_terms:   # the verify-batch kernel's x terms (the decode kernel keeps
+        # them in shared memory)
+        tc.update(
+            tc_x_terms=sl(v.tc_x_terms, 2 * mt * H, torch.uint8).view(2, mt, H),
+            tc_x_scale=sl(v.tc_x_scale, mt, torch.float32))
 
     return dict(
         topk_ids=sl(v.topk_ids, M * k, torch.int32), topk_w=sl(v.topk_w, M * k, torch.float32),

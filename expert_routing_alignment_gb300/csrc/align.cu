@@ -30,6 +30,9 @@ struct AlignArgs {
   int n, E, BS, max_total, max_blocks, cap;
   int32_t *sti, *sei, *off, *ttp, *act, *act_count, *ntpp;
   uint32_t *err;
+  // optional (the layer's tensor-core kernels): per active-list index,
+  // {run offset, expert, slot count, 0}
+  int4 *items;
 };
 
 // Expert id of slot i, or -1 when it lies outside [0, E).
@@ -172,7 +175,10 @@ __global__ void __launch_bounds__(NT) align_kernel(AlignArgs a) {
   // ---- stage-2 outputs: offsets, active list, block map, sentinels ---------
   for (int e = tid; e <= E; e += NT) a.off[e] = offs[e];
   for (int e = tid; e < E; e += NT)
-    if (count[e] > 0) a.act[apos[e]] = e;
+    if (count[e] > 0) {
+      a.act[apos[e]] = e;
+      if (a.items) a.items[apos[e]] = make_int4(offs[e], e, count[e], 0);
+    }
   for (int x = nact + tid; x < a.cap; x += NT) a.act[x] = -1;
   if (tid == 0) {
     *a.act_count = nact;
@@ -252,11 +258,16 @@ extern "C" int moe_align_sizes(int n, int num_experts, int block_size, int *max_
   return MOE_OK;
 }
 
-extern "C" int moe_align(const void *topk_ids, int ids_is_int64, int n, int num_experts,
-                         int block_size, int32_t *sorted_token_ids, int32_t *sorted_expert_ids,
-                         int32_t *expert_offsets, int32_t *token_to_perm,
-                         int32_t *active_experts, int32_t *active_count,
-                         int32_t *num_tokens_post_padded, uint32_t *err_word, void *stream) {
+namespace moe {
+
+// moe_align, plus (when items is not NULL) the active table of the layer's
+// tensor-core kernels: items[a] = {expert_offsets[e], e, count[e], 0} for the
+// a-th active expert e.
+int align_launch(const void *topk_ids, int ids_is_int64, int n, int num_experts, int block_size,
+                 int32_t *sorted_token_ids, int32_t *sorted_expert_ids, int32_t *expert_offsets,
+                 int32_t *token_to_perm, int32_t *active_experts, int32_t *active_count,
+                 int32_t *num_tokens_post_padded, uint32_t *err_word, int4 *items,
+                 void *stream) {
   int max_total, max_blocks, cap;
   int st = moe_align_sizes(n, num_experts, block_size, &max_total, &max_blocks, &cap);
   if (st != MOE_OK) return st;
@@ -265,7 +276,7 @@ extern "C" int moe_align(const void *topk_ids, int ids_is_int64, int n, int num_
   if (n > 0 && (!topk_ids || !sorted_token_ids || !sorted_expert_ids || !token_to_perm ||
                 !active_experts))
     return MOE_EINVAL;
-  moe::AlignArgs a;
+  AlignArgs a;
   a.ids = topk_ids;
   a.is64 = ids_is_int64 ? 1 : 0;
   a.n = n;
@@ -282,9 +293,22 @@ extern "C" int moe_align(const void *topk_ids, int ids_is_int64, int n, int num_
   a.act_count = active_count;
   a.ntpp = num_tokens_post_padded;
   a.err = err_word;
+  a.items = items;
   // One CTA; its width grows with n (a launch tuple fixed per shape class).
-  if (n <= 512) return moe::launch_align<128>(a, stream);
-  if (n <= 4096) return moe::launch_align<256>(a, stream);
-  if (n <= 16384) return moe::launch_align<512>(a, stream);
-  return moe::launch_align<1024>(a, stream);
+  if (n <= 512) return launch_align<128>(a, stream);
+  if (n <= 4096) return launch_align<256>(a, stream);
+  if (n <= 16384) return launch_align<512>(a, stream);
+  return launch_align<1024>(a, stream);
+}
+
+}  // namespace moe
+
+extern "C" int moe_align(const void *topk_ids, int ids_is_int64, int n, int num_experts,
+                         int block_size, int32_t *sorted_token_ids, int32_t *sorted_expert_ids,
+                         int32_t *expert_offsets, int32_t *token_to_perm,
+                         int32_t *active_experts, int32_t *active_count,
+                         int32_t *num_tokens_post_padded, uint32_t *err_word, void *stream) {
+  return moe::align_launch(topk_ids, ids_is_int64, n, num_experts, block_size, sorted_token_ids,
+                           sorted_expert_ids, expert_offsets, token_to_perm, active_experts,
+                           active_count, num_tokens_post_padded, err_word, nullptr, stream);
 }

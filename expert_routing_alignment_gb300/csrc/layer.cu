@@ -22,10 +22,22 @@ int launch_blend(const float *y, const float *w, const int32_t *ttp, const float
 bool fused_fits(const moe_layer_desc *L, int M, int sms);
 bool tc_fits(const moe_layer_desc *L, int M);
 void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]);
-int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *ids,
-              const float *w, const int32_t *ttp, const int32_t *off, const int32_t *act,
-              const int32_t *act_count, uint16_t *out, void *ws, const moe_workspace_view &v,
-              uint32_t *err, void *stream);
+size_t tc_counter_ints(const moe_layer_desc *L);
+int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
+              const int32_t *ttp, const int32_t *act_count, uint16_t *out, void *ws,
+              const moe_workspace_view &v, uint32_t *err, void *stream);
+bool dec_fits(const moe_layer_desc *L, int M);
+size_t dec_counter_ints(const moe_layer_desc *L);
+void dec_workspace(const moe_layer_desc *L, int M, int max_total, int cap, size_t (&bytes)[4]);
+int launch_dec(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
+               const int32_t *ttp, const int32_t *sti, const int32_t *act_count,
+               uint16_t *out, void *ws, const moe_workspace_view &v, uint32_t *err,
+               void *stream);
+int align_launch(const void *topk_ids, int ids_is_int64, int n, int num_experts, int block_size,
+                 int32_t *sorted_token_ids, int32_t *sorted_expert_ids, int32_t *expert_offsets,
+                 int32_t *token_to_perm, int32_t *active_experts, int32_t *active_count,
+                 int32_t *num_tokens_post_padded, uint32_t *err_word, int4 *items,
+                 void *stream);
 int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float *logits,
                  const int32_t *ids, const float *w, uint16_t *out, void *ws,
                  const moe_workspace_view &v, uint32_t *err, void *stream);
@@ -47,27 +59,35 @@ static int resolve_path(const moe_experts *routed, int M, int top_k, int path) {
 }
 
 // How moe_decode_layer runs a shape class: the fused CUDA-core kernel, the
-// tensor-core kernel, or the staged CUDA-core kernels.  It depends on the
+// tensor-core kernel of the verify batches, the tensor-core kernel of decode
+// batches (M <= 16), or the staged CUDA-core kernels.  It depends on the
 // shapes only, never on the routing, so a captured graph stays valid for
 // every routing.
-enum { kRunFused = 0, kRunTc = 1, kRunStaged = 2 };
-
-static bool tc_allowed(const moe_layer_desc *L, int M) {
-  return (L->path == MOE_PATH_AUTO || L->path == MOE_PATH_TC) && tc_fits(L, M);
-}
+enum { kRunFused = 0, kRunTc = 1, kRunStaged = 2, kRunTcDec = 3 };
 
 static int layer_run(const moe_layer_desc *L, int M) {
   switch (L->path) {
     case MOE_PATH_TC:
+      if (dec_fits(L, M)) return kRunTcDec;
       return tc_fits(L, M) ? kRunTc : -1;
     case MOE_PATH_SIMT_STAGED:
       return kRunStaged;
     case MOE_PATH_SIMT:
       return fused_fits(L, M, sm_count()) ? kRunFused : kRunStaged;
     default:   // the tensor cores for every FP8 shape they admit, else CUDA cores
+      if (dec_fits(L, M)) return kRunTcDec;
       if (tc_fits(L, M)) return kRunTc;
       return fused_fits(L, M, sm_count()) ? kRunFused : kRunStaged;
   }
+}
+
+static bool is_tc(int run) { return run == kRunTc || run == kRunTcDec; }
+
+// Bytes of the tensor-core kernels' counters (both kernels share the region;
+// each call leaves it at zero): sized by the layer alone.
+size_t tc_counter_bytes(const moe_layer_desc *L) {
+  const size_t a = tc_counter_ints(L), b = dec_counter_ints(L);
+  return 4 * (a > b ? a : b);
 }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -85,9 +105,6 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   const int E = L->routed.num_experts, k = L->top_k;
   if (M < 1 || k < 1 || k > E || L->block_size < 1) return MOE_EINVAL;
   if (M > MOE_MAX_ROWS || k > 32) return MOE_EUNSUPPORTED;
-  if (L->path != MOE_PATH_AUTO && L->path != MOE_PATH_SIMT && L->path != MOE_PATH_TC &&
-      L->path != MOE_PATH_SIMT_STAGED)
-    return MOE_EINVAL;
   const int n = M * k;
   int max_total, max_blocks, cap;
   st = moe_align_sizes(n, E, L->block_size, &max_total, &max_blocks, &cap);
@@ -105,10 +122,12 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   // the one it was sized for: the grid-barrier count at 0, then the
   // tensor-core path's counters (sized by the layer alone).
   v->blend_counters = take(8);
-  const bool tc = tc_allowed(L, M);
-  size_t tcb[5] = {0, 0, 0, 0, 0};
-  if (tc) tc_workspace(L, max_total, cap, tcb);
-  v->tc_done = tc ? take(tcb[4]) : 0;
+  if (L->path != MOE_PATH_AUTO && L->path != MOE_PATH_SIMT && L->path != MOE_PATH_TC &&
+      L->path != MOE_PATH_SIMT_STAGED)
+    return MOE_EINVAL;
+  const int run = layer_run(L, M);
+  const bool tc = is_tc(run);
+  v->tc_done = tc ? take(tc_counter_bytes(L)) : 0;
   v->topk_ids = take((size_t)n * 4);
   v->topk_w = take((size_t)n * 4);
   v->sorted_token_ids = take((size_t)max_total * 4);
@@ -125,11 +144,22 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   v->router_logits = take((size_t)M * E * 4);
   v->shared_gate = take((size_t)M * 4);
   v->tc_x_terms = v->tc_x_scale = v->tc_h_terms = v->tc_h_scale = 0;
-  if (tc) {
-    v->tc_x_terms = take(tcb[0]);
-    v->tc_x_scale = take(tcb[1]);
-    v->tc_h_terms = take(tcb[2]);
-    v->tc_h_scale = take(tcb[3]);
+  v->tc_items = v->tc_part = 0;
+  if (run == kRunTc) {
+    size_t b[5];
+    tc_workspace(L, max_total, cap, b);
+    v->tc_x_terms = take(b[0]);
+    v->tc_x_scale = take(b[1]);
+    v->tc_h_terms = take(b[2]);
+    v->tc_h_scale = take(b[3]);
+    v->tc_items = take(b[4]);
+  } else if (run == kRunTcDec) {
+    size_t b[4];
+    dec_workspace(L, M, max_total, cap, b);
+    v->tc_h_terms = take(b[0]);
+    v->tc_h_scale = take(b[1]);
+    v->tc_items = take(b[2]);
+    v->tc_part = b[3] ? take(b[3]) : 0;
   }
   v->total_bytes = off;
   v->max_total = max_total;
@@ -186,7 +216,7 @@ extern "C" int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int
   if (with_logits == 2 && !layer->router_weight) return -1;
   const int router = with_logits == 2;   // the logits kernel ahead of the route
   if (run == moe::kRunFused) return 1 + router;
-  if (run == moe::kRunTc) return (with_logits ? 3 : 2) + router;
+  if (moe::is_tc(run)) return (with_logits ? 3 : 2) + router;
   return (with_logits ? 5 : 4) + router;
 }
 
@@ -246,10 +276,14 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
     ids = I32(v.topk_ids);
     w = F32(v.topk_w);
   }
-  st = moe_align(ids, 0, M * k, E, layer->block_size, I32(v.sorted_token_ids),
-                 I32(v.sorted_expert_ids), I32(v.expert_offsets), I32(v.token_to_perm),
-                 I32(v.active_experts), I32(v.active_count), I32(v.num_tokens_post_padded),
-                 err_word, stream);
+  // the tensor-core kernels also take the active table (offset, expert and
+  // slot count of each active expert) from the alignment launch
+  st = moe::align_launch(ids, 0, M * k, E, layer->block_size, I32(v.sorted_token_ids),
+                         I32(v.sorted_expert_ids), I32(v.expert_offsets), I32(v.token_to_perm),
+                         I32(v.active_experts), I32(v.active_count),
+                         I32(v.num_tokens_post_padded), err_word,
+                         moe::is_tc(run) ? reinterpret_cast<int4 *>(ws + v.tc_items) : nullptr,
+                         stream);
   if (st) return st;
   return moe::run_experts(layer, run, x, M, ids, w, out, workspace, v, err_word, stream);
 }
@@ -267,10 +301,13 @@ int run_experts(const moe_layer_desc *layer, int run, const uint16_t *x, int M,
   auto F32 = [&](size_t o) { return reinterpret_cast<float *>(ws + o); };
   const int k = layer->top_k, H = layer->routed.hidden;
   const moe_experts *S = layer->shared;
+  (void)ids;
   if (run == kRunTc)
-    return launch_tc(layer, x, M, ids, w, I32(v.token_to_perm), I32(v.expert_offsets),
-                     I32(v.active_experts), I32(v.active_count), out, workspace, v, err_word,
-                     stream);
+    return launch_tc(layer, x, M, w, I32(v.token_to_perm), I32(v.active_count), out, workspace,
+                     v, err_word, stream);
+  if (run == kRunTcDec)
+    return launch_dec(layer, x, M, w, I32(v.token_to_perm), I32(v.sorted_token_ids),
+                      I32(v.active_count), out, workspace, v, err_word, stream);
   int st = simt_gate_up(&layer->routed, S, x, M, k, I32(v.expert_offsets),
                         I32(v.sorted_token_ids), I32(v.active_experts), I32(v.active_count),
                         F32(v.h), S ? F32(v.h_shared) : nullptr, stream);

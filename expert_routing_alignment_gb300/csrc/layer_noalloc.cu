@@ -24,6 +24,7 @@ namespace moe {
 int check_layer_call(const moe_layer_desc *layer, const uint16_t *x, int M,
                      const float *router_logits, const int32_t *topk_ids, const float *topk_w,
                      const uint16_t *out, moe_workspace_view *v);
+size_t tc_counter_bytes(const moe_layer_desc *L);
 }
 
 namespace {
@@ -117,8 +118,8 @@ extern "C" int moe_decode_layer_noalloc(const moe_layer_desc *layer, const uint1
   cudaError_t e = cudaMemsetAsync(static_cast<char *>(ws) + v.blend_counters, 0, 8,
                                   (cudaStream_t)stream);
   if (e == cudaSuccess && v.tc_done)
-    e = cudaMemsetAsync(static_cast<char *>(ws) + v.tc_done, 0,
-                        ((size_t)layer->routed.num_experts + 1) * 4, (cudaStream_t)stream);
+    e = cudaMemsetAsync(static_cast<char *>(ws) + v.tc_done, 0, moe::tc_counter_bytes(layer),
+                        (cudaStream_t)stream);
   if (e != cudaSuccess) {
     moe::set_last_cuda_error(e);
     return MOE_ECUDA;

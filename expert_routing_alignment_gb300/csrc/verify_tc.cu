@@ -34,16 +34,15 @@
 //    published its h terms through a per-expert counter.
 //  * Every wait gives up after about two seconds with MOE_ERR_TIMEOUT; the
 //    CTA then stops issuing, drains its copies and MMAs and frees its TMEM.
-#include <cudaTypedefs.h>
-
 #include <mutex>
 #include <unordered_map>
 
-#include "async.cuh"
-#include "common.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 constexpr int kEpiWarps = 16;
 constexpr int kWarps = 2 + kEpiWarps;
@@ -54,19 +53,17 @@ constexpr int kAccs = 16;                      // k-block accumulator barriers (
 constexpr int kTfree = 16;                     // per-stage TMEM release barriers
 constexpr int kIQ = 32;                        // item queue (copy thread -> MMA, promotion)
 constexpr int kRowTile = 64;                   // token rows per item (MMA N <= 64)
-constexpr int kTileBytes = 128 * 128;          // one 128-row x 128-byte weight box
 constexpr int kXTerms = 2, kHTerms = 3;
 constexpr int kMaxKB = 64;                     // k blocks of 128 (H <= 8192)
 constexpr int kMaxKBd = 32;                    // down k blocks (I <= 4096)
 constexpr uint32_t kTmemCols = 512;            // the circular accumulator range
-constexpr uint64_t kWaitNs = 2000000000ull;    // a wait gives up after ~2 s
 
 struct TcArgs {
   int M, k, n, E, H, I, cap, max_total;
   const uint16_t *x;
-  const int32_t *ids;                        // [n] expert of each slot
   const float *w;                            // [n] routing weight of each slot
-  const int32_t *ttp, *off, *act, *act_count;   // the alignment's tables
+  const int32_t *ttp, *act_count;            // the alignment's tables
+  const int4 *items;                         // [cap] {offset, expert, slot count, 0}
   uint16_t *out;                             // [M][H] bf16
   const float *sg, *su, *sd;                 // block scales [E][R/128][K/128]
   uint8_t *xq;                               // x terms [2][max_total][H] E4M3
@@ -150,12 +147,6 @@ __device__ Smem carve(uint8_t *base, const TcArgs &a) {
 // small device helpers
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ uint64_t gtime() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 __device__ __forceinline__ void fail(const Smem &S, const TcArgs &a) {
   if (!S.misc[0]) {
     S.misc[0] = 1;
@@ -163,155 +154,16 @@ __device__ __forceinline__ void fail(const Smem &S, const TcArgs &a) {
   }
 }
 
-// One potentially blocking test of an mbarrier phase: the hardware may park
-// the thread until the phase completes or a short time limit passes, so
-// waiting warps leave the issue slots to the MMA and copy threads.
-__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for the phase of `parity` of an mbarrier; false when the CTA has
-// failed meanwhile or after about two seconds.
+// Bounded waits that also give up once another role of the CTA failed.
 __device__ __forceinline__ bool wait_bar(const Smem &S, uint64_t *bar, uint32_t parity) {
-  if (mbar_poll(bar, parity)) return true;
-  const uint64_t t0 = gtime();
-  for (uint32_t i = 1; i < (1u << 28); ++i) {
-    if (mbar_try(bar, parity)) return true;
-    if ((i & 15) == 0 && (S.misc[0] || gtime() - t0 > kWaitNs)) return false;
-  }
-  return false;
+  return wait_phase(S.misc, bar, parity);
 }
-
-__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t n) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(n)
-               : "memory");
-}
-
-__device__ __forceinline__ int ld_acquire(const int *p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Wait until *p >= target (written by other CTAs with release); bounded.
-__device__ bool wait_count(const Smem &S, const int *p, int target) {
-  const uint64_t t0 = gtime();
-  for (uint32_t i = 0; i < (1u << 26); ++i) {
-    if (ld_acquire(p) >= target) return true;
-    if (S.misc[0] || gtime() - t0 > kWaitNs) return false;
-    __nanosleep(64);
-  }
-  return false;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
+__device__ __forceinline__ bool wait_count(const Smem &S, const int *p, int target) {
+  return wait_at_least(S.misc, p, target);
 }
 
 __device__ __forceinline__ void group_sync(int g) {
   asm volatile("bar.sync %0, 128;" ::"r"(2 + g) : "memory");
-}
-
-__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
-
-// Power-of-two exponent s such that amax * 2^s lies in [128, 256) (0 for a
-// zero maximum), kept where 2^s and 2^-s are normal floats.
-__device__ __forceinline__ int term_shift(uint32_t amax_bits) {
-  if (amax_bits == 0) return 0;
-  const int e = (int)(amax_bits >> 23) - 127;
-  const int s = 7 - e;
-  return s < -126 ? -126 : (s > 126 ? 126 : s);
-}
-
-// Two floats -> two E4M3 bytes (first in the low byte), nearest-even,
-// saturating at 448.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// ---------------------------------------------------------------------------
-// tcgen05
-// ---------------------------------------------------------------------------
-
-// Shared-memory matrix descriptor of a K-major operand tile written with the
-// 128-byte swizzle (rows of 128 bytes, groups of 8 rows 1024 bytes apart).
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
-  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor: E4M3 x E4M3 -> f32, both K-major, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_e4m3(int n) {
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_e4m3(uint32_t d, uint64_t ad, uint64_t bd, uint32_t id,
-                                         uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(ad), "l"(bd), "r"(id), "r"(acc));
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// ---------------------------------------------------------------------------
-// tensor copies
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ void tma_3d_hint(void *dst, const CUtensorMap *map, int x, int y,
-                                            int z, uint64_t *bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
-      "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
-                                       uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
-      : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -370,15 +222,6 @@ __device__ __forceinline__ uint32_t acc_cols(const Item &it) {
   return 2u * (uint32_t)(it.gu ? kXTerms : kHTerms) * (16u << it.box);
 }
 
-// Placement of the next range of `len` units in a ring of `cap` units: at
-// the head, or at 0 when it does not fit before the end.  Ranges depend only
-// on the sequence of lengths, so every role computes the same positions.
-__device__ __forceinline__ uint32_t ring_place(uint32_t &head, uint32_t len, uint32_t cap) {
-  const uint32_t pos = head + len <= cap ? head : 0u;
-  head = pos + len;
-  return pos;
-}
-
 // Bytes of one stage of an item: kps k blocks of the two weight tiles and of
 // the item's activation terms.
 __device__ __forceinline__ uint32_t stage_bytes(const Item &it) {
@@ -398,7 +241,7 @@ __device__ __forceinline__ uint32_t stage_bytes(const Item &it) {
 // lose bits of at most 2^-18 of that maximum).  One warp per slot, its
 // row's loads in flight together (16 per lane for H = 4096).
 __device__ void prep_x(const TcArgs &a) {
-  const int ew = (threadIdx.x >> 5) - 2, lane = threadIdx.x & 31, et = threadIdx.x - 64;
+  const int ew = (threadIdx.x >> 5) - 2, lane = threadIdx.x & 31;
   const int nw = gridDim.x * kEpiWarps;
   const size_t plane = (size_t)a.max_total * a.H;
   for (int i = blockIdx.x * kEpiWarps + ew; i < a.n; i += nw) {
@@ -506,27 +349,15 @@ __device__ bool grid_barrier(const Smem &S, unsigned long long *ctr) {
 }
 
 // The active list as row tiles: info[a] = {run offset, expert | rows << 16},
-// rtp = exclusive prefix of ceil(rows / 64).  An expert's rows are its slot
-// count, taken here from the ids (a shared-memory histogram in the ring,
-// which is not in use yet).  Returns the active count.
+// rtp = exclusive prefix of ceil(rows / 64).  The alignment launch wrote the
+// active table (offset, expert and slot count of each active expert), so
+// this is one coalesced load and a scan.  Returns the active count.
 __device__ int build_table(const TcArgs &a, const Smem &S) {
-  int *cnt = reinterpret_cast<int *>(S.ring);
-  for (int e = threadIdx.x; e < a.E; e += kThreads) cnt[e] = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < a.n; i += kThreads) {
-    const int e = __ldcg(a.ids + i);
-    if (e >= 0 && e < a.E) atomicAdd(&cnt[e], 1);
-  }
-  __syncthreads();
   const int A = min(max(__ldcg(a.act_count), 0), a.cap);
   for (int i = threadIdx.x; i < A; i += kThreads) {
-    const int e = __ldcg(a.act + i);
-    int o = 0, rows = 0;
-    if (e >= 0 && e < a.E) {
-      o = __ldcg(a.off + e);
-      rows = min(cnt[e], 0x7FFF);
-    }
-    S.info[i] = make_int2(o, (e & 0xFFFF) | (rows << 16));
+    const int4 inf = __ldcg(a.items + i);
+    const int rows = min(inf.z, 0x7FFF);
+    S.info[i] = make_int2(inf.x, (inf.y & 0xFFFF) | (rows << 16));
     S.rtp[i] = (rows + kRowTile - 1) / kRowTile;   // counts; scanned below
   }
   __syncthreads();
@@ -1097,34 +928,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host
 // ---------------------------------------------------------------------------
 
-// cuTensorMapEncodeTiled, from the driver through the runtime (no -lcuda).
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// A tiled u8 map with the 128-byte swizzle (the operand layout of the MMAs).
-int encode(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
-           const cuuint64_t *strides, const cuuint32_t *box) {
-  auto fn = encode_fn();
-  if (!fn) return MOE_ECUDA;
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void *>(ptr), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MOE_OK : MOE_EUNSUPPORTED;
-}
-
 // Maps of one call, cached by (weights, workspace, shape): encoding is host
 // work that would otherwise repeat on every call.
 int tc_maps(const moe_experts *X, uint8_t *xq, uint8_t *hq, int max_total, TcMaps *out) {
@@ -1162,7 +965,7 @@ int tc_maps(const moe_experts *X, uint8_t *xq, uint8_t *hq, int max_total, TcMap
     const cuuint64_t str[2] = {(cuuint64_t)K, 128};
     for (int nb = 1; nb <= 2; ++nb) {
       const cuuint32_t box[3] = {128, 128, (cuuint32_t)nb};
-      const int st = encode(&m.w[j][nb - 1], codes[j], 3, dims, str, box);
+      const int st = encode_u8_sw128(&m.w[j][nb - 1], codes[j], 3, dims, str, box);
       if (st) return st;
     }
   }
@@ -1170,12 +973,12 @@ int tc_maps(const moe_experts *X, uint8_t *xq, uint8_t *hq, int max_total, TcMap
     const cuuint32_t xbox[3] = {128, (cuuint32_t)(16 << b), (cuuint32_t)kXTerms};
     const cuuint64_t xd[3] = {(cuuint64_t)H, (cuuint64_t)max_total, (cuuint64_t)kXTerms};
     const cuuint64_t xs[2] = {(cuuint64_t)H, (cuuint64_t)H * max_total};
-    int st = encode(&m.xq[b], xq, 3, xd, xs, xbox);
+    int st = encode_u8_sw128(&m.xq[b], xq, 3, xd, xs, xbox);
     if (st) return st;
     const cuuint32_t hbox[3] = {128, (cuuint32_t)(16 << b), (cuuint32_t)kHTerms};
     const cuuint64_t hd[3] = {(cuuint64_t)I, (cuuint64_t)max_total, (cuuint64_t)kHTerms};
     const cuuint64_t hs[2] = {(cuuint64_t)I, (cuuint64_t)I * max_total};
-    st = encode(&m.hq[b], hq, 3, hd, hs, hbox);
+    st = encode_u8_sw128(&m.hq[b], hq, 3, hd, hs, hbox);
     if (st) return st;
   }
   if (cache.size() > 1024) cache.clear();
@@ -1211,23 +1014,24 @@ bool tc_fits(const moe_layer_desc *L, int M) {
 }
 
 // Workspace of the tensor-core path: the term tables, their scales and the
-// per-expert counters (byte sizes, in order).
+// active table (byte sizes, in order: x terms, x scales, h terms, h scales,
+// active table).
 void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]) {
   const size_t H = L->routed.hidden, I = L->routed.inter;
   bytes[0] = (size_t)kXTerms * max_total * H;
   bytes[1] = (size_t)max_total * 4;
   bytes[2] = (size_t)kHTerms * max_total * I;
   bytes[3] = (size_t)max_total * (I / 128) * 4;
-  // counters: one per active-list index (at most E), then the item counter;
-  // sized by the layer alone so that their place does not move with M
-  (void)cap;
-  bytes[4] = ((size_t)L->routed.num_experts + 1) * 4;
+  bytes[4] = (size_t)cap * 16;
 }
 
-int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *ids,
-              const float *w, const int32_t *ttp, const int32_t *off, const int32_t *act,
-              const int32_t *act_count, uint16_t *out, void *ws, const moe_workspace_view &v,
-              uint32_t *err, void *stream) {
+// Counters of the tensor-core path, in ints, sized by the layer alone: one per
+// active-list index (at most E), then the item counter.
+size_t tc_counter_ints(const moe_layer_desc *L) { return (size_t)L->routed.num_experts + 1; }
+
+int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
+              const int32_t *ttp, const int32_t *act_count, uint16_t *out, void *ws,
+              const moe_workspace_view &v, uint32_t *err, void *stream) {
   const moe_experts &R = L->routed;
   char *base = static_cast<char *>(ws);
   TcArgs a = {};
@@ -1240,12 +1044,10 @@ int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const int32_t *
   a.cap = v.cap;
   a.max_total = v.max_total;
   a.x = x;
-  a.ids = ids;
   a.w = w;
   a.ttp = ttp;
-  a.off = off;
-  a.act = act;
   a.act_count = act_count;
+  a.items = reinterpret_cast<const int4 *>(base + v.tc_items);
   a.out = out;
   a.sg = static_cast<const float *>(R.gate.scale);
   a.su = static_cast<const float *>(R.up.scale);

@@ -285,6 +285,13 @@ typedef struct moe_workspace_view {
     size_t tc_x_terms, tc_x_scale, tc_h_terms, tc_h_scale, tc_done;
     size_t total_bytes;
     int max_total, max_blocks, cap;
+    /* tensor-core paths only (else 0): the active table the alignment launch
+     * writes for them, [cap] x {run offset, expert, slot count, 0} int32; and,
+     * on the decode tensor-core path (M <= 16) when H > 512, the k-part
+     * partial sums of gate and up [H/128/4][M*top_k][2][I] float.  On that
+     * path tc_x_terms and tc_x_scale are 0: its x terms never leave shared
+     * memory. */
+    size_t tc_items, tc_part;
 } moe_workspace_view;
 
 /* Host only.  Workspace bytes moe_decode_layer needs for any M <= max_M
@@ -346,15 +353,14 @@ int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,
 /* The expert half of moe_decode_layer ("fp8_moe_grouped.rs": the grouped
  * gate+up and down launchers and moe_weighted_sum_blend_fp8_grouped, which
  * run after moe_fp8_grouped_sort): the same grouped gate+up, down and blend,
- * on routing and alignment tables that the workspace already holds for these
- * M rows -- topk_ids, topk_w, token_to_perm, expert_offsets, active_experts,
- * active_count and sorted_token_ids at the offsets of
- * moe_decode_layer_workspace_view, as moe_topk_softmax and moe_align write
- * them or as an earlier moe_decode_layer call left them.  The kernels and the
- * results are those of moe_decode_layer on the same tables: one launch on
- * the tensor-core path and on the fused CUDA-core path (which aligns the
- * given ids again, to the same tables), three on the staged path (gate+up,
- * down, blend).  The workspace rules are moe_decode_layer's.
+ * on the routing and alignment tables that an earlier moe_decode_layer call
+ * with the same layer and M left in this workspace (topk_ids, topk_w,
+ * token_to_perm, sorted_token_ids, the active list and, on the tensor-core
+ * paths, the active table of tc_items), with the x given here.  The kernels
+ * and the results are those of moe_decode_layer on the same tables: one
+ * launch on the tensor-core paths and on the fused CUDA-core path (which
+ * aligns the ids again, to the same tables), three on the staged path
+ * (gate+up, down, blend).  The workspace rules are moe_decode_layer's.
  * Errors: MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA (as moe_decode_layer). */
 int moe_decode_experts(const moe_layer_desc *layer, const uint16_t *x, int M,
                        uint16_t *out, void *workspace, size_t workspace_bytes,

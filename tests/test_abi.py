@@ -151,6 +151,33 @@ def test_tensor_core_workspace_host_only():
         assert v.tc_x_terms == v.tc_h_terms == v.tc_done == 0
 
 
+def test_decode_tensor_core_workspace_host_only():
+    """FP8 decode batches (M <= 16) take the decode tensor-core kernel: no x
+    terms in the workspace (they stay in shared memory), the h terms, the
+    active table and, with H = 2048 (four k parts of 512), the k-part partial
+    sums [4][M*k][2][I]; the counters sit at 256 as on the verify kernel."""
+    lib = moe.load()
+    layer = moe.LayerDesc(top_k=8, block_size=16, routed=_fake_experts(E=128, H=2048, I=768))
+    for M in (1, 8, 16):
+        v = moe._WsView()
+        assert lib.moe_decode_layer_workspace_view(ctypes.pointer(layer._struct), M,
+                                                   ctypes.byref(v)) == 0
+        mt, _, cap = oracle.align_sizes(M * 8, 128, 16)
+        assert (v.blend_counters, v.tc_done) == (0, 256)
+        assert v.tc_x_terms == v.tc_x_scale == 0
+        offs = [v.tc_h_terms, v.tc_h_scale, v.tc_items, v.tc_part]
+        assert all(o % 256 == 0 and o > 0 for o in offs) and offs == sorted(offs)
+        assert v.tc_h_scale - v.tc_h_terms >= 3 * mt * 768
+        assert v.tc_part - v.tc_items >= cap * 16
+        assert v.total_bytes - v.tc_part >= 4 * M * 8 * 2 * 768 * 4
+        assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), M, 1) == 3
+    # above 16 rows: the verify-batch kernel, with its x terms and no partial sums
+    v = moe._WsView()
+    assert lib.moe_decode_layer_workspace_view(ctypes.pointer(layer._struct), 17,
+                                               ctypes.byref(v)) == 0
+    assert v.tc_x_terms > 0 and v.tc_part == 0 and v.tc_items > 0
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(fmt=moe.FMT_FP8_B128, H=2000), moe.MOE_EUNSUPPORTED),   # FP8 needs H % 128
     (dict(fmt=moe.FMT_NVFP4_G16, I=784), moe.MOE_EUNSUPPORTED),   # NVFP4 needs I % 32

@@ -167,7 +167,7 @@ def test_layer_matches_oracle(moe, shape, path):
             assert H.rel_l2(hs_gpu, hs_ref) < H.STAGE_REL_L2
         y_ref, ys_ref = oracle.grouped_down(X, S, h_gpu, hs_gpu, shape.M, shape.top_k, tables)
         y_gpu = view["y"].cpu().numpy().astype(np.float64)
-        y_tol = TC_Y_REL_L2 if "tc_x_terms" in view else H.STAGE_REL_L2
+        y_tol = TC_Y_REL_L2 if "tc_h_terms" in view else H.STAGE_REL_L2
         assert H.rel_l2(y_gpu[real], y_ref[real]) < y_tol
         if S:
             assert H.rel_l2(view["y_shared"].cpu().numpy(), ys_ref) < H.STAGE_REL_L2
@@ -197,10 +197,11 @@ def test_verify_batch_sampled_rows(moe):
 
 
 @pytest.mark.parametrize("path", list(PATHS), ids=str)
-@pytest.mark.parametrize("shape", [synth.decode_nvfp4(32), synth.decode_fp8(8)],
-                         ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", [synth.decode_nvfp4(32), synth.decode_fp8(8),
+                                   synth.decode_fp8(16)], ids=lambda s: s.name)
 def test_row_invariance(moe, shape, path):
-    """Row 0's output bits are the same whether the batch has 1 or M rows."""
+    """Row 0's output bits are the same whether the batch has 1 or M rows (on
+    the tensor cores, M = 1..16 share the decode kernel)."""
     inp = layer_inputs(shape)
     out_m, _, _ = H.gpu_layer(moe, inp, path=PATHS[path])
     one = synth.LayerInputs(
@@ -295,11 +296,14 @@ def test_one_workspace_serves_alternating_rows(moe, path):
 
 
 @pytest.mark.parametrize("path", [0, 1, 3], ids=["auto", "simt", "staged"])
-def test_decode_experts_on_tables_in_the_workspace(moe, path):
-    """moe_decode_experts runs the expert half of the layer on the tables the
-    workspace holds: those a moe_decode_layer call left, and those written
-    there by moe_topk_softmax and moe_align; the output is the layer's bits."""
-    shape = synth.decode_fp8(4)
+@pytest.mark.parametrize("M", [4, 32], ids=["m4", "m32"])
+def test_decode_experts_on_tables_in_the_workspace(moe, path, M):
+    """moe_decode_experts runs the expert half of the layer on the routing and
+    alignment tables an earlier moe_decode_layer call left in the workspace:
+    again on the same x it gives the same bits, and on another x the bits of
+    moe_decode_layer on that x with the same logits."""
+    shape = synth.LayerShape(f"decode_h2048_i768_e128_k8_fp8_m{M}", M, 2048, 768, 128, 8, 16,
+                             synth.FMT_FP8)
     inp = synth.make_layer(shape, 5150, device="cuda")
     out, view, (layer, ws) = H.gpu_layer(moe, inp, path=path)
     again = torch.full_like(out, float("nan"))
@@ -308,18 +312,11 @@ def test_decode_experts_on_tables_in_the_workspace(moe, path):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(again.view(torch.int16), out.view(torch.int16))
-    # tables written by the stand-alone routing and alignment entry points
-    ws2 = moe.alloc_workspace(layer, shape.M)
-    v2 = moe.workspace_view(layer, shape.M, ws2)
-    moe.moe_topk_softmax(inp.logits, shape.top_k, ids=v2["topk_ids"].view(shape.M, shape.top_k),
-                         w=v2["topk_w"].view(shape.M, shape.top_k))
-    moe.moe_align(v2["topk_ids"], shape.E, shape.BS,
-                  out={key: v2[key] for key in ("sorted_token_ids", "sorted_expert_ids",
-                                                 "expert_offsets", "token_to_perm",
-                                                 "active_experts", "active_count",
-                                                 "num_tokens_post_padded")})
+    x2 = synth.make_x(M, shape.H, 5151, "cuda")
+    ref2 = torch.empty_like(out)
+    moe.moe_decode_layer(layer, x2, ref2, moe.alloc_workspace(layer, M), router_logits=inp.logits)
     third = torch.full_like(out, float("nan"))
-    moe.moe_decode_experts(layer, inp.x, third, ws2, err_word=err)
+    moe.moe_decode_experts(layer, x2, third, ws, err_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert torch.equal(third.view(torch.int16), out.view(torch.int16))
+    assert torch.equal(third.view(torch.int16), ref2.view(torch.int16))

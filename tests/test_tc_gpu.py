@@ -1,5 +1,6 @@
 """The tensor-core (tcgen05) expert path of the decode MoE layer against the
-oracle.
+oracle: the decode kernel (M <= 16: k-split gate+up units, x terms built in
+shared memory, per-token blend) and the verify-batch kernel (M > 16).
 
 The path multiplies the E4M3 weight codes by E4M3 splits of the activations
 (x = t0 + t1 exactly, h = t0 + t1 + t2 to 12 significant bits, each with a
@@ -45,7 +46,9 @@ def _shape(name, M, H_, I, E, k, BS):
     return synth.LayerShape(name, M, H_, I, E, k, BS, synth.FMT_FP8)
 
 
-SHAPES = [synth.tiny(), synth.decode_fp8(1), synth.decode_fp8(8),
+SHAPES = [synth.tiny(), synth.decode_fp8(1), synth.decode_fp8(8), synth.decode_fp8(16),
+          _shape("decode_h4096_i1536_e64_k8_fp8_m5", 5, 4096, 1536, 64, 8, 16),
+          _shape("decode_h2048_i768_e128_k8_fp8_m17", 17, 2048, 768, 128, 8, 16),
           _shape("decode_h2048_i768_e128_k8_fp8_m64", 64, 2048, 768, 128, 8, 16)]
 
 
@@ -90,15 +93,31 @@ def _e4m3(t: torch.Tensor) -> torch.Tensor:
     return t.contiguous().view(torch.float8_e4m3fn).to(torch.float64)
 
 
-def test_tc_x_terms_exact_and_h_terms_bounded(moe):
-    shape = synth.decode_fp8(8)
+@pytest.mark.parametrize("M", [8, 32], ids=["decode_kernel", "verify_kernel"])
+def test_tc_x_terms_exact_and_h_terms_bounded(moe, M):
+    shape = _shape(f"decode_h2048_i768_e128_k8_fp8_m{M}", M, 2048, 768, 128, 8, 16)
     inp = synth.make_layer(shape, 321, device="cuda")
     _, view, _ = H.gpu_layer(moe, inp, path=TC)
     tables, real = _tables_and_real(view, shape)
     pos = np.nonzero(real)[0]
     tok = tables["sorted_token_ids"][pos] // shape.top_k
     pos_t = torch.as_tensor(pos, device="cuda")
+    # the active table the alignment wrote for the tensor-core kernels:
+    # {run offset, expert, slot count, 0} per active expert
+    A = int(tables["active_count"][0])
+    act = tables["active_experts"][:A]
+    items = view["tc_items"][:A].cpu().numpy()
+    np.testing.assert_array_equal(items[:, 1], act)
+    np.testing.assert_array_equal(items[:, 0], tables["expert_offsets"][act])
+    counts = np.bincount(view["topk_ids"].cpu().numpy(), minlength=shape.E)
+    np.testing.assert_array_equal(items[:, 2], counts[act])
+    assert ("tc_x_terms" in view) == (M > 16)   # the decode kernel keeps x terms on chip
+    if M > 16:
+        _check_x_terms(view, inp, pos_t, tok)
+    _check_h_terms(view, shape, pos_t, len(pos))
 
+
+def _check_x_terms(view, inp, pos_t, tok):
     # x: (t0 + t1) * xs == x exactly where |x| * 2^s >= 2^-2, and within 2^-10
     # of the scale elsewhere; the row maximum lands in [128, 256)
     xq = view["tc_x_terms"][:, pos_t]
@@ -112,22 +131,26 @@ def test_tc_x_terms_exact_and_h_terms_bounded(moe):
     mx = scaled.amax(dim=1)
     assert bool(((mx >= 128) & (mx < 256)).all())
 
+
+def _check_h_terms(view, shape, pos_t, npos):
     # h: |sum of three terms * hs - h| <= 2^-12 |h| + 2^-10 hs per (row, block)
     I = shape.I
     hq = view["tc_h_terms"][:, pos_t]
     hs = view["tc_h_scale"][pos_t].to(torch.float64).repeat_interleave(128, dim=1)
     rec = (_e4m3(hq[0]) + _e4m3(hq[1]) + _e4m3(hq[2])) * hs
     h = view["h"][pos_t].to(torch.float64)
-    assert rec.shape == h.shape == (len(pos), I)
+    assert rec.shape == h.shape == (npos, I)
     assert bool(((rec - h).abs() <= h.abs() * 2.0 ** -12 + hs * 2.0 ** -10).all())
-    bmax = (h.abs() / hs).reshape(len(pos), I // 128, 128).amax(dim=2)
+    bmax = (h.abs() / hs).reshape(npos, I // 128, 128).amax(dim=2)
     assert bool(((bmax >= 128) & (bmax < 256)).all())
 
 
-@pytest.mark.parametrize("rows", [(16, 17), (64, 1), (65, 63), (128,)], ids=str)
+@pytest.mark.parametrize("rows", [(1,), (16,), (7, 9), (16, 17), (64, 1), (65, 63), (128,)],
+                         ids=str)
 def test_tc_row_tile_edges(moe, rows):
     """Given ids (top_k = 1): expert 3 takes rows[0] tokens, expert 5 the next
-    rows[1], and so on -- item boundaries at 16-row MMA steps and 64-row tiles."""
+    rows[1], and so on -- item boundaries at 16-row MMA steps and 64-row tiles
+    (M <= 16: the decode kernel; above: the verify-batch kernel)."""
     M = sum(rows)
     shape = _shape(f"tc_edges_m{M}", M, 256, 512, 8, 1, 16)
     inp = synth.make_layer(shape, 55, device="cuda")
@@ -144,8 +167,29 @@ def test_tc_row_tile_edges(moe, rows):
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
 
 
-def test_tc_deterministic_and_graph_replayable(moe):
-    shape = _shape("decode_h2048_i768_e128_k8_fp8_m32", 32, 2048, 768, 128, 8, 16)
+def test_tc_repeated_expert_in_a_token(moe):
+    """Given ids that list one expert twice in every token (top_k = 2, M = 16):
+    the expert's run holds 32 rows, two 16-row tiles on the decode kernel."""
+    M = 16
+    shape = _shape("tc_repeat_m16", M, 2048, 768, 16, 2, 16)
+    inp = synth.make_layer(shape, 57, device="cuda")
+    ids = np.full((M, 2), 3, np.int32)
+    ids[::3, 1] = 7
+    w = np.full((M, 2), 0.5, np.float32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, view, _ = H.gpu_layer(moe, inp, path=TC, use_logits=False,
+                               ids=torch.as_tensor(ids, device="cuda"),
+                               w=torch.as_tensor(w, device="cuda"), err=err)
+    assert int(err.item()) == 0
+    _, ref_b, bad = H.oracle_layer(inp, ids=ids, w=w.astype(np.float64))
+    assert bad == 0
+    rl2, mx = H.compare_bf16(out, ref_b)
+    assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
+
+
+@pytest.mark.parametrize("M", [8, 32], ids=["decode_kernel", "verify_kernel"])
+def test_tc_deterministic_and_graph_replayable(moe, M):
+    shape = _shape(f"decode_h2048_i768_e128_k8_fp8_m{M}", M, 2048, 768, 128, 8, 16)
     inp = synth.make_layer(shape, 9, device="cuda")
     out1, _, (layer, ws) = H.gpu_layer(moe, inp, path=TC)
     out2 = torch.empty_like(out1)
@@ -189,18 +233,19 @@ def test_tc_verify_batch_matches_staged_path(moe):
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
 
 
-@pytest.mark.parametrize("shape", [synth.decode_fp8(8),
-                                   _shape("decode_h2048_i768_e128_k8_fp8_m64", 64, 2048, 768,
-                                          128, 8, 16)], ids=lambda s: s.name)
-def test_tc_row_invariance(moe, shape):
-    """On the tensor-core path row 0's output bits are the same whether the
-    batch has 1 or M rows: each row has its own x scale, every MMA column is
-    one row, and promotion, SiLU, the h scales and the blend are per row."""
+@pytest.mark.parametrize("M,m", [(8, 1), (16, 1), (16, 5), (64, 17), (128, 33)], ids=str)
+def test_tc_row_invariance(moe, M, m):
+    """On the tensor-core path the first m rows' output bits are the same
+    whether the batch has m or M rows, within one kernel family (decode: M <=
+    16; verify batch: M > 16): each row has its own x scale, every MMA column
+    is one row, the k parts of a tile are summed in a fixed order, and
+    promotion, SiLU, the h scales and the blend are per row."""
+    shape = _shape(f"decode_h2048_i768_e128_k8_fp8_m{M}", M, 2048, 768, 128, 8, 16)
     inp = synth.make_layer(shape, 1000, device="cuda")
     out_m, _, _ = H.gpu_layer(moe, inp, path=TC)
-    one = synth.LayerInputs(
-        synth.LayerShape(shape.name + "_row0", 1, shape.H, shape.I, shape.E, shape.top_k,
+    few = synth.LayerInputs(
+        synth.LayerShape(shape.name + f"_rows{m}", m, shape.H, shape.I, shape.E, shape.top_k,
                          shape.BS, shape.fmt),
-        inp.x[:1].contiguous(), inp.logits[:1].contiguous(), inp.experts)
-    out_1, _, _ = H.gpu_layer(moe, one, path=TC)
-    assert torch.equal(out_m[:1].view(torch.int16), out_1.view(torch.int16))
+        inp.x[:m].contiguous(), inp.logits[:m].contiguous(), inp.experts)
+    out_1, _, _ = H.gpu_layer(moe, few, path=TC)
+    assert torch.equal(out_m[:m].view(torch.int16), out_1.view(torch.int16))
