@@ -38,6 +38,7 @@ PATH_SIMT_STAGED = 3
 MOE_ERR_TIMEOUT = 0x2
 MAX_EXPERTS = 1024
 MAX_ROWS = 128
+TOKEN_FORM_ROWS = 16   # tensor-core path: up to this M, x terms are kept by token
 
 LIB_PATH = _build.LIB
 
@@ -80,7 +81,7 @@ class _WsView(ctypes.Structure):
         "h_shared", "y", "y_shared", "blend_counters", "router_logits", "shared_gate", "tc_x_terms", "tc_x_scale",
         "tc_h_terms", "tc_h_scale", "tc_done", "total_bytes")] + [
         ("max_total", ctypes.c_int), ("max_blocks", ctypes.c_int), ("cap", ctypes.c_int),
-        ("tc_items", ctypes.c_size_t), ("tc_part", ctypes.c_size_t)]
+        ("tc_items", ctypes.c_size_t)]
 
 
 _P = ctypes.c_void_p
@@ -356,8 +357,11 @@ def workspace_view(layer: LayerDesc, M: int, ws: torch.Tensor) -> dict:
             tc_h_terms=sl(v.tc_h_terms, 3 * mt * I, torch.uint8).view(3, mt, I),
             tc_h_scale=sl(v.tc_h_scale, mt * (I // 128), torch.float32).view(mt, I // 128),
             tc_items=sl(v.tc_items, 4 * v.cap, torch.int32).view(v.cap, 4))
-    if v.tc_x_terms:   # the verify-batch kernel's x terms (the decode kernel keeps
-        # them in shared memory)
+    if v.tc_x_terms and M <= TOKEN_FORM_ROWS:   # x terms by token [H/128][2][16][128]
+        tc.update(
+            tc_x_table=sl(v.tc_x_terms, 2 * 16 * H, torch.uint8).view(H // 128, 2, 16, 128),
+            tc_x_scale=sl(v.tc_x_scale, 16, torch.float32))
+    elif v.tc_x_terms:   # x terms by sorted row [2][max_total][H]
         tc.update(
             tc_x_terms=sl(v.tc_x_terms, 2 * mt * H, torch.uint8).view(2, mt, H),
             tc_x_scale=sl(v.tc_x_scale, mt, torch.float32))

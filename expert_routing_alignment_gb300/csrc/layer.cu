@@ -21,18 +21,11 @@ int launch_blend(const float *y, const float *w, const int32_t *ttp, const float
                  void *stream);
 bool fused_fits(const moe_layer_desc *L, int M, int sms);
 bool tc_fits(const moe_layer_desc *L, int M);
-void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]);
+void tc_workspace(const moe_layer_desc *L, int M, int max_total, int cap, size_t (&bytes)[5]);
 size_t tc_counter_ints(const moe_layer_desc *L);
 int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
               const int32_t *ttp, const int32_t *act_count, uint16_t *out, void *ws,
               const moe_workspace_view &v, uint32_t *err, void *stream);
-bool dec_fits(const moe_layer_desc *L, int M);
-size_t dec_counter_ints(const moe_layer_desc *L);
-void dec_workspace(const moe_layer_desc *L, int M, int max_total, int cap, size_t (&bytes)[4]);
-int launch_dec(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
-               const int32_t *ttp, const int32_t *sti, const int32_t *act_count,
-               uint16_t *out, void *ws, const moe_workspace_view &v, uint32_t *err,
-               void *stream);
 int align_launch(const void *topk_ids, int ids_is_int64, int n, int num_experts, int block_size,
                  int32_t *sorted_token_ids, int32_t *sorted_expert_ids, int32_t *expert_offsets,
                  int32_t *token_to_perm, int32_t *active_experts, int32_t *active_count,
@@ -59,36 +52,30 @@ static int resolve_path(const moe_experts *routed, int M, int top_k, int path) {
 }
 
 // How moe_decode_layer runs a shape class: the fused CUDA-core kernel, the
-// tensor-core kernel of the verify batches, the tensor-core kernel of decode
-// batches (M <= 16), or the staged CUDA-core kernels.  It depends on the
+// tensor-core kernel, or the staged CUDA-core kernels.  It depends on the
 // shapes only, never on the routing, so a captured graph stays valid for
 // every routing.
-enum { kRunFused = 0, kRunTc = 1, kRunStaged = 2, kRunTcDec = 3 };
+enum { kRunFused = 0, kRunTc = 1, kRunStaged = 2 };
 
 static int layer_run(const moe_layer_desc *L, int M) {
   switch (L->path) {
     case MOE_PATH_TC:
-      if (dec_fits(L, M)) return kRunTcDec;
       return tc_fits(L, M) ? kRunTc : -1;
     case MOE_PATH_SIMT_STAGED:
       return kRunStaged;
     case MOE_PATH_SIMT:
       return fused_fits(L, M, sm_count()) ? kRunFused : kRunStaged;
     default:   // the tensor cores for every FP8 shape they admit, else CUDA cores
-      if (dec_fits(L, M)) return kRunTcDec;
       if (tc_fits(L, M)) return kRunTc;
       return fused_fits(L, M, sm_count()) ? kRunFused : kRunStaged;
   }
 }
 
-static bool is_tc(int run) { return run == kRunTc || run == kRunTcDec; }
+static bool is_tc(int run) { return run == kRunTc; }
 
-// Bytes of the tensor-core kernels' counters (both kernels share the region;
-// each call leaves it at zero): sized by the layer alone.
-size_t tc_counter_bytes(const moe_layer_desc *L) {
-  const size_t a = tc_counter_ints(L), b = dec_counter_ints(L);
-  return 4 * (a > b ? a : b);
-}
+// Bytes of the tensor-core kernel's counters (each call leaves them at zero):
+// sized by the layer alone.
+size_t tc_counter_bytes(const moe_layer_desc *L) { return 4 * tc_counter_ints(L); }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -144,22 +131,15 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   v->router_logits = take((size_t)M * E * 4);
   v->shared_gate = take((size_t)M * 4);
   v->tc_x_terms = v->tc_x_scale = v->tc_h_terms = v->tc_h_scale = 0;
-  v->tc_items = v->tc_part = 0;
+  v->tc_items = 0;
   if (run == kRunTc) {
     size_t b[5];
-    tc_workspace(L, max_total, cap, b);
+    tc_workspace(L, M, max_total, cap, b);
     v->tc_x_terms = take(b[0]);
     v->tc_x_scale = take(b[1]);
     v->tc_h_terms = take(b[2]);
     v->tc_h_scale = take(b[3]);
     v->tc_items = take(b[4]);
-  } else if (run == kRunTcDec) {
-    size_t b[4];
-    dec_workspace(L, M, max_total, cap, b);
-    v->tc_h_terms = take(b[0]);
-    v->tc_h_scale = take(b[1]);
-    v->tc_items = take(b[2]);
-    v->tc_part = b[3] ? take(b[3]) : 0;
   }
   v->total_bytes = off;
   v->max_total = max_total;
@@ -305,9 +285,6 @@ int run_experts(const moe_layer_desc *layer, int run, const uint16_t *x, int M,
   if (run == kRunTc)
     return launch_tc(layer, x, M, w, I32(v.token_to_perm), I32(v.active_count), out, workspace,
                      v, err_word, stream);
-  if (run == kRunTcDec)
-    return launch_dec(layer, x, M, w, I32(v.token_to_perm), I32(v.sorted_token_ids),
-                      I32(v.active_count), out, workspace, v, err_word, stream);
   int st = simt_gate_up(&layer->routed, S, x, M, k, I32(v.expert_offsets),
                         I32(v.sorted_token_ids), I32(v.active_experts), I32(v.active_count),
                         F32(v.h), S ? F32(v.h_shared) : nullptr, stream);

@@ -73,6 +73,21 @@ __device__ __forceinline__ bool wait_at_least(const volatile int *failed, const 
   return false;
 }
 
+// Add v to *p at gpu scope with release semantics, without waiting for the
+// result (every write ordered before it -- this thread's, and those of the
+// threads it synchronised with at a CTA barrier -- is visible to a thread
+// that acquires the new value).
+__device__ __forceinline__ void red_release_add(int *p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// The same with acquire-release semantics, returning the previous value.
+__device__ __forceinline__ int atom_acq_rel_add(int *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // Generic-proxy writes to global memory made visible to later tensor copies
 // (async proxy) of any CTA.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -158,6 +173,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+// 8 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() {

@@ -53,6 +53,7 @@ constexpr int kAccs = 16;                      // k-block accumulator barriers (
 constexpr int kTfree = 16;                     // per-stage TMEM release barriers
 constexpr int kIQ = 32;                        // item queue (copy thread -> MMA, promotion)
 constexpr int kRowTile = 64;                   // token rows per item (MMA N <= 64)
+constexpr int kTokMax = 16;                    // batches up to 16 rows: token columns
 constexpr int kXTerms = 2, kHTerms = 3;
 constexpr int kMaxKB = 64;                     // k blocks of 128 (H <= 8192)
 constexpr int kMaxKBd = 32;                    // down k blocks (I <= 4096)
@@ -60,14 +61,23 @@ constexpr uint32_t kTmemCols = 512;            // the circular accumulator range
 
 struct TcArgs {
   int M, k, n, E, H, I, cap, max_total;
+  // Token-column form (M <= 16): the gate+up MMAs take all 16 token columns
+  // of a per-token x-term table instead of the item's rows, items are 16-row
+  // tiles, and no grid barrier precedes the first copies.
+  int tok;
+  int row_tile;                              // rows per item: 16 (token form) or 64
   const uint16_t *x;
   const float *w;                            // [n] routing weight of each slot
   const int32_t *ttp, *act_count;            // the alignment's tables
+  const int32_t *sti;                        // sorted_token_ids
   const int4 *items;                         // [cap] {offset, expert, slot count, 0}
   uint16_t *out;                             // [M][H] bf16
   const float *sg, *su, *sd;                 // block scales [E][R/128][K/128]
-  uint8_t *xq;                               // x terms [2][max_total][H] E4M3
-  float *xs;                                 // 2^-s of each x row [max_total]
+  uint8_t *xq;                               // x terms [2][max_total][H] E4M3 by sorted row,
+                                             // or (token form) [H/128][2][16][128] by token
+  float *xs;                                 // 2^-s of each x row [max_total] (token form: [16])
+  int *xflag;                                // token form: [16] epoch of each token's terms
+  int *epoch;                                // the last call's epoch
   uint8_t *hq;                               // h terms [3][max_total][I] E4M3
   float *hs;                                 // 2^-s per (row, 128-block) [max_total][I/128]
   float *h, *y;                              // [max_total][I], [max_total][H]
@@ -84,6 +94,7 @@ struct TcArgs {
 struct TcMaps {
   CUtensorMap w[3][2];
   CUtensorMap xq[3], hq[3];
+  CUtensorMap xt;   // token form: {128, 16 tokens, 2 * H/128}, box {128, 16, 2}
 };
 
 struct Smem {
@@ -96,7 +107,9 @@ struct Smem {
   int *twait;          // [kRecs] the stage whose TMEM release it waits for (-1: none)
   volatile int *misc;  // [0] failed, [1] TMEM base, [2] active count, [3] row tiles
   float *sc;           // [2][kMaxKB] weight block scales of the current item
-  float *cs;           // [kMaxKBd][kRowTile] per-row factors of the current item
+  float *cs;           // [I/128][row tile] per-row factors of the current item
+  int *tokrow;         // [kRowTile] token form: each row's token
+  float *xtok;         // [kTokMax] token form: 2^-s of each token's x row
   uint32_t *red;       // [4 groups][4 quadrants][16] column maxima
   int *rtp;            // [cap + 1] row-tile prefix over the active list
   int2 *info;          // [cap] {offset, expert | rows << 16}
@@ -104,11 +117,18 @@ struct Smem {
 
 __host__ __device__ inline size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
 
-__host__ __device__ inline size_t fixed_bytes(int cap) {
+// Fixed shared memory beside the ring: barriers, records, the item queue,
+// scales, the per-row factors of one item, the column maxima, the row tokens
+// and the active table.  (A ring of exactly three 72 KB decode stages was
+// measured slower than the two stages this leaves room for.)
+__host__ __device__ inline size_t fixed_bytes(int cap, int KBd, int RT) {
+  (void)KBd;
+  (void)RT;
   size_t b = 0;
   b += al16(8 * (2 * kRecs + kAccs + kTfree + kIQ + 1));
   b += 4 * al16(4 * kRecs) + al16(4 * kIQ) + al16(4 * 16);
   b += al16(4 * 2 * kMaxKB) + al16(4 * kMaxKBd * kRowTile) + al16(4 * 4 * 4 * 16);
+  b += al16(4 * kRowTile) + al16(4 * kTokMax);
   b += al16(4 * ((size_t)cap + 1)) + al16(8 * (size_t)cap);
   return b;
 }
@@ -136,7 +156,9 @@ __device__ Smem carve(uint8_t *base, const TcArgs &a) {
   S.iq = reinterpret_cast<volatile int *>(take(4 * kIQ));
   S.misc = reinterpret_cast<volatile int *>(take(4 * 16));
   S.sc = reinterpret_cast<float *>(take(4 * 2 * kMaxKB));
-  S.cs = reinterpret_cast<float *>(take(4 * kMaxKBd * kRowTile));
+  S.cs = reinterpret_cast<float *>(take(4 * (size_t)(a.I / 128) * a.row_tile));
+  S.tokrow = reinterpret_cast<int *>(take(4 * kRowTile));
+  S.xtok = reinterpret_cast<float *>(take(4 * kTokMax));
   S.red = reinterpret_cast<uint32_t *>(take(4 * 4 * 4 * 16));
   S.rtp = reinterpret_cast<int *>(take(4 * ((size_t)a.cap + 1)));
   S.info = reinterpret_cast<int2 *>(take(8 * (size_t)a.cap));
@@ -181,7 +203,8 @@ struct Item {
   int tile;      // gate+up: 128-row tile of I; down: pair of 128-row tiles of H
 };
 
-__device__ __forceinline__ Item decode(const Smem &S, int A, int i, int TR, int FT, int FD) {
+__device__ __forceinline__ Item decode(const Smem &S, int A, int i, int TR, int FT, int FD,
+                                       int RT) {
   Item it;
   int rtg;
   if (i < TR * FT) {
@@ -207,8 +230,8 @@ __device__ __forceinline__ Item decode(const Smem &S, int A, int i, int TR, int 
   const int rows_e = inf.y >> 16;
   it.a = lo;
   it.e = inf.y & 0xFFFF;
-  it.pos0 = inf.x + rt * kRowTile;
-  it.rows = min(kRowTile, rows_e - rt * kRowTile);
+  it.pos0 = inf.x + rt * RT;
+  it.rows = min(RT, rows_e - rt * RT);
   it.n16 = (it.rows + 15) & ~15;
   it.box = it.n16 <= 16 ? 0 : (it.n16 <= 32 ? 1 : 2);
   it.kps = it.n16 <= 32 ? 2 : 1;
@@ -293,6 +316,72 @@ __device__ void prep_x(const TcArgs &a) {
   }
 }
 
+// Token form: CTA t < M writes token t's two E4M3 terms (the split rule of
+// prep_x, with the token's own power-of-two scale) into the table at
+// [kb][term][t][128] and its 2^-s, then publishes them by storing this
+// call's epoch into xflag[t] (release, after the terms are visible to the
+// tensor copies of every CTA).  The 16 promotion warps split the row.
+__device__ void prep_token(const TcArgs &a, const Smem &S, uint32_t ep) {
+  const int t = blockIdx.x;
+  if (t >= a.M) return;
+  const int ew = (threadIdx.x >> 5) - 2, lane = threadIdx.x & 31, et = threadIdx.x - 64;
+  const uint16_t *xr = a.x + (size_t)t * a.H;
+  uint32_t mx = 0;
+  for (int c = et * 8; c < a.H; c += kEpiThreads * 8) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + c));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      mx = max(mx, (w[h] & 0x7FFFu) << 16);
+      mx = max(mx, (w[h] >> 16 & 0x7FFFu) << 16);
+    }
+  }
+  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+  if (lane == 0) S.red[ew] = mx;
+  asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+  mx = 0;
+  for (int w = 0; w < kEpiWarps; ++w) mx = max(mx, S.red[w]);
+  const int sh = term_shift(mx);
+  const float scl = pow2f(sh);
+  if (et == 0) a.xs[t] = pow2f(-sh);
+  // element c of k block kb: term r at byte (kb * 2 + r) * 16 * 128 + t * 128 + c % 128
+  for (int c = et * 4; c < a.H; c += kEpiThreads * 4) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(xr + c));
+    uint32_t t0a, t1a, t0b, t1b;
+    e4m3_split2(bf16_to_float((uint16_t)(v.x & 0xFFFFu)) * scl,
+                bf16_to_float((uint16_t)(v.x >> 16)) * scl, t0a, t1a);
+    e4m3_split2(bf16_to_float((uint16_t)(v.y & 0xFFFFu)) * scl,
+                bf16_to_float((uint16_t)(v.y >> 16)) * scl, t0b, t1b);
+    uint8_t *dst = a.xq + (size_t)(c / 128) * 2 * kTokMax * 128 + (size_t)t * 128 + c % 128;
+    *reinterpret_cast<uint32_t *>(dst) = t0a | (t0b << 16);
+    *reinterpret_cast<uint32_t *>(dst + kTokMax * 128) = t1a | (t1b << 16);
+  }
+  fence_proxy_async_global();
+  __threadfence();
+  asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+  if (et == 0) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.xflag + t), "r"(ep)
+                            : "memory");
+}
+
+// Token form: every token's terms are published (bounded wait on the M
+// flags), and the token scales are in shared memory.
+__device__ bool wait_tokens(const TcArgs &a, const Smem &S, uint32_t ep) {
+  const int et = threadIdx.x - 64;
+  bool ok = true;
+  if (et < a.M) {
+    const uint64_t t0 = gtime();
+    while (ld_acquire(a.xflag + et) != (int)ep) {
+      if (S.misc[0] || gtime() - t0 > kWaitNs) {
+        ok = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+    S.xtok[et] = __ldcg(a.xs + et);
+  }
+  return ok;
+}
+
 // Grid barrier among the promotion warps of every CTA (named barrier 1 in the
 // CTA, then one thread's arrival on the monotonic count); true when all CTAs
 // arrived within the wait limit.
@@ -358,7 +447,7 @@ __device__ int build_table(const TcArgs &a, const Smem &S) {
     const int4 inf = __ldcg(a.items + i);
     const int rows = min(inf.z, 0x7FFF);
     S.info[i] = make_int2(inf.x, (inf.y & 0xFFFF) | (rows << 16));
-    S.rtp[i] = (rows + kRowTile - 1) / kRowTile;   // counts; scanned below
+    S.rtp[i] = (rows + a.row_tile - 1) / a.row_tile;   // counts; scanned below
   }
   __syncthreads();
   if (threadIdx.x < 32) {
@@ -417,7 +506,7 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
     S.iq[jq % kIQ] = i;
     mbar_arrive(&S.iqbar[jq % kIQ]);
     ++jq;
-    const Item it = decode(S, A, i, TR, FT, FD);
+    const Item it = decode(S, A, i, TR, FT, FD, a.row_tile);
     if (!it.gu) {
       const int need = (S.rtp[it.a + 1] - S.rtp[it.a]) * FT;
       if (!wait_count(S, a.done + it.a, need)) {
@@ -499,8 +588,12 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
         fence_proxy_async_global();
         x_ready = true;
       }
-      for (int j = 0; j < it.kps; ++j)
-        tma_3d(dst + 2 * abytes + j * bterm, bmap, (kb + j) * 128, it.pos0, 0, fb);
+      for (int j = 0; j < it.kps; ++j) {
+        if (a.tok && it.gu)   // all 16 token columns of k block kb + j
+          tma_3d(dst + 2 * abytes + j * bterm, &m.xt, 0, 0, 2 * (kb + j), fb);
+        else
+          tma_3d(dst + 2 * abytes + j * bterm, bmap, (kb + j) * 128, it.pos0, 0, fb);
+      }
       ++s;
     }
     // the next item, taken once this one's copies are all issued (taken any
@@ -531,7 +624,7 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
     const int i = next_item(S, jq);
     if (i < 0) ok = false;
     if (i < 0 || i >= total) break;
-    const Item it = decode(S, A, i, TR, FT, FD);
+    const Item it = decode(S, A, i, TR, FT, FD, a.row_tile);
     const int KB = it.gu ? a.H / 128 : a.I / 128;
     const int T = it.gu ? kXTerms : kHTerms;
     const uint32_t nt = 16u << it.box;
@@ -596,7 +689,17 @@ __device__ void finish_gate_up(const TcArgs &a, const Smem &S, const Item &it, i
     hv[jj] = 0.f;
     if (c0 + jj < it.rows) {
       const float xi = S.cs[c0 + jj];
-      hv[jj] = silu_f32(acc0[jj] * xi) * (acc1[jj] * xi);
+      float g = acc0[jj], u = acc1[jj];
+      if (a.tok) {   // the MMA columns are tokens: take the row's own
+        const int t = S.tokrow[c0 + jj];
+        g = u = 0.f;
+#pragma unroll
+        for (int tt = 0; tt < kTokMax; ++tt) {
+          g = tt == t ? acc0[tt] : g;
+          u = tt == t ? acc1[tt] : u;
+        }
+      }
+      hv[jj] = silu_f32(g * xi) * (u * xi);
       a.h[(size_t)(it.pos0 + c0 + jj) * a.I + o] = hv[jj];
       const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv[jj])));
       if (lane == 0) S.red[(grp * 4 + q) * 16 + jj] = m;
@@ -681,7 +784,7 @@ __device__ __forceinline__ bool epi_sync_or(bool v) {
 // group g = (w-2)/4 of the item's token rows).  Every decision to leave the
 // item loop is taken after a vote over all 16 warps.
 __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int total,
-                         uint32_t tmem) {
+                         uint32_t tmem, uint32_t ep) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ew = warp - 2, q = warp & 3, grp = ew >> 2;
   const int et = threadIdx.x - 64;
@@ -693,13 +796,22 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
   uint32_t thead = 0;   // the copy thread's TMEM placement, recomputed
   int pending = -1;   // active index of a finished gate+up item not yet published
   bool bad = false;
-  // the x terms of this CTA's share of the slots, then the grid barrier that
-  // makes all of them (and the zeroed counters) visible to the copies
-  prep_x(a);
-  fence_proxy_async_global();
-  if (!epi_grid_barrier(S, a.grid_ctr)) {
-    bad = true;
-    fail(S, a);
+  if (a.tok) {
+    // token form: the CTA's own token (if any), then every token's flag
+    prep_token(a, S, ep);
+    if (epi_sync_or(!wait_tokens(a, S, ep))) {
+      bad = true;
+      fail(S, a);
+    }
+  } else {
+    // the x terms of this CTA's share of the slots, then the grid barrier
+    // that makes all of them (and the zeroed counters) visible to the copies
+    prep_x(a);
+    fence_proxy_async_global();
+    if (!epi_grid_barrier(S, a.grid_ctr)) {
+      bad = true;
+      fail(S, a);
+    }
   }
   if (et == 0) {
     fence_proxy_async_global();
@@ -715,7 +827,7 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
       break;
     }
     if (i >= total) break;
-    const Item it = decode(S, A, i, TR, FT, FD);
+    const Item it = decode(S, A, i, TR, FT, FD, a.row_tile);
     const int KB = it.gu ? a.H / 128 : KBd;
     fence_proxy_async_global();   // this thread's h terms before the publish
     if (epi_sync_or(bad || S.misc[0])) {
@@ -740,8 +852,16 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
         S.sc[j] = __ldg(a.sg + sb + j);
         S.sc[kMaxKB + j] = __ldg(a.su + sb + j);
       }
-      for (int j = et; j < kRowTile; j += kEpiThreads)
-        S.cs[j] = j < it.rows ? __ldcg(a.xs + it.pos0 + j) : 0.f;
+      if (a.tok) {   // each row's token and that token's x scale
+        for (int j = et; j < a.row_tile; j += kEpiThreads) {
+          const int t = j < it.rows ? __ldcg(a.sti + it.pos0 + j) / a.k : 0;
+          S.tokrow[j] = t;
+          S.cs[j] = j < it.rows ? S.xtok[t] : 0.f;
+        }
+      } else {
+        for (int j = et; j < a.row_tile; j += kEpiThreads)
+          S.cs[j] = j < it.rows ? __ldcg(a.xs + it.pos0 + j) : 0.f;
+      }
     } else {
       const size_t sb = ((size_t)it.e * (a.H / 128) + 2 * it.tile) * KB;
       for (int j = et; j < KB; j += kEpiThreads) {
@@ -755,8 +875,8 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
       break;
     }
     if (!it.gu) {
-      for (int idx = et; idx < KB * kRowTile; idx += kEpiThreads) {
-        const int kb = idx / kRowTile, j = idx - kb * kRowTile;
+      for (int idx = et; idx < KB * a.row_tile; idx += kEpiThreads) {
+        const int kb = idx / a.row_tile, j = idx - kb * a.row_tile;
         S.cs[idx] = j < it.rows ? __ldcg(a.hs + (size_t)(it.pos0 + j) * KBd + kb) : 0.f;
       }
       epi_sync_or(false);
@@ -789,7 +909,7 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
       }
       tc_fence_after();
       const uint32_t col = lane_base + pos + (uint32_t)c0;
-      const float *hf = it.gu ? nullptr : S.cs + kb * kRowTile + c0;
+      const float *hf = it.gu ? nullptr : S.cs + kb * a.row_tile + c0;
       promote(col, nt, T, S.sc[kb], hf, acc0);
       promote(col + (uint32_t)T * nt, nt, T, S.sc[kMaxKB + kb], hf, acc1);
       ++s;
@@ -863,6 +983,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if ((smem_addr(S.ring) & 1023u) != 0) fail(S, a);
 
   pdl_wait();   // the tables of the alignment are final
+  // this call's epoch: one more than the last call's (written by the
+  // previous kernel on this workspace after its final grid barrier)
+  const uint32_t ep = (uint32_t)__ldcg(a.epoch) + 1u;
   // The item table first (it needs only the alignment's tables); the x terms
   // are written by the promotion warps while the copy warp already streams
   // weight tiles, which do not depend on them (misc[6]: x terms ready).
@@ -877,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((threadIdx.x & 31) == 0) mma_issuer(a, S, A, TR, total, tmem);
     __syncwarp();
   } else {
-    epilogue(a, S, A, TR, total, tmem);
+    epilogue(a, S, A, TR, total, tmem, ep);
   }
 
   tc_fence_before();
@@ -899,7 +1022,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every item of every CTA is done: the counters start the next call at zero
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < a.cap; i += kThreads) a.done[i] = 0;
-    if (threadIdx.x == 0) *a.work = 0;
+    if (threadIdx.x == 0) {
+      *a.work = 0;
+      *a.epoch = (int)ep;
+    }
   }
   const long long T4 = (long long)a.M * a.H / 4;
   const long long o1 = T4 * (blockIdx.x + 1) / gridDim.x;
@@ -981,6 +1107,13 @@ int tc_maps(const moe_experts *X, uint8_t *xq, uint8_t *hq, int max_total, TcMap
     st = encode_u8_sw128(&m.hq[b], hq, 3, hd, hs, hbox);
     if (st) return st;
   }
+  {   // the token-form x-term table over the same buffer (used when M <= 16)
+    const cuuint32_t tbox[3] = {128, (cuuint32_t)kTokMax, 2};
+    const cuuint64_t td[3] = {128, (cuuint64_t)kTokMax, (cuuint64_t)2 * (H / 128)};
+    const cuuint64_t ts[2] = {128, (cuuint64_t)kTokMax * 128};
+    const int st = encode_u8_sw128(&m.xt, xq, 3, td, ts, tbox);
+    if (st) return st;
+  }
   if (cache.size() > 1024) cache.clear();
   cache.emplace(key, m);
   *out = m;
@@ -992,8 +1125,8 @@ constexpr size_t kSmemLimit = 227 * 1024;
 // terms, or one k block with 64 rows
 constexpr size_t kMaxStage = 4 * kTileBytes + 2 * kHTerms * 32 * 128;
 
-size_t ring_bytes_for(int cap) {
-  const size_t fixed = fixed_bytes(cap);
+size_t ring_bytes_for(int cap, int KBd, int RT) {
+  const size_t fixed = fixed_bytes(cap, KBd, RT);
   if (fixed + 2 * kMaxStage > kSmemLimit) return 0;
   return (kSmemLimit - fixed) / 1024 * 1024;
 }
@@ -1010,24 +1143,29 @@ bool tc_fits(const moe_layer_desc *L, int M) {
     return false;
   const int n = M * L->top_k;
   const int cap = n < R.num_experts ? n : R.num_experts;
-  return ring_bytes_for(cap) != 0;
+  return ring_bytes_for(cap, R.inter / 128, M <= kTokMax ? 16 : kRowTile) != 0;
 }
 
 // Workspace of the tensor-core path: the term tables, their scales and the
 // active table (byte sizes, in order: x terms, x scales, h terms, h scales,
 // active table).
-void tc_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]) {
+void tc_workspace(const moe_layer_desc *L, int M, int max_total, int cap, size_t (&bytes)[5]) {
   const size_t H = L->routed.hidden, I = L->routed.inter;
-  bytes[0] = (size_t)kXTerms * max_total * H;
-  bytes[1] = (size_t)max_total * 4;
+  // x terms: by sorted row, or (M <= 16) the token table [H/128][2][16][128]
+  const size_t rows = M <= kTokMax ? (size_t)kTokMax : (size_t)max_total;
+  bytes[0] = (size_t)kXTerms * rows * H;
+  bytes[1] = rows * 4;
   bytes[2] = (size_t)kHTerms * max_total * I;
   bytes[3] = (size_t)max_total * (I / 128) * 4;
   bytes[4] = (size_t)cap * 16;
 }
 
 // Counters of the tensor-core path, in ints, sized by the layer alone: one per
-// active-list index (at most E), then the item counter.
-size_t tc_counter_ints(const moe_layer_desc *L) { return (size_t)L->routed.num_experts + 1; }
+// active-list index (at most E), the item counter, and the token form's 16
+// token flags.  (The call epoch sits beside the grid-barrier count.)
+size_t tc_counter_ints(const moe_layer_desc *L) {
+  return (size_t)L->routed.num_experts + 1 + kTokMax;
+}
 
 int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
               const int32_t *ttp, const int32_t *act_count, uint16_t *out, void *ws,
@@ -1043,9 +1181,12 @@ int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
   a.I = R.inter;
   a.cap = v.cap;
   a.max_total = v.max_total;
+  a.tok = M <= kTokMax;
+  a.row_tile = a.tok ? 16 : kRowTile;
   a.x = x;
   a.w = w;
   a.ttp = ttp;
+  a.sti = reinterpret_cast<const int32_t *>(base + v.sorted_token_ids);
   a.act_count = act_count;
   a.items = reinterpret_cast<const int4 *>(base + v.tc_items);
   a.out = out;
@@ -1060,15 +1201,17 @@ int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
   a.y = reinterpret_cast<float *>(base + v.y);
   a.done = reinterpret_cast<int *>(base + v.tc_done);
   a.work = a.done + a.E;
+  a.xflag = a.work + 1;
   a.grid_ctr = reinterpret_cast<unsigned long long *>(base + v.blend_counters);
+  a.epoch = reinterpret_cast<int *>(base + v.blend_counters + 8);
   a.err = err;
-  const size_t ring = ring_bytes_for(v.cap);
+  const size_t ring = ring_bytes_for(v.cap, a.I / 128, a.row_tile);
   if (!ring) return MOE_EUNSUPPORTED;
   a.ring_bytes = (uint32_t)ring;
   TcMaps maps;
   int st = tc_maps(&R, a.xq, a.hq, v.max_total, &maps);
   if (st) return st;
-  const size_t smem = ring + fixed_bytes(v.cap);
+  const size_t smem = ring + fixed_bytes(v.cap, a.I / 128, a.row_tile);
   st = ensure_smem_limit((const void *)verify_ffn_kernel, smem);
   if (st) return st;
   return launch_pdl_coop(verify_ffn_kernel, dim3(sm_count()), dim3(kThreads), smem, stream, a,

@@ -267,8 +267,10 @@ typedef struct moe_workspace_view {
     size_t active_experts, active_count;           /* [cap], [1] */
     size_t num_tokens_post_padded;                 /* [1] */
     size_t h, h_shared, y, y_shared;               /* float tables */
-    size_t blend_counters;                         /* internal: [1] uint64 grid-barrier count,
-                                                      always at offset 0 */
+    size_t blend_counters;                         /* internal: [1] uint64 grid-barrier count
+                                                      and, after it, the decode tensor-core
+                                                      kernel's int32 call epoch; always at
+                                                      offset 0 */
     size_t router_logits;                          /* [M][E] float: the logits of a call that
                                                       computed them from x (else unwritten) */
     size_t shared_gate;                            /* [M] float: the shared expert's gates
@@ -285,13 +287,12 @@ typedef struct moe_workspace_view {
     size_t tc_x_terms, tc_x_scale, tc_h_terms, tc_h_scale, tc_done;
     size_t total_bytes;
     int max_total, max_blocks, cap;
-    /* tensor-core paths only (else 0): the active table the alignment launch
-     * writes for them, [cap] x {run offset, expert, slot count, 0} int32; and,
-     * on the decode tensor-core path (M <= 16) when H > 512, the k-part
-     * partial sums of gate and up [H/128/4][M*top_k][2][I] float.  On that
-     * path tc_x_terms and tc_x_scale are 0: its x terms never leave shared
-     * memory. */
-    size_t tc_items, tc_part;
+    /* tensor-core path only (else 0): the active table the alignment launch
+     * writes for it, [cap] x {run offset, expert, slot count, 0} int32.  For
+     * M <= 16 the x terms are kept by token instead of by sorted row: the
+     * tc_x_terms region holds [H/128][2][16][128] u8 (k block, term, token,
+     * 128 k values) and tc_x_scale [16] float. */
+    size_t tc_items;
 } moe_workspace_view;
 
 /* Host only.  Workspace bytes moe_decode_layer needs for any M <= max_M

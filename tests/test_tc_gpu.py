@@ -1,6 +1,7 @@
 """The tensor-core (tcgen05) expert path of the decode MoE layer against the
-oracle: the decode kernel (M <= 16: k-split gate+up units, x terms built in
-shared memory, per-token blend) and the verify-batch kernel (M > 16).
+oracle, in both its forms: up to 16 rows the gate+up MMAs take the 16 token
+columns of a per-token x-term table (no grid barrier before the first
+copies), above that the item's own rows of x terms by sorted position.
 
 The path multiplies the E4M3 weight codes by E4M3 splits of the activations
 (x = t0 + t1 exactly, h = t0 + t1 + t2 to 12 significant bits, each with a
@@ -93,7 +94,7 @@ def _e4m3(t: torch.Tensor) -> torch.Tensor:
     return t.contiguous().view(torch.float8_e4m3fn).to(torch.float64)
 
 
-@pytest.mark.parametrize("M", [8, 32], ids=["decode_kernel", "verify_kernel"])
+@pytest.mark.parametrize("M", [8, 32], ids=["token_form", "row_form"])
 def test_tc_x_terms_exact_and_h_terms_bounded(moe, M):
     shape = _shape(f"decode_h2048_i768_e128_k8_fp8_m{M}", M, 2048, 768, 128, 8, 16)
     inp = synth.make_layer(shape, 321, device="cuda")
@@ -111,9 +112,13 @@ def test_tc_x_terms_exact_and_h_terms_bounded(moe, M):
     np.testing.assert_array_equal(items[:, 0], tables["expert_offsets"][act])
     counts = np.bincount(view["topk_ids"].cpu().numpy(), minlength=shape.E)
     np.testing.assert_array_equal(items[:, 2], counts[act])
-    assert ("tc_x_terms" in view) == (M > 16)   # the decode kernel keeps x terms on chip
     if M > 16:
         _check_x_terms(view, inp, pos_t, tok)
+    else:   # the token table: token t's terms are x[t] times its scale
+        table = view["tc_x_table"]                       # [H/128][2][16][128]
+        xq = table.permute(1, 2, 0, 3).reshape(2, 16, shape.H)[:, :M]
+        _check_x_terms(dict(tc_x_terms=xq, tc_x_scale=view["tc_x_scale"][:M]), inp,
+                       torch.arange(M, device="cuda"), np.arange(M))
     _check_h_terms(view, shape, pos_t, len(pos))
 
 
@@ -150,7 +155,7 @@ def _check_h_terms(view, shape, pos_t, npos):
 def test_tc_row_tile_edges(moe, rows):
     """Given ids (top_k = 1): expert 3 takes rows[0] tokens, expert 5 the next
     rows[1], and so on -- item boundaries at 16-row MMA steps and 64-row tiles
-    (M <= 16: the decode kernel; above: the verify-batch kernel)."""
+    (M <= 16: the token form's 16-row items)."""
     M = sum(rows)
     shape = _shape(f"tc_edges_m{M}", M, 256, 512, 8, 1, 16)
     inp = synth.make_layer(shape, 55, device="cuda")
@@ -169,7 +174,8 @@ def test_tc_row_tile_edges(moe, rows):
 
 def test_tc_repeated_expert_in_a_token(moe):
     """Given ids that list one expert twice in every token (top_k = 2, M = 16):
-    the expert's run holds 32 rows, two 16-row tiles on the decode kernel."""
+    the expert's run holds 32 rows, two 16-row items of the token form, each
+    row taking its token's column."""
     M = 16
     shape = _shape("tc_repeat_m16", M, 2048, 768, 16, 2, 16)
     inp = synth.make_layer(shape, 57, device="cuda")
@@ -187,7 +193,7 @@ def test_tc_repeated_expert_in_a_token(moe):
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
 
 
-@pytest.mark.parametrize("M", [8, 32], ids=["decode_kernel", "verify_kernel"])
+@pytest.mark.parametrize("M", [8, 32], ids=["token_form", "row_form"])
 def test_tc_deterministic_and_graph_replayable(moe, M):
     shape = _shape(f"decode_h2048_i768_e128_k8_fp8_m{M}", M, 2048, 768, 128, 8, 16)
     inp = synth.make_layer(shape, 9, device="cuda")
@@ -233,13 +239,14 @@ def test_tc_verify_batch_matches_staged_path(moe):
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
 
 
-@pytest.mark.parametrize("M,m", [(8, 1), (16, 1), (16, 5), (64, 17), (128, 33)], ids=str)
+@pytest.mark.parametrize("M,m", [(8, 1), (16, 1), (16, 5), (64, 17), (64, 1), (128, 33)],
+                         ids=str)
 def test_tc_row_invariance(moe, M, m):
     """On the tensor-core path the first m rows' output bits are the same
-    whether the batch has m or M rows, within one kernel family (decode: M <=
-    16; verify batch: M > 16): each row has its own x scale, every MMA column
-    is one row, the k parts of a tile are summed in a fixed order, and
-    promotion, SiLU, the h scales and the blend are per row."""
+    whether the batch has m or M rows, across the token form (M <= 16) and
+    the row form alike: each row has its own x scale (its token's), every MMA
+    column is one row or one token, and promotion, SiLU, the h scales and the
+    blend are per row."""
     shape = _shape(f"decode_h2048_i768_e128_k8_fp8_m{M}", M, 2048, 768, 128, 8, 16)
     inp = synth.make_layer(shape, 1000, device="cuda")
     out_m, _, _ = H.gpu_layer(moe, inp, path=TC)
