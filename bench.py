@@ -607,10 +607,11 @@ def time_e2e(moe, shape, layer, x_host, logits_host, out_host, ws, K: int, W: in
 
 
 def oracle_experts(d):
-    """synth expert data -> the oracle's host structures."""
+    """synth expert data -> the oracle's host structures (each projection in
+    its own format)."""
     import oracle
-    fmt = oracle.FMT_FP8_B128 if d.fmt == "fp8" else oracle.FMT_NVFP4_G16
-    P = lambda p: oracle.Proj(fmt, p.rows, p.cols, p.codes.cpu().numpy(), p.scale.cpu().numpy(),
+    P = lambda p: oracle.Proj(oracle.FMT_FP8_B128 if p.fmt == "fp8" else oracle.FMT_NVFP4_G16,
+                              p.rows, p.cols, p.codes.cpu().numpy(), p.scale.cpu().numpy(),
                               None if p.glob is None else p.glob.cpu().numpy())
     return oracle.Experts(d.E, d.H, d.I, P(d.gate), P(d.up), P(d.down))
 

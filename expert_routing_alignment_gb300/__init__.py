@@ -31,6 +31,7 @@ MOE_ERR_BAD_ID = 0x1
 
 FMT_FP8_B128 = 1
 FMT_NVFP4_G16 = 2
+FMT_NVFP4_GATE_UP = 3   # gate and up NVFP4_G16, down FP8_B128
 PATH_AUTO = 0
 PATH_SIMT = 1
 PATH_TC = 2
@@ -38,6 +39,7 @@ PATH_SIMT_STAGED = 3
 MOE_ERR_TIMEOUT = 0x2
 MAX_EXPERTS = 1024
 MAX_ROWS = 128
+MAX_ROWS_TC = 4096   # M admitted on the tensor-core path (FP8 experts)
 TOKEN_FORM_ROWS = 16   # tensor-core path: up to this M, x terms are kept by token
 
 LIB_PATH = _build.LIB
@@ -176,7 +178,8 @@ class Experts:
     @staticmethod
     def from_synth(d) -> "Experts":
         """From a ``synth.ExpertData`` already on the device."""
-        fmt = FMT_FP8_B128 if d.fmt == "fp8" else FMT_NVFP4_G16
+        fmt = {"fp8": FMT_FP8_B128, "nvfp4": FMT_NVFP4_G16,
+               "nvfp4_gate_up": FMT_NVFP4_GATE_UP}[d.fmt]
         t = lambda p: (p.codes, p.scale, p.glob)
         return Experts(fmt, d.E, d.H, d.I, t(d.gate), t(d.up), t(d.down))
 

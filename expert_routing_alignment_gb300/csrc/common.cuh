@@ -87,6 +87,14 @@ int launch_pdl_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem
 
 inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// The format of one projection of an expert set (0 gate, 1 up, 2 down): the
+// set's format, except under the nvfp4-gate-up tier (NVFP4 gate and up, FP8
+// down).
+inline int proj_fmt(int set_fmt, int proj) {
+  if (set_fmt == MOE_FMT_NVFP4_GATE_UP) return proj == 2 ? MOE_FMT_FP8_B128 : MOE_FMT_NVFP4_G16;
+  return set_fmt;
+}
+
 // ---------------------------------------------------------------------------
 // device side
 // ---------------------------------------------------------------------------

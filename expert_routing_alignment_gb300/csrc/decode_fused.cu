@@ -1038,6 +1038,9 @@ bool plan_shape(const moe_layer_desc *L, int M, int sms, Shape &sp) {
   const moe_experts *S = L->shared;
   const int n = M * L->top_k;
   if (n > kMaxN || M > kMaxM || L->top_k > 32 || sms < 1 || R.num_experts > 1024) return false;
+  // one format per expert set: the nvfp4-gate-up tier runs on the staged
+  // kernels, which take each projection in its own format
+  if (R.fmt == MOE_FMT_NVFP4_GATE_UP || (S && S->fmt == MOE_FMT_NVFP4_GATE_UP)) return false;
   const int H = R.hidden;
   // K and R multiples of 128 in [256, 2048] (NVFP4: K of 256, so that a code
   // row is whole 128-byte boxes and a scale row whole 16-byte boxes)

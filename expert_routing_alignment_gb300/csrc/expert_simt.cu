@@ -466,25 +466,28 @@ int launch_down_fmt(const GroupArgs &a, int cpl, void *stream) {
 // Validation shared with the layer: 0 = ok.
 int validate_experts(const moe_experts *X, bool shared) {
   if (!X) return MOE_EINVAL;
-  if (X->fmt != MOE_FMT_FP8_B128 && X->fmt != MOE_FMT_NVFP4_G16) return MOE_EINVAL;
+  if (X->fmt != MOE_FMT_FP8_B128 && X->fmt != MOE_FMT_NVFP4_G16 &&
+      X->fmt != MOE_FMT_NVFP4_GATE_UP)
+    return MOE_EINVAL;
   if (X->num_experts < 1 || X->hidden < 1 || X->inter < 1) return MOE_EINVAL;
   if (shared && X->num_experts != 1) return MOE_EINVAL;
   if (X->num_experts > MOE_MAX_EXPERTS) return MOE_EUNSUPPORTED;
   const moe_proj *P[3] = {&X->gate, &X->up, &X->down};
-  for (const moe_proj *p : P) {
+  for (int j = 0; j < 3; ++j) {
+    const moe_proj *p = P[j];
+    const int f = proj_fmt(X->fmt, j);
     if (!p->codes || !p->scale) return MOE_EINVAL;
-    if (X->fmt == MOE_FMT_NVFP4_G16 && !p->global_scale) return MOE_EINVAL;
+    if (f == MOE_FMT_NVFP4_G16 && !p->global_scale) return MOE_EINVAL;
     if (((uintptr_t)p->codes & 15) != 0) return MOE_EINVAL;
-    if (X->fmt == MOE_FMT_NVFP4_G16 && ((uintptr_t)p->scale & 1) != 0) return MOE_EINVAL;
-    if (X->fmt == MOE_FMT_FP8_B128 && ((uintptr_t)p->scale & 3) != 0) return MOE_EINVAL;
+    if (f == MOE_FMT_NVFP4_G16 && ((uintptr_t)p->scale & 1) != 0) return MOE_EINVAL;
+    if (f == MOE_FMT_FP8_B128 && ((uintptr_t)p->scale & 3) != 0) return MOE_EINVAL;
   }
-  if (X->fmt == MOE_FMT_FP8_B128) {
-    if (X->hidden % 128 || X->inter % 128) return MOE_EUNSUPPORTED;
-  } else {
-    if (X->hidden % 32 || X->inter % 32) return MOE_EUNSUPPORTED;
-  }
-  if (cpl_bucket(chunks_per_lane(X->fmt, X->hidden)) == 0 ||
-      cpl_bucket(chunks_per_lane(X->fmt, X->inter)) == 0)
+  // FP8 projections need 128-wide blocks on both sides, NVFP4 ones 32
+  const int fg = proj_fmt(X->fmt, 0), fd = proj_fmt(X->fmt, 2);
+  const int qh = (fg == MOE_FMT_FP8_B128 || fd == MOE_FMT_FP8_B128) ? 128 : 32;
+  if (X->hidden % qh || X->inter % qh) return MOE_EUNSUPPORTED;
+  if (cpl_bucket(chunks_per_lane(fg, X->hidden)) == 0 ||
+      cpl_bucket(chunks_per_lane(fd, X->inter)) == 0)
     return MOE_EUNSUPPORTED;
   if ((size_t)kRowsPerPass * (X->hidden > X->inter ? X->hidden : X->inter) * 4 > 200 * 1024)
     return MOE_EUNSUPPORTED;
@@ -554,10 +557,11 @@ int simt_gate_up(const moe_experts *routed, const moe_experts *shared, const uin
   a.x = x;
   a.out = h;
   a.out_sh = h_sh;
-  int need = chunks_per_lane(routed->fmt, routed->hidden);
-  if (shared) need = max(need, chunks_per_lane(shared->fmt, shared->hidden));
-  const int sf = shared ? shared->fmt : routed->fmt;
-  return MOE_DISPATCH_FMT(routed->fmt, sf, launch_gate_up_fmt, a, cpl_bucket(need), stream);
+  const int rf = proj_fmt(routed->fmt, 0);
+  const int sf = shared ? proj_fmt(shared->fmt, 0) : rf;
+  int need = chunks_per_lane(rf, routed->hidden);
+  if (shared) need = max(need, chunks_per_lane(sf, shared->hidden));
+  return MOE_DISPATCH_FMT(rf, sf, launch_gate_up_fmt, a, cpl_bucket(need), stream);
 }
 
 int simt_down(const moe_experts *routed, const moe_experts *shared, const float *h,
@@ -571,10 +575,11 @@ int simt_down(const moe_experts *routed, const moe_experts *shared, const float 
   a.hin_sh = h_sh;
   a.out = y;
   a.out_sh = y_sh;
-  int need = chunks_per_lane(routed->fmt, routed->inter);
-  if (shared) need = max(need, chunks_per_lane(shared->fmt, shared->inter));
-  const int sf = shared ? shared->fmt : routed->fmt;
-  return MOE_DISPATCH_FMT(routed->fmt, sf, launch_down_fmt, a, cpl_bucket(need), stream);
+  const int rf = proj_fmt(routed->fmt, 2);
+  const int sf = shared ? proj_fmt(shared->fmt, 2) : rf;
+  int need = chunks_per_lane(rf, routed->inter);
+  if (shared) need = max(need, chunks_per_lane(sf, shared->inter));
+  return MOE_DISPATCH_FMT(rf, sf, launch_down_fmt, a, cpl_bucket(need), stream);
 }
 
 }  // namespace moe

@@ -91,7 +91,9 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   if (L->shared_gate && (!L->shared || ((uintptr_t)L->shared_gate & 15))) return MOE_EINVAL;
   const int E = L->routed.num_experts, k = L->top_k;
   if (M < 1 || k < 1 || k > E || L->block_size < 1) return MOE_EINVAL;
-  if (M > MOE_MAX_ROWS || k > 32) return MOE_EUNSUPPORTED;
+  if (k > 32 || M > MOE_MAX_ROWS_TC) return MOE_EUNSUPPORTED;
+  // above MOE_MAX_ROWS only the tensor-core path (prefill-sized batches)
+  if (M > MOE_MAX_ROWS && layer_run(L, M) != kRunTc) return MOE_EUNSUPPORTED;
   const int n = M * k;
   int max_total, max_blocks, cap;
   st = moe_align_sizes(n, E, L->block_size, &max_total, &max_blocks, &cap);

@@ -54,6 +54,11 @@ extern "C" {
 /* ---- formats and paths -------------------------------------------------- */
 #define MOE_FMT_FP8_B128 1  /* E4M3 codes, fp32 scale per 128x128 block      */
 #define MOE_FMT_NVFP4_G16 2 /* E2M1 codes, E4M3 scale per 16, fp32 global    */
+/* The "nvfp4-gate-up" tier ("forward_nvfp4_grouped_decode.rs", module notes
+ * and the down-projection choice in forward_nvfp4_grouped_decode): gate and
+ * up in NVFP4_G16, the down projection in FP8_B128.  hidden and inter must be
+ * multiples of 128. */
+#define MOE_FMT_NVFP4_GATE_UP 3
 
 #define MOE_PATH_AUTO 0     /* chosen per shape class (never per routing)    */
 #define MOE_PATH_SIMT 1     /* CUDA-core kernels, in-register dequant         */
@@ -65,9 +70,13 @@ extern "C" {
 #define MOE_MAX_EXPERTS 1024      /* experts the alignment handles            */
 #define MOE_MAX_SLOTS (1 << 20)   /* n = M * top_k the alignment handles      */
 #define MOE_MAX_ROWS 128          /* M the expert kernels and layer admit     */
+#define MOE_MAX_ROWS_TC 4096      /* M the layer admits on the tensor-core path
+                                     (prefill-sized batches of FP8 experts)     */
 
 /* One projection of all experts of a set.  Layout for `rows` x `cols`
- * (gate/up: rows = inter, cols = hidden; down: rows = hidden, cols = inter):
+ * (gate/up: rows = inter, cols = hidden; down: rows = hidden, cols = inter),
+ * by the projection's format (the set's format, except that under
+ * MOE_FMT_NVFP4_GATE_UP gate and up are NVFP4_G16 and down is FP8_B128):
  *   FP8_B128:  codes  uint8 [E][rows][cols] E4M3;
  *              scale  float [E][rows/128][cols/128], w = e4m3(code) * scale;
  *              global_scale unused (NULL).
@@ -343,7 +352,8 @@ int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logit
  *   (the blend_counters region) that every call leaves consistent for the
  *   next.  After a call that reported MOE_ERR_TIMEOUT, zero it again.
  * Shape admission (host, nothing launched on failure):
- *   1 <= M <= MOE_MAX_ROWS, 1 <= top_k <= min(E, 32), E <= MOE_MAX_EXPERTS,
+ *   1 <= M <= MOE_MAX_ROWS (MOE_MAX_ROWS_TC when the layer runs on the
+ *   tensor-core path), 1 <= top_k <= min(E, 32), E <= MOE_MAX_EXPERTS,
  *   block_size >= 1, and the format's hidden/inter rules.
  * Errors: MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA. */
 int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,

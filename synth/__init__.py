@@ -34,6 +34,7 @@ import torch
 
 FMT_FP8 = "fp8"
 FMT_NVFP4 = "nvfp4"
+FMT_NVFP4_GATE_UP = "nvfp4_gate_up"   # gate and up NVFP4, down FP8
 
 E4M3_MAX = 448.0
 E2M1_MAX = 6.0
@@ -72,6 +73,13 @@ def decode_fp8(M: int) -> LayerShape:
 def decode_nvfp4(M: int) -> LayerShape:
     return LayerShape(f"decode_h2048_i768_e128_k8_nvfp4_shared512_m{M}", M, 2048, 768, 128, 8,
                       16, FMT_NVFP4, shared_I=512)
+
+
+def decode_nvfp4_gate_up(M: int) -> LayerShape:
+    """The same 128-expert shape under the nvfp4-gate-up tier: NVFP4 gate and
+    up, FP8 down, and the FP8 shared expert of inter 512."""
+    return LayerShape(f"decode_h2048_i768_e128_k8_nvfp4gu_shared512_m{M}", M, 2048, 768, 128, 8,
+                      16, FMT_NVFP4_GATE_UP, shared_I=512)
 
 
 # Zipf bias strength for the verify batch: log-pmf times this scale.  With
@@ -187,12 +195,15 @@ def _proj(E: int, rows: int, cols: int, fmt: str, gen: torch.Generator, device,
 
 def make_experts(E: int, H: int, I: int, fmt: str, seed: int, device="cpu",
                  std: float = 0.02) -> ExpertData:
-    """E experts, gate/up [I, H] and down [H, I], from N(0, std) encoded as fmt."""
+    """E experts, gate/up [I, H] and down [H, I], from N(0, std) encoded as fmt
+    (FMT_NVFP4_GATE_UP: gate and up as NVFP4, down as FP8)."""
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
-    gate = _proj(E, I, H, fmt, gen, device, std)
-    up = _proj(E, I, H, fmt, gen, device, std)
-    down = _proj(E, H, I, fmt, gen, device, std)
+    gu_fmt = FMT_NVFP4 if fmt == FMT_NVFP4_GATE_UP else fmt
+    dn_fmt = FMT_FP8 if fmt == FMT_NVFP4_GATE_UP else fmt
+    gate = _proj(E, I, H, gu_fmt, gen, device, std)
+    up = _proj(E, I, H, gu_fmt, gen, device, std)
+    down = _proj(E, H, I, dn_fmt, gen, device, std)
     return ExpertData(E, H, I, fmt, gate, up, down)
 
 

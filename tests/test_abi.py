@@ -191,7 +191,16 @@ def test_layer_rejects_rows_and_topk():
     layer = moe.LayerDesc(top_k=8, block_size=16, routed=_fake_experts())
     p = ctypes.pointer(layer._struct)
     assert lib.moe_decode_layer_workspace_view(p, 0, ctypes.byref(v)) == moe.MOE_EINVAL
-    assert lib.moe_decode_layer_workspace_view(p, 129, ctypes.byref(v)) == moe.MOE_EUNSUPPORTED
+    # above 128 rows only on the tensor-core path, up to 4096
+    assert lib.moe_decode_layer_workspace_view(p, 129, ctypes.byref(v)) == 0
+    assert lib.moe_decode_layer_workspace_view(p, 4096, ctypes.byref(v)) == 0
+    assert lib.moe_decode_layer_workspace_view(p, 4097, ctypes.byref(v)) == moe.MOE_EUNSUPPORTED
+    simt = moe.LayerDesc(top_k=8, block_size=16, path=moe.PATH_SIMT, routed=_fake_experts())
+    assert lib.moe_decode_layer_workspace_view(ctypes.pointer(simt._struct), 129,
+                                               ctypes.byref(v)) == moe.MOE_EUNSUPPORTED
+    nv = moe.LayerDesc(top_k=8, block_size=16, routed=_fake_experts(fmt=moe.FMT_NVFP4_G16))
+    assert lib.moe_decode_layer_workspace_view(ctypes.pointer(nv._struct), 129,
+                                               ctypes.byref(v)) == moe.MOE_EUNSUPPORTED
     bad_k = moe.LayerDesc(top_k=200, block_size=16, routed=_fake_experts())
     assert lib.moe_decode_layer_workspace_view(ctypes.pointer(bad_k._struct), 8,
                                                ctypes.byref(v)) == moe.MOE_EINVAL

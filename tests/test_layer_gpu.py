@@ -320,3 +320,69 @@ def test_decode_experts_on_tables_in_the_workspace(moe, path, M):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(third.view(torch.int16), ref2.view(torch.int16))
+
+
+@pytest.mark.parametrize("path", [0, 1, 3], ids=["auto", "simt", "staged"])
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_nvfp4_gate_up_tier_matches_oracle(moe, M, path):
+    """The nvfp4-gate-up tier (NVFP4 gate and up, FP8 down, FP8 shared expert)
+    runs on the staged CUDA-core kernels, each projection in its own format:
+    the layer output within the layer tolerance of the oracle, h and y within
+    the stage tolerance of the oracle's stages, and row 0 the same bits at M
+    rows as alone."""
+    shape = synth.decode_nvfp4_gate_up(M)
+    inp = layer_inputs(shape)
+    out, view, (layer, _) = H.gpu_layer(moe, inp, path=path)
+    assert moe.moe_decode_layer_launches(layer, M) == 5
+    _, ref_b, bad = H.oracle_layer(inp)
+    assert bad == 0
+    rl2, mx = H.compare_bf16(out, ref_b)
+    assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
+    tables = oracle.align(view["topk_ids"].cpu().numpy(), shape.E, shape.BS)
+    real = tables["sorted_token_ids"] < shape.n
+    X = H.oracle_experts(inp.experts.to("cpu"))
+    S = H.oracle_experts(inp.shared.to("cpu"))
+    h_ref, hs_ref = oracle.grouped_gate_up(X, S, synth.bf16_bits(inp.x), M, shape.top_k, tables)
+    h_gpu = view["h"].cpu().numpy().astype(np.float64)
+    assert H.rel_l2(h_gpu[real], h_ref[real]) < H.STAGE_REL_L2
+    hs_gpu = view["h_shared"].cpu().numpy().astype(np.float64)
+    assert H.rel_l2(hs_gpu, hs_ref) < H.STAGE_REL_L2
+    y_ref, ys_ref = oracle.grouped_down(X, S, h_gpu, hs_gpu, M, shape.top_k, tables)
+    assert H.rel_l2(view["y"].cpu().numpy().astype(np.float64)[real], y_ref[real]) < H.STAGE_REL_L2
+    assert H.rel_l2(view["y_shared"].cpu().numpy(), ys_ref) < H.STAGE_REL_L2
+    one = synth.LayerInputs(
+        synth.LayerShape(shape.name + "_row0", 1, shape.H, shape.I, shape.E, shape.top_k,
+                         shape.BS, shape.fmt, shape.shared_I),
+        inp.x[:1].contiguous(), inp.logits[:1].contiguous(), inp.experts, inp.shared)
+    out_1, _, _ = H.gpu_layer(moe, one, path=path)
+    assert torch.equal(out[:1].view(torch.int16), out_1.view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [256, 1024])
+def test_prefill_batch_sampled_rows(moe, M):
+    """Prefill-sized batches (M > 128, FP8 experts of the verify shape: H=4096,
+    I=1536, E=256, k=8, BS=64) run on the tensor-core path: the alignment's
+    tables bit-exact, and sampled rows within the layer tolerance of the
+    oracle (each row's output depends on that row only)."""
+    shape = synth.LayerShape(f"prefill_h4096_i1536_e256_k8_fp8_m{M}", M, 4096, 1536, 256, 8, 64,
+                             synth.FMT_FP8)
+    inp = layer_inputs(shape)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, view, (layer, _) = H.gpu_layer(moe, inp, err=err)
+    assert moe.moe_decode_layer_launches(layer, M) == 3
+    assert int(err.item()) == 0
+    rid, rw = oracle.topk_softmax(inp.logits.cpu().numpy(), shape.top_k)
+    np.testing.assert_array_equal(view["topk_ids"].cpu().numpy(), rid.ravel())
+    tables = oracle.align(rid.ravel(), shape.E, shape.BS)
+    for key in ("sorted_token_ids", "expert_offsets", "token_to_perm", "sorted_expert_ids",
+                "active_experts"):
+        np.testing.assert_array_equal(view[key].cpu().numpy(), tables[key], err_msg=key)
+    rows = [0, 1, M // 3, M // 2 + 7, M - 1]
+    uniq = sorted(set(rid[rows].ravel().tolist()))
+    remap = {e: i for i, e in enumerate(uniq)}
+    X = H.oracle_experts(H.subset_experts(inp.experts, uniq))
+    ids_sub = np.vectorize(remap.get)(rid[rows]).astype(np.int32)
+    _, ref_b, _ = oracle.moe_layer(X, None, synth.bf16_bits(inp.x[rows]), len(rows),
+                                   shape.top_k, shape.BS, ids=ids_sub, w=rw[rows])
+    rl2, mx = H.compare_bf16(out[rows], ref_b)
+    assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)

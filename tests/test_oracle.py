@@ -336,7 +336,11 @@ def _small_inputs(fmt, shared, M=4, H=256, I=256, E=8, k=2, seed=21):
     return synth.make_layer(shape, seed)
 
 
-@pytest.mark.parametrize("fmt,shared", [(synth.FMT_FP8, False), (synth.FMT_NVFP4, True)])
+# (the nvfp4-gate-up tier: NVFP4 gate and up, FP8 down, with an FP8 shared expert)
+FMT_CASES = [(synth.FMT_FP8, False), (synth.FMT_NVFP4, True), (synth.FMT_NVFP4_GATE_UP, True)]
+
+
+@pytest.mark.parametrize("fmt,shared", FMT_CASES)
 def test_grouped_stages_match_torch(fmt, shared):
     inp = _small_inputs(fmt, shared)
     s = inp.shape
@@ -369,7 +373,7 @@ def test_grouped_stages_match_torch(fmt, shared):
     np.testing.assert_array_equal(out_b, oracle.bf16_round_array(out_d))
 
 
-@pytest.mark.parametrize("fmt,shared", [(synth.FMT_FP8, False), (synth.FMT_NVFP4, True)])
+@pytest.mark.parametrize("fmt,shared", FMT_CASES)
 def test_layer_matches_torch(fmt, shared):
     inp = _small_inputs(fmt, shared, M=5, seed=33)
     s = inp.shape
