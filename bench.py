@@ -26,7 +26,9 @@ host core and on all of them (threads over the rows of the layer calls).
 The line also carries `align_grid`: µs per moe_align call over the alignment
 stress grid (n = 8·{1, 64, 1024, 4096}, E in {64, 256, 1024}, BS in {16, 64, 128},
 uniform ids); `nvfp4_decode`: the NVFP4 layer with its FP8 shared expert at
-M in {1, 8, 32} (the fused CUDA-core kernel) and at M=64 (the staged kernels).
+M in {1, 8, 32} (the fused CUDA-core kernel) and at M=64 (the staged kernels);
+`nvfp4_gate_up_tier`: the layer with NVFP4 gate and up and FP8 down at M=8;
+`prefill`: M in {512, 2048} rows of the verify shape on the tensor cores.
 
 The line also carries `router_logits`: the router matrix-vector product ahead of the
 top-k (bf16 x times bf16 router weights) at the decode and verify widths, timed over
@@ -480,6 +482,83 @@ def run_nvfp4_decode(moe, stream, K: int, W: int, peaks: dict) -> dict:
     return dict(workload="decode_h2048_i768_e128_k8_nvfp4_shared512", steps=K, rows=rows)
 
 
+def run_nvfp4_gate_up(moe, stream, M: int, K: int, W: int, peaks: dict) -> dict:
+    """The nvfp4-gate-up tier (NVFP4 gate and up, FP8 down, FP8 shared expert
+    of inter 512) at M rows: K graph-replayed steps over 4 weight copies,
+    fresh logits every step (the staged CUDA-core kernels)."""
+    import synth
+    shape = synth.decode_nvfp4_gate_up(M)
+    base = synth.make_experts(shape.E, shape.H, shape.I, shape.fmt, SEED + 20, "cuda")
+    sh = synth.make_experts(1, shape.H, shape.shared_I, synth.FMT_FP8, SEED + 21, "cuda")
+    copies = [base] + [_clone_experts(base) for _ in range(3)]
+    shared = moe.Experts.from_synth(sh)
+    layers = [moe.LayerDesc(top_k=shape.top_k, block_size=shape.BS,
+                            routed=moe.Experts.from_synth(c), shared=shared) for c in copies]
+    x = synth.make_x(M, shape.H, SEED + 22, "cuda")
+    logits = torch.stack([synth.make_logits(M, shape.E, SEED + 900 + s, "cuda")
+                          for s in range(K)])
+    ws = moe.alloc_workspace(layers[0], M)
+    out = torch.empty(M, shape.H, dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(stream):
+        for s in range(W):
+            moe.moe_decode_layer(layers[s % 4], x, out, ws, router_logits=logits[s % K])
+    stream.synchronize()
+    ms = _graph_ms(stream, K, lambda s: moe.moe_decode_layer(layers[s % 4], x, out, ws,
+                                                             router_logits=logits[s]))
+    n_act = active_expert_counts(logits, shape.top_k)
+    nbytes = float(np.mean([layer_bytes(shape, base, a) for a in n_act])) + sh.bytes_per_expert()
+    us = 1e3 * ms
+    gbs = nbytes / (us * 1e-6) / 1e9
+    res = dict(workload=shape.name, M=M, steps=K, us_per_layer=round(us, 3),
+               tokens_per_s=round(M / (us * 1e-6), 1), weight_stream_gbs=round(gbs, 1),
+               pct_of_measured_hbm=round(100 * gbs / peaks["hbm_gbs"], 1),
+               launches_per_layer=moe.moe_decode_layer_launches(layers[0], M),
+               algorithmic_bytes_per_layer=int(nbytes))
+    del copies, layers, base, sh, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_prefill(moe, stream, M: int, K: int, W: int, peaks: dict) -> dict:
+    """A prefill-sized batch on the tensor-core path: M rows of the verify
+    shape (H=4096, I=1536, E=256, k=8, BS=64, uniform N(0,1) logits, fresh
+    every step), K graph-replayed steps over 2 weight copies of 4.8 GB.
+    Reported as tokens/s, effective TFLOP/s (2 n 3 H I per layer, the
+    products the layer asks for) and weight-stream GB/s."""
+    import synth
+    shape = synth.LayerShape(f"prefill_h4096_i1536_e256_k8_fp8_m{M}", M, 4096, 1536, 256, 8, 64,
+                             synth.FMT_FP8)
+    base = synth.make_experts(shape.E, shape.H, shape.I, shape.fmt, SEED + 30, "cuda")
+    copies = [base, _clone_experts(base)]
+    layers = [moe.LayerDesc(top_k=shape.top_k, block_size=shape.BS,
+                            routed=moe.Experts.from_synth(c)) for c in copies]
+    x = synth.make_x(M, shape.H, SEED + 31, "cuda")
+    logits = torch.stack([synth.make_logits(M, shape.E, SEED + 1000 + s, "cuda")
+                          for s in range(K)])
+    ws = moe.alloc_workspace(layers[0], M)
+    out = torch.empty(M, shape.H, dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(stream):
+        for s in range(W):
+            moe.moe_decode_layer(layers[s % 2], x, out, ws, router_logits=logits[s % K])
+    stream.synchronize()
+    ms = _graph_ms(stream, K, lambda s: moe.moe_decode_layer(layers[s % 2], x, out, ws,
+                                                             router_logits=logits[s]))
+    n_act = active_expert_counts(logits, shape.top_k)
+    nbytes = float(np.mean([layer_bytes(shape, base, a) for a in n_act]))
+    us = 1e3 * ms
+    flops = 2.0 * shape.n * 3 * shape.H * shape.I
+    res = dict(workload=shape.name, M=M, steps=K, us_per_layer=round(us, 3),
+               tokens_per_s=round(M / (us * 1e-6), 1),
+               effective_tflops=round(flops / (us * 1e-6) / 1e12, 1),
+               weight_stream_gbs=round(nbytes / (us * 1e-6) / 1e9, 1),
+               mean_active_experts=round(float(np.mean(n_act)), 2),
+               launches_per_layer=moe.moe_decode_layer_launches(layers[0], M),
+               path="tensor cores: verify_ffn_kernel")
+    del copies, layers, base, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_align_grid(moe, stream) -> list:
     """µs per moe_align call over the alignment stress grid (uniform int64
     ids): 32 calls in one CUDA graph, rotating over 4 id sets."""
@@ -809,6 +888,10 @@ def run_gpu(args, rank: int, world: int):
     gated = None if args.no_verify else run_gated_shared(moe, stream, 8, min(K, 16), 3, peaks)
     nvfp4 = None if args.no_verify else run_nvfp4_decode(moe, stream, min(K, 16), 3, peaks)
     align_grid = None if args.no_verify else run_align_grid(moe, stream)
+    gate_up_tier = None if args.no_verify else run_nvfp4_gate_up(moe, stream, 8, min(K, 16), 3,
+                                                                   peaks)
+    prefill = None if args.no_verify else [run_prefill(moe, stream, m, 8, 3, peaks)
+                                           for m in (512, 2048)]
     # max over ranks
     ms_t = torch.tensor([results["ms"]], device="cuda")
     if world > 1:
@@ -837,6 +920,8 @@ def run_gpu(args, rank: int, world: int):
         hidden_in=hidden_in,
         gated_shared=gated,
         nvfp4_decode=nvfp4,
+        nvfp4_gate_up_tier=gate_up_tier,
+        prefill=prefill,
         align_grid=align_grid,
         roofline=dict(bound="hbm",
                       kernel=KERNELS[r["kernel"]][0],
