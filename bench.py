@@ -730,8 +730,8 @@ def cpu_baseline(shape, base, x, logits, budget_s: float = 8.0) -> dict:
     lg = logits.cpu().numpy()
     threads = max(1, min(os.cpu_count() or 1, shape.M))
     calls, dt = _oracle_rows(X, xb, lg, shape.M, shape.top_k, shape.BS, threads, budget_s,
-                             len(lg))
-    calls1, dt1 = _oracle_rows(X, xb, lg, shape.M, shape.top_k, shape.BS, 1, budget_s, len(lg))
+                             1 << 20)
+    calls1, dt1 = _oracle_rows(X, xb, lg, shape.M, shape.top_k, shape.BS, 1, budget_s, 1 << 20)
     return dict(value=shape.M * calls / dt, unit="tokens/s", cores=threads, kind="oracle",
                 host_cpus=os.cpu_count(),
                 sample=f"{calls} whole layer calls of {shape.name} ({shape.M} rows each, one "
