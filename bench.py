@@ -440,44 +440,57 @@ def _graph_ms(stream, K: int, body) -> float:
 def run_nvfp4_decode(moe, stream, K: int, W: int, peaks: dict) -> dict:
     """The NVFP4 layer with its FP8 shared expert (inter 512) at M in {1, 8, 32}
     and 64: K graph-replayed steps over 4 weight copies of 340 MB, fresh
-    logits every step, ungated.  M <= 32 runs the fused CUDA-core kernel; M=64
-    the staged CUDA-core kernels (the shapes outside the fused admission)."""
+    logits every step, ungated.  M <= 32 runs both on the NVFP4 tensor-core
+    kernel (after the shared expert's two CUDA-core kernels) and on the fused
+    CUDA-core kernel, each row naming its path and whether the layer's
+    default takes it; M=64 the staged CUDA-core kernels."""
     import synth
     shape0 = synth.decode_nvfp4(1)
     base = synth.make_experts(shape0.E, shape0.H, shape0.I, shape0.fmt, SEED + 8, "cuda")
     sh = synth.make_experts(1, shape0.H, shape0.shared_I, synth.FMT_FP8, SEED + 9, "cuda")
     copies = [base] + [_clone_experts(base) for _ in range(3)]
     shared = moe.Experts.from_synth(sh)
-    layers = [moe.LayerDesc(top_k=shape0.top_k, block_size=shape0.BS,
-                            routed=moe.Experts.from_synth(c), shared=shared) for c in copies]
+
+    def layers_for(path):
+        return [moe.LayerDesc(top_k=shape0.top_k, block_size=shape0.BS,
+                              routed=moe.Experts.from_synth(c), shared=shared, path=path)
+                for c in copies]
+
+    by_path = {"tc": layers_for(moe.PATH_TC), "fused": layers_for(moe.PATH_SIMT),
+               "auto": layers_for(moe.PATH_AUTO)}
     rows = []
     for M in (1, 8, 32, 64):
         shape = synth.decode_nvfp4(M)
         x = synth.make_x(M, shape.H, SEED + 11, "cuda")
         logits = torch.stack([synth.make_logits(M, shape.E, SEED + 800 + s, "cuda")
                               for s in range(K)])
-        ws = moe.alloc_workspace(layers[0], M)
-        out = torch.empty(M, shape.H, dtype=torch.bfloat16, device="cuda")
-        with torch.cuda.stream(stream):
-            for s in range(W):
-                moe.moe_decode_layer(layers[s % 4], x, out, ws, router_logits=logits[s % K])
-        stream.synchronize()
-        ms = _graph_ms(stream, K, lambda s: moe.moe_decode_layer(layers[s % 4], x, out, ws,
-                                                                 router_logits=logits[s]))
         n_act = active_expert_counts(logits, shape.top_k)
         nbytes = float(np.mean([layer_bytes(shape, base, a) for a in n_act])) + \
             sh.bytes_per_expert()
-        us = 1e3 * ms
-        gbs = nbytes / (us * 1e-6) / 1e9
-        launches = moe.moe_decode_layer_launches(layers[0], M)
-        rows.append(dict(M=M, us_per_layer=round(us, 3), tokens_per_s=round(M / (us * 1e-6), 1),
-                         weight_stream_gbs=round(gbs, 1),
-                         pct_of_measured_hbm=round(100 * gbs / peaks["hbm_gbs"], 1),
-                         launches_per_layer=launches,
-                         mean_active_experts=round(float(np.mean(n_act)), 2),
-                         algorithmic_bytes_per_layer=int(nbytes)))
-        del ws
-    del copies, layers, base, sh
+        auto_launches = moe.moe_decode_layer_launches(by_path["auto"][0], M)
+        for name in (("tc", "fused") if M <= 32 else ("auto",)):
+            layers = by_path[name]
+            ws = moe.alloc_workspace(layers[0], M)
+            out = torch.empty(M, shape.H, dtype=torch.bfloat16, device="cuda")
+            with torch.cuda.stream(stream):
+                for s in range(W):
+                    moe.moe_decode_layer(layers[s % 4], x, out, ws, router_logits=logits[s % K])
+            stream.synchronize()
+            ms = _graph_ms(stream, K, lambda s: moe.moe_decode_layer(
+                layers[s % 4], x, out, ws, router_logits=logits[s]))
+            us = 1e3 * ms
+            gbs = nbytes / (us * 1e-6) / 1e9
+            launches = moe.moe_decode_layer_launches(layers[0], M)
+            rows.append(dict(M=M, path=name if name != "auto" else "staged",
+                             default=name == "auto" or launches == auto_launches,
+                             us_per_layer=round(us, 3), tokens_per_s=round(M / (us * 1e-6), 1),
+                             weight_stream_gbs=round(gbs, 1),
+                             pct_of_measured_hbm=round(100 * gbs / peaks["hbm_gbs"], 1),
+                             launches_per_layer=launches,
+                             mean_active_experts=round(float(np.mean(n_act)), 2),
+                             algorithmic_bytes_per_layer=int(nbytes)))
+            del ws
+    del copies, by_path, base, sh
     torch.cuda.empty_cache()
     return dict(workload="decode_h2048_i768_e128_k8_nvfp4_shared512", steps=K, rows=rows)
 

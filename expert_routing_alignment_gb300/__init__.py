@@ -41,6 +41,8 @@ MAX_EXPERTS = 1024
 MAX_ROWS = 128
 MAX_ROWS_TC = 4096   # M admitted on the tensor-core path (FP8 experts)
 TOKEN_FORM_ROWS = 16   # tensor-core path: up to this M, x terms are kept by token
+F4_TOKEN_COLUMNS_SMALL = 16   # NVFP4 tensor-core kernel: token columns for M <= 16
+F4_TOKEN_COLUMNS = 32         # and for 16 < M <= 32 (its largest M)
 
 LIB_PATH = _build.LIB
 
@@ -355,16 +357,27 @@ def workspace_view(layer: LayerDesc, M: int, ws: torch.Tensor) -> dict:
 
     tc = {}
     mt = v.max_total
-    if v.tc_h_terms:   # the tensor-core paths' h terms and the active table
+    if v.tc_h_terms and layer.routed.fmt == FMT_NVFP4_G16:
+        # the NVFP4 tensor-core kernel: f16 h terms (hi, lo) [2][max_total][I],
+        # the f16 x table [H/128][2][NT][64] of NT = 16 or 32 token columns
+        nt = F4_TOKEN_COLUMNS_SMALL if M <= F4_TOKEN_COLUMNS_SMALL else F4_TOKEN_COLUMNS
+        tc = dict(
+            tc_h_terms=sl(v.tc_h_terms, 2 * mt * I, torch.float16).view(2, mt, I),
+            tc_h_scale=sl(v.tc_h_scale, mt * (I // 128), torch.float32).view(mt, I // 128),
+            tc_items=sl(v.tc_items, 4 * v.cap, torch.int32).view(v.cap, 4),
+            tc_x_table=sl(v.tc_x_terms, nt * H, torch.float16).view(H // 128, 2, nt, 64),
+            tc_x_scale=sl(v.tc_x_scale, nt, torch.float32))
+    elif v.tc_h_terms:   # the FP8 tensor-core kernel's h terms and the active table
         tc = dict(
             tc_h_terms=sl(v.tc_h_terms, 3 * mt * I, torch.uint8).view(3, mt, I),
             tc_h_scale=sl(v.tc_h_scale, mt * (I // 128), torch.float32).view(mt, I // 128),
             tc_items=sl(v.tc_items, 4 * v.cap, torch.int32).view(v.cap, 4))
-    if v.tc_x_terms and M <= TOKEN_FORM_ROWS:   # x terms by token [H/128][2][16][128]
+    f4 = layer.routed.fmt == FMT_NVFP4_G16
+    if v.tc_x_terms and not f4 and M <= TOKEN_FORM_ROWS:   # x terms by token [H/128][2][16][128]
         tc.update(
             tc_x_table=sl(v.tc_x_terms, 2 * 16 * H, torch.uint8).view(H // 128, 2, 16, 128),
             tc_x_scale=sl(v.tc_x_scale, 16, torch.float32))
-    elif v.tc_x_terms:   # x terms by sorted row [2][max_total][H]
+    elif v.tc_x_terms and not f4:   # x terms by sorted row [2][max_total][H]
         tc.update(
             tc_x_terms=sl(v.tc_x_terms, 2 * mt * H, torch.uint8).view(2, mt, H),
             tc_x_scale=sl(v.tc_x_scale, mt, torch.float32))

@@ -31,6 +31,14 @@ int align_launch(const void *topk_ids, int ids_is_int64, int n, int num_experts,
                  int32_t *token_to_perm, int32_t *active_experts, int32_t *active_count,
                  int32_t *num_tokens_post_padded, uint32_t *err_word, int4 *items,
                  void *stream);
+bool f4_fits(const moe_layer_desc *L, int M);
+void f4_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]);
+size_t f4_counter_ints(const moe_layer_desc *L);
+int launch_f4(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
+              const int32_t *ttp, const int32_t *act_count, const float *y_sh, uint16_t *out,
+              void *ws, const moe_workspace_view &v, uint32_t *err, void *stream);
+int simt_shared(const moe_experts *shared, const uint16_t *x, int M, float *h_sh, float *y_sh,
+                void *stream);
 int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float *logits,
                  const int32_t *ids, const float *w, uint16_t *out, void *ws,
                  const moe_workspace_view &v, uint32_t *err, void *stream);
@@ -52,30 +60,43 @@ static int resolve_path(const moe_experts *routed, int M, int top_k, int path) {
 }
 
 // How moe_decode_layer runs a shape class: the fused CUDA-core kernel, the
-// tensor-core kernel, or the staged CUDA-core kernels.  It depends on the
-// shapes only, never on the routing, so a captured graph stays valid for
-// every routing.
-enum { kRunFused = 0, kRunTc = 1, kRunStaged = 2 };
+// FP8 tensor-core kernel, the staged CUDA-core kernels, or the NVFP4
+// tensor-core kernel (after the shared expert on the staged kernels).  It
+// depends on the shapes only, never on the routing, so a captured graph stays
+// valid for every routing.
+enum { kRunFused = 0, kRunTc = 1, kRunStaged = 2, kRunTcF4 = 3 };
 
 static int layer_run(const moe_layer_desc *L, int M) {
   switch (L->path) {
     case MOE_PATH_TC:
-      return tc_fits(L, M) ? kRunTc : -1;
+      if (tc_fits(L, M)) return kRunTc;
+      return f4_fits(L, M) ? kRunTcF4 : -1;
     case MOE_PATH_SIMT_STAGED:
       return kRunStaged;
     case MOE_PATH_SIMT:
       return fused_fits(L, M, sm_count()) ? kRunFused : kRunStaged;
-    default:   // the tensor cores for every FP8 shape they admit, else CUDA cores
+    default:   // the tensor cores for every shape they admit, else CUDA cores
       if (tc_fits(L, M)) return kRunTc;
+      if (f4_fits(L, M)) return kRunTcF4;
       return fused_fits(L, M, sm_count()) ? kRunFused : kRunStaged;
   }
 }
 
-static bool is_tc(int run) { return run == kRunTc; }
+static bool is_tc(int run) { return run == kRunTc || run == kRunTcF4; }
 
-// Bytes of the tensor-core kernel's counters (each call leaves them at zero):
-// sized by the layer alone.
-size_t tc_counter_bytes(const moe_layer_desc *L) { return 4 * tc_counter_ints(L); }
+// Whether the layer runs a tensor-core kernel at some M: its counters then
+// have their place at offset 256 for every M, so that calls at M the
+// CUDA cores take do not overwrite them.
+static bool tc_layer(const moe_layer_desc *L) {
+  if (L->path != MOE_PATH_AUTO && L->path != MOE_PATH_TC) return false;
+  return tc_fits(L, 1) || f4_fits(L, 1);
+}
+
+// Bytes of the tensor-core kernels' counters (each call leaves them
+// consistent for the next): sized by the layer alone.
+size_t tc_counter_bytes(const moe_layer_desc *L) {
+  return 4 * (L->routed.fmt == MOE_FMT_NVFP4_G16 ? f4_counter_ints(L) : tc_counter_ints(L));
+}
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -115,8 +136,7 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
       L->path != MOE_PATH_SIMT_STAGED)
     return MOE_EINVAL;
   const int run = layer_run(L, M);
-  const bool tc = is_tc(run);
-  v->tc_done = tc ? take(tc_counter_bytes(L)) : 0;
+  v->tc_done = tc_layer(L) ? take(tc_counter_bytes(L)) : 0;
   v->topk_ids = take((size_t)n * 4);
   v->topk_w = take((size_t)n * 4);
   v->sorted_token_ids = take((size_t)max_total * 4);
@@ -134,9 +154,12 @@ static int layout(const moe_layer_desc *L, int M, moe_workspace_view *v) {
   v->shared_gate = take((size_t)M * 4);
   v->tc_x_terms = v->tc_x_scale = v->tc_h_terms = v->tc_h_scale = 0;
   v->tc_items = 0;
-  if (run == kRunTc) {
+  if (is_tc(run)) {
     size_t b[5];
-    tc_workspace(L, M, max_total, cap, b);
+    if (run == kRunTc)
+      tc_workspace(L, M, max_total, cap, b);
+    else
+      f4_workspace(L, max_total, cap, b);
     v->tc_x_terms = take(b[0]);
     v->tc_x_scale = take(b[1]);
     v->tc_h_terms = take(b[2]);
@@ -198,6 +221,8 @@ extern "C" int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int
   if (with_logits == 2 && !layer->router_weight) return -1;
   const int router = with_logits == 2;   // the logits kernel ahead of the route
   if (run == moe::kRunFused) return 1 + router;
+  if (run == moe::kRunTcF4)   // the shared expert's two kernels first
+    return (with_logits ? 3 : 2) + router + (layer->shared ? 2 : 0);
   if (moe::is_tc(run)) return (with_logits ? 3 : 2) + router;
   return (with_logits ? 5 : 4) + router;
 }
@@ -273,8 +298,8 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
 namespace moe {
 
 // The expert half of a layer call, after the routing and the alignment
-// tables are in the workspace: the tensor-core kernel, or the staged
-// gate+up, down and blend.
+// tables are in the workspace: a tensor-core kernel (the NVFP4 one after the
+// shared expert's two kernels), or the staged gate+up, down and blend.
 int run_experts(const moe_layer_desc *layer, int run, const uint16_t *x, int M,
                 const int32_t *ids, const float *w, uint16_t *out, void *workspace,
                 const moe_workspace_view &v, uint32_t *err_word, void *stream) {
@@ -287,6 +312,14 @@ int run_experts(const moe_layer_desc *layer, int run, const uint16_t *x, int M,
   if (run == kRunTc)
     return launch_tc(layer, x, M, w, I32(v.token_to_perm), I32(v.active_count), out, workspace,
                      v, err_word, stream);
+  if (run == kRunTcF4) {
+    if (S) {
+      const int st = simt_shared(S, x, M, F32(v.h_shared), F32(v.y_shared), stream);
+      if (st) return st;
+    }
+    return launch_f4(layer, x, M, w, I32(v.token_to_perm), I32(v.active_count),
+                     S ? F32(v.y_shared) : nullptr, out, workspace, v, err_word, stream);
+  }
   int st = simt_gate_up(&layer->routed, S, x, M, k, I32(v.expert_offsets),
                         I32(v.sorted_token_ids), I32(v.active_experts), I32(v.active_count),
                         F32(v.h), S ? F32(v.h_shared) : nullptr, stream);

@@ -114,9 +114,10 @@ extern "C" int moe_decode_layer_noalloc(const moe_layer_desc *layer, const uint1
   if (st) return st;
   // The layer's grid-barrier count and the tensor-core path's counters must
   // start the call consistent: clear them (the rest of the workspace is fully
-  // written before it is read).  The decode kernel's call epoch, beside the
-  // grid-barrier count, is left as it is: it moves on by one every call, so
-  // its tagged partial sums of an earlier call are never taken for this one's.
+  // written before it is read).  The tensor-core kernels' call epoch, beside
+  // the grid-barrier count, is left as it is: it moves on every call and
+  // never takes the value 0 of the cleared token flags, so no token's flag
+  // reads as published before this call writes it.
   cudaError_t e = cudaMemsetAsync(static_cast<char *>(ws) + v.blend_counters, 0, 8,
                                   (cudaStream_t)stream);
   if (e == cudaSuccess && v.tc_done)

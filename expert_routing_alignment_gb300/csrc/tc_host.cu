@@ -23,16 +23,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
-int encode_u8_sw128(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
-                    const cuuint64_t *strides, const cuuint32_t *box) {
+namespace {
+int encode_u8(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
+              const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw) {
   auto fn = encode_fn();
   if (!fn) return MOE_ECUDA;
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void *>(ptr), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_EUNSUPPORTED;
+}
+}  // namespace
+
+int encode_u8_sw128(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
+                    const cuuint64_t *strides, const cuuint32_t *box) {
+  return encode_u8(m, ptr, rank, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int encode_u8_plain(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
+                    const cuuint64_t *strides, const cuuint32_t *box) {
+  return encode_u8(m, ptr, rank, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace tc

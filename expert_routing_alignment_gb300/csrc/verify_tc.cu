@@ -985,7 +985,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();   // the tables of the alignment are final
   // this call's epoch: one more than the last call's (written by the
   // previous kernel on this workspace after its final grid barrier)
-  const uint32_t ep = (uint32_t)__ldcg(a.epoch) + 1u;
+  // this call's epoch: 1 .. 2^31 - 1, never the 0 of cleared token flags
+  const uint32_t ep = (uint32_t)__ldcg(a.epoch) % 0x7FFFFFFFu + 1u;
   // The item table first (it needs only the alignment's tables); the x terms
   // are written by the promotion warps while the copy warp already streams
   // weight tiles, which do not depend on them (misc[6]: x terms ready).

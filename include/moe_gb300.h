@@ -284,14 +284,20 @@ typedef struct moe_workspace_view {
                                                       computed them from x (else unwritten) */
     size_t shared_gate;                            /* [M] float: the shared expert's gates
                                                       (fused path, gated layers; else unwritten) */
-    /* tensor-core path only (all 0 on the CUDA-core path): the activation
-     * terms it multiplies, as E4M3 planes with power-of-two scales --
-     * x = (t0 + t1) * x_scale[p] per sorted row [2][max_total][H] u8 and
-     * [max_total] float; h = (t0 + t1 + t2) * h_scale[p][c/128]
-     * [3][max_total][I] u8 and [max_total][I/128] float -- and internal
-     * int32 counters (tc_done: [E] per active-list index, then the item
-     * counter), which every call leaves at zero.  tc_done is always at offset
-     * 256: the counters that persist between calls sit where M does not move
+    /* tensor-core paths only (all 0 on the CUDA-core path): the activation
+     * terms they multiply, with power-of-two scales.  FP8 experts: E4M3
+     * planes, x = (t0 + t1) * x_scale[p] per sorted row [2][max_total][H] u8
+     * and [max_total] float; h = (t0 + t1 + t2) * h_scale[p][c/128]
+     * [3][max_total][I] u8 and [max_total][I/128] float.  NVFP4 experts (M <=
+     * 32): f16 planes, h = (hi + lo) * h_scale[p][c/128] [2][max_total][I]
+     * f16, and x by token: tc_x_terms holds [H/128][2][NT][64] f16 (k block,
+     * 64-wide half, token, 64 k values; NT = 16 for M <= 16, else 32), x =
+     * term * tc_x_scale[t] ([32] float).  Then internal int32 counters
+     * (tc_done: [E] per active-list index, the item counter, and the token
+     * flags), which every call leaves consistent for the next.  tc_done is
+     * always at offset 256 and is kept there for every M whenever the layer
+     * runs a tensor-core kernel at some M (also at M the CUDA cores take):
+     * the counters that persist between calls sit where M does not move
      * them, so one workspace serves every M up to the one it was sized for. */
     size_t tc_x_terms, tc_x_scale, tc_h_terms, tc_h_scale, tc_done;
     size_t total_bytes;
@@ -316,7 +322,8 @@ int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int M,
 
 /* Host only.  The number of kernels moe_decode_layer enqueues for M rows
  * (1 on the fused decode path; 3 with router logits, 2 with given ids on the
- * tensor-core path; otherwise 5 and 4), or -1 if the call would be
+ * tensor-core path, two more with a shared expert on the NVFP4 one;
+ * otherwise 5 and 4), or -1 if the call would be
  * rejected.  with_logits: 0 ids given, 1 logits given, 2 logits computed from
  * x and the layer's router_weight (one launch more than 1). */
 int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logits);
@@ -342,8 +349,15 @@ int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logit
  * persistent kernel of tcgen05 MMAs after the alignment ("fp8_moe_grouped.rs",
  * the tensor-core twins of the grouped launchers): E4M3 weight codes times
  * exact E4M3 splits of x and h, each 128-wide k block promoted to fp32 times
- * its block scale.  Its h and y are the same quantities as on the CUDA-core
- * path, within the layer tolerance.
+ * its block scale.  NVFP4 routed experts with M <= 32, hidden and inter
+ * multiples of 256 (hidden up to 8192, inter up to 4096) run the NVFP4 twin
+ * ("forward_nvfp4_grouped_decode.rs", the NVFP4 grouped launchers): each
+ * E2M1 code times its E4M3 scale decoded exactly to f16 into tensor memory,
+ * tcgen05 kind::f16 MMAs against an f16 x table by token and f16 hi/lo
+ * splits of h, the fp32 globals applied once per item; a shared expert runs
+ * first on the CUDA-core gate+up and down kernels (two launches more) and is
+ * blended in by the same kernel.  Either kernel's h and y are the same
+ * quantities as on the CUDA-core path, within the layer tolerance.
  *   x [M][H] bf16 bits; out [M][H] bf16 bits;
  *   workspace: device, >= moe_decode_layer_workspace_bytes(layer, M) bytes,
  *   256-byte aligned, used only by this call (its intermediates can be read

@@ -140,15 +140,51 @@ def test_tensor_core_workspace_host_only():
     # the tensor-core run is 3 launches with router logits, 2 with given ids
     assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 1) == 3
     assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), 128, 0) == 2
-    # not for NVFP4 experts, nor when the CUDA-core path is forced
-    for lay in (moe.LayerDesc(top_k=8, block_size=64,
-                              routed=_fake_experts(fmt=moe.FMT_NVFP4_G16, E=256, H=4096,
-                                                   I=1536)),
-                moe.LayerDesc(top_k=8, block_size=64, path=moe.PATH_SIMT_STAGED,
-                              routed=_fake_experts(E=256, H=4096, I=1536))):
-        assert lib.moe_decode_layer_workspace_view(ctypes.pointer(lay._struct), 128,
-                                                   ctypes.byref(v)) == 0
-        assert v.tc_x_terms == v.tc_h_terms == v.tc_done == 0
+    # not when the CUDA-core path is forced
+    lay = moe.LayerDesc(top_k=8, block_size=64, path=moe.PATH_SIMT_STAGED,
+                        routed=_fake_experts(E=256, H=4096, I=1536))
+    assert lib.moe_decode_layer_workspace_view(ctypes.pointer(lay._struct), 128,
+                                               ctypes.byref(v)) == 0
+    assert v.tc_x_terms == v.tc_h_terms == v.tc_done == 0
+    # NVFP4 experts at M = 128 run on the CUDA cores: no term tables, but the
+    # counters of the NVFP4 tensor-core kernel (M <= 32) keep their place
+    lay = moe.LayerDesc(top_k=8, block_size=64,
+                        routed=_fake_experts(fmt=moe.FMT_NVFP4_G16, E=256, H=4096, I=1536))
+    assert lib.moe_decode_layer_workspace_view(ctypes.pointer(lay._struct), 128,
+                                               ctypes.byref(v)) == 0
+    assert v.tc_x_terms == v.tc_h_terms == v.tc_items == 0 and v.tc_done == 256
+
+
+def test_nvfp4_tensor_core_workspace_host_only():
+    """NVFP4 routed experts at M <= 32 get the NVFP4 tensor-core kernel's
+    tables: an f16 x table of 16 or 32 token columns, [2][max_total][I] f16
+    h terms, their scales and the active table; the counters (E + 1 + 32
+    ints) at 256 for every M.  With a shared expert the layer is two
+    launches longer (its gate+up and down ahead of the kernel)."""
+    lib = moe.load()
+    shared = _fake_experts(E=1, H=2048, I=512)
+    for sh in (None, shared):
+        layer = moe.LayerDesc(top_k=8, block_size=16, shared=sh,
+                              routed=_fake_experts(fmt=moe.FMT_NVFP4_G16, E=128, H=2048, I=768))
+        for M in (1, 8, 16, 17, 32, 33, 64):
+            v = moe._WsView()
+            assert lib.moe_decode_layer_workspace_view(ctypes.pointer(layer._struct), M,
+                                                       ctypes.byref(v)) == 0
+            mt, _, cap = oracle.align_sizes(M * 8, 128, 16)
+            assert (v.blend_counters, v.tc_done) == (0, 256)
+            assert v.topk_ids - v.tc_done >= (128 + 1 + 32) * 4
+            launches = lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), M, 1)
+            if M > 32:   # the CUDA cores
+                assert v.tc_x_terms == v.tc_h_terms == v.tc_items == 0
+                continue
+            assert v.tc_x_scale - v.tc_x_terms >= 2 * 32 * 2048
+            assert v.tc_h_terms - v.tc_x_scale >= 32 * 4
+            assert v.tc_h_scale - v.tc_h_terms >= 2 * 2 * mt * 768
+            assert v.tc_items - v.tc_h_scale >= mt * 6 * 4
+            assert v.total_bytes - v.tc_items >= cap * 16
+            assert launches == 3 + (2 if sh is not None else 0)
+            assert lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), M, 0) == \
+                2 + (2 if sh is not None else 0)
 
 
 def test_token_form_workspace_host_only():
