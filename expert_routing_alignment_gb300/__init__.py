@@ -425,9 +425,8 @@ def moe_decode_experts(layer: LayerDesc, x: torch.Tensor, out: torch.Tensor,
                        workspace: torch.Tensor, err_word: Optional[torch.Tensor] = None,
                        stream=None) -> None:
     """The expert half of moe_decode_layer (grouped gate+up, down, blend) on
-    the routing and alignment tables the workspace already holds for these
-    rows (see workspace_view: moe_topk_softmax and moe_align can write them
-    there, or an earlier moe_decode_layer call left them)."""
+    the routing and alignment tables that an earlier moe_decode_layer call
+    with the same layer and M left in this workspace, with this x."""
     M = x.shape[0]
     _check("moe_decode_experts", load().moe_decode_experts(
         ctypes.pointer(layer._struct), _ptr(x), M, _ptr(out), _ptr(workspace),

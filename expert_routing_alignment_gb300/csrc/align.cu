@@ -20,6 +20,7 @@
 // run to run.  The pages' pairwise O(n^2) rank is replaced by this O(n) form,
 // which computes the same integers.
 #include "common.cuh"
+#include "xprep.cuh"
 
 namespace moe {
 namespace {
@@ -33,6 +34,8 @@ struct AlignArgs {
   // optional (the layer's tensor-core kernels): per active-list index,
   // {run offset, expert, slot count, 0}
   int4 *items;
+  // optional: the per-token x table, one extra CTA per token
+  XPrep xp;
 };
 
 // Expert id of slot i, or -1 when it lies outside [0, E).
@@ -63,8 +66,13 @@ __global__ void __launch_bounds__(NT) align_kernel(AlignArgs a) {
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
 
-  pdl_wait();      // topk_ids may come from the previous kernel on the stream
+  pdl_wait();      // topk_ids (and x) may come from the previous kernel on the stream
   pdl_trigger();
+  if (blockIdx.x > 0) {   // the extra CTAs: token blockIdx.x - 1 of the x table
+    __shared__ int red[8];
+    xprep_token(a.xp, (int)blockIdx.x - 1, red);
+    return;
+  }
 
   for (int i = tid; i < NW * E; i += NT) cnt[i] = 0;
   __syncthreads();
@@ -236,7 +244,15 @@ int launch_align(const AlignArgs &a, void *stream) {
   const int st = ensure_smem_limit(reinterpret_cast<const void *>(align_kernel<NT>),
                                    align_smem_bytes<NT>(kCacheIdsMax, MOE_MAX_EXPERTS));
   if (st) return st;
-  return launch_pdl(align_kernel<NT>, dim3(1), dim3(NT), smem, stream, a);
+  const int grid = 1 + (a.xp.mode != kXPrepNone ? a.xp.M : 0);
+  return launch_pdl(align_kernel<NT>, dim3(grid), dim3(NT), smem, stream, a);
+}
+
+__global__ void __launch_bounds__(kXPrepThreads) xprep_kernel(XPrep p) {
+  __shared__ int red[8];
+  pdl_wait();   // x may come from the previous kernel on the stream
+  pdl_trigger();
+  xprep_token(p, (int)blockIdx.x, red);
 }
 
 }  // namespace
@@ -262,12 +278,13 @@ namespace moe {
 
 // moe_align, plus (when items is not NULL) the active table of the layer's
 // tensor-core kernels: items[a] = {expert_offsets[e], e, count[e], 0} for the
-// a-th active expert e.
+// a-th active expert e; and (when xp is not NULL and names a format) the
+// per-token x table of those kernels, by M extra CTAs of the same launch.
 int align_launch(const void *topk_ids, int ids_is_int64, int n, int num_experts, int block_size,
                  int32_t *sorted_token_ids, int32_t *sorted_expert_ids, int32_t *expert_offsets,
                  int32_t *token_to_perm, int32_t *active_experts, int32_t *active_count,
                  int32_t *num_tokens_post_padded, uint32_t *err_word, int4 *items,
-                 void *stream) {
+                 const XPrep *xp, void *stream) {
   int max_total, max_blocks, cap;
   int st = moe_align_sizes(n, num_experts, block_size, &max_total, &max_blocks, &cap);
   if (st != MOE_OK) return st;
@@ -294,7 +311,12 @@ int align_launch(const void *topk_ids, int ids_is_int64, int n, int num_experts,
   a.ntpp = num_tokens_post_padded;
   a.err = err_word;
   a.items = items;
-  // One CTA; its width grows with n (a launch tuple fixed per shape class).
+  a.xp = xp ? *xp : XPrep{};
+  if (a.xp.mode != kXPrepNone && (a.xp.M < 1 || a.xp.M > 32 || !a.xp.x || !a.xp.table ||
+                                  !a.xp.scale || a.xp.H % 128))
+    return MOE_EINVAL;
+  // One CTA (plus the x-table CTAs); its width grows with n (a launch tuple
+  // fixed per shape class).
   if (n <= 512) return launch_align<128>(a, stream);
   if (n <= 4096) return launch_align<256>(a, stream);
   if (n <= 16384) return launch_align<512>(a, stream);
@@ -310,5 +332,17 @@ extern "C" int moe_align(const void *topk_ids, int ids_is_int64, int n, int num_
                          int32_t *num_tokens_post_padded, uint32_t *err_word, void *stream) {
   return moe::align_launch(topk_ids, ids_is_int64, n, num_experts, block_size, sorted_token_ids,
                            sorted_expert_ids, expert_offsets, token_to_perm, active_experts,
-                           active_count, num_tokens_post_padded, err_word, nullptr, stream);
+                           active_count, num_tokens_post_padded, err_word, nullptr, nullptr,
+                           stream);
 }
+
+namespace moe {
+
+// The per-token x table alone (moe_decode_experts on a new x): M CTAs.
+int xprep_launch(const XPrep &p, void *stream) {
+  if (p.mode == kXPrepNone) return MOE_OK;
+  if (p.M < 1 || p.M > 32 || !p.x || !p.table || !p.scale || p.H % 128) return MOE_EINVAL;
+  return launch_pdl(xprep_kernel, dim3(p.M), dim3(kXPrepThreads), 0, stream, p);
+}
+
+}  // namespace moe

@@ -3,6 +3,7 @@
 // ("metrale_model_layers/layers/moe/forward_nvfp4_grouped_decode.rs",
 // forward_nvfp4_grouped_decode; every step enqueued, no host read).
 #include "common.cuh"
+#include "xprep.cuh"
 
 namespace moe {
 
@@ -30,7 +31,8 @@ int align_launch(const void *topk_ids, int ids_is_int64, int n, int num_experts,
                  int32_t *sorted_token_ids, int32_t *sorted_expert_ids, int32_t *expert_offsets,
                  int32_t *token_to_perm, int32_t *active_experts, int32_t *active_count,
                  int32_t *num_tokens_post_padded, uint32_t *err_word, int4 *items,
-                 void *stream);
+                 const XPrep *xp, void *stream);
+int xprep_launch(const XPrep &p, void *stream);
 bool f4_fits(const moe_layer_desc *L, int M);
 void f4_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]);
 size_t f4_counter_ints(const moe_layer_desc *L);
@@ -83,6 +85,32 @@ static int layer_run(const moe_layer_desc *L, int M) {
 }
 
 static bool is_tc(int run) { return run == kRunTc || run == kRunTcF4; }
+
+// The per-token x table a tensor-core run reads (the FP8 kernel's up to 16
+// rows, the NVFP4 kernel's up to 32), else mode none.
+static XPrep token_table(const moe_layer_desc *L, int run, const uint16_t *x, int M, char *ws,
+                         const moe_workspace_view &v) {
+  XPrep p{};
+  if (run == kRunTc && M <= 16) {
+    p.mode = kXPrepE4M3;
+    p.NT = 16;
+  } else if (run == kRunTcF4) {
+    p.mode = kXPrepF16;
+    p.NT = M <= 16 ? 16 : 32;
+    if (L->shared && L->shared_gate) {
+      p.gate_w = L->shared_gate;
+      p.gate_vals = reinterpret_cast<float *>(ws + v.shared_gate);
+    }
+  } else {
+    return p;
+  }
+  p.M = M;
+  p.H = L->routed.hidden;
+  p.x = x;
+  p.table = reinterpret_cast<uint8_t *>(ws + v.tc_x_terms);
+  p.scale = reinterpret_cast<float *>(ws + v.tc_x_scale);
+  return p;
+}
 
 // Whether the layer runs a tensor-core kernel at some M: its counters then
 // have their place at offset 256 for every M, so that calls at M the
@@ -284,13 +312,15 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
     w = F32(v.topk_w);
   }
   // the tensor-core kernels also take the active table (offset, expert and
-  // slot count of each active expert) from the alignment launch
+  // slot count of each active expert) and their per-token x table from the
+  // alignment launch
+  const moe::XPrep xp = moe::token_table(layer, run, x, M, ws, v);
   st = moe::align_launch(ids, 0, M * k, E, layer->block_size, I32(v.sorted_token_ids),
                          I32(v.sorted_expert_ids), I32(v.expert_offsets), I32(v.token_to_perm),
                          I32(v.active_experts), I32(v.active_count),
                          I32(v.num_tokens_post_padded), err_word,
                          moe::is_tc(run) ? reinterpret_cast<int4 *>(ws + v.tc_items) : nullptr,
-                         stream);
+                         &xp, stream);
   if (st) return st;
   return moe::run_experts(layer, run, x, M, ids, w, out, workspace, v, err_word, stream);
 }
@@ -350,5 +380,8 @@ extern "C" int moe_decode_experts(const moe_layer_desc *layer, const uint16_t *x
   const float *w = reinterpret_cast<const float *>(ws + v.topk_w);
   if (run == moe::kRunFused)   // it aligns the given ids again, to the same tables
     return moe::launch_fused(layer, x, M, nullptr, ids, w, out, workspace, v, err_word, stream);
+  // the tensor-core runs' per-token x table of this x (one launch more)
+  st = moe::xprep_launch(moe::token_table(layer, run, x, M, ws, v), stream);
+  if (st) return st;
   return moe::run_experts(layer, run, x, M, ids, w, out, workspace, v, err_word, stream);
 }

@@ -114,10 +114,7 @@ extern "C" int moe_decode_layer_noalloc(const moe_layer_desc *layer, const uint1
   if (st) return st;
   // The layer's grid-barrier count and the tensor-core path's counters must
   // start the call consistent: clear them (the rest of the workspace is fully
-  // written before it is read).  The tensor-core kernels' call epoch, beside
-  // the grid-barrier count, is left as it is: it moves on every call and
-  // never takes the value 0 of the cleared token flags, so no token's flag
-  // reads as published before this call writes it.
+  // written before it is read).
   cudaError_t e = cudaMemsetAsync(static_cast<char *>(ws) + v.blend_counters, 0, 8,
                                   (cudaStream_t)stream);
   if (e == cudaSuccess && v.tc_done)

@@ -23,8 +23,10 @@
 //    h as two f16 terms (hi + lo, 22 bits) under a power-of-two scale per
 //    (row, 128-column block).
 //  * Token columns.  The gate+up MMAs take the batch's 16 or 32 token columns
-//    of a per-token x table at once; CTA t writes token t's row and publishes
-//    it with an epoch-tagged flag, so no grid barrier precedes the copies.
+//    of a per-token x table at once.  The table (and the shared expert's
+//    gates) come from extra CTAs of the alignment launch, complete when this
+//    kernel's programmatic-dependency wait returns: the first copies wait for
+//    nothing else.
 //  * Every 128-wide k block is accumulated alone in TMEM and added in fp32 in
 //    a fixed order (times the row's h scale for down); the global scale is
 //    applied once per item.  Items (expert row tile, 128-row gate+up tile),
@@ -51,7 +53,7 @@ constexpr int kWarps = kEpi0 + kEpiWarps;       // 14
 constexpr int kThreads = kWarps * 32;           // 448
 constexpr int kEpiThreads = kEpiWarps * 32;     // 256
 constexpr int kRecs = 8;                        // stage records
-constexpr int kAccs = 16;                       // k-block accumulator barriers
+constexpr int kKd = 32;                         // k-block completion barriers
 constexpr int kTfree = 16;                      // per-stage TMEM release barriers
 constexpr int kIQ = 32;                         // item queue
 constexpr int kAbuf = 4;                        // TMEM A buffers (one tile k block each)
@@ -73,15 +75,15 @@ struct F4Args {
   const int4 *items;                         // [cap] {offset, expert, slot count, 0}
   uint16_t *out;                             // [M][H] bf16
   const float *gg, *gu, *gd;                 // global scales [E]
-  uint8_t *xt;                               // f16 x table [H/128][2 atoms][NT][128 B]
-  float *xs;                                 // [32] 2^-s of each token
+  const uint8_t *xt;                         // f16 x table [H/128][2 atoms][NT][128 B]
+  const float *xs;                           // [32] 2^-s of each token
   uint16_t *hq;                              // f16 h terms [2][max_total][I]
   float *hs;                                 // [max_total][I/128] 2^-s per (row, block)
   float *h, *y;                              // [max_total][I], [max_total][H]
   const float *y_sh;                         // [M][H] shared expert output, or NULL
-  const uint16_t *gate_w;                    // [H] shared gate weight, or NULL
-  float *gate_vals;                          // [M] the gates
-  int *done, *work, *xflag, *epoch;
+  int gated;                                 // the shared term is gated
+  const float *gate_vals;                    // [M] the gates (written with the x table)
+  int *done, *work;
   unsigned long long *grid_ctr;
   uint32_t *err;
   uint32_t ring_bytes;
@@ -97,31 +99,29 @@ struct F4Maps {
 
 struct Smem {
   uint8_t *ring;
-  uint64_t *full, *empty, *accf, *tfree, *iqbar, *afull, *aempty, *drain;
+  uint64_t *full, *kdone, *tfree, *iqbar, *afull, *drain;
   volatile int *iq;
   uint32_t *rec, *rlen, *trec;
   int *twait;
-  volatile int *misc;   // [0] failed, [1] TMEM base, [3] row tiles, [4]/[5] barrier flags,
-                        // [6] x ready
+  volatile int *misc;   // [0] failed, [1] TMEM base, [3] row tiles, [4] grid barrier passed
   float *cs;            // [kMaxKBd][kRows] down: per-row h factors of the current item
   float *xinv;          // [kRows] gate+up: 2^-s of each row's token
   int *tokrow;          // [kRows] each row's token
   float *xtok;          // [kTokMax] 2^-s of each token
   float *glob;          // [2] the item's global scales
   uint32_t *red;        // [2 groups][4 quadrants][16] column maxima
-  float *part;          // [kEpiWarps] partial dots of the gate
   int *rtp;             // [cap + 1]
   int2 *info;           // [cap] {offset, expert | rows << 16}
 };
 
 __host__ __device__ inline size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
-constexpr int kBars = 2 * kRecs + kAccs + kTfree + kIQ + 2 * kAbuf + 1;
+constexpr int kBars = kRecs + kKd + kTfree + kIQ + kAbuf + 1;
 
 __host__ __device__ inline size_t fixed_bytes(int cap) {
   size_t b = al16(8 * kBars);
   b += 4 * al16(4 * kRecs) + al16(4 * kIQ) + al16(4 * 16);
   b += al16(4 * kMaxKBd * kRows) + al16(4 * kRows) + al16(4 * kRows) + al16(4 * kTokMax) +
-       al16(4 * 2) + al16(4 * 2 * 4 * 16) + al16(4 * kEpiWarps);
+       al16(4 * 2) + al16(4 * 2 * 4 * 16);
   b += al16(4 * ((size_t)cap + 1)) + al16(8 * (size_t)cap);
   return b;
 }
@@ -137,13 +137,11 @@ __device__ Smem carve(uint8_t *base, const F4Args &a) {
   };
   uint64_t *b = reinterpret_cast<uint64_t *>(take(8 * kBars));
   S.full = b;
-  S.empty = S.full + kRecs;
-  S.accf = S.empty + kRecs;
-  S.tfree = S.accf + kAccs;
+  S.kdone = S.full + kRecs;
+  S.tfree = S.kdone + kKd;
   S.iqbar = S.tfree + kTfree;
   S.afull = S.iqbar + kIQ;
-  S.aempty = S.afull + kAbuf;
-  S.drain = S.aempty + kAbuf;
+  S.drain = S.afull + kAbuf;
   S.rec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.rlen = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.trec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
@@ -156,7 +154,6 @@ __device__ Smem carve(uint8_t *base, const F4Args &a) {
   S.xtok = reinterpret_cast<float *>(take(4 * kTokMax));
   S.glob = reinterpret_cast<float *>(take(4 * 2));
   S.red = reinterpret_cast<uint32_t *>(take(4 * 2 * 4 * 16));
-  S.part = reinterpret_cast<float *>(take(4 * kEpiWarps));
   S.rtp = reinterpret_cast<int *>(take(4 * ((size_t)a.cap + 1)));
   S.info = reinterpret_cast<int2 *>(take(8 * (size_t)a.cap));
   return S;
@@ -191,23 +188,6 @@ __device__ __forceinline__ bool epi_sync_or(bool v) {
 }
 __device__ __forceinline__ void group_sync(int g) {
   asm volatile("bar.sync %0, 128;" ::"r"(2 + g) : "memory");
-}
-
-// f16 conversions (round to nearest even) and back (exact).
-__device__ __forceinline__ uint16_t f16_rn(float f) {
-  uint16_t r;
-  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(f));
-  return r;
-}
-__device__ __forceinline__ float f16_to_f32(uint16_t h) {
-  float f;
-  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
-  return f;
-}
-__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -265,102 +245,6 @@ __device__ __forceinline__ uint32_t acc_cols(const Item &it, int NT) {
 }
 
 // ---------------------------------------------------------------------------
-// tokens: the x table and the gates
-// ---------------------------------------------------------------------------
-
-// CTA t < M: token t's f16 row, x * 2^s with s putting max|x[t]| in
-// [2^14, 2^15) (exact: bf16 has 8 significant bits), into the table at
-// byte ((kb * 2 + atom) * NT + t) * 128 + (c % 64) * 2 for element
-// c = kb * 128 + atom * 64 + c % 64; its 2^-s; with a gated shared expert its
-// gate sigmoid(x[t] . gate_w); then this call's epoch into xflag[t].
-__device__ void prep_token(const F4Args &a, const Smem &S, uint32_t ep) {
-  const int t = blockIdx.x;
-  if (t >= a.M) return;
-  const int ew = (threadIdx.x >> 5) - kEpi0, lane = threadIdx.x & 31;
-  const int et = threadIdx.x - kEpi0 * 32;
-  const uint16_t *xr = a.x + (size_t)t * a.H;
-  uint32_t mx = 0;
-  float dot = 0.f;
-  for (int c = et * 8; c < a.H; c += kEpiThreads * 8) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + c));
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      mx = max(mx, (wv[h] & 0x7FFFu) << 16);
-      mx = max(mx, (wv[h] >> 16 & 0x7FFFu) << 16);
-    }
-    if (a.gate_w) {
-      const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(a.gate_w + c));
-      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        dot = fmaf(bf16_to_float((uint16_t)(wv[h] & 0xFFFFu)),
-                   bf16_to_float((uint16_t)(gw[h] & 0xFFFFu)), dot);
-        dot = fmaf(bf16_to_float((uint16_t)(wv[h] >> 16)), bf16_to_float((uint16_t)(gw[h] >> 16)),
-                   dot);
-      }
-    }
-  }
-  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, d);
-  if (lane == 0) {
-    S.red[ew] = mx;
-    S.part[ew] = dot;
-  }
-  epi_sync();
-  mx = 0;
-  for (int w = 0; w < kEpiWarps; ++w) mx = max(mx, S.red[w]);
-  int sh = 0;
-  if (mx) {
-    const int e = (int)(mx >> 23) - 127;
-    sh = 14 - e;
-    sh = sh < -126 ? -126 : (sh > 126 ? 126 : sh);
-  }
-  const float scl = pow2f(sh);
-  if (et == 0) {
-    a.xs[t] = pow2f(-sh);
-    if (a.gate_w) {   // the warps' sums added in warp order
-      float z = 0.f;
-      for (int w = 0; w < kEpiWarps; ++w) z += S.part[w];
-      a.gate_vals[t] = 1.f / (1.f + expf(-z));
-    }
-  }
-  for (int c = et * 2; c < a.H; c += kEpiThreads * 2) {
-    const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(xr + c));
-    const uint32_t hv = f16x2_rn(bf16_to_float((uint16_t)(v & 0xFFFFu)) * scl,
-                                 bf16_to_float((uint16_t)(v >> 16)) * scl);
-    const int kb = c / 128, atom = (c % 128) / 64;
-    uint8_t *dst = a.xt + ((size_t)(kb * 2 + atom) * a.NT + t) * 128 + (c % 64) * 2;
-    *reinterpret_cast<uint32_t *>(dst) = hv;
-  }
-  fence_proxy_async_global();
-  __threadfence();
-  epi_sync();
-  if (et == 0)
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.xflag + t), "r"(ep) : "memory");
-}
-
-// Every token's row is published (bounded wait on the M flags); the token
-// scales come to shared memory.
-__device__ bool wait_tokens(const F4Args &a, const Smem &S, uint32_t ep) {
-  const int et = threadIdx.x - kEpi0 * 32;
-  bool ok = true;
-  if (et < a.M) {
-    const uint64_t t0 = gtime();
-    while (ld_acquire(a.xflag + et) != (int)ep) {
-      if (S.misc[0] || gtime() - t0 > kWaitNs) {
-        ok = false;
-        break;
-      }
-      __nanosleep(64);
-    }
-    S.xtok[et] = __ldcg(a.xs + et);
-  }
-  return ok;
-}
-
-// ---------------------------------------------------------------------------
 // roles
 // ---------------------------------------------------------------------------
 
@@ -369,7 +253,6 @@ __device__ void producer(const F4Args &a, const F4Maps &m, const Smem &S, int A,
   const uint64_t pol = policy_evict_first();
   const int FT = a.I / 128, FD = a.H / 256, NT = a.NT;
   uint32_t head = 0, thead = 0;
-  bool x_ready = false;
   int s = 0, tail = 0, ttail = 0, jq = 0;
   bool ok = true;
   int i = (int)blockIdx.x < total ? (int)blockIdx.x : total;
@@ -413,7 +296,8 @@ __device__ void producer(const F4Args &a, const F4Maps &m, const Smem &S, int A,
         const bool busy =
             s - tail >= kRecs || (wrap && tp >= head) || (at < tp + tl && tp < at + size);
         if (!busy) break;
-        if (!wait_bar(S, &S.empty[dt], (uint32_t)(tail / kRecs) & 1)) {
+        const int kq = 2 * tail + 1;   // the stage's last k block: all its MMAs are done
+        if (!wait_bar(S, &S.kdone[kq % kKd], (uint32_t)(kq / kKd) & 1)) {
           ok = false;
           break;
         }
@@ -436,20 +320,6 @@ __device__ void producer(const F4Args &a, const F4Maps &m, const Smem &S, int A,
       tma_2d_hint(dst + bb + 2 * kCodeTile, &m.scales[p0], kb * 8, row0, fb, pol);
       tma_2d_hint(dst + bb + 2 * kCodeTile + kScaleTile, &m.scales[p1], kb * 8, row1, fb, pol);
       if (it.gu) {
-        if (!x_ready) {   // every token's row of the table is published
-          const uint64_t t0 = gtime();
-          while (!S.misc[6]) {
-            if (S.misc[0] || gtime() - t0 > kWaitNs) {
-              ok = false;
-              break;
-            }
-            __nanosleep(32);
-          }
-          __threadfence();
-          fence_proxy_async_global();
-          x_ready = true;
-        }
-        // issued even after a failed wait, so that the stage completes
         tma_3d(dst, &m.xt, 0, 0, 2 * kb, fb);   // 4 atoms x NT tokens
       } else {
         for (int at4 = 0; at4 < 4; ++at4)         // 4 atoms x (2 terms x 16 rows)
@@ -506,7 +376,8 @@ __device__ void decoder(const F4Args &a, const Smem &S, int A, int TR, int total
           const int ab = abn % kAbuf;
           if (abn >= kAbuf) {
             if (!__all_sync(0xFFFFFFFFu,
-                            wait_bar(S, &S.aempty[ab], (uint32_t)(abn / kAbuf - 1) & 1))) {
+                            wait_bar(S, &S.kdone[(abn / 2 - 2) % kKd],
+                                     (uint32_t)((abn / 2 - 2) / kKd) & 1))) {
               ok = false;
               break;
             }
@@ -580,6 +451,9 @@ __device__ void mma_issuer(const F4Args &a, const Smem &S, int A, int TR, int to
         if (!wait_bar(S, &S.tfree[tdone % kTfree], (uint32_t)(tdone / kTfree) & 1)) ok = false;
       }
       if (!ok) break;
+      // the stage's B operand: a descriptor moves by (bytes / 16)
+      const uint64_t bd0 = sdesc(base);
+      const uint32_t astep = atom_bytes >> 4;
       for (int kbl = 0; kbl < 2 && ok; ++kbl) {
         for (int t = 0; t < 2; ++t) {
           const int ab = abn % kAbuf;
@@ -589,22 +463,24 @@ __device__ void mma_issuer(const F4Args &a, const Smem &S, int A, int TR, int to
           }
           tc_fence_after();
           const uint32_t dcol = tbase + (uint32_t)kbl * cols + (uint32_t)t * (uint32_t)N;
+          const uint32_t acol = tmem + (uint32_t)ab * kAcols;
+          const uint64_t bk = bd0 + (uint64_t)(2u * (uint32_t)kbl * astep);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t b = base + (uint32_t)(kbl * 2 + (ks >> 2)) * atom_bytes +
-                               (uint32_t)(ks & 3) * 32u;
-            mma_f16_ta(dcol, tmem + (uint32_t)ab * kAcols + (uint32_t)ks * 8u, sdesc(b), id,
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ta(dcol, acol + (uint32_t)ks * 8u,
+                       bk + (uint64_t)((uint32_t)(ks >> 2) * astep + (uint32_t)(ks & 3) * 2u), id,
                        ks != 0);
-          }
-          mma_commit(&S.aempty[ab]);
           ++abn;
         }
         if (!ok) break;
-        mma_commit(&S.accf[q % kAccs]);
+        // One commit per k block (each commit costs the tensor pipe about as
+        // much as two MMAs): it frees the k block's two A buffers, hands its
+        // accumulators to the promotion, and after the second k block frees
+        // the ring stage.
+        mma_commit(&S.kdone[q % kKd]);
         ++q;
       }
       if (!ok) break;
-      mma_commit(&S.empty[d]);
       ++s;
     }
   }
@@ -626,10 +502,13 @@ __device__ void finish_gate_up(const F4Args &a, const Smem &S, const Item &it, i
   const float g0 = S.glob[0], g1 = S.glob[1];
   float hv[16];
 #pragma unroll
+  for (int j = 0; j < 16; ++j) hv[j] = 0.f;
+  // only the item's rows (a uniform bound: the unrolled rows keep their registers)
+#pragma unroll
   for (int j = 0; j < 16; ++j) {
-    hv[j] = 0.f;
+    if (j >= it.rows) break;
     const int t = S.tokrow[j] - 16 * grp;
-    const bool mine = j < it.rows && t >= 0 && t < 16;
+    const bool mine = t >= 0 && t < 16;
     uint32_t mx = 0;
     if (mine) {
       float gv = 0.f, uv = 0.f;
@@ -666,9 +545,10 @@ __device__ void finish_gate_up(const F4Args &a, const Smem &S, const Item &it, i
   const size_t plane = (size_t)a.max_total * a.I;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
+    if (j >= it.rows) break;
     const float sj = __shfl_sync(0xFFFFFFFFu, scl, j);
     const int t = S.tokrow[j] - 16 * grp;
-    if (j < it.rows && t >= 0 && t < 16) {
+    if (t >= 0 && t < 16) {
       const float v = hv[j] * sj;
       const uint16_t hi = f16_rn(v);
       const uint16_t lo = f16_rn(v - f16_to_f32(hi));
@@ -701,8 +581,8 @@ __device__ __forceinline__ void promote_dn(uint32_t col, const float *hf, float 
 // Warps 6-13: group g = (w - 6) / 4 holds token columns 16 g .. 16 g + 15 of a
 // gate+up item; group 0 the 16 rows of a down item.  Warp w reads TMEM lanes
 // 32 (w % 4) ..
-__device__ void epilogue(const F4Args &a, const Smem &S, int A, int TR, int total, uint32_t tmem,
-                         uint32_t ep) {
+__device__ void epilogue(const F4Args &a, const Smem &S, int A, int TR, int total,
+                         uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = (warp - kEpi0) >> 2, q = warp & 3;
   const int et = threadIdx.x - kEpi0 * 32;
@@ -711,15 +591,8 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, int TR, int tota
   int s = 0, st = 0;
   uint32_t thead = 0;
   bool bad = false;
-  prep_token(a, S, ep);
-  if (epi_sync_or(!wait_tokens(a, S, ep))) {
-    bad = true;
-    fail(S, a);
-  }
-  if (et == 0) {
-    __threadfence();
-    S.misc[6] = 1;
-  }
+  if (et < a.M) S.xtok[et] = __ldcg(a.xs + et);   // the x table is complete at launch
+  epi_sync();
   for (int jq = 0;; ++jq) {
     int i = next_item(S, jq);
     i = __shfl_sync(0xFFFFFFFFu, i, 0);
@@ -775,9 +648,8 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, int TR, int tota
     for (int kb = 0; kb < KB && mine; ++kb) {
       const int j = kb & 1;
       if (j == 0) tbase = ring_place(thead, tcols, kAccCols);
-      const int slot = s % kAccs;
       // every lane of the warp takes the same branch into the aligned TMEM loads
-      if (!__all_sync(0xFFFFFFFFu, wait_bar(S, &S.accf[slot], (uint32_t)(s / kAccs) & 1))) {
+      if (!__all_sync(0xFFFFFFFFu, wait_bar(S, &S.kdone[s % kKd], (uint32_t)(s / kKd) & 1))) {
         bad = true;
         break;
       }
@@ -816,12 +688,12 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, int TR, int tota
       const float gd = S.glob[0];
       const int c0 = it.tile * 256 + q * 32 + lane;
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj)
-        if (jj < it.rows) {
-          float *yr = a.y + (size_t)(it.pos0 + jj) * a.H + c0;
-          yr[0] = acc0[jj] * gd;
-          yr[128] = acc1[jj] * gd;
-        }
+      for (int jj = 0; jj < 16; ++jj) {
+        if (jj >= it.rows) break;
+        float *yr = a.y + (size_t)(it.pos0 + jj) * a.H + c0;
+        yr[0] = acc0[jj] * gd;
+        yr[128] = acc1[jj] * gd;
+      }
     }
   }
   if (bad) fail(S, a);
@@ -834,17 +706,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
-    for (int j = 0; j < kRecs; ++j) {
-      mbar_init(&S.full[j], 1);
-      mbar_init(&S.empty[j], 1);
-    }
-    for (int j = 0; j < kAccs; ++j) mbar_init(&S.accf[j], 1);
+    for (int j = 0; j < kRecs; ++j) mbar_init(&S.full[j], 1);
+    for (int j = 0; j < kKd; ++j) mbar_init(&S.kdone[j], 1);
     for (int j = 0; j < kTfree; ++j) mbar_init(&S.tfree[j], kEpiWarps);
     for (int j = 0; j < kIQ; ++j) mbar_init(&S.iqbar[j], 1);
-    for (int j = 0; j < kAbuf; ++j) {
-      mbar_init(&S.afull[j], kDecWarps);
-      mbar_init(&S.aempty[j], 1);
-    }
+    for (int j = 0; j < kAbuf; ++j) mbar_init(&S.afull[j], kDecWarps);
     mbar_init(S.drain, 1);
     for (int j = 0; j < 16; ++j) S.misc[j] = 0;
     fence_mbar_init();
@@ -863,8 +729,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if ((smem_addr(S.ring) & 1023u) != 0) fail(S, a);
 
   pdl_wait();
-  // this call's epoch: 1 .. 2^31 - 1, never the 0 of cleared token flags
-  const uint32_t ep = (uint32_t)__ldcg(a.epoch) % 0x7FFFFFFFu + 1u;
   // the active table as 16-row tiles: info[a] = {offset, expert | rows << 16}
   const int A = min(max(__ldcg(a.act_count), 0), a.cap);
   for (int j = threadIdx.x; j < A; j += kThreads) {
@@ -906,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kEpi0) {
     decoder(a, S, A, TR, total, tmem);
   } else {
-    epilogue(a, S, A, TR, total, tmem, ep);
+    epilogue(a, S, A, TR, total, tmem);
   }
 
   tc_fence_before();
@@ -950,7 +814,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i < a.cap; i += kThreads) a.done[i] = 0;
     if (threadIdx.x == 0) {
       *a.work = 0;
-      *a.epoch = (int)ep;
     }
   }
   const long long T4 = (long long)a.M * a.H / 4;
@@ -969,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc.w = fmaf(wj, v.w, acc.w);
     }
     if (a.y_sh) {
-      const float gt = a.gate_w ? __ldcg(a.gate_vals + t) : 1.f;
+      const float gt = a.gated ? __ldcg(a.gate_vals + t) : 1.f;
       const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.y_sh + (size_t)t * a.H + c));
       acc.x = fmaf(gt, v.x, acc.x);
       acc.y = fmaf(gt, v.y, acc.y);
@@ -988,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host
 // ---------------------------------------------------------------------------
 
-int f4_maps(const moe_experts *X, uint8_t *xt, uint16_t *hq, int max_total, int NT,
+int f4_maps(const moe_experts *X, const uint8_t *xt, uint16_t *hq, int max_total, int NT,
             F4Maps *out) {
   // every address a map holds is part of the key (codes and scales of the
   // three projections, the two workspace tables)
@@ -1090,11 +953,8 @@ void f4_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&byte
   bytes[4] = (size_t)cap * 16;
 }
 
-// Counters, in ints (sized by the layer alone): done [E], the item counter,
-// the 32 token flags.
-size_t f4_counter_ints(const moe_layer_desc *L) {
-  return (size_t)L->routed.num_experts + 1 + kTokMax;
-}
+// Counters, in ints (sized by the layer alone): done [E], the item counter.
+size_t f4_counter_ints(const moe_layer_desc *L) { return (size_t)L->routed.num_experts + 1; }
 
 int launch_f4(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
               const int32_t *ttp, const int32_t *act_count, const float *y_sh,
@@ -1129,13 +989,11 @@ int launch_f4(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
   a.h = reinterpret_cast<float *>(base + v.h);
   a.y = reinterpret_cast<float *>(base + v.y);
   a.y_sh = y_sh;
-  a.gate_w = y_sh ? L->shared_gate : nullptr;
+  a.gated = y_sh && L->shared_gate ? 1 : 0;
   a.gate_vals = reinterpret_cast<float *>(base + v.shared_gate);
   a.done = reinterpret_cast<int *>(base + v.tc_done);
   a.work = a.done + a.E;
-  a.xflag = a.work + 1;
   a.grid_ctr = reinterpret_cast<unsigned long long *>(base + v.blend_counters);
-  a.epoch = reinterpret_cast<int *>(base + v.blend_counters + 8);
   a.err = err;
   const size_t ring = ring_bytes_for(v.cap);
   if (!ring) return MOE_EUNSUPPORTED;

@@ -76,8 +76,6 @@ struct TcArgs {
   uint8_t *xq;                               // x terms [2][max_total][H] E4M3 by sorted row,
                                              // or (token form) [H/128][2][16][128] by token
   float *xs;                                 // 2^-s of each x row [max_total] (token form: [16])
-  int *xflag;                                // token form: [16] epoch of each token's terms
-  int *epoch;                                // the last call's epoch
   uint8_t *hq;                               // h terms [3][max_total][I] E4M3
   float *hs;                                 // 2^-s per (row, 128-block) [max_total][I/128]
   float *h, *y;                              // [max_total][I], [max_total][H]
@@ -316,72 +314,6 @@ __device__ void prep_x(const TcArgs &a) {
   }
 }
 
-// Token form: CTA t < M writes token t's two E4M3 terms (the split rule of
-// prep_x, with the token's own power-of-two scale) into the table at
-// [kb][term][t][128] and its 2^-s, then publishes them by storing this
-// call's epoch into xflag[t] (release, after the terms are visible to the
-// tensor copies of every CTA).  The 16 promotion warps split the row.
-__device__ void prep_token(const TcArgs &a, const Smem &S, uint32_t ep) {
-  const int t = blockIdx.x;
-  if (t >= a.M) return;
-  const int ew = (threadIdx.x >> 5) - 2, lane = threadIdx.x & 31, et = threadIdx.x - 64;
-  const uint16_t *xr = a.x + (size_t)t * a.H;
-  uint32_t mx = 0;
-  for (int c = et * 8; c < a.H; c += kEpiThreads * 8) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + c));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      mx = max(mx, (w[h] & 0x7FFFu) << 16);
-      mx = max(mx, (w[h] >> 16 & 0x7FFFu) << 16);
-    }
-  }
-  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-  if (lane == 0) S.red[ew] = mx;
-  asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
-  mx = 0;
-  for (int w = 0; w < kEpiWarps; ++w) mx = max(mx, S.red[w]);
-  const int sh = term_shift(mx);
-  const float scl = pow2f(sh);
-  if (et == 0) a.xs[t] = pow2f(-sh);
-  // element c of k block kb: term r at byte (kb * 2 + r) * 16 * 128 + t * 128 + c % 128
-  for (int c = et * 4; c < a.H; c += kEpiThreads * 4) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(xr + c));
-    uint32_t t0a, t1a, t0b, t1b;
-    e4m3_split2(bf16_to_float((uint16_t)(v.x & 0xFFFFu)) * scl,
-                bf16_to_float((uint16_t)(v.x >> 16)) * scl, t0a, t1a);
-    e4m3_split2(bf16_to_float((uint16_t)(v.y & 0xFFFFu)) * scl,
-                bf16_to_float((uint16_t)(v.y >> 16)) * scl, t0b, t1b);
-    uint8_t *dst = a.xq + (size_t)(c / 128) * 2 * kTokMax * 128 + (size_t)t * 128 + c % 128;
-    *reinterpret_cast<uint32_t *>(dst) = t0a | (t0b << 16);
-    *reinterpret_cast<uint32_t *>(dst + kTokMax * 128) = t1a | (t1b << 16);
-  }
-  fence_proxy_async_global();
-  __threadfence();
-  asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
-  if (et == 0) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.xflag + t), "r"(ep)
-                            : "memory");
-}
-
-// Token form: every token's terms are published (bounded wait on the M
-// flags), and the token scales are in shared memory.
-__device__ bool wait_tokens(const TcArgs &a, const Smem &S, uint32_t ep) {
-  const int et = threadIdx.x - 64;
-  bool ok = true;
-  if (et < a.M) {
-    const uint64_t t0 = gtime();
-    while (ld_acquire(a.xflag + et) != (int)ep) {
-      if (S.misc[0] || gtime() - t0 > kWaitNs) {
-        ok = false;
-        break;
-      }
-      __nanosleep(64);
-    }
-    S.xtok[et] = __ldcg(a.xs + et);
-  }
-  return ok;
-}
-
 // Grid barrier among the promotion warps of every CTA (named barrier 1 in the
 // CTA, then one thread's arrival on the monotonic count); true when all CTAs
 // arrived within the wait limit.
@@ -495,7 +427,7 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
   const uint64_t pol = policy_evict_first();
   const int FT = a.I / 128, FD = a.H / 256;
   uint32_t head = 0, thead = 0;   // shared-memory and TMEM ring heads
-  bool x_ready = false;            // the grid's x terms are visible
+  bool x_ready = a.tok != 0;       // the grid's x terms are visible (token form: at launch)
   int s = 0, tail = 0;
   int ttail = 0;                   // oldest stage that may still hold TMEM
   bool ok = true;
@@ -784,7 +716,7 @@ __device__ __forceinline__ bool epi_sync_or(bool v) {
 // group g = (w-2)/4 of the item's token rows).  Every decision to leave the
 // item loop is taken after a vote over all 16 warps.
 __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int total,
-                         uint32_t tmem, uint32_t ep) {
+                         uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ew = warp - 2, q = warp & 3, grp = ew >> 2;
   const int et = threadIdx.x - 64;
@@ -797,12 +729,10 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
   int pending = -1;   // active index of a finished gate+up item not yet published
   bool bad = false;
   if (a.tok) {
-    // token form: the CTA's own token (if any), then every token's flag
-    prep_token(a, S, ep);
-    if (epi_sync_or(!wait_tokens(a, S, ep))) {
-      bad = true;
-      fail(S, a);
-    }
+    // token form: the alignment launch wrote the x-term table and the token
+    // scales; they are complete at launch
+    if (et < a.M) S.xtok[et] = __ldcg(a.xs + et);
+    asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
   } else {
     // the x terms of this CTA's share of the slots, then the grid barrier
     // that makes all of them (and the zeroed counters) visible to the copies
@@ -813,7 +743,7 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
       fail(S, a);
     }
   }
-  if (et == 0) {
+  if (et == 0 && !a.tok) {
     fence_proxy_async_global();
     __threadfence();
     S.misc[6] = 1;
@@ -982,14 +912,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the swizzled operand tiles assume a 1024-byte aligned ring
   if ((smem_addr(S.ring) & 1023u) != 0) fail(S, a);
 
-  pdl_wait();   // the tables of the alignment are final
-  // this call's epoch: one more than the last call's (written by the
-  // previous kernel on this workspace after its final grid barrier)
-  // this call's epoch: 1 .. 2^31 - 1, never the 0 of cleared token flags
-  const uint32_t ep = (uint32_t)__ldcg(a.epoch) % 0x7FFFFFFFu + 1u;
-  // The item table first (it needs only the alignment's tables); the x terms
-  // are written by the promotion warps while the copy warp already streams
-  // weight tiles, which do not depend on them (misc[6]: x terms ready).
+  pdl_wait();   // the tables of the alignment (and the token form's x terms) are final
+  // The item table first (it needs only the alignment's tables); in the row
+  // form the x terms are written by the promotion warps while the copy warp
+  // already streams weight tiles, which do not depend on them (misc[6]: x
+  // terms ready).
   const int A = build_table(a, S);
   const int TR = S.misc[3];
   const int total = S.misc[0] ? 0 : TR * (a.I / 128 + a.H / 256);
@@ -1001,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((threadIdx.x & 31) == 0) mma_issuer(a, S, A, TR, total, tmem);
     __syncwarp();
   } else {
-    epilogue(a, S, A, TR, total, tmem, ep);
+    epilogue(a, S, A, TR, total, tmem);
   }
 
   tc_fence_before();
@@ -1025,7 +952,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i < a.cap; i += kThreads) a.done[i] = 0;
     if (threadIdx.x == 0) {
       *a.work = 0;
-      *a.epoch = (int)ep;
     }
   }
   const long long T4 = (long long)a.M * a.H / 4;
@@ -1162,11 +1088,8 @@ void tc_workspace(const moe_layer_desc *L, int M, int max_total, int cap, size_t
 }
 
 // Counters of the tensor-core path, in ints, sized by the layer alone: one per
-// active-list index (at most E), the item counter, and the token form's 16
-// token flags.  (The call epoch sits beside the grid-barrier count.)
-size_t tc_counter_ints(const moe_layer_desc *L) {
-  return (size_t)L->routed.num_experts + 1 + kTokMax;
-}
+// active-list index (at most E) and the item counter.
+size_t tc_counter_ints(const moe_layer_desc *L) { return (size_t)L->routed.num_experts + 1; }
 
 int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
               const int32_t *ttp, const int32_t *act_count, uint16_t *out, void *ws,
@@ -1202,9 +1125,7 @@ int launch_tc(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
   a.y = reinterpret_cast<float *>(base + v.y);
   a.done = reinterpret_cast<int *>(base + v.tc_done);
   a.work = a.done + a.E;
-  a.xflag = a.work + 1;
   a.grid_ctr = reinterpret_cast<unsigned long long *>(base + v.blend_counters);
-  a.epoch = reinterpret_cast<int *>(base + v.blend_counters + 8);
   a.err = err;
   const size_t ring = ring_bytes_for(v.cap, a.I / 128, a.row_tile);
   if (!ring) return MOE_EUNSUPPORTED;

@@ -276,10 +276,8 @@ typedef struct moe_workspace_view {
     size_t active_experts, active_count;           /* [cap], [1] */
     size_t num_tokens_post_padded;                 /* [1] */
     size_t h, h_shared, y, y_shared;               /* float tables */
-    size_t blend_counters;                         /* internal: [1] uint64 grid-barrier count
-                                                      and, after it, the decode tensor-core
-                                                      kernel's int32 call epoch; always at
-                                                      offset 0 */
+    size_t blend_counters;                         /* internal: [1] uint64 grid-barrier count,
+                                                      always at offset 0 */
     size_t router_logits;                          /* [M][E] float: the logits of a call that
                                                       computed them from x (else unwritten) */
     size_t shared_gate;                            /* [M] float: the shared expert's gates
@@ -292,9 +290,10 @@ typedef struct moe_workspace_view {
      * 32): f16 planes, h = (hi + lo) * h_scale[p][c/128] [2][max_total][I]
      * f16, and x by token: tc_x_terms holds [H/128][2][NT][64] f16 (k block,
      * 64-wide half, token, 64 k values; NT = 16 for M <= 16, else 32), x =
-     * term * tc_x_scale[t] ([32] float).  Then internal int32 counters
-     * (tc_done: [E] per active-list index, the item counter, and the token
-     * flags), which every call leaves consistent for the next.  tc_done is
+     * term * tc_x_scale[t] ([32] float).  The per-token tables are written
+     * by extra CTAs of the alignment launch.  Then internal int32 counters
+     * (tc_done: [E] per active-list index, the item counter), which every
+     * call leaves at zero.  tc_done is
      * always at offset 256 and is kept there for every M whenever the layer
      * runs a tensor-core kernel at some M (also at M the CUDA cores take):
      * the counters that persist between calls sit where M does not move
@@ -383,9 +382,12 @@ int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,
  * token_to_perm, sorted_token_ids, the active list and, on the tensor-core
  * paths, the active table of tc_items), with the x given here.  The kernels
  * and the results are those of moe_decode_layer on the same tables: one
- * launch on the tensor-core paths and on the fused CUDA-core path (which
- * aligns the ids again, to the same tables), three on the staged path
- * (gate+up, down, blend).  The workspace rules are moe_decode_layer's.
+ * launch on the fused CUDA-core path (which aligns the ids again, to the
+ * same tables); on the tensor-core paths the per-token x table of this x
+ * (one launch, when the batch uses one: FP8 up to 16 rows, NVFP4 always)
+ * then the expert kernel (NVFP4 with a shared expert: the shared expert's
+ * two kernels before it); three on the staged path (gate+up, down, blend).
+ * The workspace rules are moe_decode_layer's.
  * Errors: MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA (as moe_decode_layer). */
 int moe_decode_experts(const moe_layer_desc *layer, const uint16_t *x, int M,
                        uint16_t *out, void *workspace, size_t workspace_bytes,

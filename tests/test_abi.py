@@ -158,8 +158,8 @@ def test_tensor_core_workspace_host_only():
 def test_nvfp4_tensor_core_workspace_host_only():
     """NVFP4 routed experts at M <= 32 get the NVFP4 tensor-core kernel's
     tables: an f16 x table of 16 or 32 token columns, [2][max_total][I] f16
-    h terms, their scales and the active table; the counters (E + 1 + 32
-    ints) at 256 for every M.  With a shared expert the layer is two
+    h terms, their scales and the active table; the counters (E + 1 ints)
+    at 256 for every M.  With a shared expert the layer is two
     launches longer (its gate+up and down ahead of the kernel)."""
     lib = moe.load()
     shared = _fake_experts(E=1, H=2048, I=512)
@@ -172,7 +172,7 @@ def test_nvfp4_tensor_core_workspace_host_only():
                                                        ctypes.byref(v)) == 0
             mt, _, cap = oracle.align_sizes(M * 8, 128, 16)
             assert (v.blend_counters, v.tc_done) == (0, 256)
-            assert v.topk_ids - v.tc_done >= (128 + 1 + 32) * 4
+            assert v.topk_ids - v.tc_done >= (128 + 1) * 4
             launches = lib.moe_decode_layer_launches(ctypes.pointer(layer._struct), M, 1)
             if M > 32:   # the CUDA cores
                 assert v.tc_x_terms == v.tc_h_terms == v.tc_items == 0
