@@ -441,9 +441,9 @@ def run_nvfp4_decode(moe, stream, K: int, W: int, peaks: dict) -> dict:
     """The NVFP4 layer with its FP8 shared expert (inter 512) at M in {1, 8, 32}
     and 64: K graph-replayed steps over 4 weight copies of 340 MB, fresh
     logits every step, ungated.  M <= 32 runs both on the NVFP4 tensor-core
-    kernel (after the shared expert's two CUDA-core kernels) and on the fused
-    CUDA-core kernel, each row naming its path and whether the layer's
-    default takes it; M=64 the staged CUDA-core kernels."""
+    kernel (the shared expert inside it) and on the fused CUDA-core kernel,
+    each row naming its path and whether the layer's default takes it; M=64
+    the staged CUDA-core kernels."""
     import synth
     shape0 = synth.decode_nvfp4(1)
     base = synth.make_experts(shape0.E, shape0.H, shape0.I, shape0.fmt, SEED + 8, "cuda")

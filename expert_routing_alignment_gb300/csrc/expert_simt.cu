@@ -582,33 +582,4 @@ int simt_down(const moe_experts *routed, const moe_experts *shared, const float 
   return MOE_DISPATCH_FMT(rf, sf, launch_down_fmt, a, cpl_bucket(need), stream);
 }
 
-// The shared expert alone on the same two kernels (gate+up, then down): no
-// routed slots, one column of CTAs.  For the tensor-core layer paths, which
-// take the routed experts and leave y_sh to be blended in.
-int simt_shared(const moe_experts *shared, const uint16_t *x, int M, float *h_sh, float *y_sh,
-                void *stream) {
-  int st = validate_experts(shared, true);
-  if (st) return st;
-  if (!x || !h_sh || !y_sh || M < 1) return MOE_EINVAL;
-  if (M > MOE_MAX_ROWS) return MOE_EUNSUPPORTED;
-  GroupArgs a{};
-  a.r = a.s = to_dev(shared);
-  a.has_shared = 1;
-  a.M = M;
-  a.top_k = 1;
-  a.n = M;
-  a.cap = 0;   // every CTA takes the shared branch
-  a.x = x;
-  a.out_sh = h_sh;
-  const int gf = proj_fmt(shared->fmt, 0), df = proj_fmt(shared->fmt, 2);
-  st = MOE_DISPATCH_FMT(gf, gf, launch_gate_up_fmt, a,
-                        cpl_bucket(chunks_per_lane(gf, shared->hidden)), stream);
-  if (st) return st;
-  a.x = nullptr;
-  a.hin_sh = h_sh;
-  a.out_sh = y_sh;
-  return MOE_DISPATCH_FMT(df, df, launch_down_fmt, a,
-                          cpl_bucket(chunks_per_lane(df, shared->inter)), stream);
-}
-
 }  // namespace moe

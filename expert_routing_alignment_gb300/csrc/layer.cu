@@ -37,10 +37,8 @@ bool f4_fits(const moe_layer_desc *L, int M);
 void f4_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]);
 size_t f4_counter_ints(const moe_layer_desc *L);
 int launch_f4(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
-              const int32_t *ttp, const int32_t *act_count, const float *y_sh, uint16_t *out,
-              void *ws, const moe_workspace_view &v, uint32_t *err, void *stream);
-int simt_shared(const moe_experts *shared, const uint16_t *x, int M, float *h_sh, float *y_sh,
-                void *stream);
+              const int32_t *ttp, const int32_t *act_count, uint16_t *out, void *ws,
+              const moe_workspace_view &v, uint32_t *err, void *stream);
 int launch_fused(const moe_layer_desc *L, const uint16_t *x, int M, const float *logits,
                  const int32_t *ids, const float *w, uint16_t *out, void *ws,
                  const moe_workspace_view &v, uint32_t *err, void *stream);
@@ -63,7 +61,7 @@ static int resolve_path(const moe_experts *routed, int M, int top_k, int path) {
 
 // How moe_decode_layer runs a shape class: the fused CUDA-core kernel, the
 // FP8 tensor-core kernel, the staged CUDA-core kernels, or the NVFP4
-// tensor-core kernel (after the shared expert on the staged kernels).  It
+// tensor-core kernel (which also runs an FP8 shared expert).  It
 // depends on the shapes only, never on the routing, so a captured graph stays
 // valid for every routing.
 enum { kRunFused = 0, kRunTc = 1, kRunStaged = 2, kRunTcF4 = 3 };
@@ -249,8 +247,6 @@ extern "C" int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int
   if (with_logits == 2 && !layer->router_weight) return -1;
   const int router = with_logits == 2;   // the logits kernel ahead of the route
   if (run == moe::kRunFused) return 1 + router;
-  if (run == moe::kRunTcF4)   // the shared expert's two kernels first
-    return (with_logits ? 3 : 2) + router + (layer->shared ? 2 : 0);
   if (moe::is_tc(run)) return (with_logits ? 3 : 2) + router;
   return (with_logits ? 5 : 4) + router;
 }
@@ -328,8 +324,8 @@ extern "C" int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, 
 namespace moe {
 
 // The expert half of a layer call, after the routing and the alignment
-// tables are in the workspace: a tensor-core kernel (the NVFP4 one after the
-// shared expert's two kernels), or the staged gate+up, down and blend.
+// tables are in the workspace: a tensor-core kernel, or the staged gate+up,
+// down and blend.
 int run_experts(const moe_layer_desc *layer, int run, const uint16_t *x, int M,
                 const int32_t *ids, const float *w, uint16_t *out, void *workspace,
                 const moe_workspace_view &v, uint32_t *err_word, void *stream) {
@@ -342,14 +338,9 @@ int run_experts(const moe_layer_desc *layer, int run, const uint16_t *x, int M,
   if (run == kRunTc)
     return launch_tc(layer, x, M, w, I32(v.token_to_perm), I32(v.active_count), out, workspace,
                      v, err_word, stream);
-  if (run == kRunTcF4) {
-    if (S) {
-      const int st = simt_shared(S, x, M, F32(v.h_shared), F32(v.y_shared), stream);
-      if (st) return st;
-    }
-    return launch_f4(layer, x, M, w, I32(v.token_to_perm), I32(v.active_count),
-                     S ? F32(v.y_shared) : nullptr, out, workspace, v, err_word, stream);
-  }
+  if (run == kRunTcF4)
+    return launch_f4(layer, x, M, w, I32(v.token_to_perm), I32(v.active_count), out, workspace,
+                     v, err_word, stream);
   int st = simt_gate_up(&layer->routed, S, x, M, k, I32(v.expert_offsets),
                         I32(v.sorted_token_ids), I32(v.active_experts), I32(v.active_count),
                         F32(v.h), S ? F32(v.h_shared) : nullptr, stream);

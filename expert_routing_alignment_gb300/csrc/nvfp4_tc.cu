@@ -36,6 +36,7 @@
 //    promote (two groups of four: token columns 0-15 and 16-31).  After a
 //    grid barrier every CTA blends its share of the outputs.  Every wait
 //    gives up after about two seconds with MOE_ERR_TIMEOUT.
+#include <cstring>
 #include <mutex>
 #include <unordered_map>
 
@@ -66,6 +67,7 @@ constexpr int kMaxKBd = 32;                     // down k blocks (I <= 4096)
 constexpr int kCodeTile = 128 * 128;            // codes of one tile, two k blocks
 constexpr int kScaleTile = 128 * 16;            // scales of one tile, two k blocks
 constexpr int kHAtom = 2 * kRows * 128;         // one 64-k atom of the h terms
+constexpr int kMaxKB = 64;                      // gate+up k blocks (H <= 8192)
 
 struct F4Args {
   int M, k, n, E, H, I, cap, max_total, NT;
@@ -80,7 +82,12 @@ struct F4Args {
   uint16_t *hq;                              // f16 h terms [2][max_total][I]
   float *hs;                                 // [max_total][I/128] 2^-s per (row, block)
   float *h, *y;                              // [max_total][I], [max_total][H]
-  const float *y_sh;                         // [M][H] shared expert output, or NULL
+  // the FP8 shared expert (Is = its inter; 0 without one): rows are tokens
+  int Is;
+  const float *ssg, *ssu, *ssd;              // its block scales [Is/128][H/128], [H/128][Is/128]
+  uint16_t *hq_sh;                           // f16 h terms [2][32][Is]
+  float *hs_sh;                              // [32][Is/128]
+  float *h_sh, *y_sh;                        // [M][Is], [M][H]
   int gated;                                 // the shared term is gated
   const float *gate_vals;                    // [M] the gates (written with the x table)
   int *done, *work;
@@ -91,10 +98,13 @@ struct F4Args {
 
 // Codes {K/2 bytes, E*R rows} box {128, 128} (two k blocks, 128-byte swizzle);
 // scales {K/16 bytes, E*R rows} box {16, 128}; the x table {128, NT, 2 KB}
-// box {128, NT, 4}; the h terms {2 I bytes, max_total, 2} box {128, 16, 2}.
+// box {128, NT, 4}; the h terms {2 I bytes, max_total, 2} box {128, 16, 2};
+// the shared expert's E4M3 codes {K bytes, R rows} box {128, 128} (one k
+// block) and its h terms {2 Is bytes, 32, 2} box {128, 16, 2}.
 struct F4Maps {
   CUtensorMap codes[3], scales[3];
   CUtensorMap xt, hq;
+  CUtensorMap scodes[3], hq_sh;
 };
 
 struct Smem {
@@ -102,13 +112,14 @@ struct Smem {
   uint64_t *full, *kdone, *tfree, *iqbar, *afull, *drain;
   volatile int *iq;
   uint32_t *rec, *rlen, *trec;
-  int *twait;
+  int *twait, *kend;    // [kRecs] the stage's TMEM wait, its last k block
   volatile int *misc;   // [0] failed, [1] TMEM base, [3] row tiles, [4] grid barrier passed
   float *cs;            // [kMaxKBd][kRows] down: per-row h factors of the current item
   float *xinv;          // [kRows] gate+up: 2^-s of each row's token
   int *tokrow;          // [kRows] each row's token
   float *xtok;          // [kTokMax] 2^-s of each token
   float *glob;          // [2] the item's global scales
+  float *fs;            // [2][kMaxKB] shared items: each tile's block scale per k block
   uint32_t *red;        // [2 groups][4 quadrants][16] column maxima
   int *rtp;             // [cap + 1]
   int2 *info;           // [cap] {offset, expert | rows << 16}
@@ -119,9 +130,9 @@ constexpr int kBars = kRecs + kKd + kTfree + kIQ + kAbuf + 1;
 
 __host__ __device__ inline size_t fixed_bytes(int cap) {
   size_t b = al16(8 * kBars);
-  b += 4 * al16(4 * kRecs) + al16(4 * kIQ) + al16(4 * 16);
+  b += 5 * al16(4 * kRecs) + al16(4 * kIQ) + al16(4 * 16);
   b += al16(4 * kMaxKBd * kRows) + al16(4 * kRows) + al16(4 * kRows) + al16(4 * kTokMax) +
-       al16(4 * 2) + al16(4 * 2 * 4 * 16);
+       al16(4 * 2) + al16(4 * 2 * kMaxKB) + al16(4 * 2 * 4 * 16);
   b += al16(4 * ((size_t)cap + 1)) + al16(8 * (size_t)cap);
   return b;
 }
@@ -146,6 +157,7 @@ __device__ Smem carve(uint8_t *base, const F4Args &a) {
   S.rlen = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.trec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.twait = reinterpret_cast<int *>(take(4 * kRecs));
+  S.kend = reinterpret_cast<int *>(take(4 * kRecs));
   S.iq = reinterpret_cast<volatile int *>(take(4 * kIQ));
   S.misc = reinterpret_cast<volatile int *>(take(4 * 16));
   S.cs = reinterpret_cast<float *>(take(4 * kMaxKBd * kRows));
@@ -153,6 +165,7 @@ __device__ Smem carve(uint8_t *base, const F4Args &a) {
   S.tokrow = reinterpret_cast<int *>(take(4 * kRows));
   S.xtok = reinterpret_cast<float *>(take(4 * kTokMax));
   S.glob = reinterpret_cast<float *>(take(4 * 2));
+  S.fs = reinterpret_cast<float *>(take(4 * 2 * kMaxKB));
   S.red = reinterpret_cast<uint32_t *>(take(4 * 2 * 4 * 16));
   S.rtp = reinterpret_cast<int *>(take(4 * ((size_t)a.cap + 1)));
   S.info = reinterpret_cast<int2 *>(take(8 * (size_t)a.cap));
@@ -194,23 +207,48 @@ __device__ __forceinline__ void group_sync(int g) {
 // items
 // ---------------------------------------------------------------------------
 
+// An item: a 128-row gate+up tile (or a pair of 128-row down tiles) of one
+// 16-row tile of an expert's rows.  Shared-expert items (sh) have the tokens
+// as rows (pos0 = first token) and stream one E4M3 k block per stage; the
+// routed NVFP4 items two.  Item order: routed gate+up, shared gate+up, routed
+// down, shared down (every gate+up item is taken before any down item).
 struct Item {
-  bool gu;
+  bool gu, sh;
   int a, e, pos0, rows, tile;
 };
 
-__device__ __forceinline__ Item decode(const Smem &S, int A, int i, int TR, int FT, int FD) {
+struct Counts {
+  int TR, FT, FD, TRs, FTs;   // routed row tiles, tiles; shared row tiles, tiles
+};
+
+__device__ __forceinline__ Item decode(const Smem &S, const F4Args &a, int A, int i,
+                                       const Counts &c) {
   Item it;
+  const int G = c.TR * c.FT, Gs = c.TRs * c.FTs, D = c.TR * c.FD;
+  if ((i >= G && i < G + Gs) || i >= G + Gs + D) {   // the shared expert
+    const bool gu = i < G + Gs;
+    const int j = gu ? i - G : i - G - Gs - D, per = gu ? c.FTs : c.FD;
+    const int rt = j / per;
+    it.gu = gu;
+    it.sh = true;
+    it.tile = j - rt * per;
+    it.a = A;
+    it.e = 0;
+    it.pos0 = rt * kRows;
+    it.rows = min(kRows, a.M - rt * kRows);
+    return it;
+  }
+  it.sh = false;
   int rtg;
-  if (i < TR * FT) {
+  if (i < G) {
     it.gu = true;
-    rtg = i / FT;
-    it.tile = i - rtg * FT;
+    rtg = i / c.FT;
+    it.tile = i - rtg * c.FT;
   } else {
     it.gu = false;
-    const int j = i - TR * FT;
-    rtg = j / FD;
-    it.tile = j - rtg * FD;
+    const int j = i - G - Gs;
+    rtg = j / c.FD;
+    it.tile = j - rtg * c.FD;
   }
   int lo = 0, hi = A - 1;
   while (lo < hi) {
@@ -238,44 +276,55 @@ __device__ __forceinline__ uint32_t b_bytes(const Item &it, int NT) {
   return it.gu ? 4u * (uint32_t)NT * 128u : 4u * kHAtom;
 }
 __device__ __forceinline__ uint32_t stage_bytes(const Item &it, int NT) {
-  return b_bytes(it, NT) + 2u * kCodeTile + 2u * kScaleTile;
+  return b_bytes(it, NT) + 2u * kCodeTile + (it.sh ? 0u : 2u * kScaleTile);
 }
 __device__ __forceinline__ uint32_t acc_cols(const Item &it, int NT) {
   return 2u * (uint32_t)item_n(it, NT);
 }
+// k blocks of the item, and per stage
+__device__ __forceinline__ int item_kb(const Item &it, const F4Args &a) {
+  return it.gu ? a.H / 128 : (it.sh ? a.Is : a.I) / 128;
+}
+__device__ __forceinline__ int stage_kbs(const Item &it) { return it.sh ? 1 : 2; }
 
 // ---------------------------------------------------------------------------
 // roles
 // ---------------------------------------------------------------------------
 
-__device__ void producer(const F4Args &a, const F4Maps &m, const Smem &S, int A, int TR,
-                         int total) {
+// The gate+up tiles an expert's down items wait for (routed: its row tiles
+// times I/128; the shared expert: its row tiles times Is/128).
+__device__ __forceinline__ int gu_tiles(const Smem &S, const Item &it, const Counts &c) {
+  return it.sh ? c.TRs * c.FTs : (S.rtp[it.a + 1] - S.rtp[it.a]) * c.FT;
+}
+
+__device__ void producer(const F4Args &a, const F4Maps &m, const Smem &S, int A,
+                         const Counts &c, int total) {
   const uint64_t pol = policy_evict_first();
-  const int FT = a.I / 128, FD = a.H / 256, NT = a.NT;
+  const int NT = a.NT;
   uint32_t head = 0, thead = 0;
-  int s = 0, tail = 0, ttail = 0, jq = 0;
+  int s = 0, tail = 0, ttail = 0, jq = 0, kq = -1;
   bool ok = true;
   int i = (int)blockIdx.x < total ? (int)blockIdx.x : total;
   while (i < total && ok) {
     S.iq[jq % kIQ] = i;
     mbar_arrive(&S.iqbar[jq % kIQ]);
     ++jq;
-    const Item it = decode(S, A, i, TR, FT, FD);
+    const Item it = decode(S, a, A, i, c);
     if (!it.gu) {
-      const int need = (S.rtp[it.a + 1] - S.rtp[it.a]) * FT;
-      if (!wait_at_least(S.misc, a.done + it.a, need)) {
+      if (!wait_at_least(S.misc, a.done + it.a, gu_tiles(S, it, c))) {
         ok = false;
         break;
       }
       fence_proxy_async_global();
     }
-    const int KB = it.gu ? a.H / 128 : a.I / 128;
+    const int KB = item_kb(it, a), kbs = stage_kbs(it);
     const uint32_t size = stage_bytes(it, NT), bb = b_bytes(it, NT);
-    const uint32_t tcols = 2u * acc_cols(it, NT);
+    const uint32_t tcols = (uint32_t)kbs * acc_cols(it, NT);
     const int p0 = it.gu ? 0 : 2, p1 = it.gu ? 1 : 2;
-    const int row0 = it.gu ? it.e * a.I + it.tile * 128 : it.e * a.H + it.tile * 256;
+    const int R = it.gu ? (it.sh ? a.Is : a.I) : a.H;
+    const int row0 = it.e * R + it.tile * (it.gu ? 128 : 256);
     const int row1 = it.gu ? row0 : row0 + 128;
-    for (int kb = 0; kb < KB; kb += 2) {
+    for (int kb = 0; kb < KB; kb += kbs) {
       int need_t = -1;
       {
         const bool twrap = thead + tcols > kAccCols;
@@ -296,8 +345,8 @@ __device__ void producer(const F4Args &a, const F4Maps &m, const Smem &S, int A,
         const bool busy =
             s - tail >= kRecs || (wrap && tp >= head) || (at < tp + tl && tp < at + size);
         if (!busy) break;
-        const int kq = 2 * tail + 1;   // the stage's last k block: all its MMAs are done
-        if (!wait_bar(S, &S.kdone[kq % kKd], (uint32_t)(kq / kKd) & 1)) {
+        const int ke = S.kend[dt];   // the stage's last k block: all its MMAs are done
+        if (!wait_bar(S, &S.kdone[ke % kKd], (uint32_t)(ke / kKd) & 1)) {
           ok = false;
           break;
         }
@@ -307,26 +356,34 @@ __device__ void producer(const F4Args &a, const F4Maps &m, const Smem &S, int A,
       const uint32_t pos = ring_place(head, size, a.ring_bytes);
       const uint32_t tpos = ring_place(thead, tcols, kAccCols);
       const int d = s % kRecs;
+      kq += kbs;
       S.rec[d] = pos;
       S.rlen[d] = size;
       S.trec[d] = tpos | (tcols << 16);
       S.twait[d] = need_t;
+      S.kend[d] = kq;
       uint64_t *fb = &S.full[d];
       mbar_expect_tx(fb, size);
       uint8_t *dst = S.ring + pos;
-      // the weights first: they do not wait for the x table
-      tma_2d_hint(dst + bb, &m.codes[p0], kb * 64, row0, fb, pol);
-      tma_2d_hint(dst + bb + kCodeTile, &m.codes[p1], kb * 64, row1, fb, pol);
-      tma_2d_hint(dst + bb + 2 * kCodeTile, &m.scales[p0], kb * 8, row0, fb, pol);
-      tma_2d_hint(dst + bb + 2 * kCodeTile + kScaleTile, &m.scales[p1], kb * 8, row1, fb, pol);
+      if (it.sh) {   // one E4M3 k block of each tile
+        tma_2d_hint(dst + bb, &m.scodes[p0], kb * 128, row0, fb, pol);
+        tma_2d_hint(dst + bb + kCodeTile, &m.scodes[p1], kb * 128, row1, fb, pol);
+      } else {       // two k blocks of E2M1 codes and their scales
+        tma_2d_hint(dst + bb, &m.codes[p0], kb * 64, row0, fb, pol);
+        tma_2d_hint(dst + bb + kCodeTile, &m.codes[p1], kb * 64, row1, fb, pol);
+        tma_2d_hint(dst + bb + 2 * kCodeTile, &m.scales[p0], kb * 8, row0, fb, pol);
+        tma_2d_hint(dst + bb + 2 * kCodeTile + kScaleTile, &m.scales[p1], kb * 8, row1, fb, pol);
+      }
+      // the B operand: 4 atoms of 64 k (a shared stage uses the first two;
+      // atoms past the end read as zeros)
       if (it.gu) {
-        tma_3d(dst, &m.xt, 0, 0, 2 * kb, fb);   // 4 atoms x NT tokens
+        tma_3d(dst, &m.xt, 0, 0, 2 * kb, fb);   // x 4 atoms x NT tokens
       } else {
+        const CUtensorMap *hm = it.sh ? &m.hq_sh : &m.hq;
         for (int at4 = 0; at4 < 4; ++at4)         // 4 atoms x (2 terms x 16 rows)
-          tma_3d(dst + at4 * kHAtom, &m.hq, kb * 256 + at4 * 128, it.pos0, 0, fb);
+          tma_3d(dst + at4 * kHAtom, hm, kb * 256 + at4 * 128, it.pos0, 0, fb);
       }
       ++s;
-      if (!ok) break;
     }
     i = (int)gridDim.x + atomicAdd(a.work, 1);
   }
@@ -340,13 +397,54 @@ __device__ void producer(const F4Args &a, const F4Maps &m, const Smem &S, int A,
   }
 }
 
+// One weight row's 128 k of a routed tile (k block kbl of the two in the
+// 128-byte row): w / global = e2m1 * e4m3 scale, exact in f16, as 64 packed
+// pairs (column c = k 2c, 2c + 1).  The row's bytes sit in 16-byte chunks
+// permuted by the 128-byte swizzle (chunk j at j ^ (row % 8)).
+__device__ __forceinline__ void decode_e2m1(const uint8_t *crow, const uint8_t *srow, int r,
+                                            int kbl, uint32_t (&v)[64]) {
+  const uint2 sv = *reinterpret_cast<const uint2 *>(srow + kbl * 8);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int chunk = kbl * 4 + c;   // 16 bytes: 32 codes, groups 2c and 2c + 1
+    const uint4 cv = *reinterpret_cast<const uint4 *>(crow + ((chunk ^ (r & 7)) << 4));
+    const uint32_t words[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+    for (int g2 = 0; g2 < 2; ++g2) {
+      const int g = 2 * c + g2;
+      const uint32_t sbyte = (g < 4 ? sv.x >> (8 * g) : sv.y >> (8 * (g - 4))) & 0xFFu;
+      const uint32_t s2 = e4m3x2_to_f16x2((uint16_t)(sbyte | (sbyte << 8)));
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const uint32_t byte = (words[g2 * 2 + b / 4] >> (8 * (b % 4))) & 0xFFu;
+        uint32_t f = e2m1x2_to_f16x2(byte);
+        asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(f) : "r"(s2));
+        v[c * 16 + g2 * 8 + b] = f;
+      }
+    }
+  }
+}
+
+// One weight row's 128 k of a shared-expert tile: the E4M3 codes as f16
+// (exact); the block scale is applied when the k block is promoted.
+__device__ __forceinline__ void decode_e4m3(const uint8_t *crow, int r, uint32_t (&v)[64]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 cv = *reinterpret_cast<const uint4 *>(crow + ((c ^ (r & 7)) << 4));
+    const uint32_t words[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+    for (int p = 0; p < 8; ++p)
+      v[c * 8 + p] = e4m3x2_to_f16x2((uint16_t)((words[p / 2] >> (16 * (p % 2))) & 0xFFFFu));
+  }
+}
+
 // Warps 2-5: each thread decodes one weight row (warp w: rows 32 (w % 4) ..)
-// of a tile's k block into the A buffer: w / global = e2m1 * e4m3 scale,
-// exact in f16, 64 columns of packed pairs.
-__device__ void decoder(const F4Args &a, const Smem &S, int A, int TR, int total, uint32_t tmem) {
+// of a tile's k block into an A buffer of tensor memory.
+__device__ void decoder(const F4Args &a, const Smem &S, int A, const Counts &cn, int total,
+                        uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3;
   const int r = q * 32 + lane;
-  const int FT = a.I / 128, FD = a.H / 256, NT = a.NT;
+  const int NT = a.NT;
   const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
   uint32_t head = 0;
   int s = 0, abn = 0;
@@ -359,10 +457,10 @@ __device__ void decoder(const F4Args &a, const Smem &S, int A, int TR, int total
       break;
     }
     if (i >= total) break;
-    const Item it = decode(S, A, i, TR, FT, FD);
-    const int KB = it.gu ? a.H / 128 : a.I / 128;
+    const Item it = decode(S, a, A, i, cn);
+    const int KB = item_kb(it, a), kbs = stage_kbs(it);
     const uint32_t size = stage_bytes(it, NT), bb = b_bytes(it, NT);
-    for (int kb = 0; kb < KB && ok; kb += 2) {
+    for (int kb = 0; kb < KB && ok; kb += kbs) {
       const uint32_t pos = ring_place(head, size, a.ring_bytes);
       const int d = s % kRecs;
       if (!__all_sync(0xFFFFFFFFu, wait_bar(S, &S.full[d], (uint32_t)(s / kRecs) & 1))) {
@@ -371,10 +469,10 @@ __device__ void decoder(const F4Args &a, const Smem &S, int A, int TR, int total
       }
       const uint8_t *codes = S.ring + pos + bb;
       const uint8_t *scales = codes + 2 * kCodeTile;
-      for (int kbl = 0; kbl < 2 && ok; ++kbl)
+      for (int kbl = 0; kbl < kbs && ok; ++kbl)
         for (int t = 0; t < 2; ++t) {
           const int ab = abn % kAbuf;
-          if (abn >= kAbuf) {
+          if (abn >= kAbuf) {   // the k block that read this buffer (two buffers per k block)
             if (!__all_sync(0xFFFFFFFFu,
                             wait_bar(S, &S.kdone[(abn / 2 - 2) % kKd],
                                      (uint32_t)((abn / 2 - 2) / kKd) & 1))) {
@@ -384,29 +482,11 @@ __device__ void decoder(const F4Args &a, const Smem &S, int A, int TR, int total
             tc_fence_after();   // the MMAs that read the buffer are complete
           }
           const uint8_t *crow = codes + t * kCodeTile + r * 128;
-          const uint2 sv =
-              *reinterpret_cast<const uint2 *>(scales + t * kScaleTile + r * 16 + kbl * 8);
           uint32_t v[64];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int chunk = kbl * 4 + c;   // 16 bytes: 32 codes, groups 2c and 2c + 1
-            const uint4 cv =
-                *reinterpret_cast<const uint4 *>(crow + ((chunk ^ (r & 7)) << 4));
-            const uint32_t words[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-            for (int g2 = 0; g2 < 2; ++g2) {
-              const int g = 2 * c + g2;
-              const uint32_t sbyte = (g < 4 ? sv.x >> (8 * g) : sv.y >> (8 * (g - 4))) & 0xFFu;
-              const uint32_t s2 = e4m3x2_to_f16x2((uint16_t)(sbyte | (sbyte << 8)));
-#pragma unroll
-              for (int b = 0; b < 8; ++b) {
-                const uint32_t byte = (words[g2 * 2 + b / 4] >> (8 * (b % 4))) & 0xFFu;
-                uint32_t f = e2m1x2_to_f16x2(byte);
-                asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(f) : "r"(s2));
-                v[c * 16 + g2 * 8 + b] = f;
-              }
-            }
-          }
+          if (it.sh)
+            decode_e4m3(crow, r, v);
+          else
+            decode_e2m1(crow, scales + t * kScaleTile + r * 16, r, kbl, v);
           tmem_st64(lane_base + (uint32_t)ab * kAcols, v);
           tmem_wait_st();
           tc_fence_before();
@@ -420,9 +500,9 @@ __device__ void decoder(const F4Args &a, const Smem &S, int A, int TR, int total
   if (!ok) fail(S, a);
 }
 
-__device__ void mma_issuer(const F4Args &a, const Smem &S, int A, int TR, int total,
+__device__ void mma_issuer(const F4Args &a, const Smem &S, int A, const Counts &cn, int total,
                            uint32_t tmem) {
-  const int FT = a.I / 128, FD = a.H / 256, NT = a.NT;
+  const int NT = a.NT;
   const uint32_t ring = smem_addr(S.ring);
   uint32_t head = 0, thead = 0;
   int s = 0, q = 0, abn = 0, tdone = -1;
@@ -431,13 +511,13 @@ __device__ void mma_issuer(const F4Args &a, const Smem &S, int A, int TR, int to
     const int i = next_item(S, jq);
     if (i < 0) ok = false;
     if (i < 0 || i >= total) break;
-    const Item it = decode(S, A, i, TR, FT, FD);
-    const int KB = it.gu ? a.H / 128 : a.I / 128;
+    const Item it = decode(S, a, A, i, cn);
+    const int KB = item_kb(it, a), kbs = stage_kbs(it);
     const int N = item_n(it, NT);
     const uint32_t id = idesc_f16(N), cols = acc_cols(it, NT);
-    const uint32_t size = stage_bytes(it, NT), tcols = 2u * cols;
+    const uint32_t size = stage_bytes(it, NT), tcols = (uint32_t)kbs * cols;
     const uint32_t atom_bytes = it.gu ? (uint32_t)NT * 128u : (uint32_t)kHAtom;
-    for (int kb = 0; kb < KB; kb += 2) {
+    for (int kb = 0; kb < KB; kb += kbs) {
       const uint32_t base = ring + ring_place(head, size, a.ring_bytes);
       const uint32_t tbase = tmem + kAccBase + ring_place(thead, tcols, kAccCols);
       const int d = s % kRecs;
@@ -454,7 +534,7 @@ __device__ void mma_issuer(const F4Args &a, const Smem &S, int A, int TR, int to
       // the stage's B operand: a descriptor moves by (bytes / 16)
       const uint64_t bd0 = sdesc(base);
       const uint32_t astep = atom_bytes >> 4;
-      for (int kbl = 0; kbl < 2 && ok; ++kbl) {
+      for (int kbl = 0; kbl < kbs && ok; ++kbl) {
         for (int t = 0; t < 2; ++t) {
           const int ab = abn % kAbuf;
           if (!wait_bar(S, &S.afull[ab], (uint32_t)(abn / kAbuf) & 1)) {
@@ -475,8 +555,8 @@ __device__ void mma_issuer(const F4Args &a, const Smem &S, int A, int TR, int to
         if (!ok) break;
         // One commit per k block (each commit costs the tensor pipe about as
         // much as two MMAs): it frees the k block's two A buffers, hands its
-        // accumulators to the promotion, and after the second k block frees
-        // the ring stage.
+        // accumulators to the promotion, and after the stage's last k block
+        // frees the ring stage.
         mma_commit(&S.kdone[q % kKd]);
         ++q;
       }
@@ -498,7 +578,12 @@ __device__ void mma_issuer(const F4Args &a, const Smem &S, int A, int TR, int to
 __device__ void finish_gate_up(const F4Args &a, const Smem &S, const Item &it, int grp, int q,
                                int lane, const float (&acc0)[16], const float (&acc1)[16]) {
   const int f = q * 32 + lane, o = it.tile * 128 + f;
-  const int KBd = a.I / 128;
+  // routed rows by sorted position, the shared expert's by token
+  const int Iw = it.sh ? a.Is : a.I, KBd = Iw / 128;
+  float *const hb = it.sh ? a.h_sh : a.h;
+  uint16_t *const hqb = it.sh ? a.hq_sh : a.hq;
+  float *const hsb = it.sh ? a.hs_sh : a.hs;
+  const size_t plane = it.sh ? (size_t)kTokMax * a.Is : (size_t)a.max_total * a.I;
   const float g0 = S.glob[0], g1 = S.glob[1];
   float hv[16];
 #pragma unroll
@@ -519,7 +604,7 @@ __device__ void finish_gate_up(const F4Args &a, const Smem &S, const Item &it, i
       }
       const float xi = S.xinv[j];
       hv[j] = silu_f32(gv * g0 * xi) * (uv * g1 * xi);
-      a.h[(size_t)(it.pos0 + j) * a.I + o] = hv[j];
+      hb[(size_t)(it.pos0 + j) * Iw + o] = hv[j];
       mx = __float_as_uint(fabsf(hv[j]));
     }
     mx = __reduce_max_sync(0xFFFFFFFFu, mx);
@@ -540,9 +625,8 @@ __device__ void finish_gate_up(const F4Args &a, const Smem &S, const Item &it, i
     scl = pow2f(sh);
     const int t = S.tokrow[lane] - 16 * grp;
     if (q == 0 && lane < it.rows && t >= 0 && t < 16)
-      a.hs[(size_t)(it.pos0 + lane) * KBd + it.tile] = pow2f(-sh);
+      hsb[(size_t)(it.pos0 + lane) * KBd + it.tile] = pow2f(-sh);
   }
-  const size_t plane = (size_t)a.max_total * a.I;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     if (j >= it.rows) break;
@@ -552,41 +636,44 @@ __device__ void finish_gate_up(const F4Args &a, const Smem &S, const Item &it, i
       const float v = hv[j] * sj;
       const uint16_t hi = f16_rn(v);
       const uint16_t lo = f16_rn(v - f16_to_f32(hi));
-      uint16_t *dst = a.hq + (size_t)(it.pos0 + j) * a.I + o;
+      uint16_t *dst = hqb + (size_t)(it.pos0 + j) * Iw + o;
       dst[0] = hi;
       dst[plane] = lo;
     }
   }
 }
 
-// acc[j] += sum over n of the column values (scale 1; gate+up) or
-// acc[j] += hf[j] * (term 0 + term 1) (down): 16 columns of this warp's lanes.
-__device__ __forceinline__ void promote_gu(uint32_t col, float (&acc)[16]) {
+// acc[j] += f * (column value) (gate+up), or acc[j] += hf[j] f (term 0 +
+// term 1) (down), for 16 columns of this warp's lanes; f is the shared
+// expert's block scale of the k block (1 for routed items, whose scales are
+// in the decoded weights).
+__device__ __forceinline__ void promote_gu(uint32_t col, float f, float (&acc)[16]) {
   uint32_t r[16];
   tmem_ld16(col, r);
   tmem_wait_ld();
 #pragma unroll
-  for (int jj = 0; jj < 16; ++jj) acc[jj] += __uint_as_float(r[jj]);
+  for (int jj = 0; jj < 16; ++jj) acc[jj] = fmaf(f, __uint_as_float(r[jj]), acc[jj]);
 }
-__device__ __forceinline__ void promote_dn(uint32_t col, const float *hf, float (&acc)[16]) {
+__device__ __forceinline__ void promote_dn(uint32_t col, const float *hf, float f,
+                                           float (&acc)[16]) {
   uint32_t r[16], r2[16];
   tmem_ld16(col, r);
   tmem_ld16(col + kRows, r2);
   tmem_wait_ld();
 #pragma unroll
   for (int jj = 0; jj < 16; ++jj)
-    acc[jj] = fmaf(hf[jj], __uint_as_float(r[jj]) + __uint_as_float(r2[jj]), acc[jj]);
+    acc[jj] = fmaf(hf[jj] * f, __uint_as_float(r[jj]) + __uint_as_float(r2[jj]), acc[jj]);
 }
 
 // Warps 6-13: group g = (w - 6) / 4 holds token columns 16 g .. 16 g + 15 of a
 // gate+up item; group 0 the 16 rows of a down item.  Warp w reads TMEM lanes
 // 32 (w % 4) ..
-__device__ void epilogue(const F4Args &a, const Smem &S, int A, int TR, int total,
+__device__ void epilogue(const F4Args &a, const Smem &S, int A, const Counts &cn, int total,
                          uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = (warp - kEpi0) >> 2, q = warp & 3;
   const int et = threadIdx.x - kEpi0 * 32;
-  const int FT = a.I / 128, FD = a.H / 256, KBd = a.I / 128, NT = a.NT;
+  const int NT = a.NT, KBh = a.H / 128;
   const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
   int s = 0, st = 0;
   uint32_t thead = 0;
@@ -601,38 +688,47 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, int TR, int tota
       break;
     }
     if (i >= total) break;
-    const Item it = decode(S, A, i, TR, FT, FD);
-    const int KB = it.gu ? a.H / 128 : KBd;
+    const Item it = decode(S, a, A, i, cn);
+    const int KB = item_kb(it, a), kbs = stage_kbs(it);
+    const int KBd = (it.sh ? a.Is : a.I) / 128;
     // the item's rows, scales and (down) its dependency
-    if (et == 0 && !it.gu) {
-      const int need = (S.rtp[it.a + 1] - S.rtp[it.a]) * FT;
-      if (!wait_at_least(S.misc, a.done + it.a, need)) fail(S, a);
-    }
+    if (et == 0 && !it.gu && !wait_at_least(S.misc, a.done + it.a, gu_tiles(S, it, cn)))
+      fail(S, a);
     if (et < kRows) {
-      const int t = et < it.rows ? __ldcg(a.sti + it.pos0 + et) / a.k : 0;
+      int t = 0;
+      if (et < it.rows) t = it.sh ? it.pos0 + et : __ldcg(a.sti + it.pos0 + et) / a.k;
       S.tokrow[et] = et < it.rows ? t : -1;
       S.xinv[et] = et < it.rows ? S.xtok[t] : 0.f;
     }
     if (et == 0) {
-      S.glob[0] = it.gu ? __ldg(a.gg + it.e) : __ldg(a.gd + it.e);
-      S.glob[1] = it.gu ? __ldg(a.gu + it.e) : 0.f;
+      S.glob[0] = it.sh ? 1.f : (it.gu ? __ldg(a.gg + it.e) : __ldg(a.gd + it.e));
+      S.glob[1] = it.sh ? 1.f : (it.gu ? __ldg(a.gu + it.e) : 0.f);
     }
+    // (the down item's h scales are read only after the dependency wait)
     if (epi_sync_or(S.misc[0])) {
       bad = true;
       break;
     }
+    if (it.sh) {   // each tile's block scale per k block
+      for (int idx = et; idx < 2 * KB; idx += kEpiThreads) {
+        const int t = idx / KB, kb = idx - t * KB;
+        S.fs[t * kMaxKB + kb] = it.gu ? __ldg((t ? a.ssu : a.ssg) + it.tile * KBh + kb)
+                                      : __ldg(a.ssd + (2 * it.tile + t) * KBd + kb);
+      }
+    }
     if (!it.gu) {
+      const float *hsb = it.sh ? a.hs_sh : a.hs;
       for (int idx = et; idx < KB * kRows; idx += kEpiThreads) {
         const int kb = idx / kRows, j = idx - kb * kRows;
-        S.cs[idx] = j < it.rows ? __ldcg(a.hs + (size_t)(it.pos0 + j) * KBd + kb) : 0.f;
+        S.cs[idx] = j < it.rows ? __ldcg(hsb + (size_t)(it.pos0 + j) * KBd + kb) : 0.f;
       }
-      epi_sync();
     }
+    if (it.sh || !it.gu) epi_sync();
     float acc0[16], acc1[16];
 #pragma unroll
     for (int jj = 0; jj < 16; ++jj) acc0[jj] = acc1[jj] = 0.f;
     const int N = item_n(it, NT);
-    const uint32_t cols = acc_cols(it, NT), tcols = 2u * cols;
+    const uint32_t cols = acc_cols(it, NT), tcols = (uint32_t)kbs * cols;
     // Only the groups that hold columns of the item read TMEM; the first
     // warp also arrives for the warps of the other group, which skip the
     // k blocks.
@@ -640,13 +736,13 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, int TR, int tota
     const int nmine = it.gu && NT > 16 ? kEpiWarps : 4;
     const uint32_t arrivals = warp == kEpi0 ? (uint32_t)(kEpiWarps - nmine + 1) : 1u;
     if (!mine) {
-      for (int kb = 0; kb < KB; kb += 2) ring_place(thead, tcols, kAccCols);
+      for (int kb = 0; kb < KB; kb += kbs) ring_place(thead, tcols, kAccCols);
       s += KB;
-      st += KB / 2;
+      st += KB / kbs;
     }
     uint32_t tbase = 0;
     for (int kb = 0; kb < KB && mine; ++kb) {
-      const int j = kb & 1;
+      const int j = kb % kbs;
       if (j == 0) tbase = ring_place(thead, tcols, kAccCols);
       // every lane of the warp takes the same branch into the aligned TMEM loads
       if (!__all_sync(0xFFFFFFFFu, wait_bar(S, &S.kdone[s % kKd], (uint32_t)(s / kKd) & 1))) {
@@ -655,15 +751,16 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, int TR, int tota
       }
       tc_fence_after();
       const uint32_t col = lane_base + kAccBase + tbase + (uint32_t)j * cols;
+      const float f0 = it.sh ? S.fs[kb] : 1.f, f1 = it.sh ? S.fs[kMaxKB + kb] : 1.f;
       if (it.gu) {
-        promote_gu(col + 16u * (uint32_t)grp, acc0);
-        promote_gu(col + (uint32_t)N + 16u * (uint32_t)grp, acc1);
+        promote_gu(col + 16u * (uint32_t)grp, f0, acc0);
+        promote_gu(col + (uint32_t)N + 16u * (uint32_t)grp, f1, acc1);
       } else {
-        promote_dn(col, S.cs + kb * kRows, acc0);
-        promote_dn(col + (uint32_t)N, S.cs + kb * kRows, acc1);
+        promote_dn(col, S.cs + kb * kRows, f0, acc0);
+        promote_dn(col + (uint32_t)N, S.cs + kb * kRows, f1, acc1);
       }
       ++s;
-      if (j == 1) {   // the stage's accumulators are free
+      if (j == kbs - 1) {   // the stage's accumulators are free
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_n(&S.tfree[st % kTfree], arrivals);
@@ -687,10 +784,11 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, int TR, int tota
     } else if (mine) {
       const float gd = S.glob[0];
       const int c0 = it.tile * 256 + q * 32 + lane;
+      float *const yb = it.sh ? a.y_sh : a.y;
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) {
         if (jj >= it.rows) break;
-        float *yr = a.y + (size_t)(it.pos0 + jj) * a.H + c0;
+        float *yr = yb + (size_t)(it.pos0 + jj) * a.H + c0;
         yr[0] = acc0[jj] * gd;
         yr[128] = acc1[jj] * gd;
       }
@@ -758,19 +856,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  const int TR = S.misc[3];
-  const int total = S.misc[0] ? 0 : TR * (a.I / 128 + a.H / 256);
+  Counts cn;
+  cn.TR = S.misc[3];
+  cn.FT = a.I / 128;
+  cn.FD = a.H / 256;
+  cn.TRs = a.Is ? (a.M + kRows - 1) / kRows : 0;
+  cn.FTs = a.Is / 128;
+  const int total = S.misc[0] ? 0 : cn.TR * (cn.FT + cn.FD) + cn.TRs * (cn.FTs + cn.FD);
 
   if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) producer(a, maps, S, A, TR, total);
+    if ((threadIdx.x & 31) == 0) producer(a, maps, S, A, cn, total);
     __syncwarp();
   } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0) mma_issuer(a, S, A, TR, total, tmem);
+    if ((threadIdx.x & 31) == 0) mma_issuer(a, S, A, cn, total, tmem);
     __syncwarp();
   } else if (warp < kEpi0) {
-    decoder(a, S, A, TR, total, tmem);
+    decoder(a, S, A, cn, total, tmem);
   } else {
-    epilogue(a, S, A, TR, total, tmem);
+    epilogue(a, S, A, cn, total, tmem);
   }
 
   tc_fence_before();
@@ -811,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < a.cap; i += kThreads) a.done[i] = 0;
+    for (int i = threadIdx.x; i <= a.cap; i += kThreads) a.done[i] = 0;
     if (threadIdx.x == 0) {
       *a.work = 0;
     }
@@ -851,33 +954,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host
 // ---------------------------------------------------------------------------
 
-int f4_maps(const moe_experts *X, const uint8_t *xt, uint16_t *hq, int max_total, int NT,
-            F4Maps *out) {
+int f4_maps(const moe_experts *X, const moe_experts *Sx, const uint8_t *xt, uint16_t *hq,
+            uint16_t *hq_sh, int max_total, int NT, F4Maps *out) {
   // every address a map holds is part of the key (codes and scales of the
-  // three projections, the two workspace tables)
+  // three projections, the shared expert's codes, the workspace tables)
   struct Key {
-    const void *g, *u, *d, *gs, *us, *ds, *xt, *hq;
-    int E, H, I, mt, nt;
+    const void *p[11];
+    int E, H, I, Is, mt, nt;
     bool operator==(const Key &o) const {
-      return g == o.g && u == o.u && d == o.d && gs == o.gs && us == o.us && ds == o.ds &&
-             xt == o.xt && hq == o.hq && E == o.E && H == o.H && I == o.I && mt == o.mt &&
-             nt == o.nt;
+      for (int j = 0; j < 11; ++j)
+        if (p[j] != o.p[j]) return false;
+      return E == o.E && H == o.H && I == o.I && Is == o.Is && mt == o.mt && nt == o.nt;
     }
   };
   struct KeyHash {
     size_t operator()(const Key &k) const {
-      size_t h = std::hash<const void *>()(k.g);
-      for (const void *p : {k.u, k.d, k.gs, k.us, k.ds, k.xt, k.hq})
-        h = h * 1000003u ^ std::hash<const void *>()(p);
+      size_t h = 0;
+      for (int j = 0; j < 11; ++j) h = h * 1000003u ^ std::hash<const void *>()(k.p[j]);
       return h ^ ((size_t)k.E << 40) ^ ((size_t)k.H << 20) ^ (size_t)k.I ^ ((size_t)k.mt << 50) ^
-             ((size_t)k.nt << 58);
+             ((size_t)k.nt << 58) ^ ((size_t)k.Is << 30);
     }
   };
   static std::mutex mu;
   static std::unordered_map<Key, F4Maps, KeyHash> cache;
-  const int E = X->num_experts, H = X->hidden, I = X->inter;
-  const Key key = {X->gate.codes, X->up.codes, X->down.codes, X->gate.scale, X->up.scale,
-                   X->down.scale, xt, hq, E, H, I, max_total, NT};
+  const int E = X->num_experts, H = X->hidden, I = X->inter, Is = Sx ? Sx->inter : 0;
+  const Key key = {{X->gate.codes, X->up.codes, X->down.codes, X->gate.scale, X->up.scale,
+                    X->down.scale, xt, hq, Sx ? Sx->gate.codes : nullptr,
+                    Sx ? Sx->up.codes : nullptr, Sx ? Sx->down.codes : nullptr},
+                   E, H, I, Is, max_total, NT};
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it != cache.end()) {
@@ -885,6 +989,7 @@ int f4_maps(const moe_experts *X, const uint8_t *xt, uint16_t *hq, int max_total
     return MOE_OK;
   }
   F4Maps m;
+  memset(&m, 0, sizeof(m));
   const moe_proj *P[3] = {&X->gate, &X->up, &X->down};
   for (int j = 0; j < 3; ++j) {
     const int K = j < 2 ? H : I, R = j < 2 ? I : H;
@@ -913,6 +1018,22 @@ int f4_maps(const moe_experts *X, const uint8_t *xt, uint16_t *hq, int max_total
     const int st = encode_u8_sw128(&m.hq, hq, 3, d, s, box);
     if (st) return st;
   }
+  if (Sx) {   // the shared expert: E4M3 codes [R][K], its h terms [2][32][Is]
+    const moe_proj *Q[3] = {&Sx->gate, &Sx->up, &Sx->down};
+    for (int j = 0; j < 3; ++j) {
+      const int K = j < 2 ? H : Is, R = j < 2 ? Is : H;
+      const cuuint64_t cd[2] = {(cuuint64_t)K, (cuuint64_t)R};
+      const cuuint64_t cs[1] = {(cuuint64_t)K};
+      const cuuint32_t cbox[2] = {128, 128};
+      const int st = encode_u8_sw128(&m.scodes[j], Q[j]->codes, 2, cd, cs, cbox);
+      if (st) return st;
+    }
+    const cuuint64_t d[3] = {(cuuint64_t)2 * Is, (cuuint64_t)kTokMax, 2};
+    const cuuint64_t s[2] = {(cuuint64_t)2 * Is, (cuuint64_t)2 * Is * kTokMax};
+    const cuuint32_t box[3] = {128, (cuuint32_t)kRows, 2};
+    const int st = encode_u8_sw128(&m.hq_sh, hq_sh, 3, d, s, box);
+    if (st) return st;
+  }
   if (cache.size() > 1024) cache.clear();
   cache.emplace(key, m);
   *out = m;
@@ -931,36 +1052,43 @@ size_t ring_bytes_for(int cap) {
 }  // namespace
 
 // Shape admission (host): NVFP4 routed experts, M <= 32, H and I multiples of
-// 256 (H up to 8192, I up to 4096), room for the ring.  A shared expert runs
-// on the CUDA-core kernels ahead of this one.
+// 256 (H up to 8192, I up to 4096), a shared expert (if any) in FP8 with its
+// inter a multiple of 128 up to 4096, room for the ring.
 bool f4_fits(const moe_layer_desc *L, int M) {
   const moe_experts &R = L->routed;
   if (R.fmt != MOE_FMT_NVFP4_G16 || M > kTokMax) return false;
-  if (R.hidden % 256 || R.hidden > 8192 || R.inter % 256 || R.inter > 128 * kMaxKBd) return false;
+  if (R.hidden % 256 || R.hidden > 128 * kMaxKB || R.inter % 256 || R.inter > 128 * kMaxKBd)
+    return false;
+  if (L->shared && (L->shared->fmt != MOE_FMT_FP8_B128 || L->shared->inter % 128 ||
+                    L->shared->inter > 128 * kMaxKBd))
+    return false;
   const int n = M * L->top_k;
   const int cap = n < R.num_experts ? n : R.num_experts;
   return ring_bytes_for(cap) != 0;
 }
 
 // Workspace of this path (byte sizes, in order): the x table, the token
-// scales, the h terms, their scales and the active table.
+// scales, the h terms (routed [2][max_total][I], then the shared expert's
+// [2][32][Is]), their scales (routed, then shared) and the active table.
 void f4_workspace(const moe_layer_desc *L, int max_total, int cap, size_t (&bytes)[5]) {
   const size_t H = L->routed.hidden, I = L->routed.inter;
+  const size_t Is = L->shared ? L->shared->inter : 0;
   bytes[0] = 2 * (size_t)kTokMax * H;
   bytes[1] = (size_t)kTokMax * 4;
-  bytes[2] = 2 * 2 * (size_t)max_total * I;
-  bytes[3] = (size_t)max_total * (I / 128) * 4;
+  bytes[2] = 2 * 2 * ((size_t)max_total * I + (size_t)kTokMax * Is);
+  bytes[3] = ((size_t)max_total * (I / 128) + (size_t)kTokMax * (Is / 128)) * 4;
   bytes[4] = (size_t)cap * 16;
 }
 
-// Counters, in ints (sized by the layer alone): done [E], the item counter.
-size_t f4_counter_ints(const moe_layer_desc *L) { return (size_t)L->routed.num_experts + 1; }
+// Counters, in ints (sized by the layer alone): done [E + 1] (the last one
+// can be the shared expert's), the item counter.
+size_t f4_counter_ints(const moe_layer_desc *L) { return (size_t)L->routed.num_experts + 2; }
 
 int launch_f4(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
-              const int32_t *ttp, const int32_t *act_count, const float *y_sh,
-              uint16_t *out, void *ws, const moe_workspace_view &v, uint32_t *err,
-              void *stream) {
+              const int32_t *ttp, const int32_t *act_count, uint16_t *out, void *ws,
+              const moe_workspace_view &v, uint32_t *err, void *stream) {
   const moe_experts &R = L->routed;
+  const moe_experts *Sx = L->shared;
   char *base = static_cast<char *>(ws);
   F4Args a = {};
   a.M = M;
@@ -988,18 +1116,27 @@ int launch_f4(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
   a.hs = reinterpret_cast<float *>(base + v.tc_h_scale);
   a.h = reinterpret_cast<float *>(base + v.h);
   a.y = reinterpret_cast<float *>(base + v.y);
-  a.y_sh = y_sh;
-  a.gated = y_sh && L->shared_gate ? 1 : 0;
+  if (Sx) {
+    a.Is = Sx->inter;
+    a.ssg = static_cast<const float *>(Sx->gate.scale);
+    a.ssu = static_cast<const float *>(Sx->up.scale);
+    a.ssd = static_cast<const float *>(Sx->down.scale);
+    a.hq_sh = a.hq + (size_t)2 * v.max_total * a.I;
+    a.hs_sh = a.hs + (size_t)v.max_total * (a.I / 128);
+    a.h_sh = reinterpret_cast<float *>(base + v.h_shared);
+    a.y_sh = reinterpret_cast<float *>(base + v.y_shared);
+    a.gated = L->shared_gate ? 1 : 0;
+  }
   a.gate_vals = reinterpret_cast<float *>(base + v.shared_gate);
   a.done = reinterpret_cast<int *>(base + v.tc_done);
-  a.work = a.done + a.E;
+  a.work = a.done + a.E + 1;
   a.grid_ctr = reinterpret_cast<unsigned long long *>(base + v.blend_counters);
   a.err = err;
   const size_t ring = ring_bytes_for(v.cap);
   if (!ring) return MOE_EUNSUPPORTED;
   a.ring_bytes = (uint32_t)ring;
   F4Maps maps;
-  int st = f4_maps(&R, a.xt, a.hq, v.max_total, a.NT, &maps);
+  int st = f4_maps(&R, Sx, a.xt, a.hq, a.hq_sh, v.max_total, a.NT, &maps);
   if (st) return st;
   const size_t smem = ring + fixed_bytes(v.cap);
   st = ensure_smem_limit((const void *)nvfp4_ffn_kernel, smem);

@@ -288,7 +288,8 @@ typedef struct moe_workspace_view {
      * and [max_total] float; h = (t0 + t1 + t2) * h_scale[p][c/128]
      * [3][max_total][I] u8 and [max_total][I/128] float.  NVFP4 experts (M <=
      * 32): f16 planes, h = (hi + lo) * h_scale[p][c/128] [2][max_total][I]
-     * f16, and x by token: tc_x_terms holds [H/128][2][NT][64] f16 (k block,
+     * f16 (then the FP8 shared expert's [2][32][Is] by token, and after the
+     * [max_total][I/128] scales its [32][Is/128]), and x by token: tc_x_terms holds [H/128][2][NT][64] f16 (k block,
      * 64-wide half, token, 64 k values; NT = 16 for M <= 16, else 32), x =
      * term * tc_x_scale[t] ([32] float).  The per-token tables are written
      * by extra CTAs of the alignment launch.  Then internal int32 counters
@@ -321,8 +322,7 @@ int moe_decode_layer_workspace_view(const moe_layer_desc *layer, int M,
 
 /* Host only.  The number of kernels moe_decode_layer enqueues for M rows
  * (1 on the fused decode path; 3 with router logits, 2 with given ids on the
- * tensor-core path, two more with a shared expert on the NVFP4 one;
- * otherwise 5 and 4), or -1 if the call would be
+ * tensor-core paths; otherwise 5 and 4), or -1 if the call would be
  * rejected.  with_logits: 0 ids given, 1 logits given, 2 logits computed from
  * x and the layer's router_weight (one launch more than 1). */
 int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logits);
@@ -353,9 +353,9 @@ int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logit
  * ("forward_nvfp4_grouped_decode.rs", the NVFP4 grouped launchers): each
  * E2M1 code times its E4M3 scale decoded exactly to f16 into tensor memory,
  * tcgen05 kind::f16 MMAs against an f16 x table by token and f16 hi/lo
- * splits of h, the fp32 globals applied once per item; a shared expert runs
- * first on the CUDA-core gate+up and down kernels (two launches more) and is
- * blended in by the same kernel.  Either kernel's h and y are the same
+ * splits of h, the fp32 globals applied once per item; an FP8 shared expert
+ * (inter a multiple of 128 up to 4096) runs in the same kernel, its E4M3
+ * codes decoded to f16 and its block scale applied per k block.  Either kernel's h and y are the same
  * quantities as on the CUDA-core path, within the layer tolerance.
  *   x [M][H] bf16 bits; out [M][H] bf16 bits;
  *   workspace: device, >= moe_decode_layer_workspace_bytes(layer, M) bytes,
@@ -385,8 +385,7 @@ int moe_decode_layer(const moe_layer_desc *layer, const uint16_t *x, int M,
  * launch on the fused CUDA-core path (which aligns the ids again, to the
  * same tables); on the tensor-core paths the per-token x table of this x
  * (one launch, when the batch uses one: FP8 up to 16 rows, NVFP4 always)
- * then the expert kernel (NVFP4 with a shared expert: the shared expert's
- * two kernels before it); three on the staged path (gate+up, down, blend).
+ * then the expert kernel; three on the staged path (gate+up, down, blend).
  * The workspace rules are moe_decode_layer's.
  * Errors: MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA (as moe_decode_layer). */
 int moe_decode_experts(const moe_layer_desc *layer, const uint16_t *x, int M,
