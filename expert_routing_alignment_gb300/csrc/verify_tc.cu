@@ -49,7 +49,7 @@ constexpr int kWarps = 2 + kEpiWarps;
 constexpr int kThreads = kWarps * 32;          // 576
 constexpr int kEpiThreads = kEpiWarps * 32;    // 512
 constexpr int kRecs = 8;                       // stage records (ring slots in flight)
-constexpr int kAccs = 16;                      // k-block accumulator barriers (TMEM)
+constexpr int kAccs = 32;                      // k-block completion barriers
 constexpr int kTfree = 16;                     // per-stage TMEM release barriers
 constexpr int kIQ = 32;                        // item queue (copy thread -> MMA, promotion)
 constexpr int kRowTile = 64;                   // token rows per item (MMA N <= 64)
@@ -97,12 +97,13 @@ struct TcMaps {
 
 struct Smem {
   uint8_t *ring;
-  uint64_t *full, *empty, *accf, *tfree, *iqbar, *drain;
+  uint64_t *full, *accf, *tfree, *iqbar, *drain;
   volatile int *iq;    // [kIQ] the CTA's items in the order it takes them
   uint32_t *rec;       // [kRecs] byte offset of each stage in the ring
   uint32_t *rlen;      // [kRecs] its size
   uint32_t *trec;      // [kRecs] its accumulators: TMEM column | count << 16
   int *twait;          // [kRecs] the stage whose TMEM release it waits for (-1: none)
+  int *kend;           // [kRecs] the stage's last k block (its MMAs' completion frees the stage)
   volatile int *misc;  // [0] failed, [1] TMEM base, [2] active count, [3] row tiles
   float *sc;           // [2][kMaxKB] weight block scales of the current item
   float *cs;           // [I/128][row tile] per-row factors of the current item
@@ -123,8 +124,8 @@ __host__ __device__ inline size_t fixed_bytes(int cap, int KBd, int RT) {
   (void)KBd;
   (void)RT;
   size_t b = 0;
-  b += al16(8 * (2 * kRecs + kAccs + kTfree + kIQ + 1));
-  b += 4 * al16(4 * kRecs) + al16(4 * kIQ) + al16(4 * 16);
+  b += al16(8 * (kRecs + kAccs + kTfree + kIQ + 1));
+  b += 5 * al16(4 * kRecs) + al16(4 * kIQ) + al16(4 * 16);
   b += al16(4 * 2 * kMaxKB) + al16(4 * kMaxKBd * kRowTile) + al16(4 * 4 * 4 * 16);
   b += al16(4 * kRowTile) + al16(4 * kTokMax);
   b += al16(4 * ((size_t)cap + 1)) + al16(8 * (size_t)cap);
@@ -140,17 +141,17 @@ __device__ Smem carve(uint8_t *base, const TcArgs &a) {
     p += al16(bytes);
     return r;
   };
-  uint64_t *bars = reinterpret_cast<uint64_t *>(take(8 * (2 * kRecs + kAccs + kTfree + kIQ + 1)));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(take(8 * (kRecs + kAccs + kTfree + kIQ + 1)));
   S.full = bars;
-  S.empty = bars + kRecs;
-  S.accf = bars + 2 * kRecs;
-  S.tfree = bars + 2 * kRecs + kAccs;
-  S.iqbar = bars + 2 * kRecs + kAccs + kTfree;
-  S.drain = bars + 2 * kRecs + kAccs + kTfree + kIQ;
+  S.accf = bars + kRecs;
+  S.tfree = bars + kRecs + kAccs;
+  S.iqbar = bars + kRecs + kAccs + kTfree;
+  S.drain = bars + kRecs + kAccs + kTfree + kIQ;
   S.rec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.rlen = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.trec = reinterpret_cast<uint32_t *>(take(4 * kRecs));
   S.twait = reinterpret_cast<int *>(take(4 * kRecs));
+  S.kend = reinterpret_cast<int *>(take(4 * kRecs));
   S.iq = reinterpret_cast<volatile int *>(take(4 * kIQ));
   S.misc = reinterpret_cast<volatile int *>(take(4 * 16));
   S.sc = reinterpret_cast<float *>(take(4 * 2 * kMaxKB));
@@ -428,7 +429,7 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
   const int FT = a.I / 128, FD = a.H / 256;
   uint32_t head = 0, thead = 0;   // shared-memory and TMEM ring heads
   bool x_ready = a.tok != 0;       // the grid's x terms are visible (token form: at launch)
-  int s = 0, tail = 0;
+  int s = 0, tail = 0, kq = -1;
   int ttail = 0;                   // oldest stage that may still hold TMEM
   bool ok = true;
   int jq = 0;                      // items passed to the queue
@@ -488,7 +489,9 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
         const bool busy =
             s - tail >= kRecs || (wrap && tp >= head) || (at < tp + tl && tp < at + size);
         if (!busy) break;
-        if (!wait_bar(S, &S.empty[dt], (uint32_t)(tail / kRecs) & 1)) {
+        // the stage's last k block is done: so are all its MMAs
+        const int ke = S.kend[dt];
+        if (!wait_bar(S, &S.accf[ke % kAccs], (uint32_t)(ke / kAccs) & 1)) {
           ok = false;
           break;
         }
@@ -498,6 +501,8 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
       const uint32_t pos = ring_place(head, size, a.ring_bytes);
       const uint32_t tpos = ring_place(thead, tcols, kTmemCols);
       const int d = s % kRecs;
+      kq += it.kps;
+      S.kend[d] = kq;
       S.rec[d] = pos;
       S.rlen[d] = size;
       S.trec[d] = tpos | (tcols << 16);
@@ -594,7 +599,6 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
         mma_commit(&S.accf[q % kAccs]);
         ++q;
       }
-      mma_commit(&S.empty[d]);
       ++s;
     }
   }
@@ -887,10 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
-    for (int j = 0; j < kRecs; ++j) {
-      mbar_init(&S.full[j], 1);
-      mbar_init(&S.empty[j], 1);   // the stage's MMAs have completed
-    }
+    for (int j = 0; j < kRecs; ++j) mbar_init(&S.full[j], 1);
     for (int j = 0; j < kAccs; ++j) mbar_init(&S.accf[j], 1);
     for (int j = 0; j < kTfree; ++j) mbar_init(&S.tfree[j], kEpiWarps);
     for (int j = 0; j < kIQ; ++j) mbar_init(&S.iqbar[j], 1);
