@@ -73,6 +73,8 @@ KERNELS = {
               "decode_layer_kernel_fp8_decode.md"),
     "tc": ("verify_ffn_kernel (tcgen05; after moe_topk_softmax and moe_align)", "verify_tc.cu",
            "verify_ffn_kernel_fp8_decode.md"),
+    "f4": ("nvfp4_ffn_kernel (tcgen05 kind::f16; after moe_topk_softmax and moe_align)",
+           "nvfp4_tc.cu", "nvfp4_ffn_kernel_nvfp4_decode.md"),
 }
 
 
@@ -481,6 +483,17 @@ def run_nvfp4_decode(moe, stream, K: int, W: int, peaks: dict) -> dict:
             us = 1e3 * ms
             gbs = nbytes / (us * 1e-6) / 1e9
             launches = moe.moe_decode_layer_launches(layers[0], M)
+            half = {}
+            if name == "tc":
+                # the expert half alone on the tables the last call left: the
+                # x-table launch and the tensor-core kernel (weights rotate)
+                ms_e = _graph_ms(stream, K, lambda s: moe.moe_decode_experts(
+                    layers[s % 4], x, out, ws))
+                e_bytes = nbytes - M * shape.E * 4
+                half = dict(expert_half_us=round(1e3 * ms_e, 3),
+                            expert_half_pct_of_measured_hbm=round(
+                                100 * e_bytes / (ms_e * 1e-3) / 1e9 / peaks["hbm_gbs"], 1),
+                            kernel_traffic_bytes_per_launch=profiled_traffic(shape.name, "f4"))
             rows.append(dict(M=M, path=name if name != "auto" else "staged",
                              default=name == "auto" or launches == auto_launches,
                              us_per_layer=round(us, 3), tokens_per_s=round(M / (us * 1e-6), 1),
@@ -488,7 +501,7 @@ def run_nvfp4_decode(moe, stream, K: int, W: int, peaks: dict) -> dict:
                              pct_of_measured_hbm=round(100 * gbs / peaks["hbm_gbs"], 1),
                              launches_per_layer=launches,
                              mean_active_experts=round(float(np.mean(n_act)), 2),
-                             algorithmic_bytes_per_layer=int(nbytes)))
+                             algorithmic_bytes_per_layer=int(nbytes), **half))
             del ws
     del copies, by_path, base, sh
     torch.cuda.empty_cache()
@@ -825,6 +838,31 @@ def run_profile_verify(args):
     print(json.dumps(dict(profile_verify=shape.name, steps=args.warmup + args.steps)), flush=True)
 
 
+def run_profile_nvfp4(args):
+    """Profiler workload for the NVFP4 tensor-core kernel: the NVFP4 layer
+    with its FP8 shared expert at M = args.m rows, W + K eager calls rotating
+    over 2 weight copies (680 MB, beyond L2)."""
+    import expert_routing_alignment_gb300 as moe
+    import synth
+    moe.load()
+    shape = synth.decode_nvfp4(args.m)
+    base = synth.make_experts(shape.E, shape.H, shape.I, shape.fmt, SEED + 8, "cuda")
+    sh = synth.make_experts(1, shape.H, shape.shared_I, synth.FMT_FP8, SEED + 9, "cuda")
+    copies = [base, _clone_experts(base)]
+    shared = moe.Experts.from_synth(sh)
+    layers = [moe.LayerDesc(top_k=shape.top_k, block_size=shape.BS, path=moe.PATH_TC,
+                            routed=moe.Experts.from_synth(c), shared=shared) for c in copies]
+    x = synth.make_x(args.m, shape.H, SEED + 11, "cuda")
+    ws = moe.alloc_workspace(layers[0], args.m)
+    out = torch.empty(args.m, shape.H, dtype=torch.bfloat16, device="cuda")
+    n = args.warmup + args.steps
+    for s in range(n):
+        logits = synth.make_logits(args.m, shape.E, SEED + 800 + s, "cuda")
+        moe.moe_decode_layer(layers[s % 2], x, out, ws, router_logits=logits)
+    torch.cuda.synchronize()
+    print(json.dumps(dict(profile_nvfp4=True, M=args.m, calls=n)), flush=True)
+
+
 def run_profile_router(args):
     """The router logits kernel for ncu: W+K direct calls at the decode width
     (M=8, H=2048, E=128) and then at the verify width (M=128, H=4096, E=256)."""
@@ -967,6 +1005,8 @@ def main():
                     help="skip the M=128 verify-batch measurement")
     ap.add_argument("--profile-verify", action="store_true",
                     help="only run a small case of the verify-batch kernel (for ncu)")
+    ap.add_argument("--profile-nvfp4", action="store_true",
+                    help="profiler workload: the NVFP4 layer (tensor-core kernel) at --m rows")
     ap.add_argument("--profile-router", action="store_true",
                     help="only run the router logits kernel at two widths (for ncu)")
     ap.add_argument("--path", type=int, default=0,
@@ -995,6 +1035,8 @@ def main():
             run_profile_verify(args)
         elif args.profile_router:
             run_profile_router(args)
+        elif args.profile_nvfp4:
+            run_profile_nvfp4(args)
         else:
             run_gpu(args, rank, world)
     finally:
