@@ -357,7 +357,8 @@ def workspace_view(layer: LayerDesc, M: int, ws: torch.Tensor) -> dict:
 
     tc = {}
     mt = v.max_total
-    if v.tc_h_terms and layer.routed.fmt == FMT_NVFP4_G16:
+    f4 = layer.routed.fmt in (FMT_NVFP4_G16, FMT_NVFP4_GATE_UP)
+    if v.tc_h_terms and f4:
         # the NVFP4 tensor-core kernel: f16 h terms (hi, lo) [2][max_total][I],
         # the f16 x table [H/128][2][NT][64] of NT = 16 or 32 token columns
         nt = F4_TOKEN_COLUMNS_SMALL if M <= F4_TOKEN_COLUMNS_SMALL else F4_TOKEN_COLUMNS
@@ -372,7 +373,6 @@ def workspace_view(layer: LayerDesc, M: int, ws: torch.Tensor) -> dict:
             tc_h_terms=sl(v.tc_h_terms, 3 * mt * I, torch.uint8).view(3, mt, I),
             tc_h_scale=sl(v.tc_h_scale, mt * (I // 128), torch.float32).view(mt, I // 128),
             tc_items=sl(v.tc_items, 4 * v.cap, torch.int32).view(v.cap, 4))
-    f4 = layer.routed.fmt == FMT_NVFP4_G16
     if v.tc_x_terms and not f4 and M <= TOKEN_FORM_ROWS:   # x terms by token [H/128][2][16][128]
         tc.update(
             tc_x_table=sl(v.tc_x_terms, 2 * 16 * H, torch.uint8).view(H // 128, 2, 16, 128),

@@ -121,7 +121,8 @@ static bool tc_layer(const moe_layer_desc *L) {
 // Bytes of the tensor-core kernels' counters (each call leaves them
 // consistent for the next): sized by the layer alone.
 size_t tc_counter_bytes(const moe_layer_desc *L) {
-  return 4 * (L->routed.fmt == MOE_FMT_NVFP4_G16 ? f4_counter_ints(L) : tc_counter_ints(L));
+  const bool f4 = L->routed.fmt == MOE_FMT_NVFP4_G16 || L->routed.fmt == MOE_FMT_NVFP4_GATE_UP;
+  return 4 * (f4 ? f4_counter_ints(L) : tc_counter_ints(L));
 }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

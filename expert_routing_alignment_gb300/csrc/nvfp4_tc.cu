@@ -76,7 +76,11 @@ struct F4Args {
   const int32_t *ttp, *sti, *act_count;      // the alignment's tables
   const int4 *items;                         // [cap] {offset, expert, slot count, 0}
   uint16_t *out;                             // [M][H] bf16
-  const float *gg, *gu, *gd;                 // global scales [E]
+  const float *gg, *gu, *gd;                 // global scales [E] (gd NULL: FP8 down)
+  // the nvfp4-gate-up tier: the routed down projection in FP8 (E4M3 codes
+  // [E][H][I], block scales [E][H/128][I/128])
+  int down_fp8;
+  const float *sdown;
   const uint8_t *xt;                         // f16 x table [H/128][2 atoms][NT][128 B]
   const float *xs;                           // [32] 2^-s of each token
   uint16_t *hq;                              // f16 h terms [2][max_total][I]
@@ -214,6 +218,7 @@ __device__ __forceinline__ void group_sync(int g) {
 // down, shared down (every gate+up item is taken before any down item).
 struct Item {
   bool gu, sh;
+  bool f8;   // E4M3 codes (the shared expert; the tier's routed down): one k block per stage
   int a, e, pos0, rows, tile;
 };
 
@@ -231,6 +236,7 @@ __device__ __forceinline__ Item decode(const Smem &S, const F4Args &a, int A, in
     const int rt = j / per;
     it.gu = gu;
     it.sh = true;
+    it.f8 = true;
     it.tile = j - rt * per;
     it.a = A;
     it.e = 0;
@@ -250,6 +256,7 @@ __device__ __forceinline__ Item decode(const Smem &S, const F4Args &a, int A, in
     rtg = j / c.FD;
     it.tile = j - rtg * c.FD;
   }
+  it.f8 = !it.gu && a.down_fp8;
   int lo = 0, hi = A - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -276,7 +283,7 @@ __device__ __forceinline__ uint32_t b_bytes(const Item &it, int NT) {
   return it.gu ? 4u * (uint32_t)NT * 128u : 4u * kHAtom;
 }
 __device__ __forceinline__ uint32_t stage_bytes(const Item &it, int NT) {
-  return b_bytes(it, NT) + 2u * kCodeTile + (it.sh ? 0u : 2u * kScaleTile);
+  return b_bytes(it, NT) + 2u * kCodeTile + (it.f8 ? 0u : 2u * kScaleTile);
 }
 __device__ __forceinline__ uint32_t acc_cols(const Item &it, int NT) {
   return 2u * (uint32_t)item_n(it, NT);
@@ -285,7 +292,7 @@ __device__ __forceinline__ uint32_t acc_cols(const Item &it, int NT) {
 __device__ __forceinline__ int item_kb(const Item &it, const F4Args &a) {
   return it.gu ? a.H / 128 : (it.sh ? a.Is : a.I) / 128;
 }
-__device__ __forceinline__ int stage_kbs(const Item &it) { return it.sh ? 1 : 2; }
+__device__ __forceinline__ int stage_kbs(const Item &it) { return it.f8 ? 1 : 2; }
 
 // ---------------------------------------------------------------------------
 // roles
@@ -365,9 +372,10 @@ __device__ void producer(const F4Args &a, const F4Maps &m, const Smem &S, int A,
       uint64_t *fb = &S.full[d];
       mbar_expect_tx(fb, size);
       uint8_t *dst = S.ring + pos;
-      if (it.sh) {   // one E4M3 k block of each tile
-        tma_2d_hint(dst + bb, &m.scodes[p0], kb * 128, row0, fb, pol);
-        tma_2d_hint(dst + bb + kCodeTile, &m.scodes[p1], kb * 128, row1, fb, pol);
+      if (it.f8) {   // one E4M3 k block of each tile
+        const CUtensorMap *cm = it.sh ? m.scodes : m.codes;
+        tma_2d_hint(dst + bb, &cm[p0], kb * 128, row0, fb, pol);
+        tma_2d_hint(dst + bb + kCodeTile, &cm[p1], kb * 128, row1, fb, pol);
       } else {       // two k blocks of E2M1 codes and their scales
         tma_2d_hint(dst + bb, &m.codes[p0], kb * 64, row0, fb, pol);
         tma_2d_hint(dst + bb + kCodeTile, &m.codes[p1], kb * 64, row1, fb, pol);
@@ -483,7 +491,7 @@ __device__ void decoder(const F4Args &a, const Smem &S, int A, const Counts &cn,
           }
           const uint8_t *crow = codes + t * kCodeTile + r * 128;
           uint32_t v[64];
-          if (it.sh)
+          if (it.f8)
             decode_e4m3(crow, r, v);
           else
             decode_e2m1(crow, scales + t * kScaleTile + r * 16, r, kbl, v);
@@ -644,9 +652,9 @@ __device__ void finish_gate_up(const F4Args &a, const Smem &S, const Item &it, i
 }
 
 // acc[j] += f * (column value) (gate+up), or acc[j] += hf[j] f (term 0 +
-// term 1) (down), for 16 columns of this warp's lanes; f is the shared
-// expert's block scale of the k block (1 for routed items, whose scales are
-// in the decoded weights).
+// term 1) (down), for 16 columns of this warp's lanes; f is the k block's
+// block scale for E4M3 items (1 for the NVFP4 items, whose scales are in the
+// decoded weights).
 __device__ __forceinline__ void promote_gu(uint32_t col, float f, float (&acc)[16]) {
   uint32_t r[16];
   tmem_ld16(col, r);
@@ -701,7 +709,7 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, const Counts &cn
       S.xinv[et] = et < it.rows ? S.xtok[t] : 0.f;
     }
     if (et == 0) {
-      S.glob[0] = it.sh ? 1.f : (it.gu ? __ldg(a.gg + it.e) : __ldg(a.gd + it.e));
+      S.glob[0] = it.sh || it.f8 ? 1.f : (it.gu ? __ldg(a.gg + it.e) : __ldg(a.gd + it.e));
       S.glob[1] = it.sh ? 1.f : (it.gu ? __ldg(a.gu + it.e) : 0.f);
     }
     // (the down item's h scales are read only after the dependency wait)
@@ -709,11 +717,12 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, const Counts &cn
       bad = true;
       break;
     }
-    if (it.sh) {   // each tile's block scale per k block
+    if (it.f8) {   // each tile's block scale per k block
+      const float *sd = it.sh ? a.ssd : a.sdown + (size_t)it.e * KBh * KBd;
       for (int idx = et; idx < 2 * KB; idx += kEpiThreads) {
         const int t = idx / KB, kb = idx - t * KB;
         S.fs[t * kMaxKB + kb] = it.gu ? __ldg((t ? a.ssu : a.ssg) + it.tile * KBh + kb)
-                                      : __ldg(a.ssd + (2 * it.tile + t) * KBd + kb);
+                                      : __ldg(sd + (2 * it.tile + t) * KBd + kb);
       }
     }
     if (!it.gu) {
@@ -723,7 +732,7 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, const Counts &cn
         S.cs[idx] = j < it.rows ? __ldcg(hsb + (size_t)(it.pos0 + j) * KBd + kb) : 0.f;
       }
     }
-    if (it.sh || !it.gu) epi_sync();
+    if (it.f8 || !it.gu) epi_sync();
     float acc0[16], acc1[16];
 #pragma unroll
     for (int jj = 0; jj < 16; ++jj) acc0[jj] = acc1[jj] = 0.f;
@@ -751,7 +760,7 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, const Counts &cn
       }
       tc_fence_after();
       const uint32_t col = lane_base + kAccBase + tbase + (uint32_t)j * cols;
-      const float f0 = it.sh ? S.fs[kb] : 1.f, f1 = it.sh ? S.fs[kMaxKB + kb] : 1.f;
+      const float f0 = it.f8 ? S.fs[kb] : 1.f, f1 = it.f8 ? S.fs[kMaxKB + kb] : 1.f;
       if (it.gu) {
         promote_gu(col + 16u * (uint32_t)grp, f0, acc0);
         promote_gu(col + (uint32_t)N + 16u * (uint32_t)grp, f1, acc1);
@@ -981,7 +990,7 @@ int f4_maps(const moe_experts *X, const moe_experts *Sx, const uint8_t *xt, uint
   const Key key = {{X->gate.codes, X->up.codes, X->down.codes, X->gate.scale, X->up.scale,
                     X->down.scale, xt, hq, Sx ? Sx->gate.codes : nullptr,
                     Sx ? Sx->up.codes : nullptr, Sx ? Sx->down.codes : nullptr},
-                   E, H, I, Is, max_total, NT};
+                   E * 8 + X->fmt, H, I, Is, max_total, NT};
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it != cache.end()) {
@@ -993,9 +1002,16 @@ int f4_maps(const moe_experts *X, const moe_experts *Sx, const uint8_t *xt, uint
   const moe_proj *P[3] = {&X->gate, &X->up, &X->down};
   for (int j = 0; j < 3; ++j) {
     const int K = j < 2 ? H : I, R = j < 2 ? I : H;
+    const cuuint32_t cbox[2] = {128, 128};
+    if (proj_fmt(X->fmt, j) == MOE_FMT_FP8_B128) {   // E4M3 codes [E][R][K], one k block per box
+      const cuuint64_t cd[2] = {(cuuint64_t)K, (cuuint64_t)E * R};
+      const cuuint64_t cs[1] = {(cuuint64_t)K};
+      const int st = encode_u8_sw128(&m.codes[j], P[j]->codes, 2, cd, cs, cbox);
+      if (st) return st;
+      continue;
+    }
     const cuuint64_t cd[2] = {(cuuint64_t)K / 2, (cuuint64_t)E * R};
     const cuuint64_t cs[1] = {(cuuint64_t)K / 2};
-    const cuuint32_t cbox[2] = {128, 128};
     int st = encode_u8_sw128(&m.codes[j], P[j]->codes, 2, cd, cs, cbox);
     if (st) return st;
     const cuuint64_t sd[2] = {(cuuint64_t)K / 16, (cuuint64_t)E * R};
@@ -1051,12 +1067,13 @@ size_t ring_bytes_for(int cap) {
 
 }  // namespace
 
-// Shape admission (host): NVFP4 routed experts, M <= 32, H and I multiples of
-// 256 (H up to 8192, I up to 4096), a shared expert (if any) in FP8 with its
-// inter a multiple of 128 up to 4096, room for the ring.
+// Shape admission (host): NVFP4 routed experts (or the nvfp4-gate-up tier:
+// NVFP4 gate and up, FP8 down), M <= 32, H and I multiples of 256 (H up to
+// 8192, I up to 4096), a shared expert (if any) in FP8 with its inter a
+// multiple of 128 up to 4096, room for the ring.
 bool f4_fits(const moe_layer_desc *L, int M) {
   const moe_experts &R = L->routed;
-  if (R.fmt != MOE_FMT_NVFP4_G16 || M > kTokMax) return false;
+  if ((R.fmt != MOE_FMT_NVFP4_G16 && R.fmt != MOE_FMT_NVFP4_GATE_UP) || M > kTokMax) return false;
   if (R.hidden % 256 || R.hidden > 128 * kMaxKB || R.inter % 256 || R.inter > 128 * kMaxKBd)
     return false;
   if (L->shared && (L->shared->fmt != MOE_FMT_FP8_B128 || L->shared->inter % 128 ||
@@ -1109,7 +1126,9 @@ int launch_f4(const moe_layer_desc *L, const uint16_t *x, int M, const float *w,
   a.out = out;
   a.gg = R.gate.global_scale;
   a.gu = R.up.global_scale;
-  a.gd = R.down.global_scale;
+  a.down_fp8 = R.fmt == MOE_FMT_NVFP4_GATE_UP ? 1 : 0;
+  a.gd = a.down_fp8 ? nullptr : R.down.global_scale;
+  a.sdown = a.down_fp8 ? static_cast<const float *>(R.down.scale) : nullptr;
   a.xt = reinterpret_cast<uint8_t *>(base + v.tc_x_terms);
   a.xs = reinterpret_cast<float *>(base + v.tc_x_scale);
   a.hq = reinterpret_cast<uint16_t *>(base + v.tc_h_terms);

@@ -62,7 +62,7 @@ extern "C" {
 
 #define MOE_PATH_AUTO 0     /* chosen per shape class (never per routing)    */
 #define MOE_PATH_SIMT 1     /* CUDA-core kernels, in-register dequant         */
-#define MOE_PATH_TC 2       /* tcgen05 tensor-core kernels (FP8 only)         */
+#define MOE_PATH_TC 2       /* tcgen05 tensor-core kernels (moe_decode_layer) */
 #define MOE_PATH_SIMT_STAGED 3 /* moe_decode_layer only: CUDA-core kernels as the
                                   five separate launches (router, align, gate+up,
                                   down, blend) instead of the fused decode pair */
@@ -348,8 +348,10 @@ int moe_decode_layer_launches(const moe_layer_desc *layer, int M, int with_logit
  * persistent kernel of tcgen05 MMAs after the alignment ("fp8_moe_grouped.rs",
  * the tensor-core twins of the grouped launchers): E4M3 weight codes times
  * exact E4M3 splits of x and h, each 128-wide k block promoted to fp32 times
- * its block scale.  NVFP4 routed experts with M <= 32, hidden and inter
- * multiples of 256 (hidden up to 8192, inter up to 4096) run the NVFP4 twin
+ * its block scale.  NVFP4 routed experts (and the nvfp4-gate-up tier, its
+ * FP8 down projection decoded like the shared expert) with M <= 32, hidden
+ * and inter multiples of 256 (hidden up to 8192, inter up to 4096) run the
+ * NVFP4 twin
  * ("forward_nvfp4_grouped_decode.rs", the NVFP4 grouped launchers): each
  * E2M1 code times its E4M3 scale decoded exactly to f16 into tensor memory,
  * tcgen05 kind::f16 MMAs against an f16 x table by token and f16 hi/lo

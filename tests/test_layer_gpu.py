@@ -322,18 +322,19 @@ def test_decode_experts_on_tables_in_the_workspace(moe, path, M):
     assert torch.equal(third.view(torch.int16), ref2.view(torch.int16))
 
 
-@pytest.mark.parametrize("path", [0, 1, 3], ids=["auto", "simt", "staged"])
+@pytest.mark.parametrize("path", [0, 2, 1, 3], ids=["auto", "tc", "simt", "staged"])
 @pytest.mark.parametrize("M", [1, 8, 32])
 def test_nvfp4_gate_up_tier_matches_oracle(moe, M, path):
     """The nvfp4-gate-up tier (NVFP4 gate and up, FP8 down, FP8 shared expert)
-    runs on the staged CUDA-core kernels, each projection in its own format:
-    the layer output within the layer tolerance of the oracle, h and y within
-    the stage tolerance of the oracle's stages, and row 0 the same bits at M
-    rows as alone."""
+    runs on the NVFP4 tensor-core kernel (default and MOE_PATH_TC: its down
+    projection as E4M3 items) or on the staged CUDA-core kernels (each
+    projection in its own format): the layer output within the layer
+    tolerance of the oracle, h and y within the stage tolerance of the
+    oracle's stages, and row 0 the same bits at M rows as alone."""
     shape = synth.decode_nvfp4_gate_up(M)
     inp = layer_inputs(shape)
     out, view, (layer, _) = H.gpu_layer(moe, inp, path=path)
-    assert moe.moe_decode_layer_launches(layer, M) == 5
+    assert moe.moe_decode_layer_launches(layer, M) == (3 if path in (0, 2) else 5)
     _, ref_b, bad = H.oracle_layer(inp)
     assert bad == 0
     rl2, mx = H.compare_bf16(out, ref_b)
