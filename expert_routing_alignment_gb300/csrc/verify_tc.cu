@@ -112,6 +112,13 @@ struct Smem {
   uint32_t *red;       // [4 groups][4 quadrants][16] column maxima
   int *rtp;            // [cap + 1] row-tile prefix over the active list
   int2 *info;          // [cap] {offset, expert | rows << 16}
+  // token form: a second buffer of the per-item arrays above (group 1 stages
+  // the next item into one while group 0 works on the other), the item of
+  // each buffer, and their handover barriers
+  float *sc2, *cs2;
+  int *tok2;
+  volatile int *slot;  // [2]
+  uint64_t *staged, *consumed;   // [2] each
 };
 
 __host__ __device__ inline size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
@@ -122,8 +129,10 @@ __host__ __device__ inline size_t al16(size_t v) { return (v + 15) & ~size_t(15)
 // measured slower than the two stages this leaves room for.)
 __host__ __device__ inline size_t fixed_bytes(int cap, int KBd, int RT) {
   (void)KBd;
-  (void)RT;
   size_t b = 0;
+  if (RT == 16)   // the token form's second buffers and handover barriers
+    b += al16(4 * 2 * kMaxKB) + al16(4 * kMaxKBd * 16) + al16(4 * 16) + al16(4 * 2) +
+         al16(8 * 4);
   b += al16(8 * (kRecs + kAccs + kTfree + kIQ + 1));
   b += 5 * al16(4 * kRecs) + al16(4 * kIQ) + al16(4 * 16);
   b += al16(4 * 2 * kMaxKB) + al16(4 * kMaxKBd * kRowTile) + al16(4 * 4 * 4 * 16);
@@ -161,6 +170,19 @@ __device__ Smem carve(uint8_t *base, const TcArgs &a) {
   S.red = reinterpret_cast<uint32_t *>(take(4 * 4 * 4 * 16));
   S.rtp = reinterpret_cast<int *>(take(4 * ((size_t)a.cap + 1)));
   S.info = reinterpret_cast<int2 *>(take(8 * (size_t)a.cap));
+  if (a.tok) {
+    S.sc2 = reinterpret_cast<float *>(take(4 * 2 * kMaxKB));
+    S.cs2 = reinterpret_cast<float *>(take(4 * (size_t)(a.I / 128) * 16));
+    S.tok2 = reinterpret_cast<int *>(take(4 * 16));
+    S.slot = reinterpret_cast<volatile int *>(take(4 * 2));
+    S.staged = reinterpret_cast<uint64_t *>(take(8 * 4));
+    S.consumed = S.staged + 2;
+  } else {
+    S.sc2 = S.cs2 = nullptr;
+    S.tok2 = nullptr;
+    S.slot = nullptr;
+    S.staged = S.consumed = nullptr;
+  }
   return S;
 }
 
@@ -614,7 +636,8 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
 // fp32 and as three E4M3 terms with a power-of-two scale per (row, this
 // 128-feature block); then the item is published.
 __device__ void finish_gate_up(const TcArgs &a, const Smem &S, const Item &it, int grp, int q,
-                               int lane, const float (&acc0)[16], const float (&acc1)[16]) {
+                               int lane, const float (&acc0)[16], const float (&acc1)[16],
+                               const float *csb, const int *tokb) {
   const int c0 = grp * 16, f = q * 32 + lane, o = it.tile * 128 + f;
   const int KBd = a.I / 128;
   // only the item's real rows are finished (the condition is the same for the
@@ -624,10 +647,10 @@ __device__ void finish_gate_up(const TcArgs &a, const Smem &S, const Item &it, i
   for (int jj = 0; jj < 16; ++jj) {
     hv[jj] = 0.f;
     if (c0 + jj < it.rows) {
-      const float xi = S.cs[c0 + jj];
+      const float xi = csb[c0 + jj];
       float g = acc0[jj], u = acc1[jj];
       if (a.tok) {   // the MMA columns are tokens: take the row's own
-        const int t = S.tokrow[c0 + jj];
+        const int t = tokb[c0 + jj];
         g = u = 0.f;
 #pragma unroll
         for (int tt = 0; tt < kTokMax; ++tt) {
@@ -715,6 +738,173 @@ __device__ __forceinline__ bool epi_sync_or(bool v) {
   return r != 0;
 }
 
+// Barrier over one group of four promotion warps (named barrier 2 + g) that
+// also ORs a flag across them.
+__device__ __forceinline__ bool group_sync_or(int g, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(2 + g)
+      : "memory");
+  return r != 0;
+}
+
+// Token form (M <= 16): every item has one 16-column block, held by group 0
+// (warps 2-5).  Group 1 (warps 6-9) stages the next item into the other of
+// two buffers -- its block scales, its rows' tokens and x scales, or (after
+// the wait for its expert's gate+up items) a down item's h scales -- while
+// group 0 promotes and finishes the current one, so no item waits for its
+// own loads.  Groups 2 and 3 hold no columns and have no part here.
+__device__ void epilogue_token(const TcArgs &a, const Smem &S, int A, int TR, int total,
+                               uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ew = warp - 2, q = warp & 3, grp = ew >> 2;
+  const int lt = (threadIdx.x - 64) & 127;   // index within the group
+  const int FT = a.I / 128, FD = a.H / 256, KBd = a.I / 128;
+  bool bad = false;
+  if (grp == 1) {
+    for (int jq = 0;; ++jq) {
+      const int b = jq & 1;
+      int i = lane == 0 ? next_item(S, jq) : 0;
+      i = __shfl_sync(0xFFFFFFFFu, i, 0);
+      bool ok = i >= 0;
+      // the buffer is free once group 0 is done with item jq - 2
+      if (ok && jq >= 2)
+        ok = __all_sync(0xFFFFFFFFu,
+                        wait_bar(S, &S.consumed[b], (uint32_t)((jq - 2) >> 1) & 1));
+      if (group_sync_or(1, !ok)) {
+        bad = true;
+        break;
+      }
+      if (i >= total) {   // no more items: hand over the end
+        if (lt == 0) {
+          S.slot[b] = total;
+          mbar_arrive(&S.staged[b]);
+        }
+        break;
+      }
+      const Item it = decode(S, A, i, TR, FT, FD, a.row_tile);
+      const int KB = it.gu ? a.H / 128 : KBd;
+      float *sc = b ? S.sc2 : S.sc;
+      float *cs = b ? S.cs2 : S.cs;
+      int *tk = b ? S.tok2 : S.tokrow;
+      bool dep = true;
+      if (it.gu) {
+        const size_t sb = ((size_t)it.e * FT + it.tile) * KB;
+        for (int j = lt; j < KB; j += 128) {
+          sc[j] = __ldg(a.sg + sb + j);
+          sc[kMaxKB + j] = __ldg(a.su + sb + j);
+        }
+        if (lt < 16) {   // each row's token and that token's x scale
+          const int t = lt < it.rows ? __ldcg(a.sti + it.pos0 + lt) / a.k : 0;
+          tk[lt] = t;
+          cs[lt] = lt < it.rows ? S.xtok[t] : 0.f;
+        }
+      } else {
+        const size_t sb = ((size_t)it.e * (a.H / 128) + 2 * it.tile) * KB;
+        for (int j = lt; j < KB; j += 128) {
+          sc[j] = __ldg(a.sd + sb + j);
+          sc[kMaxKB + j] = __ldg(a.sd + sb + KB + j);
+        }
+        if (lt == 0) dep = wait_count(S, a.done + it.a, (S.rtp[it.a + 1] - S.rtp[it.a]) * FT);
+      }
+      // a down item's h scales are read only after the dependency wait
+      if (group_sync_or(1, !dep || S.misc[0])) {
+        bad = true;
+        break;
+      }
+      if (!it.gu) {
+        for (int idx = lt; idx < KB * 16; idx += 128) {
+          const int kb = idx >> 4, j = idx & 15;
+          cs[idx] = j < it.rows ? __ldcg(a.hs + (size_t)(it.pos0 + j) * KBd + kb) : 0.f;
+        }
+        group_sync(1);
+      }
+      if (lt == 0) {
+        S.slot[b] = i;
+        mbar_arrive(&S.staged[b]);   // release: the group's stores above are visible
+      }
+    }
+  } else if (grp == 0) {
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t arrivals = ew == 0 ? (uint32_t)(kEpiWarps - 4 + 1) : 1u;
+    int s = 0, st = 0;
+    uint32_t thead = 0;
+    for (int jq = 0;; ++jq) {
+      const int b = jq & 1;
+      const bool ok = __all_sync(0xFFFFFFFFu, wait_bar(S, &S.staged[b], (uint32_t)(jq >> 1) & 1));
+      if (group_sync_or(0, !ok)) {
+        bad = true;
+        break;
+      }
+      const int i = S.slot[b];
+      if (i >= total) break;
+      const Item it = decode(S, A, i, TR, FT, FD, a.row_tile);
+      const int KB = it.gu ? a.H / 128 : KBd;
+      const float *sc = b ? S.sc2 : S.sc;
+      const float *cs = b ? S.cs2 : S.cs;
+      const int *tk = b ? S.tok2 : S.tokrow;
+      float acc0[16], acc1[16];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) acc0[jj] = acc1[jj] = 0.f;
+      const int T = it.gu ? kXTerms : kHTerms;
+      const uint32_t nt = 16u << it.box, cols = acc_cols(it), tcols = (uint32_t)it.kps * cols;
+      uint32_t tbase = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int j = kb % it.kps;
+        if (j == 0) tbase = ring_place(thead, tcols, kTmemCols);
+        const uint32_t pos = tbase + (uint32_t)j * cols;
+        const int slot = s % kAccs;
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(S, &S.accf[slot], (uint32_t)(s / kAccs) & 1))) {
+          bad = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t col = lane_base + pos;
+        const float *hf = it.gu ? nullptr : cs + kb * 16;
+        promote(col, nt, T, sc[kb], hf, acc0);
+        promote(col + (uint32_t)T * nt, nt, T, sc[kMaxKB + kb], hf, acc1);
+        ++s;
+        if (j == it.kps - 1) {   // the stage's accumulators are free
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_n(&S.tfree[st % kTfree], arrivals);
+          ++st;
+        }
+      }
+      if (group_sync_or(0, bad)) {
+        bad = true;
+        break;
+      }
+      if (it.gu) {
+        finish_gate_up(a, S, it, 0, q, lane, acc0, acc1, cs, tk);
+        // every h of the tile is visible to every CTA and its tensor copies
+        // before the tile is counted
+        fence_proxy_async_global();
+        group_sync(0);
+        if (lt == 0) {
+          __threadfence();
+          atomicAdd(a.done + it.a, 1);
+        }
+      } else {
+        const int o0 = it.tile * 256 + q * 32 + lane;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          if (jj >= it.rows) break;
+          float *yr = a.y + (size_t)(it.pos0 + jj) * a.H + o0;
+          yr[0] = acc0[jj];
+          yr[128] = acc1[jj];
+        }
+        group_sync(0);
+      }
+      if (lt == 0) mbar_arrive(&S.consumed[b]);   // the buffer may be staged again
+    }
+  }
+  if (bad) fail(S, a);
+}
+
 // The 16 promotion warps.  Warp w (2..17) reads TMEM lanes 32*(w%4)..+31
 // (its quadrant q of the 128 weight rows) and columns 16*g..16*g+15 (its
 // group g = (w-2)/4 of the item's token rows).  Every decision to leave the
@@ -737,6 +927,8 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
     // scales; they are complete at launch
     if (et < a.M) S.xtok[et] = __ldcg(a.xs + et);
     asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+    epilogue_token(a, S, A, TR, total, tmem);
+    return;
   } else {
     // the x terms of this CTA's share of the slots, then the grid barrier
     // that makes all of them (and the zeroed counters) visible to the copies
@@ -860,7 +1052,7 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
       break;
     }
     if (it.gu) {
-      if (mine) finish_gate_up(a, S, it, grp, q, lane, acc0, acc1);
+      if (mine) finish_gate_up(a, S, it, grp, q, lane, acc0, acc1, S.cs, S.tokrow);
       pending = it.a;
     } else if (mine) {
       const int f = q * 32 + lane;
@@ -895,6 +1087,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < kAccs; ++j) mbar_init(&S.accf[j], 1);
     for (int j = 0; j < kTfree; ++j) mbar_init(&S.tfree[j], kEpiWarps);
     for (int j = 0; j < kIQ; ++j) mbar_init(&S.iqbar[j], 1);
+    if (a.tok)
+      for (int j = 0; j < 4; ++j) mbar_init(&S.staged[j], 1);   // staged[2], consumed[2]
     mbar_init(S.drain, 1);
     for (int j = 0; j < 16; ++j) S.misc[j] = 0;
     fence_mbar_init();
