@@ -135,7 +135,7 @@ __host__ __device__ inline size_t fixed_bytes(int cap, int KBd, int RT) {
          al16(8 * 4);
   b += al16(8 * (kRecs + kAccs + kTfree + kIQ + 1));
   b += 5 * al16(4 * kRecs) + al16(4 * kIQ) + al16(4 * 16);
-  b += al16(4 * 2 * kMaxKB) + al16(4 * kMaxKBd * kRowTile) + al16(4 * 4 * 4 * 16);
+  b += al16(4 * 2 * kMaxKB) + al16(4 * kMaxKBd * RT) + al16(4 * 4 * 4 * 16);
   b += al16(4 * kRowTile) + al16(4 * kTokMax);
   b += al16(4 * ((size_t)cap + 1)) + al16(8 * (size_t)cap);
   return b;
