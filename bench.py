@@ -26,7 +26,8 @@ host core and on all of them (threads over the rows of the layer calls).
 The line also carries `align_grid`: µs per moe_align call over the alignment
 stress grid (n = 8·{1, 64, 1024, 4096}, E in {64, 256, 1024}, BS in {16, 64, 128},
 uniform ids); `nvfp4_decode`: the NVFP4 layer with its FP8 shared expert at
-M in {1, 8, 32} (the fused CUDA-core kernel) and at M=64 (the staged kernels);
+M in {1, 8, 32} on the tensor-core kernel (the default) and on the fused CUDA-core
+kernel, and at M=64 (the staged kernels);
 `nvfp4_gate_up_tier`: the layer with NVFP4 gate and up and FP8 down at M=8;
 `prefill`: M in {512, 2048} rows of the verify shape on the tensor cores.
 
