@@ -786,10 +786,7 @@ __device__ void epilogue(const F4Args &a, const Smem &S, int A, const Counts &cn
       // before the tile is counted
       fence_proxy_async_global();
       epi_sync();
-      if (et == 0) {
-        __threadfence();
-        atomicAdd(a.done + it.a, 1);
-      }
+      if (et == 0) red_release_add(a.done + it.a, 1);
     } else if (mine) {
       const float gd = S.glob[0];
       const int c0 = it.tile * 256 + q * 32 + lane;
@@ -896,11 +893,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- blend: every y row is written before any CTA blends its share ------
   //   out[t][c] = bf16_rn(sum_j w[t][j] * y[token_to_perm[t*k+j]][c]
   //                       + g[t] * y_sh[t][c]), fp32, j ascending
-  __threadfence();
+  // (one thread's arrival with release semantics covers every write of the
+  // CTA before the CTA barrier; its acquire of the full count, every write of
+  // the grid)
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned long long G = gridDim.x;
-    const unsigned long long v = atomicAdd(a.grid_ctr, 1ull);
+    unsigned long long v;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(v) : "l"(a.grid_ctr)
+                 : "memory");
     const unsigned long long target = (v / G + 1) * G;
     bool ok = false;
     const uint64_t t0 = gtime();
@@ -914,7 +915,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (gtime() - t0 > kWaitNs) break;
       __nanosleep(64);
     }
-    __threadfence();
     S.misc[4] = ok;
   }
   __syncthreads();

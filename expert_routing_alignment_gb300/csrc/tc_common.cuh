@@ -88,6 +88,11 @@ __device__ __forceinline__ int atom_acq_rel_add(int *p, int v) {
   return old;
 }
 
+// A tensor map's descriptor fetched ahead of its first copy.
+__device__ __forceinline__ void prefetch_tensormap(const void *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // Generic-proxy writes to global memory made visible to later tensor copies
 // (async proxy) of any CTA.
 __device__ __forceinline__ void fence_proxy_async_global() {

@@ -366,12 +366,15 @@ __device__ bool epi_grid_barrier(const Smem &S, unsigned long long *ctr) {
   return S.misc[5] != 0;
 }
 
+// Grid barrier of all threads: one thread's arrival with release semantics
+// (covering every write of the CTA before the CTA barrier), its acquire of
+// the full count, then the CTA barrier again.
 __device__ bool grid_barrier(const Smem &S, unsigned long long *ctr) {
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned long long G = gridDim.x;
-    const unsigned long long v = atomicAdd(ctr, 1ull);
+    unsigned long long v;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(v) : "l"(ctr) : "memory");
     const unsigned long long target = (v / G + 1) * G;
     bool ok = false;
     const uint64_t t0 = gtime();
@@ -385,7 +388,6 @@ __device__ bool grid_barrier(const Smem &S, unsigned long long *ctr) {
       if (gtime() - t0 > kWaitNs) break;
       __nanosleep(64);
     }
-    __threadfence();
     S.misc[4] = ok;
   }
   __syncthreads();
@@ -471,14 +473,14 @@ __device__ void producer(const TcArgs &a, const TcMaps &m, const Smem &S, int A,
       fence_proxy_async_global();
     }
     const int KB = it.gu ? a.H / 128 : a.I / 128;
-    const uint32_t bterm = (uint32_t)(it.gu ? kXTerms : kHTerms) * (16u << it.box) * 128u;
-    const uint32_t abytes = (uint32_t)it.kps * kTileBytes;
-    const uint32_t size = stage_bytes(it);
-    const uint32_t tcols = (uint32_t)it.kps * acc_cols(it);
     const int wrow0 = it.gu ? it.e * a.I + it.tile * 128 : it.e * a.H + it.tile * 256;
     const CUtensorMap *w0 = it.gu ? &m.w[0][it.kps - 1] : &m.w[2][it.kps - 1];
     const CUtensorMap *w1 = it.gu ? &m.w[1][it.kps - 1] : w0;
     const int wrow1 = it.gu ? wrow0 : wrow0 + 128;
+    const uint32_t bterm = (uint32_t)(it.gu ? kXTerms : kHTerms) * (16u << it.box) * 128u;
+    const uint32_t abytes = (uint32_t)it.kps * kTileBytes;
+    const uint32_t size = stage_bytes(it);
+    const uint32_t tcols = (uint32_t)it.kps * acc_cols(it);
     const CUtensorMap *bmap = it.gu ? &m.xq[it.box] : &m.hq[it.box];
     for (int kb = 0; kb < KB; kb += it.kps) {
       // Ring placement.  A stage holds a range of the shared-memory ring (its
@@ -633,16 +635,16 @@ __device__ void mma_issuer(const TcArgs &a, const Smem &S, int A, int TR, int to
 }
 
 // Gate+up finish of one item: h = silu(g) * u per (row, feature), written as
-// fp32 and as three E4M3 terms with a power-of-two scale per (row, this
-// 128-feature block); then the item is published.
+// three E4M3 terms with a power-of-two scale per (row, this 128-feature
+// block) and returned in hv as fp32 (stored by store_h once the item is
+// published).
 __device__ void finish_gate_up(const TcArgs &a, const Smem &S, const Item &it, int grp, int q,
                                int lane, const float (&acc0)[16], const float (&acc1)[16],
-                               const float *csb, const int *tokb) {
+                               const float *csb, const int *tokb, float (&hv)[16]) {
   const int c0 = grp * 16, f = q * 32 + lane, o = it.tile * 128 + f;
   const int KBd = a.I / 128;
   // only the item's real rows are finished (the condition is the same for the
   // whole warp; at decode sizes most of a warp's 16 columns are padding)
-  float hv[16];
 #pragma unroll
   for (int jj = 0; jj < 16; ++jj) {
     hv[jj] = 0.f;
@@ -659,7 +661,6 @@ __device__ void finish_gate_up(const TcArgs &a, const Smem &S, const Item &it, i
         }
       }
       hv[jj] = silu_f32(g * xi) * (u * xi);
-      a.h[(size_t)(it.pos0 + c0 + jj) * a.I + o] = hv[jj];
       const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv[jj])));
       if (lane == 0) S.red[(grp * 4 + q) * 16 + jj] = m;
     }
@@ -697,6 +698,16 @@ __device__ void finish_gate_up(const TcArgs &a, const Smem &S, const Item &it, i
       }
     }
   }
+}
+
+// The fp32 h of a finished gate+up tile (read by no item of the kernel, so
+// written after the tile is published).
+__device__ __forceinline__ void store_h(const TcArgs &a, const Item &it, int grp, int q, int lane,
+                                        const float (&hv)[16]) {
+  const int c0 = grp * 16, o = it.tile * 128 + q * 32 + lane;
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj)
+    if (c0 + jj < it.rows) a.h[(size_t)(it.pos0 + c0 + jj) * a.I + o] = hv[jj];
 }
 
 // acc += scale * (sum of the T term partials of this warp's 16 columns),
@@ -879,15 +890,14 @@ __device__ void epilogue_token(const TcArgs &a, const Smem &S, int A, int TR, in
         break;
       }
       if (it.gu) {
-        finish_gate_up(a, S, it, 0, q, lane, acc0, acc1, cs, tk);
-        // every h of the tile is visible to every CTA and its tensor copies
-        // before the tile is counted
+        float hv[16];
+        finish_gate_up(a, S, it, 0, q, lane, acc0, acc1, cs, tk, hv);
+        // every h term of the tile is visible to every CTA and its tensor
+        // copies before the tile is counted
         fence_proxy_async_global();
         group_sync(0);
-        if (lt == 0) {
-          __threadfence();
-          atomicAdd(a.done + it.a, 1);
-        }
+        if (lt == 0) red_release_add(a.done + it.a, 1);
+        store_h(a, it, 0, q, lane, hv);
       } else {
         const int o0 = it.tile * 256 + q * 32 + lane;
 #pragma unroll
@@ -961,10 +971,7 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
       break;
     }
     if (et == 0) {
-      if (pending >= 0) {
-        __threadfence();
-        atomicAdd(a.done + pending, 1);
-      }
+      if (pending >= 0) red_release_add(a.done + pending, 1);
       if (!it.gu) {
         const int need = (S.rtp[it.a + 1] - S.rtp[it.a]) * FT;
         if (!wait_count(S, a.done + it.a, need)) fail(S, a);
@@ -1052,7 +1059,11 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
       break;
     }
     if (it.gu) {
-      if (mine) finish_gate_up(a, S, it, grp, q, lane, acc0, acc1, S.cs, S.tokrow);
+      if (mine) {
+        float hv[16];
+        finish_gate_up(a, S, it, grp, q, lane, acc0, acc1, S.cs, S.tokrow, hv);
+        store_h(a, it, grp, q, lane, hv);
+      }
       pending = it.a;
     } else if (mine) {
       const int f = q * 32 + lane;
@@ -1070,10 +1081,7 @@ __device__ void epilogue(const TcArgs &a, const Smem &S, int A, int TR, int tota
   // publish the last gate+up item
   fence_proxy_async_global();
   epi_sync_or(false);
-  if (et == 0 && pending >= 0 && !bad) {
-    __threadfence();
-    atomicAdd(a.done + pending, 1);
-  }
+  if (et == 0 && pending >= 0 && !bad) red_release_add(a.done + pending, 1);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -1107,6 +1115,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the swizzled operand tiles assume a 1024-byte aligned ring
   if ((smem_addr(S.ring) & 1023u) != 0) fail(S, a);
 
+  if (threadIdx.x == 0) {   // the copy thread's descriptors, ahead of the first copies
+    for (int j = 0; j < 3; ++j) prefetch_tensormap(&maps.w[j][a.tok ? 1 : 0]);
+    prefetch_tensormap(a.tok ? &maps.xt : &maps.xq[0]);
+  }
   pdl_wait();   // the tables of the alignment (and the token form's x terms) are final
   // The item table first (it needs only the alignment's tables); in the row
   // form the x terms are written by the promotion warps while the copy warp
