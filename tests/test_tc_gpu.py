@@ -239,8 +239,8 @@ def test_tc_verify_batch_matches_staged_path(moe):
     assert rl2 < H.LAYER_REL_L2 and mx < H.LAYER_MAX_ABS, (rl2, mx)
 
 
-@pytest.mark.parametrize("M,m", [(8, 1), (16, 1), (16, 5), (64, 17), (64, 1), (128, 33)],
-                         ids=str)
+@pytest.mark.parametrize("M,m", [(8, 1), (8, 4), (4, 1), (4, 3), (5, 2), (16, 1), (16, 5),
+                                 (64, 17), (64, 1), (128, 33)], ids=str)
 def test_tc_row_invariance(moe, M, m):
     """On the tensor-core path the first m rows' output bits are the same
     whether the batch has m or M rows, across the token form (M <= 16) and
