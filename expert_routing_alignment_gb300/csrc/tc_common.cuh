@@ -88,6 +88,39 @@ __device__ __forceinline__ int atom_acq_rel_add(int *p, int v) {
   return old;
 }
 
+// sum_j w[t][j] * y[token_to_perm[t*k + j]][c .. c+3] in fp32, j ascending,
+// slots with a negative position skipped: the blend's weighted sum.  The
+// loads of 8 slots go out together (one round trip for the positions and
+// weights, one for the rows) before the sums, which keep the slot order.
+__device__ __forceinline__ float4 blend_slots(const float *y, const float *w, const int32_t *ttp,
+                                              int t, int k, int H, int c) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    int p[8];
+    float wv[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = j0 + jj;
+      p[jj] = j < k ? __ldcg(ttp + (size_t)t * k + j) : -1;
+      wv[jj] = j < k ? __ldcg(w + (size_t)t * k + j) : 0.f;
+    }
+    float4 v[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj)
+      v[jj] = p[jj] >= 0 ? __ldcg(reinterpret_cast<const float4 *>(y + (size_t)p[jj] * H + c))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (p[jj] < 0) continue;
+      acc.x = fmaf(wv[jj], v[jj].x, acc.x);
+      acc.y = fmaf(wv[jj], v[jj].y, acc.y);
+      acc.z = fmaf(wv[jj], v[jj].z, acc.z);
+      acc.w = fmaf(wv[jj], v[jj].w, acc.w);
+    }
+  }
+  return acc;
+}
+
 // A tensor map's descriptor fetched ahead of its first copy.
 __device__ __forceinline__ void prefetch_tensormap(const void *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

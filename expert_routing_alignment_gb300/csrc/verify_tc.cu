@@ -1165,17 +1165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long o1 = T4 * (blockIdx.x + 1) / gridDim.x;
   for (long long o = T4 * blockIdx.x / gridDim.x + threadIdx.x; o < o1; o += kThreads) {
     const int t = (int)(o * 4 / a.H), c = (int)(o * 4 % a.H);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < a.k; ++j) {
-      const int p = __ldcg(a.ttp + (size_t)t * a.k + j);
-      if (p < 0) continue;
-      const float wj = __ldcg(a.w + (size_t)t * a.k + j);
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.y + (size_t)p * a.H + c));
-      acc.x = fmaf(wj, v.x, acc.x);
-      acc.y = fmaf(wj, v.y, acc.y);
-      acc.z = fmaf(wj, v.z, acc.z);
-      acc.w = fmaf(wj, v.w, acc.w);
-    }
+    const float4 acc = blend_slots(a.y, a.w, a.ttp, t, a.k, a.H, c);
     const uint32_t lo =
         (uint32_t)float_to_bf16_rn(acc.x) | ((uint32_t)float_to_bf16_rn(acc.y) << 16);
     const uint32_t hi =
