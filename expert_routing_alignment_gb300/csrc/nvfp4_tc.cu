@@ -834,9 +834,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   pdl_wait();
   // the active table as 16-row tiles: info[a] = {offset, expert | rows << 16}
+  // (the first kThreads entries are loaded together with the count; entries
+  // past the count are read but not used)
+  const int j0 = threadIdx.x;
+  const int4 pre = j0 < a.cap ? __ldcg(a.items + j0) : make_int4(0, 0, 0, 0);
   const int A = min(max(__ldcg(a.act_count), 0), a.cap);
-  for (int j = threadIdx.x; j < A; j += kThreads) {
-    const int4 inf = __ldcg(a.items + j);
+  for (int j = j0; j < A; j += kThreads) {
+    const int4 inf = j == j0 ? pre : __ldcg(a.items + j);
     const int rows = min(inf.z, 0x7FFF);
     S.info[j] = make_int2(inf.x, (inf.y & 0xFFFF) | (rows << 16));
     S.rtp[j] = (rows + kRows - 1) / kRows;

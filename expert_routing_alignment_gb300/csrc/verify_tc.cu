@@ -399,9 +399,13 @@ __device__ bool grid_barrier(const Smem &S, unsigned long long *ctr) {
 // active table (offset, expert and slot count of each active expert), so
 // this is one coalesced load and a scan.  Returns the active count.
 __device__ int build_table(const TcArgs &a, const Smem &S) {
+  // the first kThreads entries are loaded together with the count (entries
+  // past the count are read but not used): one round trip
+  const int i0 = threadIdx.x;
+  const int4 pre = i0 < a.cap ? __ldcg(a.items + i0) : make_int4(0, 0, 0, 0);
   const int A = min(max(__ldcg(a.act_count), 0), a.cap);
-  for (int i = threadIdx.x; i < A; i += kThreads) {
-    const int4 inf = __ldcg(a.items + i);
+  for (int i = i0; i < A; i += kThreads) {
+    const int4 inf = i == i0 ? pre : __ldcg(a.items + i);
     const int rows = min(inf.z, 0x7FFF);
     S.info[i] = make_int2(inf.x, (inf.y & 0xFFFF) | (rows << 16));
     S.rtp[i] = (rows + a.row_tile - 1) / a.row_tile;   // counts; scanned below
