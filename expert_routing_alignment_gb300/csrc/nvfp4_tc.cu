@@ -32,6 +32,10 @@
 //    applied once per item.  Items (expert row tile, 128-row gate+up tile),
 //    then (row tile, pair of 128-row down tiles), are taken dynamically; a
 //    down item waits (bounded) until its expert's gate+up tiles are counted.
+//  * FP8 items.  The FP8 shared expert (its items follow the routed ones of
+//    each kind) and the FP8 down projection of the nvfp4-gate-up tier run in
+//    the same kernel: their E4M3 codes decode to exact f16 and the 128 x 128
+//    block scale is applied when each k block is promoted.
 //  * Roles: warp 0 copies, warp 1 issues MMAs, warps 2-5 decode, warps 6-13
 //    promote (two groups of four: token columns 0-15 and 16-31).  After a
 //    grid barrier every CTA blends its share of the outputs.  Every wait

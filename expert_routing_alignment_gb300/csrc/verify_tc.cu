@@ -1,6 +1,7 @@
 // verify_tc.cu -- the grouped expert FFN of the decode MoE layer on the
-// tensor cores (tcgen05 MMA with TMEM accumulators), for batches whose active
-// experts receive many rows each (the M = 128 verify batch).
+// tensor cores (tcgen05 MMA with TMEM accumulators) for FP8 experts: decode
+// batches (a token form up to 16 rows), the M = 128 verify batch and prefill
+// batches up to 4096 rows.
 //
 // What it computes is the same as the CUDA-core kernels: for every active
 // expert e and every real sorted position p of its run, token t,
@@ -29,9 +30,13 @@
 //    issues the MMAs from one thread; 16 warps promote, finish h (SiLU
 //    product, the three terms of the down projection's input) or y.
 //    Items are (expert row tile, 128-row gate+up tile) then (expert row
-//    tile, pair of 128-row down tiles), dealt round-robin over the CTAs; a
-//    down item waits (bounded) until every gate+up item of its expert has
-//    published its h terms through a per-expert counter.
+//    tile, pair of 128-row down tiles), taken in that order from a grid-wide
+//    counter; a down item waits (bounded) until every gate+up item of its
+//    expert has published its h terms through a per-expert counter.
+//  * Token form (up to 16 rows): the gate+up MMAs take the 16 token columns
+//    of a per-token x-term table that the alignment launch wrote, items are
+//    16-row tiles, and one promotion group works while a second stages the
+//    next item's scales, tokens and h scales.
 //  * Every wait gives up after about two seconds with MOE_ERR_TIMEOUT; the
 //    CTA then stops issuing, drains its copies and MMAs and frees its TMEM.
 #include <mutex>
